@@ -1,0 +1,278 @@
+"""fp64 CPU oracle for the CosmoFlow conv3d block -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never links or
+calls it, and it imports nothing from the product package.
+
+The arithmetic lives in ``cf_oracle.c`` (direct nested loops in double
+precision, see its header for the sources and the readings of the pages).
+This module only compiles it with gcc, marshals numpy arrays, and chains the
+per-layer routines into the five-block stack ("mirrored" mode rounds the
+tensors that cross a block boundary to bf16 at the same points where the GPU
+path stores bf16).
+
+Parity of every routine is pinned in ``tests/test_oracle_pins.py`` against
+things other than the oracle itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "cf_oracle.c")
+_LIB = os.path.join(_HERE, "libcforacle.so")
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_U8 = ctypes.POINTER(ctypes.c_uint8)
+_U16 = ctypes.POINTER(ctypes.c_uint16)
+_I64 = ctypes.POINTER(ctypes.c_int64)
+_F32 = ctypes.POINTER(ctypes.c_float)
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP, no fast-math).  Returns the path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        dims = [_i64, _i64, _i64, _i64, _i32, _i32]
+        lib.oracle_conv3d_fwd.argtypes = dims + [_D, _D, _D]
+        lib.oracle_conv3d_dgrad.argtypes = dims + [_D, _D, _D]
+        lib.oracle_conv3d_wgrad.argtypes = dims + [_D, _D, _D]
+        pdims = [_i64, _i64, _i64, _i64, _i32]
+        lib.oracle_pool_fwd.argtypes = pdims + [_D, _D, ctypes.c_double, _D, _U8]
+        lib.oracle_pool_bwd.argtypes = pdims + [_D, _D, _U8, ctypes.c_double, _D, _D, _D]
+        pts = [_i64, _I64, _D, _D]
+        lib.oracle_conv3d_fwd_pts_bf16.argtypes = dims + [_U16, _U16] + pts
+        lib.oracle_conv3d_dgrad_pts_bf16.argtypes = dims + [_U16, _U16] + pts
+        lib.oracle_conv3d_wgrad_pts_bf16.argtypes = dims + [_U16, _U16] + pts
+        lib.oracle_block_fwd_pts_bf16.argtypes = dims + [_U16, _U16, _F32, ctypes.c_double,
+                                                         _i64, _I64, _D, _U8, _D, _D]
+        for f in (lib.oracle_conv3d_fwd, lib.oracle_conv3d_dgrad, lib.oracle_conv3d_wgrad,
+                  lib.oracle_pool_fwd, lib.oracle_pool_bwd, lib.oracle_conv3d_fwd_pts_bf16,
+                  lib.oracle_conv3d_dgrad_pts_bf16, lib.oracle_conv3d_wgrad_pts_bf16,
+                  lib.oracle_block_fwd_pts_bf16):
+            f.restype = None
+        _lib = lib
+    return _lib
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t) if a is not None else None
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def bf16_bits_to_f64(u16: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 bit patterns (uint16) as float64."""
+    u = np.ascontiguousarray(u16, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def round_to_bf16(v: np.ndarray) -> np.ndarray:
+    """Round float64 values to bf16 (via fp32, round-to-nearest-even at each
+    step) and return the rounded values as float64.  Used by mirrored mode."""
+    f = np.ascontiguousarray(v, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16).astype(np.uint32)
+    nan = np.isnan(f)
+    r = np.where(nan, (f.view(np.uint32) >> 16) | 0x40, r).astype(np.uint32)
+    return (r << 16).view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# full-tensor routines (float64 in, float64 out; NDHWC / [Co][3][3][3][Ci])
+
+def conv3d_fwd(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """z = cross-correlation of x [N,D,H,W,Ci] with w [Co,3,3,3,Ci], pad 1."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    N, D, H, W, Ci = x.shape
+    Co = w.shape[0]
+    assert w.shape == (Co, 3, 3, 3, Ci)
+    z = np.empty((N, D, H, W, Co), np.float64)
+    lib.oracle_conv3d_fwd(N, D, H, W, Ci, Co, _p(x, _D), _p(w, _D), _p(z, _D))
+    return z
+
+
+def conv3d_dgrad(dz: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """dx [N,D,H,W,Ci] from dz [N,D,H,W,Co] and w [Co,3,3,3,Ci]."""
+    lib = _load()
+    dz, w = _f64(dz), _f64(w)
+    N, D, H, W, Co = dz.shape
+    Ci = w.shape[4]
+    assert w.shape == (Co, 3, 3, 3, Ci)
+    dx = np.empty((N, D, H, W, Ci), np.float64)
+    lib.oracle_conv3d_dgrad(N, D, H, W, Ci, Co, _p(dz, _D), _p(w, _D), _p(dx, _D))
+    return dx
+
+
+def conv3d_wgrad(x: np.ndarray, dz: np.ndarray) -> np.ndarray:
+    """dW [Co,3,3,3,Ci] from x [N,D,H,W,Ci] and dz [N,D,H,W,Co]."""
+    lib = _load()
+    x, dz = _f64(x), _f64(dz)
+    N, D, H, W, Ci = x.shape
+    Co = dz.shape[4]
+    dw = np.empty((Co, 3, 3, 3, Ci), np.float64)
+    lib.oracle_conv3d_wgrad(N, D, H, W, Ci, Co, _p(x, _D), _p(dz, _D), _p(dw, _D))
+    return dw
+
+
+def pool_fwd(z: np.ndarray, bias, slope: float):
+    """(y, idx) = bias + leaky ReLU + 2x2x2 max-pool of z [N,D,H,W,C]."""
+    lib = _load()
+    z = _f64(z)
+    N, D, H, W, C = z.shape
+    b = None if bias is None else _f64(bias)
+    y = np.empty((N, D // 2, H // 2, W // 2, C), np.float64)
+    idx = np.empty((N, D // 2, H // 2, W // 2, C), np.uint8)
+    lib.oracle_pool_fwd(N, D, H, W, C, _p(z, _D), _p(b, _D), slope, _p(y, _D), _p(idx, _U8))
+    return y, idx
+
+
+def pool_bwd(dy: np.ndarray, y, idx: np.ndarray, slope: float):
+    """(dz, dy_pre, db) of the pool/LReLU stage; y=None means dy is already the
+    gradient w.r.t. the pooled pre-activation."""
+    lib = _load()
+    dy = _f64(dy)
+    N, D2, H2, W2, C = dy.shape
+    yy = None if y is None else _f64(y)
+    idx = np.ascontiguousarray(idx, dtype=np.uint8)
+    dz = np.empty((N, 2 * D2, 2 * H2, 2 * W2, C), np.float64)
+    dyp = np.empty_like(dy)
+    db = np.empty((C,), np.float64)
+    lib.oracle_pool_bwd(N, 2 * D2, 2 * H2, 2 * W2, C, _p(dy, _D), _p(yy, _D), _p(idx, _U8), slope,
+                        _p(dz, _D), _p(dyp, _D), _p(db, _D))
+    return dz, dyp, db
+
+
+# ----------------------------------------------------------------------------
+# sampled routines on bf16 bit patterns (for sizes too large for full fp64)
+
+def _u16(a):
+    return np.ascontiguousarray(a, dtype=np.uint16)
+
+
+def conv3d_fwd_pts(x16, w16, pts):
+    """Exact z and S = sum|w*x| at points (n,d,h,w,co)."""
+    lib = _load()
+    x16, w16 = _u16(x16), _u16(w16)
+    N, D, H, W, Ci = x16.shape
+    Co = w16.shape[0]
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 5)
+    out = np.empty(len(pts)); s = np.empty(len(pts))
+    lib.oracle_conv3d_fwd_pts_bf16(N, D, H, W, Ci, Co, _p(x16, _U16), _p(w16, _U16), len(pts),
+                                   _p(pts, _I64), _p(out, _D), _p(s, _D))
+    return out, s
+
+
+def conv3d_dgrad_pts(dz16, w16, pts):
+    """Exact dx and S = sum|w*dz| at points (n,d,h,w,ci)."""
+    lib = _load()
+    dz16, w16 = _u16(dz16), _u16(w16)
+    N, D, H, W, Co = dz16.shape
+    Ci = w16.shape[4]
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 5)
+    out = np.empty(len(pts)); s = np.empty(len(pts))
+    lib.oracle_conv3d_dgrad_pts_bf16(N, D, H, W, Ci, Co, _p(dz16, _U16), _p(w16, _U16), len(pts),
+                                     _p(pts, _I64), _p(out, _D), _p(s, _D))
+    return out, s
+
+
+def conv3d_wgrad_pts(x16, dz16, pts):
+    """Exact dW and S = sum|dz*x| at points (co,kd,kh,kw,ci)."""
+    lib = _load()
+    x16, dz16 = _u16(x16), _u16(dz16)
+    N, D, H, W, Ci = x16.shape
+    Co = dz16.shape[4]
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 5)
+    out = np.empty(len(pts)); s = np.empty(len(pts))
+    lib.oracle_conv3d_wgrad_pts_bf16(N, D, H, W, Ci, Co, _p(x16, _U16), _p(dz16, _U16), len(pts),
+                                     _p(pts, _I64), _p(out, _D), _p(s, _D))
+    return out, s
+
+
+def block_fwd_pts(x16, w16, bias, slope, pts):
+    """Fused block at pooled points (n,pd,ph,pw,co): (y, idx, S, top-two gap)."""
+    lib = _load()
+    x16, w16 = _u16(x16), _u16(w16)
+    N, D, H, W, Ci = x16.shape
+    Co = w16.shape[0]
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 5)
+    n = len(pts)
+    y = np.empty(n); idx = np.empty(n, np.uint8); s = np.empty(n); gap = np.empty(n)
+    lib.oracle_block_fwd_pts_bf16(N, D, H, W, Ci, Co, _p(x16, _U16), _p(w16, _U16), _p(b, _F32),
+                                  slope, n, _p(pts, _I64), _p(y, _D), _p(idx, _U8), _p(s, _D),
+                                  _p(gap, _D))
+    return y, idx, s, gap
+
+
+# ----------------------------------------------------------------------------
+# the stack (config-level chains)
+
+def block_fwd(x, w, bias, slope):
+    """One block: z = conv(x, w); (y, idx) = pool(z + b) with LReLU.  Returns
+    (z, y, idx)."""
+    z = conv3d_fwd(x, w)
+    y, idx = pool_fwd(z, bias, slope)
+    return z, y, idx
+
+
+def stack_fwd(x, ws, bs, slope, mirrored=True):
+    """Forward through the blocks.  In mirrored mode each block output is
+    rounded to bf16 before it feeds the next block (as the GPU stores it).
+    Returns lists (xs, zs, ys, idxs) with xs[l] the input of block l."""
+    xs, zs, ys, idxs = [], [], [], []
+    cur = _f64(x)
+    for w, b in zip(ws, bs):
+        xs.append(cur)
+        z, y, idx = block_fwd(cur, w, b, slope)
+        if mirrored:
+            y = round_to_bf16(y)
+        zs.append(z); ys.append(y); idxs.append(idx)
+        cur = y
+    return xs, zs, ys, idxs
+
+
+def stack_bwd(xs, ys, idxs, ws, dy, slope, mirrored=True):
+    """Backward through the blocks from dy at the last pooled output.
+    Returns per block (dW, db) and the dense dZ of each block, plus the
+    gradient w.r.t. each block's input (None for block 0, never computed)."""
+    L = len(ws)
+    dws, dbs, dzs, dxs = [None] * L, [None] * L, [None] * L, [None] * L
+    g = _f64(dy)
+    use_y = True
+    for l in range(L - 1, -1, -1):
+        dz, dyp, db = pool_bwd(g, ys[l] if use_y else None, idxs[l], slope)
+        if mirrored:
+            dz = round_to_bf16(dz)
+        dzs[l], dbs[l] = dz, db
+        dws[l] = conv3d_wgrad(xs[l], dz)
+        if l > 0:
+            dx = conv3d_dgrad(dz, ws[l])
+            # LReLU' of the previous block's activation (= this block's input)
+            g = dx * np.where(xs[l] > 0, 1.0, slope)
+            if mirrored:
+                g = round_to_bf16(g)
+            dxs[l] = g
+            use_y = False
+    return dws, dbs, dzs, dxs

@@ -1,0 +1,309 @@
+"""Pins for the fp64 oracle: each check compares it with something other than
+itself (an independently built dense operator, a library correlation routine,
+closed forms, identities, finite differences, the pages' printed numbers).
+CPU only."""
+import os
+
+import numpy as np
+import pytest
+
+import synthdata
+
+RNG = np.random.default_rng(1234)
+
+
+def _dense_shift(n, k):
+    """1D shift matrix S with (S v)[i] = v[i + k - 1] (zero outside)."""
+    return np.eye(n, k=k - 1)
+
+
+def _shift3(D, H, W, kd, kh, kw):
+    return np.kron(np.kron(_dense_shift(D, kd), _dense_shift(H, kh)), _dense_shift(W, kw))
+
+
+def dense_conv_operator(N, D, H, W, w):
+    """Matrix A (rows (n,v,co), cols (n,u,ci)) of the pad-1 cross-correlation,
+    built from Kronecker products of 1D shift matrices and the per-tap
+    channel-mixing blocks w[:, kd, kh, kw, :]."""
+    Co, _, _, _, Ci = w.shape
+    V = D * H * W
+    A = np.zeros((N * V * Co, N * V * Ci))
+    for kd in range(3):
+        for kh in range(3):
+            for kw in range(3):
+                S = np.kron(np.eye(N), _shift3(D, H, W, kd, kh, kw))
+                A += np.kron(S, w[:, kd, kh, kw, :])
+    return A
+
+
+def dense_weight_jacobian(x, Co):
+    """Matrix J with z_flat = J @ w_flat for fixed x (w flat in [Co][3][3][3][Ci])."""
+    N, D, H, W, Ci = x.shape
+    V = D * H * W
+    J = np.zeros((N * V * Co, Co * 27 * Ci))
+    xf = x.reshape(N, V, Ci)
+    for t in range(27):
+        kd, kh, kw = t // 9, (t // 3) % 3, t % 3
+        S = _shift3(D, H, W, kd, kh, kw)
+        xs = np.einsum("uv,nvc->nuc", S, xf).reshape(N * V, Ci)
+        for co in range(Co):
+            rows = np.arange(N * V) * Co + co
+            cols = co * 27 * Ci + t * Ci + np.arange(Ci)
+            J[np.ix_(rows, cols)] = xs
+    return J
+
+
+SHAPES = [
+    (1, 2, 3, 4, 1, 1),
+    (1, 3, 3, 3, 2, 2),
+    (2, 4, 2, 5, 3, 2),
+    (1, 5, 4, 3, 2, 3),
+]
+
+
+@pytest.mark.parametrize("N,D,H,W,Ci,Co", SHAPES)
+def test_conv_matches_dense_operator(oracle_mod, N, D, H, W, Ci, Co):
+    x = RNG.normal(size=(N, D, H, W, Ci))
+    w = RNG.normal(size=(Co, 3, 3, 3, Ci))
+    dz = RNG.normal(size=(N, D, H, W, Co))
+    A = dense_conv_operator(N, D, H, W, w)
+    z = oracle_mod.conv3d_fwd(x, w)
+    np.testing.assert_allclose(z.ravel(), A @ x.ravel(), rtol=1e-12, atol=1e-12)
+    dx = oracle_mod.conv3d_dgrad(dz, w)
+    np.testing.assert_allclose(dx.ravel(), A.T @ dz.ravel(), rtol=1e-12, atol=1e-12)
+    J = dense_weight_jacobian(x, Co)
+    np.testing.assert_allclose(J @ w.ravel(), z.ravel(), rtol=1e-12, atol=1e-12)
+    dw = oracle_mod.conv3d_wgrad(x, dz)
+    np.testing.assert_allclose(dw.ravel(), J.T @ dz.ravel(), rtol=1e-12, atol=1e-12)
+
+
+def test_conv_matches_scipy_correlate(oracle_mod):
+    from scipy.signal import correlate
+    N, D, H, W, Ci, Co = 2, 6, 5, 7, 3, 4
+    x = RNG.normal(size=(N, D, H, W, Ci))
+    w = RNG.normal(size=(Co, 3, 3, 3, Ci))
+    z = oracle_mod.conv3d_fwd(x, w)
+    ref = np.zeros_like(z)
+    for n in range(N):
+        for co in range(Co):
+            for ci in range(Ci):
+                ref[n, :, :, :, co] += correlate(x[n, :, :, :, ci], w[co, :, :, :, ci],
+                                                 mode="same", method="direct")
+    np.testing.assert_allclose(z, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("t0", [0, 4, 13, 22, 26])
+def test_delta_kernel_shift(oracle_mod, t0):
+    N, D, H, W, C = 1, 4, 5, 6, 3
+    kd, kh, kw = t0 // 9, (t0 // 3) % 3, t0 % 3
+    x = RNG.normal(size=(N, D, H, W, C))
+    w = np.zeros((C, 3, 3, 3, C))
+    for c in range(C):
+        w[c, kd, kh, kw, c] = 1.0
+    z = oracle_mod.conv3d_fwd(x, w)
+    xp = np.pad(x, ((0, 0), (1, 1), (1, 1), (1, 1), (0, 0)))
+    expect = xp[:, kd:kd + D, kh:kh + H, kw:kw + W, :]
+    np.testing.assert_array_equal(z, expect)
+    if t0 == 13:
+        np.testing.assert_array_equal(z, x)
+
+
+def test_constant_input_tap_counts(oracle_mod):
+    N, D, H, W, Ci, Co = 1, 5, 5, 5, 2, 1
+    c = 0.75
+    x = np.full((N, D, H, W, Ci), c)
+    w = np.ones((Co, 3, 3, 3, Ci))
+    z = oracle_mod.conv3d_fwd(x, w)[0, :, :, :, 0] / (c * Ci)
+    assert z[2, 2, 2] == 27  # interior
+    assert z[0, 2, 2] == 18  # face
+    assert z[0, 0, 2] == 12  # edge
+    assert z[0, 0, 0] == 8   # corner
+    assert z[4, 4, 4] == 8
+    # with random weights: sum over the valid taps only
+    w = RNG.normal(size=(2, 3, 3, 3, Ci))
+    z = oracle_mod.conv3d_fwd(x, w)
+    np.testing.assert_allclose(z[0, 2, 2, 2], c * w.sum(axis=(1, 2, 3, 4)), rtol=1e-13)
+    np.testing.assert_allclose(z[0, 0, 0, 0], c * w[:, 1:, 1:, 1:, :].sum(axis=(1, 2, 3, 4)),
+                               rtol=1e-13)
+
+
+def test_linearity(oracle_mod):
+    x1 = RNG.normal(size=(2, 4, 3, 5, 3))
+    x2 = RNG.normal(size=x1.shape)
+    w = RNG.normal(size=(2, 3, 3, 3, 3))
+    a, b = 1.7, -0.4
+    lhs = oracle_mod.conv3d_fwd(a * x1 + b * x2, w)
+    rhs = a * oracle_mod.conv3d_fwd(x1, w) + b * oracle_mod.conv3d_fwd(x2, w)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-11, atol=1e-11)
+
+
+def test_adjoint_identities(oracle_mod):
+    x = RNG.normal(size=(2, 6, 5, 4, 3))
+    w = RNG.normal(size=(4, 3, 3, 3, 3))
+    g = RNG.normal(size=(2, 6, 5, 4, 4))
+    lhs = np.vdot(oracle_mod.conv3d_fwd(x, w), g)
+    mid = np.vdot(x, oracle_mod.conv3d_dgrad(g, w))
+    rhs = np.vdot(w, oracle_mod.conv3d_wgrad(x, g))
+    assert abs(lhs - mid) <= 1e-10 * abs(lhs)
+    assert abs(lhs - rhs) <= 1e-10 * abs(lhs)
+
+
+def _block_loss(oracle_mod, x, w, b, g, slope):
+    z = oracle_mod.conv3d_fwd(x, w)
+    y, idx = oracle_mod.pool_fwd(z, b, slope)
+    return np.vdot(g, y), z, y, idx
+
+
+def test_finite_difference_gradients(oracle_mod):
+    slope = 0.3
+    rng = np.random.default_rng(7)
+    # resample until there is no kink: every pre-activation away from 0 and
+    # every window's top-two gap above 1e-3
+    for _ in range(200):
+        x = rng.normal(size=(1, 4, 4, 6, 2))
+        w = rng.normal(size=(3, 3, 3, 3, 2))
+        b = rng.normal(size=(3,))
+        z = oracle_mod.conv3d_fwd(x, w)
+        y, idx = oracle_mod.pool_fwd(z, b, slope)
+        win = z.reshape(1, 2, 2, 2, 2, 3, 2, 3).transpose(0, 1, 3, 5, 7, 2, 4, 6).reshape(1, 2, 2, 3, 3, 8)
+        srt = np.sort(win, axis=-1)
+        pre = srt[..., -1] + b
+        if np.min(srt[..., -1] - srt[..., -2]) > 1e-3 and np.min(np.abs(pre)) > 1e-3:
+            break
+    else:
+        pytest.fail("could not draw a kink-free case")
+    g = rng.normal(size=y.shape)
+    dz, dyp, db = oracle_mod.pool_bwd(g, y, idx, slope)
+    dw = oracle_mod.conv3d_wgrad(x, dz)
+    dx = oracle_mod.conv3d_dgrad(dz, w)
+    h = 1e-6
+
+    def fd(arr, pos, which):
+        a = arr.copy(); a[pos] += h
+        lp = _block_loss(oracle_mod, *(which(a)), g, slope)[0]
+        a = arr.copy(); a[pos] -= h
+        lm = _block_loss(oracle_mod, *(which(a)), g, slope)[0]
+        return (lp - lm) / (2 * h)
+
+    for _ in range(6):
+        pos = tuple(rng.integers(0, s) for s in x.shape)
+        num = fd(x, pos, lambda a: (a, w, b))
+        assert abs(num - dx[pos]) <= 1e-5 * max(1.0, abs(num)), (pos, num, dx[pos])
+        pos = tuple(rng.integers(0, s) for s in w.shape)
+        num = fd(w, pos, lambda a: (x, a, b))
+        assert abs(num - dw[pos]) <= 1e-5 * max(1.0, abs(num)), (pos, num, dw[pos])
+    for c in range(3):
+        num = fd(b, (c,), lambda a: (x, w, a))
+        assert abs(num - db[c]) <= 1e-5 * max(1.0, abs(num))
+
+
+def test_pool_closed_forms(oracle_mod):
+    N, D, H, W, C = 1, 4, 4, 6, 2
+    d, h, w = np.meshgrid(np.arange(D), np.arange(H), np.arange(W), indexing="ij")
+    ramp = ((d * H) + h) * W + w
+    z = np.repeat(ramp[None, :, :, :, None].astype(float), C, axis=4)
+    y, idx = oracle_mod.pool_fwd(z, None, 0.3)
+    assert np.all(idx == 7)
+    # the maximum of each window is its (1,1,1) corner
+    np.testing.assert_array_equal(y, z[:, 1::2, 1::2, 1::2, :])
+    y, idx = oracle_mod.pool_fwd(-z, None, 0.3)
+    assert np.all(idx == 0)
+    np.testing.assert_allclose(y, 0.3 * (-z[:, 0::2, 0::2, 0::2, :]))
+    y, idx = oracle_mod.pool_fwd(np.full((1, 2, 2, 2, 1), 5.0), None, 0.3)
+    assert idx.item() == 0 and y.item() == 5.0  # ties: first maximum wins
+    y, _ = oracle_mod.pool_fwd(np.full((1, 2, 2, 2, 1), -1.0), None, 0.3)
+    assert y.item() == pytest.approx(-0.3, abs=1e-15)
+    y, _ = oracle_mod.pool_fwd(np.full((1, 2, 2, 2, 1), 2.0), None, 0.3)
+    assert y.item() == 2.0
+    # bias shifts before the activation
+    y, _ = oracle_mod.pool_fwd(np.full((1, 2, 2, 2, 1), 1.0), np.array([-3.0]), 0.3)
+    assert y.item() == pytest.approx(-0.6, abs=1e-15)
+
+
+def test_pool_commutes_with_activation(oracle_mod):
+    z = RNG.normal(size=(2, 4, 6, 4, 3))
+    y, _ = oracle_mod.pool_fwd(z, None, 0.3)
+    act = np.where(z > 0, z, 0.3 * z)
+    # pool the activated tensor with a plain numpy window max
+    win = act.reshape(2, 2, 2, 3, 2, 2, 2, 3).max(axis=(2, 4, 6))
+    np.testing.assert_array_equal(y, win)
+
+
+def test_pool_bwd_routes_to_argmax(oracle_mod):
+    z = RNG.normal(size=(1, 4, 4, 4, 2))
+    b = np.array([0.1, -0.2])
+    y, idx = oracle_mod.pool_fwd(z, b, 0.3)
+    dy = RNG.normal(size=y.shape)
+    dz, dyp, db = oracle_mod.pool_bwd(dy, y, idx, 0.3)
+    np.testing.assert_allclose(dyp, dy * np.where(y > 0, 1.0, 0.3))
+    np.testing.assert_allclose(db, dyp.sum(axis=(0, 1, 2, 3)))
+    # exactly one nonzero per window and channel, at the window's argmax of z
+    win = dz.reshape(1, 2, 2, 2, 2, 2, 2, 2).transpose(0, 1, 3, 5, 7, 2, 4, 6).reshape(1, 2, 2, 2, 2, 8)
+    zw = z.reshape(1, 2, 2, 2, 2, 2, 2, 2).transpose(0, 1, 3, 5, 7, 2, 4, 6).reshape(1, 2, 2, 2, 2, 8)
+    am = np.argmax(zw, axis=-1)
+    np.testing.assert_array_equal(am, idx)
+    np.testing.assert_array_equal(np.take_along_axis(win, am[..., None], -1)[..., 0], dyp)
+    assert np.count_nonzero(win) == np.count_nonzero(dyp)
+    # y=None: dy is taken as the pre-activation gradient
+    dz2, dyp2, db2 = oracle_mod.pool_bwd(dyp, None, idx, 0.3)
+    np.testing.assert_array_equal(dz2, dz)
+
+
+def test_point_routines_match_full(oracle_mod):
+    c = synthdata.random_case(11, 2, 4, 6, 8, 16, 8)
+    x = oracle_mod.bf16_bits_to_f64(c["x"])
+    w = oracle_mod.bf16_bits_to_f64(c["w"])
+    dz = oracle_mod.bf16_bits_to_f64(c["dz"])
+    z = oracle_mod.conv3d_fwd(x, w)
+    dx = oracle_mod.conv3d_dgrad(dz, w)
+    dw = oracle_mod.conv3d_wgrad(x, dz)
+    rng = np.random.default_rng(3)
+    pts = np.stack([rng.integers(0, s, 40) for s in z.shape], 1)
+    v, s = oracle_mod.conv3d_fwd_pts(c["x"], c["w"], pts)
+    np.testing.assert_array_equal(v, z[tuple(pts.T)])
+    assert np.all(s >= np.abs(v))
+    pts = np.stack([rng.integers(0, s, 40) for s in dx.shape], 1)
+    v, s = oracle_mod.conv3d_dgrad_pts(c["dz"], c["w"], pts)
+    np.testing.assert_array_equal(v, dx[tuple(pts.T)])
+    pts = np.stack([rng.integers(0, s, 40) for s in dw.shape], 1)
+    v, s = oracle_mod.conv3d_wgrad_pts(c["x"], c["dz"], pts)
+    np.testing.assert_allclose(v, dw[tuple(pts.T)], rtol=1e-12, atol=1e-12)
+    # fused block at pooled points
+    y, idx = oracle_mod.pool_fwd(z, c["b"].astype(np.float64), 0.3)
+    pts = np.stack([rng.integers(0, s, 40) for s in y.shape], 1)
+    yv, iv, sv, gap = oracle_mod.block_fwd_pts(c["x"], c["w"], c["b"], 0.3, pts)
+    np.testing.assert_array_equal(yv, y[tuple(pts.T)])
+    np.testing.assert_array_equal(iv, idx[tuple(pts.T)])
+    assert np.all(gap >= 0)
+
+
+def test_bf16_rounding_agrees_with_torch(oracle_mod):
+    torch = pytest.importorskip("torch")
+    v = np.concatenate([RNG.normal(size=5000) * 10.0 ** RNG.integers(-8, 8, 5000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.005859375, -3.0e38]])
+    ref = torch.tensor(v.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle_mod.round_to_bf16(v), ref)
+    np.testing.assert_array_equal(
+        synthdata.bf16_bits_to_f32(synthdata.to_bf16_bits(v)).astype(np.float64), ref)
+
+
+def _golden_rows():
+    path = os.path.join(os.path.dirname(__file__), "golden", "p3_table1_flops.txt")
+    rows = []
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([float(t) for t in line.split()])
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_rows())
+def test_flop_convention_reproduces_table1(row):
+    from cnn_conv3d_gb300 import flops
+    wi, ops, fwd, params = row
+    f = flops.p3_table1_forward_flops(int(wi)) / 1e9
+    # the page prints 4 significant digits; agree to the printed precision
+    assert abs(f - fwd) <= 0.5 * 10 ** (np.floor(np.log10(fwd)) - 3) + 1e-9, (f, fwd)
+    assert abs(3 * f - ops) <= 0.5 * 10 ** (np.floor(np.log10(ops)) - 3) + 1e-9, (3 * f, ops)
+    assert round(flops.p3_table1_params() / 1e6, 2) == params
