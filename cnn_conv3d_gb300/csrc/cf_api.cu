@@ -1,0 +1,260 @@
+// cf_api.cu -- the C ABI of libcfconv3d.so (declared in include/cf_conv3d.h):
+// argument validation, workspace layout, per-device context (SM count,
+// device status word, tensor-map encoder) and the launch sequence of each
+// operation.  No entry point allocates or frees device memory.
+#include <mutex>
+
+#include "cf_internal.h"
+#include "cf_ptx.cuh"
+
+namespace cf {
+
+__device__ int g_status;  // device status word (0 = OK)
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+int g_num_sms[kMaxDevices] = {0};
+int* g_status_ptr[kMaxDevices] = {nullptr};
+uint64_t g_wait_ns = 2000000000ull;
+
+// Per-device set-up, once: SM count and the device address of the status word.
+bool device_ctx(LaunchCtx* ctx, void* stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_num_sms[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            return false;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return false;
+        g_status_ptr[dev] = static_cast<int*>(p);
+        g_num_sms[dev] = sms;
+    }
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return false;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    ctx->num_sms = g_num_sms[dev];
+    ctx->status = g_status_ptr[dev];
+    ctx->wait_ns = g_wait_ns;
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool desc_ok(const cf_conv_desc* d) {
+    if (d == nullptr) return false;
+    if (d->n <= 0 || d->d <= 0 || d->h <= 0 || d->w <= 0 || d->c_in <= 0 || d->c_out <= 0) return false;
+    // every index the kernels form stays below 2^31 per dimension and 2^62 in total
+    if (d->d > (1 << 20) || d->h > (1 << 20) || d->w > (1 << 20) || d->n > (1 << 24)) return false;
+    const double elems = (double)d->n * d->d * d->h * d->w * (double)(d->c_in > d->c_out ? d->c_in : d->c_out);
+    return elems < 4.0e18;
+}
+
+int64_t dense_grad_elems(const cf_conv_desc* d) { return d->n * d->d * d->h * d->w * (int64_t)d->c_out; }
+
+}  // namespace
+
+bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
+    if (g_encode == nullptr) return false;
+    cuuint64_t gd[5];
+    cuuint64_t gs[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i < rank - 1) gs[i] = strides_bytes[i];
+    }
+    CUresult r = g_encode(m, dt, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace cf
+
+using namespace cf;
+
+extern "C" {
+
+const char* cf_status_string(cf_status s) {
+    switch (s) {
+        case CF_OK: return "ok";
+        case CF_ERR_INVALID_ARG: return "invalid argument";
+        case CF_ERR_UNSUPPORTED: return "unsupported shape or layout";
+        case CF_ERR_WORKSPACE: return "workspace too small";
+        case CF_ERR_CUDA: return "CUDA error";
+        case CF_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+cf_status cf_set_wait_limit_ns(uint64_t ns) {
+    if (ns == 0) return CF_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_wait_ns = ns;
+    return CF_OK;
+}
+
+cf_status cf_last_device_status(void* stream) {
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    if (cudaStreamSynchronize(ctx.stream) != cudaSuccess) return CF_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ctx.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CF_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(ctx.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return CF_ERR_CUDA;
+        return CF_ERR_TIMEOUT;
+    }
+    return CF_OK;
+}
+
+cf_status cf_debug_wait_timeout_probe(void* stream) {
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_timeout_probe(ctx);
+}
+
+size_t cf_workspace_size(int op, const cf_conv_desc* desc) {
+    if (!desc_ok(desc)) return 0;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, nullptr)) return 0;
+    const size_t wt = round_up((size_t)desc->c_out * 27 * desc->c_in * 2, 256);
+    const size_t dense = round_up((size_t)dense_grad_elems(desc) * 2, 256);
+    const size_t part = round_up(
+        wgrad_workspace_bytes(ctx.num_sms, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out), 256);
+    switch (op) {
+        case CF_OP_FWD: return 0;
+        case CF_OP_DGRAD: return wt;
+        case CF_OP_DGRAD_ROUTED: return wt + dense;
+        case CF_OP_WGRAD: return part;
+        case CF_OP_WGRAD_ROUTED: return part + dense;
+        case CF_OP_POOL_BWD: return round_up(pool_bwd_workspace_bytes(ctx.num_sms, desc->c_out), 256);
+    }
+    return 0;
+}
+
+cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* w, const cf_pool_epi* epi,
+                        uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (!desc_ok(desc) || x == nullptr || w == nullptr || y == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return CF_ERR_INVALID_ARG;
+    if (epi != nullptr) {
+        if ((epi->bias && !aligned16(epi->bias)) || (epi->argmax && !aligned16(epi->argmax)))
+            return CF_ERR_INVALID_ARG;
+        if ((desc->d | desc->h | desc->w) & 1) return CF_ERR_UNSUPPORTED;
+    }
+    const int ci = desc->c_in, co = desc->c_out;
+    const bool small = ci == 1 || ci == 4;
+    if (!small && ci % 32 != 0) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    const int mode = epi ? EPI_POOL : EPI_PLAIN;
+    const float* bias = epi ? epi->bias : nullptr;
+    uint8_t* idx = epi ? epi->argmax : nullptr;
+    const float slope = epi ? epi->slope : 0.f;
+    if (small) return launch_conv_smallc(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, slope);
+    return launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, nullptr, slope);
+}
+
+cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx, const uint16_t* w,
+                          const uint16_t* x_act, float slope, uint16_t* dx, void* ws, size_t ws_bytes,
+                          void* stream) {
+    if (!desc_ok(desc) || dz == nullptr || w == nullptr || dx == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(dz) || !aligned16(w) || !aligned16(dx) || (x_act && !aligned16(x_act)) ||
+        (idx && !aligned16(idx)) || (ws && !aligned16(ws)))
+        return CF_ERR_INVALID_ARG;
+    const int ci = desc->c_in, co = desc->c_out;
+    if (co % 32 != 0 || ci % 16 != 0) return CF_ERR_UNSUPPORTED;
+    if (idx && ((desc->d | desc->h | desc->w) & 1)) return CF_ERR_UNSUPPORTED;
+    const size_t wt_bytes = round_up((size_t)co * 27 * ci * 2, 256);
+    const size_t need = wt_bytes + (idx ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0);
+    if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    uint16_t* wt = static_cast<uint16_t*>(ws);
+    cf_status st = launch_flip_transpose(ctx, co, ci, w, wt);
+    if (st != CF_OK) return st;
+    const uint16_t* dz_dense = dz;
+    if (idx) {
+        uint16_t* buf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + wt_bytes);
+        st = launch_pool_bwd(ctx, desc->n, desc->d, desc->h, desc->w, co, dz, nullptr, idx, 1.f, buf, nullptr,
+                             nullptr, nullptr, 0);
+        if (st != CF_OK) return st;
+        dz_dense = buf;
+    }
+    // backward data = forward conv of dZ with the flipped, transposed filter:
+    // GEMM input channels c_out, output channels c_in
+    return launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt,
+                             x_act ? EPI_DGRAD : EPI_PLAIN, dx, nullptr, nullptr, x_act, slope);
+}
+
+cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* dz, const uint8_t* idx,
+                          float* dw, int accumulate, void* ws, size_t ws_bytes, void* stream) {
+    if (!desc_ok(desc) || x == nullptr || dz == nullptr || dw == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(dz) || !aligned16(dw) || (idx && !aligned16(idx)) || (ws && !aligned16(ws)))
+        return CF_ERR_INVALID_ARG;
+    if (idx && ((desc->d | desc->h | desc->w) & 1)) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    const size_t part = round_up(
+        wgrad_workspace_bytes(ctx.num_sms, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out), 256);
+    const size_t need = part + (idx ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0);
+    if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
+    const uint16_t* dz_dense = dz;
+    if (idx) {
+        uint16_t* buf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + part);
+        cf_status st = launch_pool_bwd(ctx, desc->n, desc->d, desc->h, desc->w, desc->c_out, dz, nullptr, idx, 1.f,
+                                       buf, nullptr, nullptr, nullptr, 0);
+        if (st != CF_OK) return st;
+        dz_dense = buf;
+    }
+    return launch_wgrad(ctx, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out, x, dz_dense, dw,
+                        accumulate, ws, part);
+}
+
+cf_status cf_bias_lrelu_pool_fwd(int64_t n, int64_t d, int64_t h, int64_t w, int32_t c, const uint16_t* z,
+                                 const float* bias, float slope, uint16_t* y, uint8_t* idx, void* stream) {
+    if (n <= 0 || d <= 0 || h <= 0 || w <= 0 || c <= 0 || z == nullptr || y == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(z) || !aligned16(y) || (bias && !aligned16(bias)) || (idx && !aligned16(idx)))
+        return CF_ERR_INVALID_ARG;
+    if (c % 8 != 0 || ((d | h | w) & 1)) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_pool_fwd(ctx, n, d, h, w, c, z, bias, slope, y, idx);
+}
+
+cf_status cf_bias_lrelu_pool_bwd(int64_t n, int64_t d, int64_t h, int64_t w, int32_t c, const uint16_t* dy,
+                                 const uint16_t* y, const uint8_t* idx, float slope, uint16_t* dz, uint16_t* dy_pre,
+                                 float* dbias, void* ws, size_t ws_bytes, void* stream) {
+    if (n <= 0 || d <= 0 || h <= 0 || w <= 0 || c <= 0 || dy == nullptr) return CF_ERR_INVALID_ARG;
+    if (dz != nullptr && idx == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(dy) || (y && !aligned16(y)) || (idx && !aligned16(idx)) || (dz && !aligned16(dz)) ||
+        (dy_pre && !aligned16(dy_pre)) || (dbias && !aligned16(dbias)) || (ws && !aligned16(ws)))
+        return CF_ERR_INVALID_ARG;
+    if (c % 8 != 0 || c > 2048 || ((d | h | w) & 1)) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_pool_bwd(ctx, n, d, h, w, c, dy, y, idx, slope, dz, dy_pre, dbias, ws, ws_bytes);
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// cf_internal.h -- host-side declarations shared by the library's translation
+// units (launchers implemented in the .cu files, called from cf_api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/cf_conv3d.h"
+
+namespace cf {
+
+// Status codes written into the device status word by a bounded wait that gave
+// up (any non-zero value maps to CF_ERR_TIMEOUT on the host).
+enum : int {
+    WAIT_PRODUCER_EMPTY = 0x101,
+    WAIT_MMA_TMEM_EMPTY = 0x102,
+    WAIT_MMA_FULL = 0x103,
+    WAIT_EPI_TMEM_FULL = 0x104,
+    WAIT_DRAIN = 0x105,
+    WAIT_PROBE = 0x1FF,
+};
+
+enum EpiMode : int { EPI_PLAIN = 0, EPI_POOL = 1, EPI_DGRAD = 2 };
+
+struct LaunchCtx {
+    cudaStream_t stream;
+    int num_sms;
+    int* status;       // device status word
+    uint64_t wait_ns;  // bounded-wait limit
+};
+
+// Geometry of the 128-voxel output tile of the implicit GEMM: a box of
+// td x th x tw voxels (td = 2 so that pooled tiles hold whole windows).
+struct TileGeom {
+    int tw, th, td;
+};
+TileGeom choose_tile(int64_t d, int64_t h, int64_t w);
+
+// Encodes a tiled TMA descriptor; returns false on failure.
+bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
+
+// conv_fwd.cu ---------------------------------------------------------------
+// Generic implicit-GEMM conv (c_in a multiple of 32): out = conv(x, wk) where
+// wk is [c_out][27][c_in] (K-major GEMM B operand).  EPI_POOL writes the pooled
+// block output and argmax; EPI_DGRAD multiplies by LReLU'(x_act).
+cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
+                            int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
+                            uint8_t* idx, const float* bias, const uint16_t* x_act, float slope);
+
+// Small-channel conv forward (c_in in {1,4}): im2col tile built in shared memory.
+cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
+                             int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
+                             uint8_t* idx, const float* bias, float slope);
+
+// conv_wgrad.cu -------------------------------------------------------------
+size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out);
+cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
+                       const uint16_t* x, const uint16_t* dz, float* dw, int accumulate, void* ws,
+                       size_t ws_bytes);
+
+// elementwise.cu ------------------------------------------------------------
+cf_status launch_pool_fwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                          const uint16_t* z, const float* bias, float slope, uint16_t* y, uint8_t* idx);
+size_t pool_bwd_workspace_bytes(int num_sms, int c);
+cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                          const uint16_t* dy, const uint16_t* y, const uint8_t* idx, float slope, uint16_t* dz,
+                          uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes);
+cf_status launch_flip_transpose(const LaunchCtx& ctx, int c_out, int c_in, const uint16_t* w, uint16_t* wt);
+cf_status launch_timeout_probe(const LaunchCtx& ctx);
+
+}  // namespace cf

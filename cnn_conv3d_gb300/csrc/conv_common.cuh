@@ -1,0 +1,165 @@
+// conv_common.cuh -- pieces shared by the forward/backward-data implicit-GEMM
+// kernels: tile decoding and the fused epilogues that read the fp32
+// accumulator out of tensor memory.
+#pragma once
+
+#include "cf_internal.h"
+#include "cf_ptx.cuh"
+
+namespace cf {
+
+// Output tile of 128 voxels: box (TD=2) x th x tw starting at (d0,h0,w0) of
+// sample n, and output channels [co0, co0 + BN).
+struct TileCoord {
+    int n, d0, h0, w0, co0;
+};
+
+struct ConvGeom {
+    int N, D, H, W;
+    int Cin, Cout;  // GEMM view: K = 27 * Cin, N-dimension = Cout
+    int tw, th, td;
+    int tiles_w, tiles_h, tiles_d;
+    int n_ntiles;
+    int num_tiles;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const ConvGeom& g, int tile, int bn) {
+    TileCoord c;
+    int nt = tile % g.n_ntiles;
+    int mt = tile / g.n_ntiles;
+    int tw = mt % g.tiles_w;
+    mt /= g.tiles_w;
+    int th = mt % g.tiles_h;
+    mt /= g.tiles_h;
+    int td = mt % g.tiles_d;
+    c.n = mt / g.tiles_d;
+    c.w0 = tw * g.tw;
+    c.h0 = th * g.th;
+    c.d0 = td * g.td;
+    c.co0 = nt * bn;
+    return c;
+}
+
+// The epilogue warps wait for an accumulator through one leader thread, which
+// then releases the other 127 with a named barrier: a wait that gives up is
+// thus seen by all of them, and none is left behind at a later named barrier.
+__device__ __forceinline__ bool epi_wait(uint64_t* bar, uint32_t parity, int et, volatile int* flag,
+                                         volatile int* abort, uint64_t limit_ns, int* status) {
+    if (et == 0) *flag = mbar_wait(bar, parity, abort, limit_ns, status, WAIT_EPI_TMEM_FULL) ? 1 : 0;
+    named_bar_sync(2, 128);
+    return *flag != 0;
+}
+
+struct EpiArgs {
+    uint16_t* y;
+    uint8_t* idx;
+    const float* bias;
+    const uint16_t* x_act;
+    float slope;
+};
+
+// Epilogue of one tile, executed by the 128 epilogue threads (4 warps whose
+// warp index modulo 4 is q; thread row = 32*q + lane is TMEM lane = GEMM row).
+//   acc_col : first TMEM column of this tile's accumulator
+//   stg     : [128][33] fp32 staging buffer (EPI_POOL only)
+//   et      : epilogue thread id 0..127
+template <int BN, int EPI>
+__device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord& tc, const EpiArgs& ea,
+                                              uint32_t tmem_base, uint32_t acc_col, int q, int lane, int et,
+                                              float* stg) {
+    constexpr int CH = BN >= 32 ? 32 : 16;
+    const int row = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
+    const int l = row % g.tw, j = (row / g.tw) % g.th, i = row / (g.tw * g.th);
+    const int d = tc.d0 + i, h = tc.h0 + j, w = tc.w0 + l;
+    const bool valid = d < g.D && h < g.H && w < g.W;
+    const int64_t vox = (((int64_t)tc.n * g.D + d) * g.H + h) * g.W + w;
+
+#pragma unroll 1
+    for (int c = 0; c < BN; c += CH) {
+        uint32_t r[32];
+        if (CH == 32)
+            tmem_ld32(lane_addr + c, r);
+        else
+            tmem_ld16(lane_addr + c, r);
+        tmem_ld_wait();
+        if (EPI == EPI_POOL) {
+#pragma unroll
+            for (int k = 0; k < CH; ++k) stg[row * 33 + k] = __uint_as_float(r[k]);
+            named_bar_sync(1, 128);
+            constexpr int CPT = CH / 8;  // channels per thread
+            const int wi = et >> 3;      // 16 windows per tile
+            const int tw2 = g.tw >> 1;
+            const int pw_l = wi % tw2, ph_l = wi / tw2;
+            const int cb = (et & 7) * CPT;
+            const int D2 = g.D >> 1, H2 = g.H >> 1, W2 = g.W >> 1;
+            const int pd = tc.d0 >> 1, ph = (tc.h0 >> 1) + ph_l, pw = (tc.w0 >> 1) + pw_l;
+            if (pd < D2 && ph < H2 && pw < W2) {
+                const int64_t po = ((((int64_t)tc.n * D2 + pd) * H2 + ph) * W2 + pw) * g.Cout + tc.co0 + c + cb;
+                float yv[CPT];
+                uint32_t codes = 0;
+#pragma unroll
+                for (int cc = 0; cc < CPT; ++cc) {
+                    float m = 0.f;
+                    int code = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+                        const int rr = (dd * g.th + 2 * ph_l + dh) * g.tw + 2 * pw_l + dw;
+                        const float v = stg[rr * 33 + cb + cc];
+                        if (k == 0 || v > m) {
+                            m = v;
+                            code = k;
+                        }
+                    }
+                    const int co = tc.co0 + c + cb + cc;
+                    const float s = m + ((ea.bias != nullptr && co < g.Cout) ? ea.bias[co] : 0.f);
+                    yv[cc] = s > 0.f ? s : ea.slope * s;
+                    codes |= (uint32_t)code << (8 * cc);
+                }
+                const int co_first = tc.co0 + c + cb;
+                if (co_first + CPT <= g.Cout) {
+                    if (CPT == 4) {
+                        uint2 pk;
+                        pk.x = pack_bf16x2(yv[0], yv[1]);
+                        pk.y = pack_bf16x2(yv[2 % CPT], yv[3 % CPT]);
+                        *reinterpret_cast<uint2*>(ea.y + po) = pk;
+                        if (ea.idx) *reinterpret_cast<uint32_t*>(ea.idx + po) = codes;
+                    } else {
+                        *reinterpret_cast<uint32_t*>(ea.y + po) = pack_bf16x2(yv[0], yv[1 % CPT]);
+                        if (ea.idx) *reinterpret_cast<uint16_t*>(ea.idx + po) = (uint16_t)codes;
+                    }
+                }
+            }
+            named_bar_sync(1, 128);
+        } else if (valid) {
+            const int64_t o = vox * g.Cout + tc.co0 + c;
+#pragma unroll
+            for (int q8 = 0; q8 < CH / 8; ++q8) {
+                if (tc.co0 + c + q8 * 8 + 8 > g.Cout) break;
+                float v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(r[q8 * 8 + k]);
+                if (EPI == EPI_DGRAD) {
+                    const uint4 xa = *reinterpret_cast<const uint4*>(ea.x_act + o + q8 * 8);
+                    const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float lo = __uint_as_float(xw[k] << 16);
+                        const float hi = __uint_as_float(xw[k] & 0xFFFF0000u);
+                        v[2 * k] *= (lo > 0.f ? 1.f : ea.slope);
+                        v[2 * k + 1] *= (hi > 0.f ? 1.f : ea.slope);
+                    }
+                }
+                uint4 pk;
+                pk.x = pack_bf16x2(v[0], v[1]);
+                pk.y = pack_bf16x2(v[2], v[3]);
+                pk.z = pack_bf16x2(v[4], v[5]);
+                pk.w = pack_bf16x2(v[6], v[7]);
+                *reinterpret_cast<uint4*>(ea.y + o + q8 * 8) = pk;
+            }
+        }
+    }
+}
+
+}  // namespace cf

@@ -1,0 +1,620 @@
+// conv_wgrad.cu -- backward-weight 3x3x3 convolution on the sm_103a tensor
+// cores, split-K over samples x voxels with a fixed-order fp32 reduction.
+//
+// (CosmoFlow page, section III-C "backward weights": the weight-gradient work
+// is divided over voxels.)
+//   dW[co, t, ci] = sum_{n,v} dZ[n,v,co] * X[n, v + t - 1, ci]
+// GEMM view: M = (t, ci) rows (128 per CTA tile), N = co (the whole c_out,
+// <= 256), K = voxels.  Both operands are MN-major in shared memory:
+//   A[(t,ci), v] = X[v + t - 1, ci]  -- TMA box of the tap-shifted activation
+//                  (zero fill outside the volume), channel rows of 32 or 64
+//   B[co, v]     = dZ[v, co]         -- TMA box of the output gradient
+// Each CTA unit = one M block x one contiguous range of 64-voxel boxes; its
+// fp32 accumulator (TMEM) is written to a partial buffer [split][co][27*c_in],
+// and a second kernel sums the splits in a fixed order into dW.
+//
+// The small-channel variant (c_in = 1 or 4) builds the A tile with producer
+// threads (im2col rows = voxels, 27*c_in columns padded to 128) because TMA
+// cannot address 2- or 8-byte channel rows; its K block is the 128-voxel box.
+#include <algorithm>
+
+#include "conv_common.cuh"
+
+namespace cf {
+
+struct WgradGeom {
+    int N, D, H, W, Cin, Cout;
+    int vw, vh, vd;           // voxel box (K block)
+    int nb_w, nb_h, nb_d;     // boxes per dimension
+    int64_t total_boxes;      // N * nb_d * nb_h * nb_w
+    int n_mblocks;            // ceil(27*Cin / 128)
+    int n_splits;
+    int64_t boxes_per_split;
+    int num_units;            // n_mblocks * n_splits
+};
+
+__device__ __forceinline__ void decode_box(const WgradGeom& g, int64_t b, int& n, int& d0, int& h0, int& w0) {
+    int bw = (int)(b % g.nb_w);
+    b /= g.nb_w;
+    int bh = (int)(b % g.nb_h);
+    b /= g.nb_h;
+    int bd = (int)(b % g.nb_d);
+    n = (int)(b / g.nb_d);
+    w0 = bw * g.vw;
+    h0 = bh * g.vh;
+    d0 = bd * g.vd;
+}
+
+// Writes the unit's accumulator rows (t,ci) < 27*Cin into part[split][co][row].
+template <int BN>
+__device__ __forceinline__ void wgrad_store_partial(const WgradGeom& g, float* part, int mb, int split,
+                                                    uint32_t tmem_base, int q, int lane) {
+    const int row = q * 32 + lane;
+    const int mrow = mb * 128 + row;
+    const int KK = 27 * g.Cin;
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+    float* base = part + (int64_t)split * g.Cout * KK + mrow;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+        uint32_t r[32];
+        tmem_ld16(lane_addr + c, r);
+        tmem_ld_wait();
+        if (mrow < KK) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (c + k < g.Cout) base[(int64_t)(c + k) * KK] = __uint_as_float(r[k]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// generic: c_in a multiple of 32
+
+template <int BN, int SUBA, int SUBB>
+struct WgCfg {
+    static constexpr int KV = 64;  // voxels per K block
+    static constexpr uint32_t A_BYTES = 128 * KV * 2;
+    static constexpr uint32_t B_BYTES = BN * KV * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t BAR_BYTES = 256;
+    static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - BAR_BYTES;
+    static constexpr int STAGES_RAW = (int)(BUDGET / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr uint32_t SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr uint32_t A_SUB_BYTES = KV * SUBA * 2;  // one MN atom column (sub-block)
+    static constexpr uint32_t B_SUB_BYTES = KV * SUBB * 2;
+    static constexpr uint32_t SWZ_A = SUBA == 64 ? SWZ_128B : (SUBA == 32 ? SWZ_64B : SWZ_32B);
+    static constexpr uint32_t SWZ_B = SUBB == 64 ? SWZ_128B : (SUBB == 32 ? SWZ_64B : SWZ_32B);
+    static constexpr uint32_t SBO_A = 8 * SUBA * 2;  // 8 K-rows
+    static constexpr uint32_t SBO_B = 8 * SUBB * 2;
+    static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    static constexpr uint32_t IDESC = idesc_bf16(128, BN, 1, 1);
+};
+
+struct WgradParams {
+    WgradGeom g;
+    float* part;
+    int* status;
+    uint64_t wait_ns;
+};
+
+template <int BN, int SUBA, int SUBB>
+__global__ void __launch_bounds__(192, 1)
+    wgrad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
+                 const WgradParams p) {
+    using C = WgCfg<BN, SUBA, SUBB>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* ring = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* tfull = bars + 2 * C::STAGES;
+    uint64_t* tempty = tfull + 1;
+    uint64_t* drain = tempty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    volatile int* epi_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WgradGeom& g = p.g;
+    const int KK = 27 * g.Cin;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmG);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
+                const int mb = u % g.n_mblocks, split = u / g.n_mblocks;
+                const int64_t b0 = (int64_t)split * g.boxes_per_split;
+                const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
+                // A sub-blocks of this M block that hold real rows
+                int nsub = 0;
+                for (int s = 0; s < 128 / SUBA; ++s)
+                    if (mb * 128 + s * SUBA < KK) ++nsub;
+                const uint32_t tx = nsub * C::A_SUB_BYTES + C::B_BYTES;
+                for (int64_t b = b0; b < b1; ++b) {
+                    int n, d0, h0, w0;
+                    decode_box(g, b, n, d0, h0, w0);
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = ring + stage * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], tx);
+                    for (int s = 0; s < nsub; ++s) {
+                        const int r0 = mb * 128 + s * SUBA;
+                        const int t = r0 / g.Cin, ci0 = r0 % g.Cin;
+                        const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
+                        tma_load_5d(sa + s * C::A_SUB_BYTES, &tmX, &full[stage], ci0, w0 + kw - 1, h0 + kh - 1,
+                                    d0 + kd - 1, n);
+                    }
+                    for (int s = 0; s < BN / SUBB; ++s)
+                        tma_load_5d(sa + C::A_BYTES + s * C::B_SUB_BYTES, &tmG, &full[stage], s * SUBB, w0, h0, d0, n);
+                    issued |= 1u << stage;
+                    par = (par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (issued & (1u << s)) mbar_wait_timed(&full[s], (par >> s) & 1, p.wait_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, local = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x, ++local) {
+                const int split = u / g.n_mblocks;
+                const int64_t b0 = (int64_t)split * g.boxes_per_split;
+                const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
+                if (!mbar_wait(tempty, (local & 1) ^ 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                bool first = true;
+                for (int64_t b = b0; b < b1; ++b) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(ring + stage * C::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < C::KV / 16; ++k) {
+                        // 16 K rows further = 2 groups of 8 rows
+                        const uint64_t ad = sdesc(a_addr + k * 16 * SUBA * 2, C::A_SUB_BYTES, C::SBO_A, C::SWZ_A);
+                        const uint64_t bd = sdesc(b_addr + k * 16 * SUBB * 2, C::B_SUB_BYTES, C::SBO_B, C::SWZ_B);
+                        umma_bf16(tmem_base, ad, bd, C::IDESC, first ? 0u : 1u);
+                        first = false;
+                    }
+                    umma_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull);
+            }
+            if (!ok) {
+                umma_commit(drain);
+                mbar_wait_timed(drain, 0, p.wait_ns);
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const int et = threadIdx.x - 64;
+        uint32_t local = 0;
+        for (int u = blockIdx.x; u < g.num_units; u += gridDim.x, ++local) {
+            const int mb = u % g.n_mblocks, split = u / g.n_mblocks;
+            if (!epi_wait(tfull, local & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
+            tc_fence_after();
+            wgrad_store_partial<BN>(g, p.part, mb, split, tmem_base, q, lane);
+            tc_fence_before();
+            mbar_arrive(tempty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// small channel count: c_in in {1, 4}; one M block (27*c_in <= 128 rows);
+// K block = one 128-voxel box (2 x th x tw); A built by 128 producer threads.
+
+template <int CIN>
+__device__ __forceinline__ void build_wg_im2col_row(uint8_t* a_tile, int row, const uint16_t* __restrict__ x,
+                                                    int D, int H, int W, int n, int d, int h, int w) {
+    // row = voxel (K index); 128 M columns (t, ci) in two 64-wide SW128 atoms,
+    // atom a at a * (128 rows * 128 B)
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+        if (CIN == 4) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int t = 2 * c + half;
+                if (t < 27) {
+                    const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
+                    const int id = d + kd - 1, ih = h + kh - 1, iw = w + kw - 1;
+                    if (id >= 0 && id < D && ih >= 0 && ih < H && iw >= 0 && iw < W) {
+                        const uint2 qv = __ldg(reinterpret_cast<const uint2*>(
+                            x + ((((int64_t)n * D + id) * H + ih) * W + iw) * 4));
+                        v[2 * half] = qv.x;
+                        v[2 * half + 1] = qv.y;
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * c + e;
+                uint32_t bits = 0;
+                if (t < 27) {
+                    const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
+                    const int id = d + kd - 1, ih = h + kh - 1, iw = w + kw - 1;
+                    if (id >= 0 && id < D && ih >= 0 && ih < H && iw >= 0 && iw < W)
+                        bits = __ldg(x + ((((int64_t)n * D + id) * H + ih) * W + iw));
+                }
+                v[e >> 1] |= bits << (16 * (e & 1));
+            }
+        }
+        const int atom = c >> 3, cin_atom = c & 7;
+        *reinterpret_cast<uint4*>(a_tile + atom * (128 * 128) + row * 128 + ((cin_atom ^ (row & 7)) << 4)) =
+            make_uint4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+template <int CIN, int BN, int SUBB>
+struct WgSmallCfg {
+    static constexpr uint32_t A_BYTES = 128 * 128 * 2;  // 128 voxels x 128 (t,ci)
+    static constexpr uint32_t B_BYTES = BN * 128 * 2;   // 128 voxels x BN
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t B_SUB_BYTES = 128 * SUBB * 2;
+    static constexpr uint32_t BAR_BYTES = 256;
+    static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - BAR_BYTES;
+    static constexpr int STAGES_RAW = (int)(BUDGET / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_RAW > 4 ? 4 : STAGES_RAW;
+    static constexpr uint32_t SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr uint32_t SWZ_B = SUBB == 64 ? SWZ_128B : (SUBB == 32 ? SWZ_64B : SWZ_32B);
+    static constexpr uint32_t SBO_B = 8 * SUBB * 2;
+    static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    static constexpr uint32_t IDESC = idesc_bf16(128, BN, 1, 1);
+};
+
+struct WgSmallParams {
+    WgradGeom g;  // vw,vh,vd = 128-voxel box
+    const uint16_t* x;
+    float* part;
+    int* status;
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+template <int CIN, int BN, int SUBB>
+__global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_constant__ CUtensorMap tmG,
+                                                              const WgSmallParams p) {
+    using C = WgSmallCfg<CIN, BN, SUBB>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* ring = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* tfull = bars + 2 * C::STAGES;
+    uint64_t* tempty = tfull + 1;
+    uint64_t* drain = tempty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    volatile int* epi_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WgradGeom& g = p.g;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 0) tma_prefetch_desc(&tmG);
+    if (warp == 4) {
+        tmem_alloc(tmem_holder, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp < 4) {
+        const int row = threadIdx.x;  // voxel within the box
+        const int l = row % g.vw, j = (row / g.vw) % g.vh, i = row / (g.vw * g.vh);
+        int stage = 0;
+        uint32_t phase = 0, issued = 0, par = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
+            const int64_t b0 = (int64_t)u * g.boxes_per_split;
+            const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
+            for (int64_t b = b0; b < b1; ++b) {
+                int n, d0, h0, w0;
+                decode_box(g, b, n, d0, h0, w0);
+                if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sa = ring + stage * C::STAGE_BYTES;
+                if (row == 0) {
+                    mbar_expect_tx(&full[stage], C::B_BYTES);
+                    for (int s = 0; s < BN / SUBB; ++s)
+                        tma_load_5d(sa + C::A_BYTES + s * C::B_SUB_BYTES, &tmG, &full[stage], s * SUBB, w0, h0, d0, n);
+                    issued |= 1u << stage;
+                    par = (par & ~(1u << stage)) | (phase << stage);
+                }
+                const int d = d0 + i, h = h0 + j, w = w0 + l;
+                if (d < g.D && h < g.H && w < g.W)
+                    build_wg_im2col_row<CIN>(sa, row, p.x, g.D, g.H, g.W, n, d, h, w);
+                else  // voxel outside the volume: its dZ row is zero-filled, keep A finite
+                    build_wg_im2col_row<CIN>(sa, row, p.x, g.D, g.H, g.W, n, -4, -4, -4);
+                fence_proxy_async_smem();
+                mbar_arrive(&full[stage]);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok && row == 0) {
+            for (int s = 0; s < C::STAGES; ++s)
+                if (issued & (1u << s)) mbar_wait_timed(&full[s], (par >> s) & 1, p.wait_ns);
+        }
+    } else if (warp == 4) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, local = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x, ++local) {
+                const int64_t b0 = (int64_t)u * g.boxes_per_split;
+                const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
+                if (!mbar_wait(tempty, (local & 1) ^ 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                bool first = true;
+                for (int64_t b = b0; b < b1; ++b) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(ring + stage * C::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < 128 / 16; ++k) {
+                        const uint64_t ad = sdesc(a_addr + k * 16 * 128, 128 * 128, 1024, SWZ_128B);
+                        const uint64_t bd = sdesc(b_addr + k * 16 * SUBB * 2, C::B_SUB_BYTES, C::SBO_B, C::SWZ_B);
+                        umma_bf16(tmem_base, ad, bd, C::IDESC, first ? 0u : 1u);
+                        first = false;
+                    }
+                    umma_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull);
+            }
+            if (!ok) {
+                umma_commit(drain);
+                mbar_wait_timed(drain, 0, p.wait_ns);
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const int et = threadIdx.x - 160;
+        uint32_t local = 0;
+        for (int u = blockIdx.x; u < g.num_units; u += gridDim.x, ++local) {
+            if (!epi_wait(tfull, local & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
+            tc_fence_after();
+            wgrad_store_partial<BN>(g, p.part, 0, u, tmem_base, q, lane);
+            tc_fence_before();
+            mbar_arrive(tempty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// dW[i] = (accumulate ? dW[i] : 0) + sum_{s < splits} part[s][i], s ascending.
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw, int64_t count,
+                                     int splits, int accumulate) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
+        float s = accumulate ? dw[i] : 0.f;
+        for (int k = 0; k < splits; ++k) s += part[(int64_t)k * count + i];
+        dw[i] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out) {
+    WgradGeom g;
+    g.N = (int)n;
+    g.D = (int)d;
+    g.H = (int)h;
+    g.W = (int)w;
+    g.Cin = c_in;
+    g.Cout = c_out;
+    const bool small = c_in == 1 || c_in == 4;
+    if (small) {
+        TileGeom t = choose_tile(d, h, w);
+        g.vw = t.tw;
+        g.vh = t.th;
+        g.vd = t.td;
+        g.n_mblocks = 1;
+    } else {
+        g.vw = w >= 64 ? 64 : (w >= 32 ? 32 : (w >= 16 ? 16 : 8));
+        g.vh = 64 / g.vw;
+        g.vd = 1;
+        g.n_mblocks = (27 * c_in + 127) / 128;
+    }
+    g.nb_w = (int)((w + g.vw - 1) / g.vw);
+    g.nb_h = (int)((h + g.vh - 1) / g.vh);
+    g.nb_d = (int)((d + g.vd - 1) / g.vd);
+    g.total_boxes = n * g.nb_d * g.nb_h * g.nb_w;
+    // about two units per SM, each unit at least 8 boxes long
+    int64_t target = std::max<int64_t>(1, (2 * (int64_t)num_sms + g.n_mblocks - 1) / g.n_mblocks);
+    target = std::min<int64_t>(target, std::max<int64_t>(1, g.total_boxes / 8));
+    g.boxes_per_split = (g.total_boxes + target - 1) / target;
+    g.n_splits = (int)((g.total_boxes + g.boxes_per_split - 1) / g.boxes_per_split);
+    g.num_units = g.n_mblocks * g.n_splits;
+    return g;
+}
+
+size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out) {
+    WgradGeom g = wgrad_geom(num_sms, n, d, h, w, c_in, c_out);
+    return (size_t)g.n_splits * c_out * 27 * c_in * sizeof(float);
+}
+
+template <typename K>
+static int wg_grid(K kernel, uint32_t smem, int threads, int num_sms, int units, uint32_t tmem_cols) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    per_sm = std::min<int>(per_sm, (int)(512 / tmem_cols));
+    return std::max(1, std::min(units, num_sms * per_sm));
+}
+
+static bool make_act_map(CUtensorMap* m, const uint16_t* base, const WgradGeom& g, int c, int box_c) {
+    const uint64_t dims[5] = {(uint64_t)c, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.D, (uint64_t)g.N};
+    const uint64_t str[4] = {(uint64_t)c * 2, (uint64_t)g.W * c * 2, (uint64_t)g.H * g.W * c * 2,
+                             (uint64_t)g.D * g.H * g.W * c * 2};
+    const uint32_t box[5] = {(uint32_t)box_c, (uint32_t)g.vw, (uint32_t)g.vh, (uint32_t)g.vd, 1u};
+    const CUtensorMapSwizzle swz = box_c == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : box_c == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                 : CU_TENSOR_MAP_SWIZZLE_32B;
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, str, box, swz);
+}
+
+template <int BN, int SUBA, int SUBB>
+static cf_status run_wgrad(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
+                           float* part) {
+    using C = WgCfg<BN, SUBA, SUBB>;
+    CUtensorMap tx, tg;
+    if (!make_act_map(&tx, x, g, g.Cin, SUBA)) return CF_ERR_CUDA;
+    if (!make_act_map(&tg, dz, g, g.Cout, SUBB)) return CF_ERR_CUDA;
+    WgradParams p{g, part, ctx.status, ctx.wait_ns};
+    auto kern = wgrad_kernel<BN, SUBA, SUBB>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+        return CF_ERR_CUDA;
+    const int grid = wg_grid(kern, C::SMEM, 192, ctx.num_sms, g.num_units, C::TMEM_COLS);
+    kern<<<grid, 192, C::SMEM, ctx.stream>>>(tx, tg, p);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+template <int CIN, int BN, int SUBB>
+static cf_status run_wgrad_small(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
+                                 float* part) {
+    using C = WgSmallCfg<CIN, BN, SUBB>;
+    CUtensorMap tg;
+    if (!make_act_map(&tg, dz, g, g.Cout, SUBB)) return CF_ERR_CUDA;
+    WgSmallParams p{g, x, part, ctx.status, ctx.wait_ns};
+    auto kern = wgrad_smallc_kernel<CIN, BN, SUBB>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+        return CF_ERR_CUDA;
+    const int grid = wg_grid(kern, C::SMEM, 288, ctx.num_sms, g.num_units, C::TMEM_COLS);
+    kern<<<grid, 288, C::SMEM, ctx.stream>>>(tg, p);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+template <int BN>
+static cf_status wgrad_bn(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
+                          float* part) {
+    constexpr int SUBB = BN >= 64 ? 64 : BN;
+    if (g.Cin == 4) return run_wgrad_small<4, BN, SUBB>(ctx, g, x, dz, part);
+    if (g.Cin == 1) return run_wgrad_small<1, BN, SUBB>(ctx, g, x, dz, part);
+    if (g.Cin % 64 == 0) return run_wgrad<BN, 64, SUBB>(ctx, g, x, dz, part);
+    return run_wgrad<BN, 32, SUBB>(ctx, g, x, dz, part);
+}
+
+cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
+                       const uint16_t* x, const uint16_t* dz, float* dw, int accumulate, void* ws, size_t ws_bytes) {
+    if (!(c_in == 1 || c_in == 4 || c_in % 32 == 0)) return CF_ERR_UNSUPPORTED;
+    if (!(c_out == 16 || c_out == 32 || c_out % 64 == 0) || c_out > 256) return CF_ERR_UNSUPPORTED;
+    WgradGeom g = wgrad_geom(ctx.num_sms, n, d, h, w, c_in, c_out);
+    const size_t need = (size_t)g.n_splits * c_out * 27 * c_in * sizeof(float);
+    if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
+    float* part = static_cast<float*>(ws);
+    cf_status st;
+    switch (c_out) {
+        case 16: st = wgrad_bn<16>(ctx, g, x, dz, part); break;
+        case 32: st = wgrad_bn<32>(ctx, g, x, dz, part); break;
+        case 64: st = wgrad_bn<64>(ctx, g, x, dz, part); break;
+        case 128: st = wgrad_bn<128>(ctx, g, x, dz, part); break;
+        case 192: st = wgrad_bn<192>(ctx, g, x, dz, part); break;
+        case 256: st = wgrad_bn<256>(ctx, g, x, dz, part); break;
+        default: return CF_ERR_UNSUPPORTED;
+    }
+    if (st != CF_OK) return st;
+    const int64_t count = (int64_t)c_out * 27 * c_in;
+    const int threads = 256;
+    const int blocks = (int)std::min<int64_t>((count + threads - 1) / threads, 4 * (int64_t)ctx.num_sms);
+    splitk_reduce_kernel<<<blocks, threads, 0, ctx.stream>>>(part, dw, count, g.n_splits, accumulate);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+}  // namespace cf

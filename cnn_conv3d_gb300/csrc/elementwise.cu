@@ -1,0 +1,236 @@
+// elementwise.cu -- the HBM-bound pieces of the block: standalone bias +
+// leaky ReLU + 2x2x2 max-pool (forward), its argmax-routed backward with the
+// bias gradient, the filter flip/transpose that turns backward-data into a
+// forward convolution, and the wait-timeout probe.
+//
+// Pooling (CosmoFlow page, section III-C: pooling works per channel over
+// KS^3 windows; hybrid-parallelism page, Table I: stride-2 pooling) is the
+// max over each 2x2x2 window; the code of the first maximum in (dd,dh,dw)
+// order (dd*4+dh*2+dw) is kept for the backward pass.
+#include <algorithm>
+
+#include "cf_internal.h"
+#include "cf_ptx.cuh"
+
+namespace cf {
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        f[2 * k] = __uint_as_float(w[k] << 16);
+        f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 v;
+    v.x = pack_bf16x2(f[0], f[1]);
+    v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]);
+    v.w = pack_bf16x2(f[6], f[7]);
+    return v;
+}
+
+// one thread = one pooled voxel x 8 channels
+__global__ void pool_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ bias, float slope,
+                                uint16_t* __restrict__ y, uint8_t* __restrict__ idx, int64_t N, int D, int H, int W,
+                                int C) {
+    const int C8 = C / 8, D2 = D / 2, H2 = H / 2, W2 = W / 2;
+    const int64_t total = N * D2 * H2 * W2 * C8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(i % C8);
+        int64_t pvox = i / C8;
+        const int pw = (int)(pvox % W2);
+        int64_t r = pvox / W2;
+        const int ph = (int)(r % H2);
+        r /= H2;
+        const int pd = (int)(r % D2);
+        const int64_t n = r / D2;
+        float m[8];
+        uint32_t code[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+            const int64_t o = ((((n * D + 2 * pd + dd) * H + 2 * ph + dh) * W) + 2 * pw + dw) * C + 8 * c8;
+            float f[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(z + o)), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                if (k == 0 || f[c] > m[c]) {
+                    m[c] = f[c];
+                    code[c] = k;
+                }
+            }
+        }
+        float out[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float s = m[c] + (bias ? bias[8 * c8 + c] : 0.f);
+            out[c] = s > 0.f ? s : slope * s;
+        }
+        const int64_t po = pvox * C + 8 * c8;
+        *reinterpret_cast<uint4*>(y + po) = pack8(out);
+        if (idx) {
+            uint2 cv;
+            cv.x = code[0] | (code[1] << 8) | (code[2] << 16) | (code[3] << 24);
+            cv.y = code[4] | (code[5] << 8) | (code[6] << 16) | (code[7] << 24);
+            *reinterpret_cast<uint2*>(idx + po) = cv;
+        }
+    }
+}
+
+// one thread = one pooled voxel x 8 channels; the thread's channel group is
+// fixed (blockDim and the grid stride are multiples of C/8) so it can keep
+// the bias-gradient partial sums in registers.  partial[block][C] receives the
+// per-block sums, added in ascending thread order.
+__global__ void pool_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ y,
+                                const uint8_t* __restrict__ idx, float slope, uint16_t* __restrict__ dz,
+                                uint16_t* __restrict__ dy_pre, float* __restrict__ partial, int64_t N, int D, int H,
+                                int W, int C) {
+    extern __shared__ float red[];  // [blockDim][8]
+    const int C8 = C / 8, D2 = D / 2, H2 = H / 2, W2 = W / 2;
+    const int64_t total = N * D2 * H2 * W2 * C8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(i % C8);
+        const int64_t pvox = i / C8;
+        const int64_t po = pvox * C + 8 * c8;
+        float g[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dy + po)), g);
+        if (y) {
+            float yy[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(y + po)), yy);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) g[c] *= (yy[c] > 0.f ? 1.f : slope);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] += g[c];
+        // dy_pre and dz store g rounded to bf16
+        const uint4 gp = pack8(g);
+        unpack8(gp, g);
+        if (dy_pre) *reinterpret_cast<uint4*>(dy_pre + po) = gp;
+        if (dz) {
+            const uint2 cv = __ldg(reinterpret_cast<const uint2*>(idx + po));
+            const uint32_t codes[2] = {cv.x, cv.y};
+            const int pw = (int)(pvox % W2);
+            int64_t r = pvox / W2;
+            const int ph = (int)(r % H2);
+            r /= H2;
+            const int pd = (int)(r % D2);
+            const int64_t n = r / D2;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+                float o[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) o[c] = ((codes[c >> 2] >> (8 * (c & 3))) & 0xFF) == (uint32_t)k ? g[c] : 0.f;
+                const int64_t zo = ((((n * D + 2 * pd + dd) * H + 2 * ph + dh) * W) + 2 * pw + dw) * C + 8 * c8;
+                *reinterpret_cast<uint4*>(dz + zo) = pack8(o);
+            }
+        }
+    }
+    if (partial) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) red[threadIdx.x * 8 + c] = acc[c];
+        __syncthreads();
+        for (int ch = threadIdx.x; ch < C; ch += blockDim.x) {
+            const int c8 = ch / 8, c = ch % 8;
+            float s = 0.f;
+            for (int t = c8; t < (int)blockDim.x; t += C8) s += red[t * 8 + c];
+            partial[(int64_t)blockIdx.x * C + ch] = s;
+        }
+    }
+}
+
+__global__ void colsum_kernel(const float* __restrict__ partial, int rows, int C, float* __restrict__ out) {
+    for (int ch = blockIdx.x * blockDim.x + threadIdx.x; ch < C; ch += gridDim.x * blockDim.x) {
+        float s = 0.f;
+        for (int r = 0; r < rows; ++r) s += partial[(int64_t)r * C + ch];
+        out[ch] = s;
+    }
+}
+
+// W'[ci][t'][co] = W[co][26 - t'][ci]: the filter of the backward-data
+// convolution written as a forward convolution.
+__global__ void flip_transpose_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ wt, int Cout, int Cin) {
+    const int64_t total = (int64_t)Cout * 27 * Cin;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int co = (int)(i % Cout);
+        const int64_t r = i / Cout;
+        const int tp = (int)(r % 27);
+        const int ci = (int)(r / 27);
+        wt[i] = w[((int64_t)co * 27 + (26 - tp)) * Cin + ci];
+    }
+}
+
+__global__ void timeout_probe_kernel(int* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, limit_ns, status, WAIT_PROBE);
+}
+
+// ---------------------------------------------------------------------------
+
+static int pool_bwd_block(int c) {
+    const int c8 = c / 8;
+    return (256 / c8) * c8;
+}
+static int pool_bwd_grid(int num_sms) { return 4 * num_sms; }
+
+size_t pool_bwd_workspace_bytes(int num_sms, int c) {
+    return (size_t)pool_bwd_grid(num_sms) * c * sizeof(float);
+}
+
+cf_status launch_pool_fwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                          const uint16_t* z, const float* bias, float slope, uint16_t* y, uint8_t* idx) {
+    const int64_t total = n * (d / 2) * (h / 2) * (w / 2) * (c / 8);
+    const int threads = 256;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads, 16LL * ctx.num_sms));
+    pool_fwd_kernel<<<blocks, threads, 0, ctx.stream>>>(z, bias, slope, y, idx, n, (int)d, (int)h, (int)w, c);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                          const uint16_t* dy, const uint16_t* y, const uint8_t* idx, float slope, uint16_t* dz,
+                          uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes) {
+    if (c / 8 > 256) return CF_ERR_UNSUPPORTED;
+    const int threads = pool_bwd_block(c);
+    const int blocks = pool_bwd_grid(ctx.num_sms);
+    float* partial = nullptr;
+    if (dbias) {
+        if (ws == nullptr || ws_bytes < pool_bwd_workspace_bytes(ctx.num_sms, c)) return CF_ERR_WORKSPACE;
+        partial = static_cast<float*>(ws);
+    }
+    pool_bwd_kernel<<<blocks, threads, threads * 8 * sizeof(float), ctx.stream>>>(
+        dy, y, idx, slope, dz, dy_pre, partial, n, (int)d, (int)h, (int)w, c);
+    if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+    if (dbias) {
+        colsum_kernel<<<(c + 127) / 128, 128, 0, ctx.stream>>>(partial, blocks, c, dbias);
+        if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+    }
+    return CF_OK;
+}
+
+cf_status launch_flip_transpose(const LaunchCtx& ctx, int c_out, int c_in, const uint16_t* w, uint16_t* wt) {
+    const int64_t total = (int64_t)c_out * 27 * c_in;
+    const int threads = 256;
+    const int blocks = (int)std::min<int64_t>((total + threads - 1) / threads, 8LL * ctx.num_sms);
+    flip_transpose_kernel<<<blocks, threads, 0, ctx.stream>>>(w, wt, c_out, c_in);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+cf_status launch_timeout_probe(const LaunchCtx& ctx) {
+    timeout_probe_kernel<<<1, 32, 0, ctx.stream>>>(ctx.status, ctx.wait_ns);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+}  // namespace cf

@@ -1,0 +1,118 @@
+"""The CosmoFlow-shaped block stack on one GPU, sequenced through the C ABI.
+
+A block is conv3d k=3 pad 1 -> + bias -> leaky ReLU -> 2x2x2 max-pool; the
+stack chains L blocks, each halving the spatial width (CosmoFlow page,
+section III-A; hybrid-parallelism page, Table I).  This class only owns the
+device buffers (torch allocations) and enqueues the library's entry points on
+one stream; every arithmetic step runs in libcfconv3d's kernels.
+
+One training step of the stack (forward + backward):
+  forward : for each block l  cf_conv3d_fwd(x_l, W_l, epi=(b_l, slope, I_l)) -> y_l
+  backward: block L-1: cf_bias_lrelu_pool_bwd(dY, y, I) -> dZ, db
+            block l < L-1: cf_bias_lrelu_pool_bwd(g_l, None, I_l) -> dZ_l, db_l
+            cf_conv3d_wgrad(x_l, dZ_l) -> dW_l
+            l > 0: cf_conv3d_dgrad(dZ_l, W_l, x_act = x_l) -> g_{l-1}
+            (g_{l-1} already carries the leaky-ReLU derivative of block l-1;
+            the first block's input gradient has no consumer and is skipped)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import cfconv as cf
+
+
+class CosmoStack:
+    def __init__(self, n: int, spatial: int, channels, slope: float = 0.3, device: str = "cuda",
+                 backward: bool = True):
+        self.n, self.spatial, self.channels, self.slope = n, spatial, tuple(channels), float(slope)
+        self.L = len(channels) - 1
+        self.device = device
+        bf, u8, f32 = torch.bfloat16, torch.uint8, torch.float32
+        s = spatial
+        self.dims = []  # (n, d, h, w) of each block's conv input/output
+        self.x = torch.empty((n, s, s, s, channels[0]), dtype=bf, device=device)
+        self.w, self.b, self.y, self.idx = [], [], [], []
+        for l in range(self.L):
+            ci, co = channels[l], channels[l + 1]
+            self.dims.append((n, s, s, s))
+            self.w.append(torch.empty((co, 3, 3, 3, ci), dtype=bf, device=device))
+            self.b.append(torch.zeros((co,), dtype=f32, device=device))
+            self.y.append(torch.empty((n, s // 2, s // 2, s // 2, co), dtype=bf, device=device))
+            self.idx.append(torch.empty((n, s // 2, s // 2, s // 2, co), dtype=u8, device=device))
+            s //= 2
+        self.backward_enabled = backward
+        ws = 0
+        if backward:
+            self.dz, self.dw, self.db, self.g = [], [], [], []
+            for l in range(self.L):
+                n_, d, h, w = self.dims[l]
+                co = channels[l + 1]
+                self.dz.append(torch.empty((n_, d, h, w, co), dtype=bf, device=device))
+                self.dw.append(torch.empty((co, 3, 3, 3, channels[l]), dtype=f32, device=device))
+                self.db.append(torch.empty((co,), dtype=f32, device=device))
+                # g[l]: gradient w.r.t. block l's pooled pre-activation (dgrad output of block l+1)
+                self.g.append(torch.empty((n_, d // 2, h // 2, w // 2, co), dtype=bf, device=device)
+                              if l < self.L - 1 else None)
+            for l in range(self.L):
+                desc = self.desc(l)
+                ws = max(ws, cf.cf_workspace_size(cf.CF_OP_WGRAD, desc))
+                ws = max(ws, cf.cf_workspace_size(cf.CF_OP_POOL_BWD, desc))
+                if l > 0:
+                    ws = max(ws, cf.cf_workspace_size(cf.CF_OP_DGRAD, desc))
+        self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=device)
+
+    def desc(self, l):
+        n, d, h, w = self.dims[l]
+        return cf.cf_conv_desc(n, d, h, w, self.channels[l], self.channels[l + 1])
+
+    def block_input(self, l):
+        return self.x if l == 0 else self.y[l - 1]
+
+    def load(self, x_u16, ws_u16, bs_f32):
+        """Copies host inputs (numpy bf16 bit patterns / fp32) into the device buffers."""
+        import numpy as np
+
+        def up(dst, a):
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+            dst.copy_(t.reshape(dst.shape))
+        up(self.x, x_u16)
+        for l in range(self.L):
+            up(self.w[l], ws_u16[l])
+            self.b[l].copy_(torch.from_numpy(np.ascontiguousarray(bs_f32[l], dtype=np.float32)))
+
+    def forward(self, stream=None):
+        for l in range(self.L):
+            cf.cf_conv3d_fwd(self.desc(l), self.block_input(l), self.w[l], (self.b[l], self.slope, self.idx[l]),
+                             self.y[l], None, 0, stream)
+
+    def backward(self, dy, stream=None):
+        ws, wsb = self.ws, self.ws.numel()
+        for l in range(self.L - 1, -1, -1):
+            n, d, h, w = self.dims[l]
+            co = self.channels[l + 1]
+            if l == self.L - 1:
+                cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope, self.dz[l],
+                                          None, self.db[l], ws, wsb, stream)
+            else:
+                cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope, self.dz[l],
+                                          None, self.db[l], ws, wsb, stream)
+            desc = self.desc(l)
+            cf.cf_conv3d_wgrad(desc, self.block_input(l), self.dz[l], None, self.dw[l], 0, ws, wsb, stream)
+            if l > 0:
+                cf.cf_conv3d_dgrad(desc, self.dz[l], None, self.w[l], self.block_input(l), self.slope,
+                                   self.g[l - 1], ws, wsb, stream)
+
+    def step(self, dy, stream=None):
+        self.forward(stream)
+        if self.backward_enabled:
+            self.backward(dy, stream)
+
+    def launches_per_step(self) -> int:
+        """Kernels one step enqueues: fwd 1 per block; pool-bwd 2 (scatter +
+        bias sum), wgrad 2 (split-K + reduce) per block; dgrad 2 (filter
+        flip + conv) for blocks 1..L-1."""
+        n = self.L
+        if self.backward_enabled:
+            n += 2 * self.L + 2 * self.L + 2 * (self.L - 1)
+        return n

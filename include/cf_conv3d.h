@@ -1,0 +1,170 @@
+/*
+ * cf_conv3d.h -- C ABI of libcfconv3d.so, the GB300 (sm_103a) conv3d block of
+ * a CosmoFlow-style volumetric CNN.
+ *
+ * What is computed (sources: "CosmoFlow: Using Deep Learning to Learn the
+ * Universe at Scale", section III-A (3D conv layers followed by leaky ReLU and
+ * pooling) and III-C (forward data, backward data, backward weight operators);
+ * "The Case for Strong Scaling in Deep Learning: Training Large 3D CNNs with
+ * Hybrid Parallelism", section IV, Table I (3^3 filters, stride-1 "same"
+ * convolution, stride-2 pooling)):
+ *
+ *   Z[n,d,h,w,co] = sum_{kd,kh,kw,ci} W[co,kd,kh,kw,ci] * X[n,d+kd-1,h+kh-1,w+kw-1,ci]
+ *                   (cross-correlation, zero padding 1, stride 1)
+ *   m   = max of Z over each 2x2x2 window (stride 2), I = its code dd*4+dh*2+dw
+ *         (first maximum in that order), taken on the fp32 accumulator
+ *   Y   = LReLU(m + b[co]),  LReLU(s) = s > 0 ? s : slope*s
+ *
+ * Conventions for every entry point:
+ *  - tensors are device pointers the caller owns; the library never allocates
+ *    or frees device memory and never synchronises the stream (except
+ *    cf_last_device_status, which says so);
+ *  - activations are NDHWC, bf16 stored as uint16_t bit patterns;
+ *    filters are [C_out][3][3][3][C_in] bf16; biases and weight gradients fp32;
+ *    argmax codes uint8 in the pooled NDHWC shape;
+ *  - every pointer must be 16-byte aligned;
+ *  - work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream);
+ *  - argument or precondition errors return before anything is launched;
+ *    a kernel that gives up on a bounded wait records CF_ERR_TIMEOUT in a
+ *    device status word read by cf_last_device_status;
+ *  - sizes use 64-bit arithmetic throughout (tensors may exceed 2^31 elements).
+ */
+#ifndef CF_CONV3D_H
+#define CF_CONV3D_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CF_OK = 0,
+    CF_ERR_INVALID_ARG = 1,  /* NULL where a tensor is required, bad sizes, misaligned pointer */
+    CF_ERR_UNSUPPORTED = 2,  /* valid request outside the shapes the kernels implement */
+    CF_ERR_WORKSPACE = 3,    /* ws_bytes smaller than cf_workspace_size() */
+    CF_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, tensor map) */
+    CF_ERR_TIMEOUT = 5       /* a kernel abandoned a bounded wait (device status word) */
+} cf_status;
+
+/* Geometry of one k=3, stride-1, pad-1 convolution: input and conv output
+ * share n,d,h,w. */
+typedef struct {
+    int64_t n, d, h, w;
+    int32_t c_in, c_out;
+} cf_conv_desc;
+
+/* Fused epilogue of the forward conv. */
+typedef struct {
+    const float* bias; /* [c_out] fp32 device, or NULL for zero bias */
+    float slope;       /* leaky-ReLU negative slope (0.3 in the CosmoFlow block) */
+    uint8_t* argmax;   /* [n][d/2][h/2][w/2][c_out] device, or NULL (inference) */
+} cf_pool_epi;
+
+/* Operation ids for cf_workspace_size. */
+enum { CF_OP_FWD = 0, CF_OP_DGRAD = 1, CF_OP_WGRAD = 2, CF_OP_DGRAD_ROUTED = 3,
+       CF_OP_WGRAD_ROUTED = 4, CF_OP_POOL_BWD = 5 };
+
+/*
+ * Forward convolution (CosmoFlow page, section III-A/III-C "forward data";
+ * hybrid-parallelism page, Table I: 3^3 filters, "same" padding).
+ *   x  : [n][d][h][w][c_in] bf16
+ *   w  : [c_out][3][3][3][c_in] bf16
+ *   epi: NULL -> y is the plain conv output Z rounded to bf16, [n][d][h][w][c_out];
+ *        else y is the pooled block output Y, [n][d/2][h/2][w/2][c_out], and
+ *        epi->argmax (if not NULL) receives the window codes.
+ *   ws : unused (pass NULL, 0).
+ * Supported: c_in in {1, 4} or a multiple of 32; c_out a multiple of 16 and
+ * <= 256 per kernel tile (multiples of 256 above that), or c_out a multiple of 8
+ * when c_in is 1 or 4; d, h, w even when pooling.
+ */
+cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* w,
+                        const cf_pool_epi* epi, uint16_t* y, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * Backward data (CosmoFlow page, section III-C "backward data"):
+ *   dX[n,u,ci] = sum_{t,co} W[co,t,ci] * dZ[n, u-(t-1), co]   (dZ = 0 outside)
+ * then, if x_act is not NULL, dX *= (x_act > 0 ? 1 : slope): the leaky-ReLU
+ * derivative of the previous block, whose pooled output x_act is this conv's
+ * input.  The result is stored bf16 in dx [n][d][h][w][c_in].
+ *   dz : idx == NULL -> dense dZ [n][d][h][w][c_out] bf16;
+ *        idx != NULL -> dz is the pooled pre-activation gradient
+ *        [n][d/2][h/2][w/2][c_out] and dZ is its argmax-routed expansion
+ *        (written to the workspace first; needs cf_workspace_size(CF_OP_DGRAD_ROUTED)).
+ *   w  : the forward filter [c_out][3][3][3][c_in] (flipped and transposed
+ *        internally into the workspace).
+ * Supported: c_out a multiple of 32, c_in a multiple of 16.
+ */
+cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx,
+                          const uint16_t* w, const uint16_t* x_act, float slope, uint16_t* dx,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward weight (CosmoFlow page, section III-C "backward weights", work
+ * split over voxels):
+ *   dW[co,t,ci] = sum_{n,v} dZ[n,v,co] * X[n, v+(t-1), ci]   (X zero-padded)
+ * accumulated in fp32 (split-K over n*d*h*w with a fixed-order reduction).
+ *   dz/idx : as in cf_conv3d_dgrad.
+ *   dw : [c_out][3][3][3][c_in] fp32; accumulate != 0 adds to it, else overwrites.
+ * Supported: c_in in {1, 4} or a multiple of 32; c_out a multiple of 16, <= 256.
+ */
+cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* dz,
+                          const uint8_t* idx, float* dw, int accumulate, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/*
+ * Standalone bias + leaky ReLU + 2x2x2 max-pool (the fused epilogue of
+ * cf_conv3d_fwd as its own HBM-bound kernel).
+ *   z   : [n][d][h][w][c] bf16 pre-activation; bias [c] fp32 or NULL
+ *   y   : [n][d/2][h/2][w/2][c] bf16;  idx: same shape uint8, or NULL
+ * The argmax is taken on the bf16 values of z.  Supported: c a multiple of 8,
+ * d, h, w even.
+ */
+cf_status cf_bias_lrelu_pool_fwd(int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                                 const uint16_t* z, const float* bias, float slope, uint16_t* y,
+                                 uint8_t* idx, void* stream);
+
+/*
+ * Pool/LReLU backward.  With g = dy * (y > 0 ? 1 : slope)  (or g = dy when
+ * y is NULL, i.e. dy is already the pre-activation gradient):
+ *   dz     : [n][d][h][w][c] bf16, g at each window's argmax voxel, 0 at the
+ *            other seven; may be NULL
+ *   dy_pre : g, pooled shape, bf16; may be NULL
+ *   dbias  : [c] fp32, sum of g over n and pooled voxels (fixed-order
+ *            reduction through the workspace, cf_workspace_size(CF_OP_POOL_BWD));
+ *            may be NULL
+ * n,d,h,w are the full-resolution sizes.  Supported: c a multiple of 8.
+ */
+cf_status cf_bias_lrelu_pool_bwd(int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                                 const uint16_t* dy, const uint16_t* y, const uint8_t* idx,
+                                 float slope, uint16_t* dz, uint16_t* dy_pre, float* dbias,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes the operation `op` (CF_OP_*) needs for `desc` (for
+ * CF_OP_POOL_BWD desc->c_out is the channel count).  0 if none. */
+size_t cf_workspace_size(int op, const cf_conv_desc* desc);
+
+/* Static description of a status code. */
+const char* cf_status_string(cf_status s);
+
+/* Synchronises `stream`, then reads and clears the device status word that
+ * kernels set when they abandon a bounded wait.  Returns CF_OK or
+ * CF_ERR_TIMEOUT (or CF_ERR_CUDA if the synchronisation itself failed). */
+cf_status cf_last_device_status(void* stream);
+
+/* Sets the limit, in nanoseconds, after which a kernel abandons a wait on an
+ * on-chip barrier (default 2e9).  Affects launches issued afterwards. */
+cf_status cf_set_wait_limit_ns(uint64_t ns);
+
+/* Launches a one-CTA kernel that waits on a barrier nothing will ever signal,
+ * under the current wait limit; it must come back with the device status word
+ * set to CF_ERR_TIMEOUT.  Exercises the timeout path without a GPU fault. */
+cf_status cf_debug_wait_timeout_probe(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CF_CONV3D_H */

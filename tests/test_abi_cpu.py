@@ -1,0 +1,56 @@
+"""The C-ABI library builds, loads and exports every symbol its header
+declares; argument errors come back as status codes (no GPU needed)."""
+import ctypes
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def cf():
+    from cnn_conv3d_gb300 import build
+    build.build()
+    from cnn_conv3d_gb300 import cfconv
+    return cfconv
+
+
+def test_exports_every_header_symbol(cf):
+    names = cf.header_symbols()
+    expected = {"cf_conv3d_fwd", "cf_conv3d_dgrad", "cf_conv3d_wgrad", "cf_bias_lrelu_pool_fwd",
+                "cf_bias_lrelu_pool_bwd", "cf_workspace_size", "cf_status_string", "cf_last_device_status",
+                "cf_set_wait_limit_ns", "cf_debug_wait_timeout_probe"}
+    assert expected <= set(names)
+    lib = ctypes.CDLL(cf.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(cf):
+    assert cf.cf_status_string(cf.CF_OK) == "ok"
+    assert "workspace" in cf.cf_status_string(cf.CF_ERR_WORKSPACE)
+    assert cf.cf_status_string(99) == "unknown status"
+
+
+def test_argument_errors_before_any_launch(cf):
+    d = cf.cf_conv_desc(1, 4, 4, 4, 32, 64)
+    assert cf.cf_conv3d_fwd(d, None, None, None, None, check=False) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_conv3d_fwd(cf.cf_conv_desc(0, 4, 4, 4, 32, 64), 16, 16, None, 16,
+                            check=False) == cf.CF_ERR_INVALID_ARG
+    # misaligned pointers are rejected before anything touches the device
+    assert cf.cf_conv3d_fwd(d, 18, 32, None, 64, check=False) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_conv3d_dgrad(d, None, None, None, None, 0.3, None, check=False) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_conv3d_wgrad(d, None, None, None, None, check=False) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_bias_lrelu_pool_fwd(1, 4, 4, 4, 8, None, None, 0.3, None, None,
+                                     check=False) == cf.CF_ERR_INVALID_ARG
+    # dz requested without argmax codes
+    assert cf.cf_bias_lrelu_pool_bwd(1, 4, 4, 4, 8, 16, None, None, 0.3, 32, None, None,
+                                     check=False) == cf.CF_ERR_INVALID_ARG
+    with pytest.raises(cf.CfError):
+        cf.cf_set_wait_limit_ns(0)
+
+
+def test_unsupported_shapes(cf):
+    # odd spatial size with pooling, and c_in not in {1, 4} or a multiple of 32
+    assert cf.cf_bias_lrelu_pool_fwd(1, 3, 4, 4, 8, 16, None, 0.3, 32, None,
+                                     check=False) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_bias_lrelu_pool_fwd(1, 4, 4, 4, 12, 16, None, 0.3, 32, None,
+                                     check=False) == cf.CF_ERR_UNSUPPORTED

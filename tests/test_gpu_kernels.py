@@ -1,0 +1,308 @@
+"""GPU parity of every entry point against the fp64 oracle on the same seeded
+bf16 inputs, at sizes that span several tiles and a ragged tail.  Calls go
+through the C ABI (ctypes binding)."""
+import numpy as np
+import pytest
+
+import synthdata
+from tests.gpu_util import assert_close, dev, dev_bf16, empty_bf16, host_bf16_f64
+
+pytestmark = pytest.mark.gpu
+
+SLOPE = 0.3
+
+
+@pytest.fixture(scope="module")
+def cf():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from cnn_conv3d_gb300 import build
+    build.build()
+    from cnn_conv3d_gb300 import cfconv
+    return cfconv
+
+
+def _f64(o, u16):
+    return o.bf16_bits_to_f64(u16)
+
+
+def _ws(cf, op, desc):
+    import torch
+    n = max(cf.cf_workspace_size(op, desc), 256)
+    return torch.empty((n,), dtype=torch.uint8, device="cuda"), n
+
+
+def test_library_loaded_and_symbols(cf):
+    import ctypes
+    for name in cf.header_symbols():
+        assert hasattr(cf._lib, name), name
+    assert isinstance(cf._lib, ctypes.CDLL)
+
+
+def test_wait_timeout_probe_reports_status(cf):
+    import torch
+    assert cf.cf_last_device_status() == cf.CF_OK
+    cf.cf_set_wait_limit_ns(20_000_000)  # 20 ms
+    try:
+        cf.cf_debug_wait_timeout_probe()
+        assert cf.cf_last_device_status() == cf.CF_ERR_TIMEOUT
+        # the status word is cleared by the read and the context stays usable
+        assert cf.cf_last_device_status() == cf.CF_OK
+        t = torch.ones(16, device="cuda")
+        assert float(t.sum()) == 16.0
+    finally:
+        cf.cf_set_wait_limit_ns(2_000_000_000)
+
+
+def test_invalid_arguments_return_codes(cf):
+    desc = cf.cf_conv_desc(1, 4, 4, 4, 32, 64)
+    assert cf.cf_conv3d_fwd(desc, None, None, None, None, check=False) == cf.CF_ERR_INVALID_ARG
+    import torch
+    x = torch.empty(1 * 4 * 4 * 4 * 48, dtype=torch.bfloat16, device="cuda")
+    w = torch.empty(64 * 27 * 48, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(4 * 4 * 4 * 64, dtype=torch.bfloat16, device="cuda")
+    bad = cf.cf_conv_desc(1, 4, 4, 4, 48, 64)  # c_in 48: not a multiple of 32
+    assert cf.cf_conv3d_fwd(bad, x, w, None, y, check=False) == cf.CF_ERR_UNSUPPORTED
+    # misaligned pointer
+    assert cf.cf_conv3d_fwd(desc, x.data_ptr() + 2, w, None, y, check=False) == cf.CF_ERR_INVALID_ARG
+    # workspace too small
+    dz = torch.empty(4 * 4 * 4 * 64, dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty(64 * 27 * 32, dtype=torch.float32, device="cuda")
+    assert cf.cf_conv3d_wgrad(desc, x, dz, None, dw, 0, None, 0, check=False) == cf.CF_ERR_WORKSPACE
+
+
+# ----------------------------------------------------------------------------- pooling
+
+def test_pool_fwd_standalone(cf, oracle_mod):
+    rng = np.random.default_rng(5)
+    N, D, H, W, C = 2, 4, 6, 10, 24
+    z16 = synthdata.to_bf16_bits(rng.normal(size=(N, D, H, W, C)))
+    # plant exact ties in a few windows (the first maximum must win)
+    z16[0, 0:2, 0:2, 0:2, 3] = z16[0, 0, 0, 0, 3]
+    z16[1, 2:4, 2:4, 4:6, 5] = synthdata.to_bf16_bits(np.array([1.5]))[0]
+    b = rng.normal(0, 0.1, size=C).astype(np.float32)
+    y = empty_bf16((N, D // 2, H // 2, W // 2, C))
+    import torch
+    idx = torch.empty(y.shape, dtype=torch.uint8, device="cuda")
+    cf.cf_bias_lrelu_pool_fwd(N, D, H, W, C, dev_bf16(z16), dev(b), SLOPE, y, idx)
+    ry, ridx = oracle_mod.pool_fwd(_f64(oracle_mod, z16), b.astype(np.float64), SLOPE)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    gy = host_bf16_f64(y)
+    np.testing.assert_allclose(gy, ry, rtol=2 ** -8, atol=1e-30)
+
+
+def test_pool_bwd_standalone(cf, oracle_mod):
+    import torch
+    rng = np.random.default_rng(6)
+    N, D, H, W, C = 2, 4, 6, 10, 16
+    z = rng.normal(size=(N, D, H, W, C))
+    b = rng.normal(0, 0.1, size=C)
+    ry, ridx = oracle_mod.pool_fwd(z, b, SLOPE)
+    y16 = synthdata.to_bf16_bits(ry)
+    dy16 = synthdata.to_bf16_bits(rng.normal(size=ry.shape))
+    dz = empty_bf16((N, D, H, W, C), fill=7.0)
+    dyp = empty_bf16(ry.shape)
+    db = torch.empty(C, dtype=torch.float32, device="cuda")
+    ws, wsb = _ws(cf, cf.CF_OP_POOL_BWD, cf.cf_conv_desc(N, D, H, W, C, C))
+    cf.cf_bias_lrelu_pool_bwd(N, D, H, W, C, dev_bf16(dy16), dev_bf16(y16), dev(ridx), SLOPE, dz, dyp, db, ws, wsb)
+    rdz, rdyp, rdb = oracle_mod.pool_bwd(_f64(oracle_mod, dy16), _f64(oracle_mod, y16), ridx, SLOPE)
+    gdz = host_bf16_f64(dz)
+    # same nonzero pattern (zeros everywhere but the argmax), values = bf16(g)
+    np.testing.assert_array_equal(gdz == 0, rdz == 0)
+    np.testing.assert_allclose(gdz, rdz, rtol=2 ** -8, atol=0)
+    np.testing.assert_allclose(host_bf16_f64(dyp), rdyp, rtol=2 ** -8, atol=0)
+    assert_close(db.cpu().numpy(), rdb, np.abs(rdyp).sum(axis=(0, 1, 2, 3)), "db")
+    # y=None: dy is already the pre-activation gradient; no dbias
+    dz2 = empty_bf16((N, D, H, W, C))
+    cf.cf_bias_lrelu_pool_bwd(N, D, H, W, C, dyp, None, dev(ridx), SLOPE, dz2, None, None)
+    np.testing.assert_array_equal(host_bf16_f64(dz2), gdz)
+
+
+# ----------------------------------------------------------------------------- forward conv
+
+FWD_SHAPES = [
+    # N, D, H, W, Cin, Cout
+    (2, 4, 6, 40, 32, 64),     # W ragged (40 = 32 + 8), several tiles in every dim
+    (1, 4, 4, 16, 64, 128),
+    (1, 2, 8, 8, 128, 256),
+    (1, 2, 8, 8, 256, 256),
+    (2, 4, 4, 12, 32, 32),
+    (1, 2, 2, 8, 64, 16),
+    (1, 2, 4, 8, 96, 96),      # three 32-channel K chunks, N tile 96
+    (1, 2, 4, 8, 64, 512),     # two N tiles of 256
+]
+
+
+def _case(shape, seed):
+    N, D, H, W, Ci, Co = shape
+    return synthdata.random_case(seed, N, D, H, W, Ci, Co)
+
+
+@pytest.mark.parametrize("shape", FWD_SHAPES)
+def test_conv_fwd_plain(cf, oracle_mod, shape):
+    N, D, H, W, Ci, Co = shape
+    c = _case(shape, 100 + Ci + Co)
+    y = empty_bf16((N, D, H, W, Co), fill=float("nan"))
+    cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), None, y)
+    x, w = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["w"])
+    ref = oracle_mod.conv3d_fwd(x, w)
+    S = oracle_mod.conv3d_fwd(np.abs(x), np.abs(w))
+    assert_close(host_bf16_f64(y), ref, S, f"fwd {shape}")
+
+
+def _check_pooled(oracle_mod, x, w, b, gy, gidx, what):
+    z = oracle_mod.conv3d_fwd(x, w)
+    S = oracle_mod.conv3d_fwd(np.abs(x), np.abs(w))
+    ry, ridx = oracle_mod.pool_fwd(z, b, SLOPE)
+    N, D, H, W, C = z.shape
+    def win(a):
+        return a.reshape(N, D // 2, 2, H // 2, 2, W // 2, 2, C).transpose(0, 1, 3, 5, 7, 2, 4, 6).reshape(
+            N, D // 2, H // 2, W // 2, C, 8)
+    zw, sw = win(z), win(S)
+    srt = np.sort(zw, axis=-1)
+    gap = srt[..., -1] - srt[..., -2]
+    s_at = np.take_along_axis(sw, ridx[..., None].astype(np.int64), -1)[..., 0] + np.abs(b)
+    tol = 1e-2 * s_at
+    notie = gap > tol
+    np.testing.assert_array_equal(gidx[notie], ridx[notie])
+    # where the pick differs (near-tie), the value must still be within tolerance
+    assert_close(gy, ry, s_at, what)
+    return int((~notie).sum())
+
+
+@pytest.mark.parametrize("shape", FWD_SHAPES[:6])
+def test_conv_fwd_pooled(cf, oracle_mod, shape):
+    import torch
+    N, D, H, W, Ci, Co = shape
+    c = _case(shape, 200 + Ci + Co)
+    y = empty_bf16((N, D // 2, H // 2, W // 2, Co), fill=float("nan"))
+    idx = torch.full(y.shape, 255, dtype=torch.uint8, device="cuda")
+    cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), (dev(c["b"]), SLOPE, idx), y)
+    x, w = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["w"])
+    _check_pooled(oracle_mod, x, w, c["b"].astype(np.float64), host_bf16_f64(y), idx.cpu().numpy(),
+                  f"pooled {shape}")
+
+
+SMALLC_SHAPES = [
+    (2, 4, 6, 40, 4, 32),
+    (1, 4, 8, 16, 4, 16),
+    (1, 2, 8, 8, 4, 64),
+    (1, 16, 16, 16, 1, 8),  # the single-block CosmoFlow case: 1 -> 8 channels at 16^3
+    (1, 4, 4, 12, 1, 16),
+]
+
+
+@pytest.mark.parametrize("shape", SMALLC_SHAPES)
+@pytest.mark.parametrize("pooled", [False, True])
+def test_conv_fwd_smallc(cf, oracle_mod, shape, pooled):
+    import torch
+    N, D, H, W, Ci, Co = shape
+    c = _case(shape, 300 + Ci + Co)
+    x, w = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["w"])
+    if not pooled:
+        y = empty_bf16((N, D, H, W, Co), fill=float("nan"))
+        cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), None, y)
+        ref = oracle_mod.conv3d_fwd(x, w)
+        S = oracle_mod.conv3d_fwd(np.abs(x), np.abs(w))
+        assert_close(host_bf16_f64(y), ref, S, f"smallc fwd {shape}")
+    else:
+        y = empty_bf16((N, D // 2, H // 2, W // 2, Co), fill=float("nan"))
+        idx = torch.full(y.shape, 255, dtype=torch.uint8, device="cuda")
+        cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), (dev(c["b"]), SLOPE, idx), y)
+        _check_pooled(oracle_mod, x, w, c["b"].astype(np.float64), host_bf16_f64(y), idx.cpu().numpy(),
+                      f"smallc pooled {shape}")
+
+
+# ----------------------------------------------------------------------------- backward data
+
+DGRAD_SHAPES = [
+    (2, 4, 6, 40, 32, 64),
+    (1, 4, 4, 16, 64, 128),
+    (1, 2, 8, 8, 128, 256),
+    (1, 2, 8, 8, 256, 256),
+    (1, 2, 4, 8, 16, 32),
+]
+
+
+@pytest.mark.parametrize("shape", DGRAD_SHAPES)
+@pytest.mark.parametrize("with_act", [False, True])
+def test_conv_dgrad(cf, oracle_mod, shape, with_act):
+    N, D, H, W, Ci, Co = shape
+    c = _case(shape, 400 + Ci + Co)
+    desc = cf.cf_conv_desc(*shape)
+    ws, wsb = _ws(cf, cf.CF_OP_DGRAD, desc)
+    dx = empty_bf16((N, D, H, W, Ci), fill=float("nan"))
+    x_act = dev_bf16(c["x"]) if with_act else None
+    cf.cf_conv3d_dgrad(desc, dev_bf16(c["dz"]), None, dev_bf16(c["w"]), x_act, SLOPE, dx, ws, wsb)
+    dz, w = _f64(oracle_mod, c["dz"]), _f64(oracle_mod, c["w"])
+    ref = oracle_mod.conv3d_dgrad(dz, w)
+    S = oracle_mod.conv3d_dgrad(np.abs(dz), np.abs(w))
+    if with_act:
+        f = np.where(_f64(oracle_mod, c["x"]) > 0, 1.0, SLOPE)
+        ref, S = ref * f, S * f
+    assert_close(host_bf16_f64(dx), ref, S, f"dgrad {shape} act={with_act}")
+
+
+# ----------------------------------------------------------------------------- backward weight
+
+WGRAD_SHAPES = [
+    (2, 4, 6, 40, 32, 64),
+    (1, 4, 4, 16, 64, 128),
+    (1, 2, 8, 8, 128, 256),
+    (2, 2, 8, 8, 256, 256),
+    (2, 4, 6, 40, 4, 32),
+    (1, 4, 8, 16, 4, 16),
+    (1, 8, 8, 8, 1, 16),
+    (1, 2, 4, 8, 32, 192),
+]
+
+
+@pytest.mark.parametrize("shape", WGRAD_SHAPES)
+def test_conv_wgrad(cf, oracle_mod, shape):
+    import torch
+    N, D, H, W, Ci, Co = shape
+    c = _case(shape, 500 + Ci + Co)
+    desc = cf.cf_conv_desc(*shape)
+    ws, wsb = _ws(cf, cf.CF_OP_WGRAD, desc)
+    dw = torch.full((Co, 3, 3, 3, Ci), float("nan"), dtype=torch.float32, device="cuda")
+    cf.cf_conv3d_wgrad(desc, dev_bf16(c["x"]), dev_bf16(c["dz"]), None, dw, 0, ws, wsb)
+    x, dz = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["dz"])
+    ref = oracle_mod.conv3d_wgrad(x, dz)
+    S = oracle_mod.conv3d_wgrad(np.abs(x), np.abs(dz))
+    g1 = dw.cpu().numpy().astype(np.float64)
+    assert_close(g1, ref, S, f"wgrad {shape}")
+    # accumulate=1 adds onto the existing values
+    cf.cf_conv3d_wgrad(desc, dev_bf16(c["x"]), dev_bf16(c["dz"]), None, dw, 1, ws, wsb)
+    assert_close(dw.cpu().numpy().astype(np.float64), 2 * ref, 2 * S, f"wgrad acc {shape}")
+
+
+# ----------------------------------------------------------------------------- argmax-routed inputs
+
+@pytest.mark.parametrize("shape", [(2, 4, 6, 40, 32, 64), (1, 4, 4, 16, 4, 32)])
+def test_routed_gradients_match_dense(cf, oracle_mod, shape):
+    import torch
+    N, D, H, W, Ci, Co = shape
+    rng = np.random.default_rng(77)
+    c = _case(shape, 600 + Ci)
+    z = rng.normal(size=(N, D, H, W, Co))
+    _, ridx = oracle_mod.pool_fwd(z, None, SLOPE)
+    g16 = synthdata.to_bf16_bits(rng.normal(size=ridx.shape))
+    desc = cf.cf_conv_desc(*shape)
+    rdz, _, _ = oracle_mod.pool_bwd(_f64(oracle_mod, g16), None, ridx, SLOPE)
+    # wgrad from (g, idx)
+    ws, wsb = _ws(cf, cf.CF_OP_WGRAD_ROUTED, desc)
+    dw = torch.empty((Co, 3, 3, 3, Ci), dtype=torch.float32, device="cuda")
+    cf.cf_conv3d_wgrad(desc, dev_bf16(c["x"]), dev_bf16(g16), dev(ridx), dw, 0, ws, wsb)
+    x = _f64(oracle_mod, c["x"])
+    ref = oracle_mod.conv3d_wgrad(x, rdz)
+    S = oracle_mod.conv3d_wgrad(np.abs(x), np.abs(rdz))
+    assert_close(dw.cpu().numpy().astype(np.float64), ref, S, "routed wgrad")
+    if Ci % 16 == 0 and Co % 32 == 0:
+        ws, wsb = _ws(cf, cf.CF_OP_DGRAD_ROUTED, desc)
+        dx = empty_bf16((N, D, H, W, Ci))
+        cf.cf_conv3d_dgrad(desc, dev_bf16(g16), dev(ridx), dev_bf16(c["w"]), None, SLOPE, dx, ws, wsb)
+        w = _f64(oracle_mod, c["w"])
+        ref = oracle_mod.conv3d_dgrad(rdz, w)
+        S = oracle_mod.conv3d_dgrad(np.abs(rdz), np.abs(w))
+        assert_close(host_bf16_f64(dx), ref, S, "routed dgrad")
