@@ -121,9 +121,19 @@ __global__ void __launch_bounds__(192, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < g.num_tiles && ok; tile += gridDim.x) {
                 const TileCoord tc = decode_tile(g, tile, BN);
+                int t = 0, cc = 0, kd = 0, kh = 0, kw = 0;
                 for (int kb = 0; kb < nk; ++kb) {
-                    const int t = kb / p.n_cchunks, cc = kb - t * p.n_cchunks;
-                    const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
+                    if (kb > 0 && ++cc == p.n_cchunks) {  // advance (tap, chunk) without divisions
+                        cc = 0;
+                        ++t;
+                        if (++kw == 3) {
+                            kw = 0;
+                            if (++kh == 3) {
+                                kh = 0;
+                                ++kd;
+                            }
+                        }
+                    }
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
                         ok = false;
                         break;

@@ -33,17 +33,31 @@ struct WgradGeom {
     int num_units;            // n_mblocks * n_splits
 };
 
-__device__ __forceinline__ void decode_box(const WgradGeom& g, int64_t b, int& n, int& d0, int& h0, int& w0) {
-    int bw = (int)(b % g.nb_w);
-    b /= g.nb_w;
-    int bh = (int)(b % g.nb_h);
-    b /= g.nb_h;
-    int bd = (int)(b % g.nb_d);
-    n = (int)(b / g.nb_d);
-    w0 = bw * g.vw;
-    h0 = bh * g.vh;
-    d0 = bd * g.vd;
-}
+// Box cursor: decodes a linear box index once, then steps through the boxes
+// with carries (no divisions on the per-stage path).
+struct BoxCursor {
+    int n, bd, bh, bw;
+    __device__ __forceinline__ void init(const WgradGeom& g, int64_t b) {
+        bw = (int)(b % g.nb_w);
+        b /= g.nb_w;
+        bh = (int)(b % g.nb_h);
+        b /= g.nb_h;
+        bd = (int)(b % g.nb_d);
+        n = (int)(b / g.nb_d);
+    }
+    __device__ __forceinline__ void next(const WgradGeom& g) {
+        if (++bw == g.nb_w) {
+            bw = 0;
+            if (++bh == g.nb_h) {
+                bh = 0;
+                if (++bd == g.nb_d) {
+                    bd = 0;
+                    ++n;
+                }
+            }
+        }
+    }
+};
 
 // Writes the unit's accumulator rows (t,ci) < 27*Cin into part[split][co][row].
 template <int BN>
@@ -153,27 +167,37 @@ __global__ void __launch_bounds__(192, 1)
                 const int mb = u % g.n_mblocks, split = u / g.n_mblocks;
                 const int64_t b0 = (int64_t)split * g.boxes_per_split;
                 const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
-                // A sub-blocks of this M block that hold real rows
+                // A sub-blocks of this M block that hold real rows, and their taps
+                constexpr int NSUB = 128 / SUBA;
                 int nsub = 0;
-                for (int s = 0; s < 128 / SUBA; ++s)
-                    if (mb * 128 + s * SUBA < KK) ++nsub;
+                int sci[NSUB], sdw[NSUB], sdh[NSUB], sdd[NSUB];
+#pragma unroll
+                for (int s = 0; s < NSUB; ++s) {
+                    const int r0 = mb * 128 + s * SUBA;
+                    const int t = r0 / g.Cin;
+                    sci[s] = r0 - t * g.Cin;
+                    sdd[s] = t / 9 - 1;
+                    sdh[s] = (t / 3) % 3 - 1;
+                    sdw[s] = t % 3 - 1;
+                    if (r0 < KK) ++nsub;
+                }
                 const uint32_t tx = nsub * C::A_SUB_BYTES + C::B_BYTES;
-                for (int64_t b = b0; b < b1; ++b) {
-                    int n, d0, h0, w0;
-                    decode_box(g, b, n, d0, h0, w0);
+                BoxCursor cur;
+                cur.init(g, b0);
+                for (int64_t b = b0; b < b1; ++b, cur.next(g)) {
+                    const int n = cur.n, d0 = cur.bd * g.vd, h0 = cur.bh * g.vh, w0 = cur.bw * g.vw;
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
                     uint8_t* sa = ring + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], tx);
-                    for (int s = 0; s < nsub; ++s) {
-                        const int r0 = mb * 128 + s * SUBA;
-                        const int t = r0 / g.Cin, ci0 = r0 % g.Cin;
-                        const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
-                        tma_load_5d(sa + s * C::A_SUB_BYTES, &tmX, &full[stage], ci0, w0 + kw - 1, h0 + kh - 1,
-                                    d0 + kd - 1, n);
-                    }
+#pragma unroll
+                    for (int s = 0; s < NSUB; ++s)
+                        if (s < nsub)
+                            tma_load_5d(sa + s * C::A_SUB_BYTES, &tmX, &full[stage], sci[s], w0 + sdw[s], h0 + sdh[s],
+                                        d0 + sdd[s], n);
+#pragma unroll
                     for (int s = 0; s < BN / SUBB; ++s)
                         tma_load_5d(sa + C::A_BYTES + s * C::B_SUB_BYTES, &tmG, &full[stage], s * SUBB, w0, h0, d0, n);
                     issued |= 1u << stage;
@@ -382,9 +406,10 @@ __global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_const
         for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
             const int64_t b0 = (int64_t)u * g.boxes_per_split;
             const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
-            for (int64_t b = b0; b < b1; ++b) {
-                int n, d0, h0, w0;
-                decode_box(g, b, n, d0, h0, w0);
+            BoxCursor cur;
+            cur.init(g, b0);
+            for (int64_t b = b0; b < b1; ++b, cur.next(g)) {
+                const int n = cur.n, d0 = cur.bd * g.vd, h0 = cur.bh * g.vh, w0 = cur.bw * g.vw;
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
                     ok = false;
                     break;

@@ -144,12 +144,20 @@ __global__ void pool_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t*
     }
 }
 
+// out[ch] = sum over rows of partial[row][ch]; one block per channel, each
+// thread sums a strided subset of rows, then a fixed-shape tree (deterministic).
 __global__ void colsum_kernel(const float* __restrict__ partial, int rows, int C, float* __restrict__ out) {
-    for (int ch = blockIdx.x * blockDim.x + threadIdx.x; ch < C; ch += gridDim.x * blockDim.x) {
-        float s = 0.f;
-        for (int r = 0; r < rows; ++r) s += partial[(int64_t)r * C + ch];
-        out[ch] = s;
+    __shared__ float red[256];
+    const int ch = blockIdx.x;
+    float s = 0.f;
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) s += partial[(int64_t)r * C + ch];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int k = blockDim.x / 2; k > 0; k >>= 1) {
+        if ((int)threadIdx.x < k) red[threadIdx.x] += red[threadIdx.x + k];
+        __syncthreads();
     }
+    if (threadIdx.x == 0) out[ch] = red[0];
 }
 
 // W'[ci][t'][co] = W[co][26 - t'][ci]: the filter of the backward-data
@@ -214,7 +222,7 @@ cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
         dy, y, idx, slope, dz, dy_pre, partial, n, (int)d, (int)h, (int)w, c);
     if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
     if (dbias) {
-        colsum_kernel<<<(c + 127) / 128, 128, 0, ctx.stream>>>(partial, blocks, c, dbias);
+        colsum_kernel<<<c, 256, 0, ctx.stream>>>(partial, blocks, c, dbias);
         if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
     }
     return CF_OK;
