@@ -3,6 +3,8 @@
 // accumulator out of tensor memory.
 #pragma once
 
+#include <algorithm>
+
 #include "cf_internal.h"
 #include "cf_ptx.cuh"
 
@@ -160,6 +162,36 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
             }
         }
     }
+}
+
+// ---- host helpers shared by the conv launchers
+inline ConvGeom make_geom(int64_t n, int64_t d, int64_t h, int64_t w, int cin, int cout, int bn) {
+    ConvGeom g;
+    g.N = (int)n;
+    g.D = (int)d;
+    g.H = (int)h;
+    g.W = (int)w;
+    g.Cin = cin;
+    g.Cout = cout;
+    TileGeom t = choose_tile(d, h, w);
+    g.tw = t.tw;
+    g.th = t.th;
+    g.td = t.td;
+    g.tiles_w = (int)((w + t.tw - 1) / t.tw);
+    g.tiles_h = (int)((h + t.th - 1) / t.th);
+    g.tiles_d = (int)((d + t.td - 1) / t.td);
+    g.n_ntiles = (cout + bn - 1) / bn;
+    g.num_tiles = (int)(n * g.tiles_d * g.tiles_h * g.tiles_w * g.n_ntiles);
+    return g;
+}
+
+template <typename K>
+inline int grid_for(K kernel, uint32_t smem, int threads, int num_sms, int num_tiles, uint32_t tmem_cols) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    per_sm = std::min<int>(per_sm, (int)(512 / tmem_cols));
+    return std::max(1, std::min(num_tiles, num_sms * per_sm));
 }
 
 }  // namespace cf

@@ -21,10 +21,8 @@
 //                 argmax (CosmoFlow block), or the backward-data epilogue that
 //                 multiplies by the leaky-ReLU derivative of the previous block.
 //
-// The small-channel variant (c_in = 1 or 4, the first CosmoFlow layer) cannot
-// feed TMA with 2- or 8-byte voxels, so four producer warps build the im2col A
-// tile (K = 27*c_in padded to a multiple of 16) directly in the swizzled
-// shared-memory layout, and the whole filter stays resident in shared memory.
+// The small-channel first layer (c_in = 1 or 4) has its own kernel in
+// conv_smallc.cu.
 #include <algorithm>
 
 #include "conv_common.cuh"
@@ -223,225 +221,6 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------------------
-// small-channel kernel: c_in in {1, 4}; the whole K = 27*c_in fits one tile.
-
-template <int CIN, int BN, int EPI>
-struct SmallCfg {
-    static constexpr int KREAL = 27 * CIN;
-    static constexpr int KP = (KREAL + 15) / 16 * 16;  // 32 or 112
-    static constexpr int ATOMS = (KP + 63) / 64;       // 64-element swizzle atoms along K
-    static constexpr uint32_t A_BYTES = 128 * 128 * ATOMS;
-    static constexpr uint32_t B_BYTES = BN * 128 * ATOMS;
-    static constexpr uint32_t STG_BYTES = EPI == EPI_POOL ? 128 * 33 * 4 : 0;
-    static constexpr uint32_t BAR_BYTES = 256;
-    static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - B_BYTES - STG_BYTES - BAR_BYTES;
-    static constexpr int STAGES_RAW = (int)(BUDGET / A_BYTES);
-    static constexpr int STAGES = STAGES_RAW > 4 ? 4 : STAGES_RAW;
-    static constexpr uint32_t SMEM = 1024 + B_BYTES + STAGES * A_BYTES + STG_BYTES + BAR_BYTES;
-    static constexpr uint32_t TMEM_COLS = (2 * BN) <= 32 ? 32 : (2 * BN) <= 64 ? 64 : (2 * BN) <= 128 ? 128
-                                                                                 : (2 * BN) <= 256 ? 256 : 512;
-    static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
-    static_assert(STAGES >= 2, "not enough shared memory");
-};
-
-struct SmallParams {
-    ConvGeom g;
-    const uint16_t* x;
-    const uint16_t* w;  // [Cout][27*CIN]
-    EpiArgs ea;
-    int* status;
-    uint64_t wait_ns;
-};
-
-// Builds one row (voxel) of the im2col tile: K index k = t*CIN + ci, value
-// X[n, d+kd-1, h+kh-1, w+kw-1, ci] or 0, written in the SW128 K-major layout
-// (atom a = k / 64 at a * 16 KB, row stride 128 B, 16-byte chunks XOR row%8).
-template <int CIN>
-__device__ __forceinline__ void build_im2col_row(uint8_t* a_tile, int row, const uint16_t* __restrict__ x,
-                                                 int D, int H, int W, int n, int d, int h, int w, bool valid) {
-    constexpr int KP = (27 * CIN + 15) / 16 * 16;
-#pragma unroll
-    for (int c = 0; c < KP / 8; ++c) {  // 16-byte chunk c holds k = 8c .. 8c+7
-        uint32_t v[4] = {0u, 0u, 0u, 0u};
-        if (valid) {
-            if (CIN == 4) {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int t = 2 * c + half;
-                    if (t < 27) {
-                        const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
-                        const int id = d + kd - 1, ih = h + kh - 1, iw = w + kw - 1;
-                        if (id >= 0 && id < D && ih >= 0 && ih < H && iw >= 0 && iw < W) {
-                            const int64_t o = ((((int64_t)n * D + id) * H + ih) * W + iw) * 4;
-                            const uint2 q = __ldg(reinterpret_cast<const uint2*>(x + o));
-                            v[2 * half] = q.x;
-                            v[2 * half + 1] = q.y;
-                        }
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int t = 8 * c + e;
-                    uint32_t bits = 0;
-                    if (t < 27) {
-                        const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
-                        const int id = d + kd - 1, ih = h + kh - 1, iw = w + kw - 1;
-                        if (id >= 0 && id < D && ih >= 0 && ih < H && iw >= 0 && iw < W)
-                            bits = __ldg(x + ((((int64_t)n * D + id) * H + ih) * W + iw));
-                    }
-                    v[e >> 1] |= bits << (16 * (e & 1));
-                }
-            }
-        }
-        const int atom = c >> 3, cin_atom = c & 7;
-        uint8_t* dst = a_tile + atom * (128 * 128) + row * 128 + ((cin_atom ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(v[0], v[1], v[2], v[3]);
-    }
-}
-
-template <int CIN, int BN, int EPI>
-__global__ void __launch_bounds__(288, 1) conv_smallc_kernel(const SmallParams p) {
-    using C = SmallCfg<CIN, BN, EPI>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* bsm = smem;
-    uint8_t* ring = smem + C::B_BYTES;
-    float* stg = reinterpret_cast<float*>(ring + C::STAGES * C::A_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + C::STAGES * C::A_BYTES + C::STG_BYTES);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + C::STAGES;
-    uint64_t* tfull = bars + 2 * C::STAGES;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    volatile int* epi_flag = abort_flag + 1;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const ConvGeom& g = p.g;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 128);
-            mbar_init(&empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    // resident filter tile: rows co < BN (zero above Cout), K padded with zeros
-    for (int e = threadIdx.x; e < BN * (C::ATOMS * 8); e += blockDim.x) {
-        const int r = e / (C::ATOMS * 8), c = e % (C::ATOMS * 8);
-        uint32_t v[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int k8 = 0; k8 < 8; ++k8) {
-            const int k = c * 8 + k8;
-            uint32_t bits = 0;
-            if (r < g.Cout && k < C::KREAL) bits = p.w[(int64_t)r * C::KREAL + k];
-            v[k8 >> 1] |= bits << (16 * (k8 & 1));
-        }
-        const int atom = c >> 3, cin_atom = c & 7;
-        *reinterpret_cast<uint4*>(bsm + atom * (BN * 128) + r * 128 + ((cin_atom ^ (r & 7)) << 4)) =
-            make_uint4(v[0], v[1], v[2], v[3]);
-    }
-    fence_proxy_async_smem();
-    if (warp == 4) {
-        tmem_alloc(tmem_holder, C::TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_holder;
-
-    if (warp < 4) {
-        // ---------------- im2col producers (128 threads, one row each)
-        const int row = threadIdx.x;
-        const int l = row % g.tw, j = (row / g.tw) % g.th, i = row / (g.tw * g.th);
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
-            const TileCoord tc = decode_tile(g, tile, BN);
-            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) break;
-            const int d = tc.d0 + i, h = tc.h0 + j, w = tc.w0 + l;
-            const bool valid = d < g.D && h < g.H && w < g.W;
-            build_im2col_row<CIN>(ring + stage * C::A_BYTES, row, p.x, g.D, g.H, g.W, tc.n, d, h, w, valid);
-            fence_proxy_async_smem();
-            mbar_arrive(&full[stage]);
-            if (++stage == C::STAGES) {
-                stage = 0;
-                phase ^= 1;
-            }
-        }
-    } else if (warp == 4) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            int stage = 0;
-            uint32_t phase = 0, local = 0;
-            bool ok = true;
-            const uint32_t b_addr = smem_u32(bsm);
-            for (int tile = blockIdx.x; tile < g.num_tiles && ok; tile += gridDim.x, ++local) {
-                const uint32_t acc = local & 1, use = local >> 1;
-                if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_TMEM_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
-                const uint32_t a_addr = smem_u32(ring + stage * C::A_BYTES);
-#pragma unroll
-                for (int k = 0; k < C::KP / 16; ++k) {
-                    const uint32_t atom = k >> 2, koff = (k & 3) * 32;
-                    const uint64_t ad = sdesc(a_addr + atom * (128 * 128) + koff, 16, 1024, SWZ_128B);
-                    const uint64_t bd = sdesc(b_addr + atom * (BN * 128) + koff, 16, 1024, SWZ_128B);
-                    umma_bf16(d_tmem, ad, bd, C::IDESC, k != 0);
-                }
-                umma_commit(&empty[stage]);
-                umma_commit(&tfull[acc]);
-                if (++stage == C::STAGES) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-            if (!ok) {
-                umma_commit(drain);
-                mbar_wait_timed(drain, 0, p.wait_ns);
-            }
-        }
-    } else {
-        // ---------------- epilogue warps 5..8
-        const int q = warp & 3;
-        const int et = threadIdx.x - 160;
-        uint32_t local = 0;
-        for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x, ++local) {
-            const uint32_t acc = local & 1, use = local >> 1;
-            if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
-            tc_fence_after();
-            const TileCoord tc = decode_tile(g, tile, BN);
-            conv_epilogue<BN, EPI>(g, tc, p.ea, tmem_base, acc * BN, q, lane, et, stg);
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 4) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
-    }
-}
-
-// ---------------------------------------------------------------------------
 // host side
 
 TileGeom choose_tile(int64_t d, int64_t h, int64_t w) {
@@ -460,35 +239,6 @@ TileGeom choose_tile(int64_t d, int64_t h, int64_t w) {
     }
     (void)h;
     return t;
-}
-
-static ConvGeom make_geom(int64_t n, int64_t d, int64_t h, int64_t w, int cin, int cout, int bn) {
-    ConvGeom g;
-    g.N = (int)n;
-    g.D = (int)d;
-    g.H = (int)h;
-    g.W = (int)w;
-    g.Cin = cin;
-    g.Cout = cout;
-    TileGeom t = choose_tile(d, h, w);
-    g.tw = t.tw;
-    g.th = t.th;
-    g.td = t.td;
-    g.tiles_w = (int)((w + t.tw - 1) / t.tw);
-    g.tiles_h = (int)((h + t.th - 1) / t.th);
-    g.tiles_d = (int)((d + t.td - 1) / t.td);
-    g.n_ntiles = (cout + bn - 1) / bn;
-    g.num_tiles = (int)(n * g.tiles_d * g.tiles_h * g.tiles_w * g.n_ntiles);
-    return g;
-}
-
-template <typename K>
-static int grid_for(K kernel, uint32_t smem, int threads, int num_sms, int num_tiles, uint32_t tmem_cols) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
-    per_sm = std::min<int>(per_sm, (int)(512 / tmem_cols));
-    return std::max(1, std::min(num_tiles, num_sms * per_sm));
 }
 
 template <int BN, int KC, int EPI>
@@ -556,57 +306,6 @@ cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
         default: return CF_ERR_UNSUPPORTED;
     }
 #undef CF_BN_CASE
-}
-
-template <int CIN, int BN, int EPI>
-static cf_status run_smallc(const LaunchCtx& ctx, const ConvGeom& g, const uint16_t* x, const uint16_t* wk,
-                            const EpiArgs& ea) {
-    using C = SmallCfg<CIN, BN, EPI>;
-    SmallParams p;
-    p.g = g;
-    p.x = x;
-    p.w = wk;
-    p.ea = ea;
-    p.status = ctx.status;
-    p.wait_ns = ctx.wait_ns;
-    auto kern = conv_smallc_kernel<CIN, BN, EPI>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-        return CF_ERR_CUDA;
-    const int grid = grid_for(kern, C::SMEM, 288, ctx.num_sms, g.num_tiles, C::TMEM_COLS);
-    kern<<<grid, 288, C::SMEM, ctx.stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
-}
-
-template <int CIN, int BN>
-static cf_status smallc_epi(const LaunchCtx& ctx, const ConvGeom& g, const uint16_t* x, const uint16_t* wk, int epi,
-                            const EpiArgs& ea) {
-    if (epi == EPI_POOL) return run_smallc<CIN, BN, EPI_POOL>(ctx, g, x, wk, ea);
-    if (epi == EPI_PLAIN) return run_smallc<CIN, BN, EPI_PLAIN>(ctx, g, x, wk, ea);
-    return CF_ERR_UNSUPPORTED;
-}
-
-cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
-                             const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
-                             const float* bias, float slope) {
-    if (c_out % 8 != 0 || c_out > 256) return CF_ERR_UNSUPPORTED;
-    const int bn = (c_out + 15) / 16 * 16;
-    EpiArgs ea{y, idx, bias, nullptr, slope};
-    ConvGeom g = make_geom(n, d, h, w, c_in, c_out, bn);
-    g.n_ntiles = 1;
-    g.num_tiles = (int)(n * g.tiles_d * g.tiles_h * g.tiles_w);
-#define CF_SC_CASE(B)                                                              \
-    case B:                                                                        \
-        return c_in == 4 ? smallc_epi<4, B>(ctx, g, x, wk, epi, ea)                \
-                         : smallc_epi<1, B>(ctx, g, x, wk, epi, ea);
-    switch (bn) {
-        CF_SC_CASE(16)
-        CF_SC_CASE(32)
-        CF_SC_CASE(64)
-        CF_SC_CASE(128)
-        CF_SC_CASE(256)
-        default: return CF_ERR_UNSUPPORTED;
-    }
-#undef CF_SC_CASE
 }
 
 }  // namespace cf

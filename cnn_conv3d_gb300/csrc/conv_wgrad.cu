@@ -18,7 +18,7 @@
 // cannot address 2- or 8-byte channel rows; its K block is the 128-voxel box.
 #include <algorithm>
 
-#include "conv_common.cuh"
+#include "smallc_common.cuh"
 
 namespace cf {
 
@@ -282,56 +282,17 @@ __global__ void __launch_bounds__(192, 1)
 
 // ---------------------------------------------------------------------------
 // small channel count: c_in in {1, 4}; one M block (27*c_in <= 128 rows);
-// K block = one 128-voxel box (2 x th x tw); A built by 128 producer threads.
-
-template <int CIN>
-__device__ __forceinline__ void build_wg_im2col_row(uint8_t* a_tile, int row, const uint16_t* __restrict__ x,
-                                                    int D, int H, int W, int n, int d, int h, int w) {
-    // row = voxel (K index); 128 M columns (t, ci) in two 64-wide SW128 atoms,
-    // atom a at a * (128 rows * 128 B)
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        uint32_t v[4] = {0u, 0u, 0u, 0u};
-        if (CIN == 4) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int t = 2 * c + half;
-                if (t < 27) {
-                    const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
-                    const int id = d + kd - 1, ih = h + kh - 1, iw = w + kw - 1;
-                    if (id >= 0 && id < D && ih >= 0 && ih < H && iw >= 0 && iw < W) {
-                        const uint2 qv = __ldg(reinterpret_cast<const uint2*>(
-                            x + ((((int64_t)n * D + id) * H + ih) * W + iw) * 4));
-                        v[2 * half] = qv.x;
-                        v[2 * half + 1] = qv.y;
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int t = 8 * c + e;
-                uint32_t bits = 0;
-                if (t < 27) {
-                    const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
-                    const int id = d + kd - 1, ih = h + kh - 1, iw = w + kw - 1;
-                    if (id >= 0 && id < D && ih >= 0 && ih < H && iw >= 0 && iw < W)
-                        bits = __ldg(x + ((((int64_t)n * D + id) * H + ih) * W + iw));
-                }
-                v[e >> 1] |= bits << (16 * (e & 1));
-            }
-        }
-        const int atom = c >> 3, cin_atom = c & 7;
-        *reinterpret_cast<uint4*>(a_tile + atom * (128 * 128) + row * 128 + ((cin_atom ^ (row & 7)) << 4)) =
-            make_uint4(v[0], v[1], v[2], v[3]);
-    }
-}
+// K block = one 128-voxel box (2 x th x tw).  A TMA producer loads the box's
+// input halo and its dZ rows; four builder warps gather each voxel's im2col
+// row from the halo (warp shuffles for the w neighbours) and store it into the
+// MN-major SW128 A tile (row = voxel, 128 (t,ci) columns in two 64-wide atoms).
 
 template <int CIN, int BN, int SUBB>
 struct WgSmallCfg {
     static constexpr uint32_t A_BYTES = 128 * 128 * 2;  // 128 voxels x 128 (t,ci)
     static constexpr uint32_t B_BYTES = BN * 128 * 2;   // 128 voxels x BN
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t HALO_MAX = 4096 + 1024;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + HALO_MAX;
     static constexpr uint32_t B_SUB_BYTES = 128 * SUBB * 2;
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - BAR_BYTES;
@@ -342,31 +303,29 @@ struct WgSmallCfg {
     static constexpr uint32_t SBO_B = 8 * SUBB * 2;
     static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
     static constexpr uint32_t IDESC = idesc_bf16(128, BN, 1, 1);
+    static_assert(STAGES >= 2, "not enough shared memory");
 };
 
 struct WgSmallParams {
-    WgradGeom g;  // vw,vh,vd = 128-voxel box
-    const uint16_t* x;
+    WgradGeom g;  // vw,vh,vd = the 128-voxel box (2 x th x tw)
     float* part;
     int* status;
     uint64_t wait_ns;
 };
 
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
 template <int CIN, int BN, int SUBB>
-__global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_constant__ CUtensorMap tmG,
-                                                              const WgSmallParams p) {
+__global__ void __launch_bounds__(320, 1)
+    wgrad_smallc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmG,
+                        const WgSmallParams p) {
     using C = WgSmallCfg<CIN, BN, SUBB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* ring = smem;
+    uint8_t* ring = smem;  // stage: [A 32 KB][B][halo]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + C::STAGES;
-    uint64_t* tfull = bars + 2 * C::STAGES;
+    uint64_t* loaded = bars;               // TMA halo + dZ landed (tx)
+    uint64_t* built = bars + C::STAGES;    // A tile written (128 builders)
+    uint64_t* empty = bars + 2 * C::STAGES;  // MMAs of the stage done
+    uint64_t* tfull = bars + 3 * C::STAGES;
     uint64_t* tempty = tfull + 1;
     uint64_t* drain = tempty + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -375,10 +334,12 @@ __global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WgradGeom& g = p.g;
+    const uint32_t halo_tx = (uint32_t)halo_bytes(g.vw, g.vh, g.vd, CIN);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 128);
+            mbar_init(&loaded[s], 1);
+            mbar_init(&built[s], 128);
             mbar_init(&empty[s], 1);
         }
         mbar_init(tfull, 1);
@@ -386,9 +347,16 @@ __global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_const
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
+        tma_prefetch_desc(&tmH);
+        tma_prefetch_desc(&tmG);
     }
-    if (threadIdx.x == 0) tma_prefetch_desc(&tmG);
-    if (warp == 4) {
+    // the A columns the builders never write (k >= 8 * words) stay zero
+    for (int e = threadIdx.x; e < C::STAGES * (int)(C::A_BYTES / 16); e += blockDim.x) {
+        const int s = e / (C::A_BYTES / 16), o = e % (C::A_BYTES / 16);
+        *reinterpret_cast<uint4*>(ring + s * C::STAGE_BYTES + o * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    if (warp == 5) {
         tmem_alloc(tmem_holder, C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -397,50 +365,84 @@ __global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    if (warp < 4) {
-        const int row = threadIdx.x;  // voxel within the box
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer: halo of the box + its dZ rows
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
+                const int64_t b0 = (int64_t)u * g.boxes_per_split;
+                const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
+                BoxCursor cur;
+                cur.init(g, b0);
+                for (int64_t b = b0; b < b1; ++b, cur.next(g)) {
+                    const int n = cur.n, d0 = cur.bd * g.vd, h0 = cur.bh * g.vh, w0 = cur.bw * g.vw;
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = ring + stage * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&loaded[stage], halo_tx + C::B_BYTES);
+                    load_halo<CIN>(st + C::A_BYTES + C::B_BYTES, &tmH, &loaded[stage], n, d0, h0, w0);
+#pragma unroll
+                    for (int s = 0; s < BN / SUBB; ++s)
+                        tma_load_5d(st + C::A_BYTES + s * C::B_SUB_BYTES, &tmG, &loaded[stage], s * SUBB, w0, h0, d0,
+                                    n);
+                    issued |= 1u << stage;
+                    par = (par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (issued & (1u << s)) mbar_wait_timed(&loaded[s], (par >> s) & 1, p.wait_ns);
+            }
+        }
+    } else if (warp < 5) {
+        // ---------------- builders (warps 1..4): one voxel row each
+        const int row = threadIdx.x - 32;
         const int l = row % g.vw, j = (row / g.vw) % g.vh, i = row / (g.vw * g.vh);
         int stage = 0;
-        uint32_t phase = 0, issued = 0, par = 0;
+        uint32_t phase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
             const int64_t b0 = (int64_t)u * g.boxes_per_split;
             const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
-            BoxCursor cur;
-            cur.init(g, b0);
-            for (int64_t b = b0; b < b1; ++b, cur.next(g)) {
-                const int n = cur.n, d0 = cur.bd * g.vd, h0 = cur.bh * g.vh, w0 = cur.bw * g.vw;
-                if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
+            for (int64_t b = b0; b < b1; ++b) {
+                // all lanes wait; the warp leaves together (shuffles need the full warp)
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&loaded[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL))) {
                     ok = false;
                     break;
                 }
-                uint8_t* sa = ring + stage * C::STAGE_BYTES;
-                if (row == 0) {
-                    mbar_expect_tx(&full[stage], C::B_BYTES);
-                    for (int s = 0; s < BN / SUBB; ++s)
-                        tma_load_5d(sa + C::A_BYTES + s * C::B_SUB_BYTES, &tmG, &full[stage], s * SUBB, w0, h0, d0, n);
-                    issued |= 1u << stage;
-                    par = (par & ~(1u << stage)) | (phase << stage);
+                uint8_t* st = ring + stage * C::STAGE_BYTES;
+                uint32_t wd[56];
+                if (CIN == 4)
+                    gather_row_c4(st + C::A_BYTES + C::B_BYTES, g.vw, g.vh, i, j, l, wd);
+                else
+                    gather_row_c1(st + C::A_BYTES + C::B_BYTES, g.vw, g.vh, i, j, l, wd);
+                constexpr int NCH = CIN == 4 ? 14 : 4;  // 16-byte chunks holding real (t,ci) columns
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    const int atom = c >> 3, cin_atom = c & 7;
+                    *reinterpret_cast<uint4*>(st + atom * (128 * 128) + row * 128 + ((cin_atom ^ (row & 7)) << 4)) =
+                        make_uint4(wd[4 * c], wd[4 * c + 1], wd[4 * c + 2], wd[4 * c + 3]);
                 }
-                const int d = d0 + i, h = h0 + j, w = w0 + l;
-                if (d < g.D && h < g.H && w < g.W)
-                    build_wg_im2col_row<CIN>(sa, row, p.x, g.D, g.H, g.W, n, d, h, w);
-                else  // voxel outside the volume: its dZ row is zero-filled, keep A finite
-                    build_wg_im2col_row<CIN>(sa, row, p.x, g.D, g.H, g.W, n, -4, -4, -4);
                 fence_proxy_async_smem();
-                mbar_arrive(&full[stage]);
+                mbar_arrive(&built[stage]);
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1;
                 }
             }
         }
-        if (!ok && row == 0) {
-            for (int s = 0; s < C::STAGES; ++s)
-                if (issued & (1u << s)) mbar_wait_timed(&full[s], (par >> s) & 1, p.wait_ns);
-        }
-    } else if (warp == 4) {
+    } else if (warp == 5) {
         if (lane == 0) {
+            // ---------------- MMA issuer
             int stage = 0;
             uint32_t phase = 0, local = 0;
             bool ok = true;
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_const
                 tc_fence_after();
                 bool first = true;
                 for (int64_t b = b0; b < b1; ++b) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                    if (!mbar_wait(&built[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
                         ok = false;
                         break;
                     }
@@ -483,8 +485,9 @@ __global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_const
             }
         }
     } else {
+        // ---------------- epilogue warps 6..9
         const int q = warp & 3;
-        const int et = threadIdx.x - 160;
+        const int et = threadIdx.x - 192;
         uint32_t local = 0;
         for (int u = blockIdx.x; u < g.num_units; u += gridDim.x, ++local) {
             if (!epi_wait(tfull, local & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(288, 1) wgrad_smallc_kernel(const __grid_const
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
@@ -595,14 +598,16 @@ template <int CIN, int BN, int SUBB>
 static cf_status run_wgrad_small(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
                                  float* part) {
     using C = WgSmallCfg<CIN, BN, SUBB>;
-    CUtensorMap tg;
+    if (halo_bytes(g.vw, g.vh, g.vd, CIN) > (int)C::HALO_MAX) return CF_ERR_UNSUPPORTED;
+    CUtensorMap th, tg;
+    if (!make_halo_map(&th, x, g.N, g.D, g.H, g.W, CIN, g.vw, g.vh, g.vd)) return CF_ERR_CUDA;
     if (!make_act_map(&tg, dz, g, g.Cout, SUBB)) return CF_ERR_CUDA;
-    WgSmallParams p{g, x, part, ctx.status, ctx.wait_ns};
+    WgSmallParams p{g, part, ctx.status, ctx.wait_ns};
     auto kern = wgrad_smallc_kernel<CIN, BN, SUBB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return CF_ERR_CUDA;
-    const int grid = wg_grid(kern, C::SMEM, 288, ctx.num_sms, g.num_units, C::TMEM_COLS);
-    kern<<<grid, 288, C::SMEM, ctx.stream>>>(tg, p);
+    const int grid = wg_grid(kern, C::SMEM, 320, ctx.num_sms, g.num_units, C::TMEM_COLS);
+    kern<<<grid, 320, C::SMEM, ctx.stream>>>(th, tg, p);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
@@ -620,6 +625,7 @@ cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, in
                        const uint16_t* x, const uint16_t* dz, float* dw, int accumulate, void* ws, size_t ws_bytes) {
     if (!(c_in == 1 || c_in == 4 || c_in % 32 == 0)) return CF_ERR_UNSUPPORTED;
     if (!(c_out == 16 || c_out == 32 || c_out % 64 == 0) || c_out > 256) return CF_ERR_UNSUPPORTED;
+    if ((c_in == 1 || c_in == 4) && (w * c_in) % 8 != 0) return CF_ERR_UNSUPPORTED;
     WgradGeom g = wgrad_geom(ctx.num_sms, n, d, h, w, c_in, c_out);
     const size_t need = (size_t)g.n_splits * c_out * 27 * c_in * sizeof(float);
     if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;

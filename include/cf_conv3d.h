@@ -78,7 +78,8 @@ enum { CF_OP_FWD = 0, CF_OP_DGRAD = 1, CF_OP_WGRAD = 2, CF_OP_DGRAD_ROUTED = 3,
  *   ws : unused (pass NULL, 0).
  * Supported: c_in in {1, 4} or a multiple of 32; c_out a multiple of 16 and
  * <= 256 per kernel tile (multiples of 256 above that), or c_out a multiple of 8
- * when c_in is 1 or 4; d, h, w even when pooling.
+ * (<= 256) when c_in is 1 or 4; w * c_in a multiple of 8 when c_in is 1 or 4;
+ * d, h, w even when pooling.
  */
 cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* w,
                         const cf_pool_epi* epi, uint16_t* y, void* ws, size_t ws_bytes,
@@ -109,7 +110,8 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
  * accumulated in fp32 (split-K over n*d*h*w with a fixed-order reduction).
  *   dz/idx : as in cf_conv3d_dgrad.
  *   dw : [c_out][3][3][3][c_in] fp32; accumulate != 0 adds to it, else overwrites.
- * Supported: c_in in {1, 4} or a multiple of 32; c_out a multiple of 16, <= 256.
+ * Supported: c_in in {1, 4} (w * c_in a multiple of 8) or a multiple of 32;
+ * c_out 16, 32 or a multiple of 64, <= 256.
  */
 cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* dz,
                           const uint8_t* idx, float* dw, int accumulate, void* ws,

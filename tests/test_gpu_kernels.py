@@ -189,8 +189,18 @@ SMALLC_SHAPES = [
     (1, 4, 8, 16, 4, 16),
     (1, 2, 8, 8, 4, 64),
     (1, 16, 16, 16, 1, 8),  # the single-block CosmoFlow case: 1 -> 8 channels at 16^3
-    (1, 4, 4, 12, 1, 16),
+    (1, 4, 6, 24, 1, 16),
+    (2, 2, 4, 10, 4, 32),   # ragged tile in w (10 = 8 + 2)
 ]
+
+
+def test_smallc_row_alignment_rule(cf):
+    import torch
+    # c_in = 1 needs w a multiple of 8 (16-byte halo rows): rejected before any launch
+    x = torch.empty(4 * 4 * 12, dtype=torch.bfloat16, device="cuda")
+    w = torch.empty(16 * 27, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(4 * 4 * 12 * 16, dtype=torch.bfloat16, device="cuda")
+    assert cf.cf_conv3d_fwd((1, 4, 4, 12, 1, 16), x, w, None, y, check=False) == cf.CF_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("shape", SMALLC_SHAPES)
