@@ -173,6 +173,9 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
     uint8_t* idx = epi ? epi->argmax : nullptr;
     const float slope = epi ? epi->slope : 0.f;
     if (small) return launch_conv_smallc(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, slope);
+    if (halo_path_supported(ci, co))
+        return launch_conv_halo(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, nullptr,
+                                slope);
     return launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, nullptr, slope);
 }
 
@@ -204,6 +207,9 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
     }
     // backward data = forward conv of dZ with the flipped, transposed filter:
     // GEMM input channels c_out, output channels c_in
+    if (halo_path_supported(co, ci))
+        return launch_conv_halo(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt,
+                                x_act ? EPI_DGRAD : EPI_PLAIN, dx, nullptr, nullptr, x_act, slope);
     return launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt,
                              x_act ? EPI_DGRAD : EPI_PLAIN, dx, nullptr, nullptr, x_act, slope);
 }

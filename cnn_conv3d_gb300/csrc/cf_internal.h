@@ -50,7 +50,14 @@ cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
                             int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
                             uint8_t* idx, const float* bias, const uint16_t* x_act, float slope);
 
-// Small-channel conv forward (c_in in {1,4}): im2col tile built in shared memory.
+// conv_halo.cu: same contract as launch_conv_igemm for c_in % 32 == 0 and
+// c_out in {32, 64, 128}, reading A from one halo tile per channel chunk.
+bool halo_path_supported(int c_in, int c_out);
+cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
+                           int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
+                           uint8_t* idx, const float* bias, const uint16_t* x_act, float slope);
+
+// conv_smallc.cu: forward conv for c_in in {1,4} (im2col operand in tensor memory).
 cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                              int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
                              uint8_t* idx, const float* bias, float slope);

@@ -1,0 +1,432 @@
+// conv_halo.cu -- forward / backward-data 3x3x3 convolution for narrow GEMM
+// N (c_out <= 128): implicit GEMM whose A operand is read from ONE halo tile
+// per input-channel chunk instead of one shifted box per tap.
+//
+// Output tile: 2 planes x 16 lines x 8 voxels (256 voxels) of sample n,
+// computed as two M=128 accumulators (plane 0, plane 1); accumulator row
+// r = 8*j + l is line j, voxel l.  For each chunk of KC input channels the
+// producer loads the halo box (KC, 10, 18, 4) -- voxels w0-1..w0+8, lines
+// h0-1..h0+16, planes d0-1..d0+2, zero outside the volume -- into shared
+// memory with TMA (row R = (dd*18 + hh)*10 + ww, KC*2 bytes per row, swizzled).
+// The A operand of tap (kd,kh,kw) for plane i is then the sub-matrix starting
+// at row ((i+kd)*18 + kh)*10 + kw: eight consecutive rows (one 8-voxel line
+// segment) form a core-matrix group, and groups (lines) are 10 rows apart, so
+// the shared-memory descriptor only changes its start address (the hardware
+// swizzle is a function of the absolute address, so any row offset reads
+// back what TMA wrote).  Each halo row is reused by up to 27 taps, cutting
+// the L2->SM traffic of A by ~10x against per-tap loads; the filter slab of
+// each tap streams through a separate ring.
+//
+// Epilogues: plain bf16 store, backward-data leaky-ReLU derivative, or the
+// CosmoFlow bias + leaky ReLU + 2x2x2 max-pool: the two planes of a window
+// are in the same TMEM lane (two accumulators), the w and h neighbours are
+// lanes +1 and +8 of the same warp, so the window max and its first-maximum
+// code (dd*4+dh*2+dw) are reduced with warp shuffles.
+#include "conv_common.cuh"
+
+namespace cf {
+
+constexpr int HT_W = 8, HT_H = 16, HT_D = 2;                 // output tile
+constexpr int HH_W = HT_W + 2, HH_H = HT_H + 2, HH_D = HT_D + 2;  // halo box
+constexpr int H_ROWS = HH_W * HH_H * HH_D;                   // 720
+
+template <int BN, int KC, int EPI>
+struct HaloCfg {
+    static constexpr uint32_t ROW = KC * 2;
+    static constexpr uint32_t HALO_BYTES = H_ROWS * ROW;                    // 46080 or 92160
+    static constexpr uint32_t HALO_STRIDE = (HALO_BYTES + 1023) / 1024 * 1024;
+    static constexpr uint32_t W_BYTES = BN * KC * 2;
+    static constexpr int HS = KC == 32 ? 3 : 2;
+    static constexpr uint32_t BAR_BYTES = 512;
+    static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - BAR_BYTES - HS * HALO_STRIDE;
+    static constexpr int WS_RAW = (int)(BUDGET / W_BYTES);
+    static constexpr int WS = WS_RAW > 12 ? 12 : WS_RAW;
+    static constexpr uint32_t SMEM = 1024 + HS * HALO_STRIDE + WS * W_BYTES + BAR_BYTES;
+    static constexpr uint32_t SWZ = KC == 64 ? SWZ_128B : SWZ_64B;
+    static constexpr uint32_t SBO_A = HH_W * ROW;  // one halo line
+    static constexpr uint32_t SBO_B = 8 * ROW;
+    static constexpr uint32_t TMEM_COLS = 4 * BN <= 128 ? 128 : (4 * BN <= 256 ? 256 : 512);
+    static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
+    static_assert(WS >= 3, "shared memory");
+    static_assert(4 * BN <= 512, "tensor memory");
+};
+
+struct HaloParams {
+    int N, D, H, W, Cin, Cout;
+    int tiles_w, tiles_h, tiles_d, n_ntiles, num_tiles, n_chunks;
+    EpiArgs ea;
+    int* status;
+    uint64_t wait_ns;
+};
+
+struct HTile {
+    int n, d0, h0, w0, co0;
+};
+
+__device__ __forceinline__ HTile halo_decode(const HaloParams& p, int tile, int bn) {
+    HTile t;
+    const int nt = tile % p.n_ntiles;
+    int m = tile / p.n_ntiles;
+    const int tw = m % p.tiles_w;
+    m /= p.tiles_w;
+    const int th = m % p.tiles_h;
+    m /= p.tiles_h;
+    const int td = m % p.tiles_d;
+    t.n = m / p.tiles_d;
+    t.w0 = tw * HT_W;
+    t.h0 = th * HT_H;
+    t.d0 = td * HT_D;
+    t.co0 = nt * bn;
+    return t;
+}
+
+// (value, code) pair of the first maximum: larger value wins, equal values
+// keep the smaller code.
+__device__ __forceinline__ void pool_combine(float& v, int& k, float v2, int k2) {
+    if (v2 > v || (v2 == v && k2 < k)) {
+        v = v2;
+        k = k2;
+    }
+}
+
+template <int BN, int EPI>
+__device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& t, uint32_t tmem_base,
+                                              uint32_t acc_col, int q, int lane) {
+    const int r = q * 32 + lane;
+    const int j = r >> 3, l = r & 7;
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
+    const int h = t.h0 + j, w = t.w0 + l;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        uint32_t a0[32], a1[32];
+        tmem_ld32(lane_addr + c, a0);
+        tmem_ld32(lane_addr + BN + c, a1);
+        tmem_ld_wait();
+        if (EPI == EPI_POOL) {
+            const int D2 = p.D >> 1, H2 = p.H >> 1, W2 = p.W >> 1;
+            const int pd = t.d0 >> 1, ph = h >> 1, pw = w >> 1;
+            const bool writer = ((j | l) & 1) == 0 && pd < D2 && ph < H2 && pw < W2;
+            const int kbase = (j & 1) * 2 + (l & 1);
+            uint32_t ybits[16];
+            uint32_t codes[8];
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                float v = __uint_as_float(a0[cc]);
+                int k = kbase;
+                pool_combine(v, k, __uint_as_float(a1[cc]), kbase + 4);
+                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 1), __shfl_xor_sync(0xffffffffu, k, 1));
+                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 8), __shfl_xor_sync(0xffffffffu, k, 8));
+                const int co = t.co0 + c + cc;
+                const float s = v + ((p.ea.bias != nullptr && co < p.Cout) ? p.ea.bias[co] : 0.f);
+                const float y = s > 0.f ? s : p.ea.slope * s;
+                if (cc & 1)
+                    ybits[cc >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y)) << 16;
+                else
+                    ybits[cc >> 1] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y));
+                if ((cc & 3) == 0) codes[cc >> 2] = 0;
+                codes[cc >> 2] |= (uint32_t)k << (8 * (cc & 3));
+            }
+            if (writer) {
+                const int64_t po = ((((int64_t)t.n * D2 + pd) * H2 + ph) * W2 + pw) * p.Cout + t.co0 + c;
+                if (t.co0 + c + 32 <= p.Cout) {
+                    uint4* yo = reinterpret_cast<uint4*>(p.ea.y + po);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        yo[q4] = make_uint4(ybits[4 * q4], ybits[4 * q4 + 1], ybits[4 * q4 + 2], ybits[4 * q4 + 3]);
+                    if (p.ea.idx) {
+                        uint4* io = reinterpret_cast<uint4*>(p.ea.idx + po);
+                        io[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+                        io[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int d = t.d0 + i;
+                if (d >= p.D || h >= p.H || w >= p.W) continue;
+                const int64_t o = ((((int64_t)t.n * p.D + d) * p.H + h) * p.W + w) * p.Cout + t.co0 + c;
+                const uint32_t* a = i == 0 ? a0 : a1;
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    if (t.co0 + c + q8 * 8 + 8 > p.Cout) break;
+                    float v[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(a[q8 * 8 + k]);
+                    if (EPI == EPI_DGRAD) {
+                        const uint4 xa = *reinterpret_cast<const uint4*>(p.ea.x_act + o + q8 * 8);
+                        const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float lo = __uint_as_float(xw[k] << 16);
+                            const float hi = __uint_as_float(xw[k] & 0xFFFF0000u);
+                            v[2 * k] *= (lo > 0.f ? 1.f : p.ea.slope);
+                            v[2 * k + 1] *= (hi > 0.f ? 1.f : p.ea.slope);
+                        }
+                    }
+                    uint4 pk;
+                    pk.x = pack_bf16x2(v[0], v[1]);
+                    pk.y = pack_bf16x2(v[2], v[3]);
+                    pk.z = pack_bf16x2(v[4], v[5]);
+                    pk.w = pack_bf16x2(v[6], v[7]);
+                    *reinterpret_cast<uint4*>(p.ea.y + o + q8 * 8) = pk;
+                }
+            }
+        }
+    }
+}
+
+template <int BN, int KC, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    conv_halo_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                     const HaloParams p) {
+    using C = HaloCfg<BN, KC, EPI>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* hring = smem;
+    uint8_t* wring = smem + C::HS * C::HALO_STRIDE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wring + C::WS * C::W_BYTES);
+    uint64_t* hfull = bars;
+    uint64_t* hempty = hfull + C::HS;
+    uint64_t* wfull = hempty + C::HS;
+    uint64_t* wempty = wfull + C::WS;
+    uint64_t* tfull = wempty + C::WS;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    volatile int* epi_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::HS; ++s) {
+            mbar_init(&hfull[s], 1);
+            mbar_init(&hempty[s], 1);
+        }
+        for (int s = 0; s < C::WS; ++s) {
+            mbar_init(&wfull[s], 1);
+            mbar_init(&wempty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer: per chunk one halo box, per tap one filter slab
+            int hs = 0, ws = 0;
+            uint32_t hph = 0, wph = 0, hiss = 0, hpar = 0, wiss = 0, wpar = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+                const HTile t = halo_decode(p, tile, BN);
+                for (int ch = 0; ch < p.n_chunks && ok; ++ch) {
+                    if (!mbar_wait(&hempty[hs], hph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&hfull[hs], C::HALO_BYTES);
+                    tma_load_5d(hring + hs * C::HALO_STRIDE, &tmX, &hfull[hs], ch * KC, t.w0 - 1, t.h0 - 1, t.d0 - 1,
+                                t.n);
+                    hiss |= 1u << hs;
+                    hpar = (hpar & ~(1u << hs)) | (hph << hs);
+                    if (++hs == C::HS) {
+                        hs = 0;
+                        hph ^= 1;
+                    }
+                    for (int tap = 0; tap < 27; ++tap) {
+                        if (!mbar_wait(&wempty[ws], wph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&wfull[ws], C::W_BYTES);
+                        tma_load_2d(wring + ws * C::W_BYTES, &tmW, &wfull[ws], tap * p.Cin + ch * KC, t.co0);
+                        wiss |= 1u << ws;
+                        wpar = (wpar & ~(1u << ws)) | (wph << ws);
+                        if (++ws == C::WS) {
+                            ws = 0;
+                            wph ^= 1;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::HS; ++s)
+                    if (hiss & (1u << s)) mbar_wait_timed(&hfull[s], (hpar >> s) & 1, p.wait_ns);
+                for (int s = 0; s < C::WS; ++s)
+                    if (wiss & (1u << s)) mbar_wait_timed(&wfull[s], (wpar >> s) & 1, p.wait_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            int hs = 0, ws = 0;
+            uint32_t hph = 0, wph = 0, local = 0;
+            bool ok = true;
+            const uint64_t adesc0 = sdesc(smem_u32(hring), 16, C::SBO_A, C::SWZ);
+            const uint64_t bdesc0 = sdesc(smem_u32(wring), 16, C::SBO_B, C::SWZ);
+            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++local) {
+                const uint32_t acc = local & 1, use = local >> 1;
+                if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + acc * 2 * BN;
+                for (int ch = 0; ch < p.n_chunks && ok; ++ch) {
+                    if (!mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t ah = adesc0 + ((hs * C::HALO_STRIDE) >> 4);
+                    for (int tap = 0; tap < 27; ++tap) {
+                        const int kd = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
+                        if (!mbar_wait(&wfull[ws], wph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t bw = bdesc0 + ((ws * C::W_BYTES) >> 4);
+#pragma unroll
+                        for (int k = 0; k < KC / 16; ++k) {
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const uint32_t row = ((i + kd) * HH_H + kh) * HH_W + kw;
+                                const uint64_t ad = ah + ((row * C::ROW + k * 32) >> 4);
+                                umma_bf16(d0 + i * BN, ad, bw + ((k * 32) >> 4), C::IDESC, (ch | tap | k) != 0);
+                            }
+                        }
+                        umma_commit(&wempty[ws]);
+                        if (++ws == C::WS) {
+                            ws = 0;
+                            wph ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(&hempty[hs]);
+                    if (++hs == C::HS) {
+                        hs = 0;
+                        hph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&tfull[acc]);
+            }
+            if (!ok) {
+                umma_commit(drain);
+                mbar_wait_timed(drain, 0, p.wait_ns);
+            }
+        }
+    } else {
+        // ---------------- epilogue warps 2..5
+        const int q = warp & 3;
+        const int et = threadIdx.x - 64;
+        uint32_t local = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+            const uint32_t acc = local & 1, use = local >> 1;
+            if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
+            tc_fence_after();
+            const HTile t = halo_decode(p, tile, BN);
+            halo_epilogue<BN, EPI>(p, t, tmem_base, acc * 2 * BN, q, lane);
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+template <int BN, int KC, int EPI>
+static cf_status run_halo(const LaunchCtx& ctx, HaloParams p, const uint16_t* x, const uint16_t* wk) {
+    using C = HaloCfg<BN, KC, EPI>;
+    CUtensorMap tx, tw;
+    const uint64_t dx[5] = {(uint64_t)p.Cin, (uint64_t)p.W, (uint64_t)p.H, (uint64_t)p.D, (uint64_t)p.N};
+    const uint64_t sx[4] = {(uint64_t)p.Cin * 2, (uint64_t)p.W * p.Cin * 2, (uint64_t)p.H * p.W * p.Cin * 2,
+                            (uint64_t)p.D * p.H * p.W * p.Cin * 2};
+    const uint32_t bx[5] = {(uint32_t)KC, (uint32_t)HH_W, (uint32_t)HH_H, (uint32_t)HH_D, 1u};
+    const CUtensorMapSwizzle swz = KC == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, dx, sx, bx, swz)) return CF_ERR_CUDA;
+    const uint64_t dw[2] = {(uint64_t)27 * p.Cin, (uint64_t)p.Cout};
+    const uint64_t sw[1] = {(uint64_t)27 * p.Cin * 2};
+    const uint32_t bw[2] = {(uint32_t)KC, (uint32_t)BN};
+    if (!encode_tmap(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wk, dw, sw, bw, swz)) return CF_ERR_CUDA;
+    p.n_chunks = p.Cin / KC;
+    auto kern = conv_halo_kernel<BN, KC, EPI>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+        return CF_ERR_CUDA;
+    const int grid = grid_for(kern, C::SMEM, 192, ctx.num_sms, p.num_tiles, C::TMEM_COLS);
+    kern<<<grid, 192, C::SMEM, ctx.stream>>>(tx, tw, p);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+template <int BN, int KC>
+static cf_status halo_epi(const LaunchCtx& ctx, const HaloParams& p, const uint16_t* x, const uint16_t* wk, int epi) {
+    switch (epi) {
+        case EPI_PLAIN: return run_halo<BN, KC, EPI_PLAIN>(ctx, p, x, wk);
+        case EPI_POOL: return run_halo<BN, KC, EPI_POOL>(ctx, p, x, wk);
+        case EPI_DGRAD: return run_halo<BN, KC, EPI_DGRAD>(ctx, p, x, wk);
+    }
+    return CF_ERR_INVALID_ARG;
+}
+
+// The halo tile pays off where the per-tap A re-fetch dominates the L2->SM
+// traffic, i.e. for narrow GEMM N; at N = 128 the per-tap kernel with
+// 64-channel chunks is as fast.
+bool halo_path_supported(int c_in, int c_out) {
+    return (c_in % 32 == 0) && (c_out == 32 || c_out == 64);
+}
+
+cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
+                           const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
+                           const float* bias, const uint16_t* x_act, float slope) {
+    if (!halo_path_supported(c_in, c_out)) return CF_ERR_UNSUPPORTED;
+    HaloParams p;
+    p.N = (int)n;
+    p.D = (int)d;
+    p.H = (int)h;
+    p.W = (int)w;
+    p.Cin = c_in;
+    p.Cout = c_out;
+    p.tiles_w = (int)((w + HT_W - 1) / HT_W);
+    p.tiles_h = (int)((h + HT_H - 1) / HT_H);
+    p.tiles_d = (int)((d + HT_D - 1) / HT_D);
+    p.n_ntiles = 1;
+    p.num_tiles = (int)(n * p.tiles_d * p.tiles_h * p.tiles_w);
+    p.n_chunks = 0;
+    p.ea = EpiArgs{y, idx, bias, x_act, slope};
+    p.status = ctx.status;
+    p.wait_ns = ctx.wait_ns;
+    // 64-channel chunks (SW128) when they fit twice in shared memory next to a
+    // filter ring, 32-channel chunks (SW64) otherwise
+    const bool kc64 = (c_in % 64 == 0);
+    switch (c_out) {
+        case 32: return kc64 ? halo_epi<32, 64>(ctx, p, x, wk, epi) : halo_epi<32, 32>(ctx, p, x, wk, epi);
+        case 64: return kc64 ? halo_epi<64, 64>(ctx, p, x, wk, epi) : halo_epi<64, 32>(ctx, p, x, wk, epi);
+    }
+    return CF_ERR_UNSUPPORTED;
+}
+
+}  // namespace cf
