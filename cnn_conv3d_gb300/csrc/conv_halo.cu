@@ -22,170 +22,48 @@
 // are in the same TMEM lane (two accumulators), the w and h neighbours are
 // lanes +1 and +8 of the same warp, so the window max and its first-maximum
 // code (dd*4+dh*2+dw) are reduced with warp shuffles.
-#include "conv_common.cuh"
+#include "halo_common.cuh"
 
 namespace cf {
 
-constexpr int HT_W = 8, HT_H = 16, HT_D = 2;                 // output tile
-constexpr int HH_W = HT_W + 2, HH_H = HT_H + 2, HH_D = HT_D + 2;  // halo box
-constexpr int H_ROWS = HH_W * HH_H * HH_D;                   // 720
-
-template <int BN, int KC, int EPI>
+template <int BN, int KC, int EPI, bool RES>
 struct HaloCfg {
     static constexpr uint32_t ROW = KC * 2;
-    static constexpr uint32_t HALO_BYTES = H_ROWS * ROW;                    // 46080 or 92160
+    static constexpr uint32_t HALO_BYTES = H_ROWS * ROW;  // 46080 or 92160
     static constexpr uint32_t HALO_STRIDE = (HALO_BYTES + 1023) / 1024 * 1024;
-    static constexpr uint32_t W_BYTES = BN * KC * 2;
-    static constexpr int HS = KC == 32 ? 3 : 2;
+    static constexpr uint32_t W_BYTES = BN * KC * 2;      // one tap's filter slab
+    static constexpr int TPS = 3;                         // taps per streamed filter stage
+    static constexpr int HS = 2;
     static constexpr uint32_t BAR_BYTES = 512;
     static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - BAR_BYTES - HS * HALO_STRIDE;
-    static constexpr int WS_RAW = (int)(BUDGET / W_BYTES);
+    static constexpr int WS_RAW = (int)(BUDGET / (TPS * W_BYTES));
     static constexpr int WS = WS_RAW > 12 ? 12 : WS_RAW;
-    static constexpr uint32_t SMEM = 1024 + HS * HALO_STRIDE + WS * W_BYTES + BAR_BYTES;
     static constexpr uint32_t SWZ = KC == 64 ? SWZ_128B : SWZ_64B;
     static constexpr uint32_t SBO_A = HH_W * ROW;  // one halo line
     static constexpr uint32_t SBO_B = 8 * ROW;
     static constexpr uint32_t TMEM_COLS = 4 * BN <= 128 ? 128 : (4 * BN <= 256 ? 256 : 512);
     static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
-    static_assert(WS >= 3, "shared memory");
+    static_assert(RES || WS >= 3, "shared memory");
     static_assert(4 * BN <= 512, "tensor memory");
-};
-
-struct HaloParams {
-    int N, D, H, W, Cin, Cout;
-    int tiles_w, tiles_h, tiles_d, n_ntiles, num_tiles, n_chunks;
-    EpiArgs ea;
-    int* status;
-    uint64_t wait_ns;
-};
-
-struct HTile {
-    int n, d0, h0, w0, co0;
-};
-
-__device__ __forceinline__ HTile halo_decode(const HaloParams& p, int tile, int bn) {
-    HTile t;
-    const int nt = tile % p.n_ntiles;
-    int m = tile / p.n_ntiles;
-    const int tw = m % p.tiles_w;
-    m /= p.tiles_w;
-    const int th = m % p.tiles_h;
-    m /= p.tiles_h;
-    const int td = m % p.tiles_d;
-    t.n = m / p.tiles_d;
-    t.w0 = tw * HT_W;
-    t.h0 = th * HT_H;
-    t.d0 = td * HT_D;
-    t.co0 = nt * bn;
-    return t;
-}
-
-// (value, code) pair of the first maximum: larger value wins, equal values
-// keep the smaller code.
-__device__ __forceinline__ void pool_combine(float& v, int& k, float v2, int k2) {
-    if (v2 > v || (v2 == v && k2 < k)) {
-        v = v2;
-        k = k2;
+    // shared memory: halo ring, then either the resident filter (n_chunks * 27
+    // slabs, sized at launch) or the streamed filter ring
+    static uint32_t smem_bytes(int n_chunks) {
+        const uint32_t w = RES ? (uint32_t)n_chunks * 27 * W_BYTES : (uint32_t)WS * TPS * W_BYTES;
+        return 1024 + HS * HALO_STRIDE + w + BAR_BYTES;
     }
-}
+};
 
-template <int BN, int EPI>
-__device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& t, uint32_t tmem_base,
-                                              uint32_t acc_col, int q, int lane) {
-    const int r = q * 32 + lane;
-    const int j = r >> 3, l = r & 7;
-    const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
-    const int h = t.h0 + j, w = t.w0 + l;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-        uint32_t a0[32], a1[32];
-        tmem_ld32(lane_addr + c, a0);
-        tmem_ld32(lane_addr + BN + c, a1);
-        tmem_ld_wait();
-        if (EPI == EPI_POOL) {
-            const int D2 = p.D >> 1, H2 = p.H >> 1, W2 = p.W >> 1;
-            const int pd = t.d0 >> 1, ph = h >> 1, pw = w >> 1;
-            const bool writer = ((j | l) & 1) == 0 && pd < D2 && ph < H2 && pw < W2;
-            const int kbase = (j & 1) * 2 + (l & 1);
-            uint32_t ybits[16];
-            uint32_t codes[8];
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                float v = __uint_as_float(a0[cc]);
-                int k = kbase;
-                pool_combine(v, k, __uint_as_float(a1[cc]), kbase + 4);
-                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 1), __shfl_xor_sync(0xffffffffu, k, 1));
-                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 8), __shfl_xor_sync(0xffffffffu, k, 8));
-                const int co = t.co0 + c + cc;
-                const float s = v + ((p.ea.bias != nullptr && co < p.Cout) ? p.ea.bias[co] : 0.f);
-                const float y = s > 0.f ? s : p.ea.slope * s;
-                if (cc & 1)
-                    ybits[cc >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y)) << 16;
-                else
-                    ybits[cc >> 1] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y));
-                if ((cc & 3) == 0) codes[cc >> 2] = 0;
-                codes[cc >> 2] |= (uint32_t)k << (8 * (cc & 3));
-            }
-            if (writer) {
-                const int64_t po = ((((int64_t)t.n * D2 + pd) * H2 + ph) * W2 + pw) * p.Cout + t.co0 + c;
-                if (t.co0 + c + 32 <= p.Cout) {
-                    uint4* yo = reinterpret_cast<uint4*>(p.ea.y + po);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        yo[q4] = make_uint4(ybits[4 * q4], ybits[4 * q4 + 1], ybits[4 * q4 + 2], ybits[4 * q4 + 3]);
-                    if (p.ea.idx) {
-                        uint4* io = reinterpret_cast<uint4*>(p.ea.idx + po);
-                        io[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-                        io[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int d = t.d0 + i;
-                if (d >= p.D || h >= p.H || w >= p.W) continue;
-                const int64_t o = ((((int64_t)t.n * p.D + d) * p.H + h) * p.W + w) * p.Cout + t.co0 + c;
-                const uint32_t* a = i == 0 ? a0 : a1;
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    if (t.co0 + c + q8 * 8 + 8 > p.Cout) break;
-                    float v[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(a[q8 * 8 + k]);
-                    if (EPI == EPI_DGRAD) {
-                        const uint4 xa = *reinterpret_cast<const uint4*>(p.ea.x_act + o + q8 * 8);
-                        const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float lo = __uint_as_float(xw[k] << 16);
-                            const float hi = __uint_as_float(xw[k] & 0xFFFF0000u);
-                            v[2 * k] *= (lo > 0.f ? 1.f : p.ea.slope);
-                            v[2 * k + 1] *= (hi > 0.f ? 1.f : p.ea.slope);
-                        }
-                    }
-                    uint4 pk;
-                    pk.x = pack_bf16x2(v[0], v[1]);
-                    pk.y = pack_bf16x2(v[2], v[3]);
-                    pk.z = pack_bf16x2(v[4], v[5]);
-                    pk.w = pack_bf16x2(v[6], v[7]);
-                    *reinterpret_cast<uint4*>(p.ea.y + o + q8 * 8) = pk;
-                }
-            }
-        }
-    }
-}
-
-template <int BN, int KC, int EPI>
+template <int BN, int KC, int EPI, bool RES>
 __global__ void __launch_bounds__(192, 1)
     conv_halo_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const HaloParams p) {
-    using C = HaloCfg<BN, KC, EPI>;
+    using C = HaloCfg<BN, KC, EPI, RES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* hring = smem;
-    uint8_t* wring = smem + C::HS * C::HALO_STRIDE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(wring + C::WS * C::W_BYTES);
+    uint8_t* wsm = smem + C::HS * C::HALO_STRIDE;
+    const uint32_t w_region = RES ? (uint32_t)p.n_chunks * 27 * C::W_BYTES : (uint32_t)C::WS * C::TPS * C::W_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wsm + w_region);
     uint64_t* hfull = bars;
     uint64_t* hempty = hfull + C::HS;
     uint64_t* wfull = hempty + C::HS;
@@ -193,7 +71,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* tfull = wempty + C::WS;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* wres = drain + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(wres + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* epi_flag = abort_flag + 1;
 
@@ -213,6 +92,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&tempty[a], 128);
         }
         mbar_init(drain, 1);
+        mbar_init(wres, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmX);
@@ -229,10 +109,18 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer: per chunk one halo box, per tap one filter slab
+            // ---------------- TMA producer: per chunk one halo box; the filter either
+            // once (resident) or TPS taps per ring stage
             int hs = 0, ws = 0;
             uint32_t hph = 0, wph = 0, hiss = 0, hpar = 0, wiss = 0, wpar = 0;
-            bool ok = true;
+            bool ok = true, res_issued = false;
+            if (RES && blockIdx.x < p.num_tiles) {
+                mbar_arrive_expect_tx(wres, (uint32_t)p.n_chunks * 27 * C::W_BYTES);
+                for (int ch = 0; ch < p.n_chunks; ++ch)
+                    for (int tap = 0; tap < 27; ++tap)
+                        tma_load_2d(wsm + (ch * 27 + tap) * C::W_BYTES, &tmW, wres, tap * p.Cin + ch * KC, 0);
+                res_issued = true;
+            }
             for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
                 const HTile t = halo_decode(p, tile, BN);
                 for (int ch = 0; ch < p.n_chunks && ok; ++ch) {
@@ -249,13 +137,16 @@ __global__ void __launch_bounds__(192, 1)
                         hs = 0;
                         hph ^= 1;
                     }
-                    for (int tap = 0; tap < 27; ++tap) {
+                    if (RES) continue;
+                    for (int g = 0; g < 27 / C::TPS; ++g) {
                         if (!mbar_wait(&wempty[ws], wph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&wfull[ws], C::W_BYTES);
-                        tma_load_2d(wring + ws * C::W_BYTES, &tmW, &wfull[ws], tap * p.Cin + ch * KC, t.co0);
+                        mbar_arrive_expect_tx(&wfull[ws], C::TPS * C::W_BYTES);
+                        for (int u = 0; u < C::TPS; ++u)
+                            tma_load_2d(wsm + (ws * C::TPS + u) * C::W_BYTES, &tmW, &wfull[ws],
+                                        (g * C::TPS + u) * p.Cin + ch * KC, t.co0);
                         wiss |= 1u << ws;
                         wpar = (wpar & ~(1u << ws)) | (wph << ws);
                         if (++ws == C::WS) {
@@ -265,11 +156,14 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
-            if (!ok) {
-                for (int s = 0; s < C::HS; ++s)
-                    if (hiss & (1u << s)) mbar_wait_timed(&hfull[s], (hpar >> s) & 1, p.wait_ns);
-                for (int s = 0; s < C::WS; ++s)
-                    if (wiss & (1u << s)) mbar_wait_timed(&wfull[s], (wpar >> s) & 1, p.wait_ns);
+            if (!ok || res_issued) {  // copies in flight must land before the CTA exits
+                if (res_issued) mbar_wait_timed(wres, 0, p.wait_ns);
+                if (!ok) {
+                    for (int s = 0; s < C::HS; ++s)
+                        if (hiss & (1u << s)) mbar_wait_timed(&hfull[s], (hpar >> s) & 1, p.wait_ns);
+                    for (int s = 0; s < C::WS; ++s)
+                        if (wiss & (1u << s)) mbar_wait_timed(&wfull[s], (wpar >> s) & 1, p.wait_ns);
+                }
             }
         }
     } else if (warp == 1) {
@@ -279,7 +173,9 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t hph = 0, wph = 0, local = 0;
             bool ok = true;
             const uint64_t adesc0 = sdesc(smem_u32(hring), 16, C::SBO_A, C::SWZ);
-            const uint64_t bdesc0 = sdesc(smem_u32(wring), 16, C::SBO_B, C::SWZ);
+            const uint64_t bdesc0 = sdesc(smem_u32(wsm), 16, C::SBO_B, C::SWZ);
+            if (RES && blockIdx.x < p.num_tiles)
+                ok = mbar_wait(wres, 0, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL);
             for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++local) {
                 const uint32_t acc = local & 1, use = local >> 1;
                 if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_TMEM_EMPTY)) {
@@ -294,27 +190,39 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     const uint64_t ah = adesc0 + ((hs * C::HALO_STRIDE) >> 4);
-                    for (int tap = 0; tap < 27; ++tap) {
-                        const int kd = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
-                        if (!mbar_wait(&wfull[ws], wph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
-                            ok = false;
-                            break;
+                    for (int g = 0; g < 27 / C::TPS; ++g) {
+                        uint64_t bg;
+                        if (RES) {
+                            bg = bdesc0 + (((ch * 27 + g * C::TPS) * C::W_BYTES) >> 4);
+                        } else {
+                            if (!mbar_wait(&wfull[ws], wph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                                ok = false;
+                                break;
+                            }
+                            bg = bdesc0 + ((ws * C::TPS * C::W_BYTES) >> 4);
                         }
                         tc_fence_after();
-                        const uint64_t bw = bdesc0 + ((ws * C::W_BYTES) >> 4);
 #pragma unroll
-                        for (int k = 0; k < KC / 16; ++k) {
+                        for (int u = 0; u < C::TPS; ++u) {
+                            const int tap = g * C::TPS + u;
+                            const int kd = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
+                            const uint64_t bw = bg + ((u * C::W_BYTES) >> 4);
 #pragma unroll
-                            for (int i = 0; i < 2; ++i) {
-                                const uint32_t row = ((i + kd) * HH_H + kh) * HH_W + kw;
-                                const uint64_t ad = ah + ((row * C::ROW + k * 32) >> 4);
-                                umma_bf16(d0 + i * BN, ad, bw + ((k * 32) >> 4), C::IDESC, (ch | tap | k) != 0);
+                            for (int k = 0; k < KC / 16; ++k) {
+#pragma unroll
+                                for (int i = 0; i < 2; ++i) {
+                                    const uint32_t row = ((i + kd) * HH_H + kh) * HH_W + kw;
+                                    const uint64_t ad = ah + ((row * C::ROW + k * 32) >> 4);
+                                    umma_bf16(d0 + i * BN, ad, bw + ((k * 32) >> 4), C::IDESC, (ch | tap | k) != 0);
+                                }
                             }
                         }
-                        umma_commit(&wempty[ws]);
-                        if (++ws == C::WS) {
-                            ws = 0;
-                            wph ^= 1;
+                        if (!RES) {
+                            umma_commit(&wempty[ws]);
+                            if (++ws == C::WS) {
+                                ws = 0;
+                                wph ^= 1;
+                            }
                         }
                     }
                     if (!ok) break;
@@ -359,9 +267,9 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------
 // host side
 
-template <int BN, int KC, int EPI>
+template <int BN, int KC, int EPI, bool RES>
 static cf_status run_halo(const LaunchCtx& ctx, HaloParams p, const uint16_t* x, const uint16_t* wk) {
-    using C = HaloCfg<BN, KC, EPI>;
+    using C = HaloCfg<BN, KC, EPI, RES>;
     CUtensorMap tx, tw;
     const uint64_t dx[5] = {(uint64_t)p.Cin, (uint64_t)p.W, (uint64_t)p.H, (uint64_t)p.D, (uint64_t)p.N};
     const uint64_t sx[4] = {(uint64_t)p.Cin * 2, (uint64_t)p.W * p.Cin * 2, (uint64_t)p.H * p.W * p.Cin * 2,
@@ -374,20 +282,22 @@ static cf_status run_halo(const LaunchCtx& ctx, HaloParams p, const uint16_t* x,
     const uint32_t bw[2] = {(uint32_t)KC, (uint32_t)BN};
     if (!encode_tmap(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wk, dw, sw, bw, swz)) return CF_ERR_CUDA;
     p.n_chunks = p.Cin / KC;
-    auto kern = conv_halo_kernel<BN, KC, EPI>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    const uint32_t smem = C::smem_bytes(p.n_chunks);
+    if (smem > 227 * 1024) return CF_ERR_UNSUPPORTED;
+    auto kern = conv_halo_kernel<BN, KC, EPI, RES>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return CF_ERR_CUDA;
-    const int grid = grid_for(kern, C::SMEM, 192, ctx.num_sms, p.num_tiles, C::TMEM_COLS);
-    kern<<<grid, 192, C::SMEM, ctx.stream>>>(tx, tw, p);
+    const int grid = grid_for(kern, smem, 192, ctx.num_sms, p.num_tiles, C::TMEM_COLS);
+    kern<<<grid, 192, smem, ctx.stream>>>(tx, tw, p);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
-template <int BN, int KC>
+template <int BN, int KC, bool RES>
 static cf_status halo_epi(const LaunchCtx& ctx, const HaloParams& p, const uint16_t* x, const uint16_t* wk, int epi) {
     switch (epi) {
-        case EPI_PLAIN: return run_halo<BN, KC, EPI_PLAIN>(ctx, p, x, wk);
-        case EPI_POOL: return run_halo<BN, KC, EPI_POOL>(ctx, p, x, wk);
-        case EPI_DGRAD: return run_halo<BN, KC, EPI_DGRAD>(ctx, p, x, wk);
+        case EPI_PLAIN: return run_halo<BN, KC, EPI_PLAIN, RES>(ctx, p, x, wk);
+        case EPI_POOL: return run_halo<BN, KC, EPI_POOL, RES>(ctx, p, x, wk);
+        case EPI_DGRAD: return run_halo<BN, KC, EPI_DGRAD, RES>(ctx, p, x, wk);
     }
     return CF_ERR_INVALID_ARG;
 }
@@ -419,12 +329,12 @@ cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
     p.ea = EpiArgs{y, idx, bias, x_act, slope};
     p.status = ctx.status;
     p.wait_ns = ctx.wait_ns;
-    // 64-channel chunks (SW128) when they fit twice in shared memory next to a
-    // filter ring, 32-channel chunks (SW64) otherwise
-    const bool kc64 = (c_in % 64 == 0);
+    // The whole filter stays in shared memory when it fits beside two halo
+    // stages of 32-channel chunks; otherwise it streams 3 taps per stage.
+    const bool resident = (size_t)27 * c_in * c_out * 2 + 2 * 46080 + 4096 <= (size_t)227 * 1024;
     switch (c_out) {
-        case 32: return kc64 ? halo_epi<32, 64>(ctx, p, x, wk, epi) : halo_epi<32, 32>(ctx, p, x, wk, epi);
-        case 64: return kc64 ? halo_epi<64, 64>(ctx, p, x, wk, epi) : halo_epi<64, 32>(ctx, p, x, wk, epi);
+        case 32: return resident ? halo_epi<32, 32, true>(ctx, p, x, wk, epi) : halo_epi<32, 32, false>(ctx, p, x, wk, epi);
+        case 64: return resident ? halo_epi<64, 32, true>(ctx, p, x, wk, epi) : halo_epi<64, 32, false>(ctx, p, x, wk, epi);
     }
     return CF_ERR_UNSUPPORTED;
 }

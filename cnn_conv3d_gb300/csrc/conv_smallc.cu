@@ -2,23 +2,26 @@
 // or 4; CosmoFlow input: four redshift channels) as an implicit GEMM whose A
 // operand lives in tensor memory.
 //
-// GEMM view as in conv_fwd.cu: D[m, co] = sum_k A[m, k] * W[co, k] with
-// m = voxel of a 128-voxel tile (box 2 x th x tw) and k = 4*t + ci
+// GEMM view: D[m, co] = sum_k A[m, k] * W[co, k] with k = 4*t + ci
 // (t = 9*kd + 3*kh + kw), K = 27*c_in padded to 112 (c_in 4) or 32 (c_in 1).
+// Output tile: 2 planes x 16 lines x 8 voxels, two M=128 accumulators (one
+// per plane, row r = 8*line + voxel), as in conv_halo.cu.
 //
 // With only 8 (or 2) bytes per voxel, an im2col tile in shared memory would
 // be written and read once per tap and bound the kernel by shared-memory
 // bandwidth.  Instead:
 //   warp 0      : TMA of the tile's input halo (one box of the input viewed as
-//                 (W*C, H, D, N); 4.6 KB for a 2 x 2 x 32 tile) into a ring;
-//   warps 2..5  : builders: each thread gathers the im2col row of its voxel
-//                 from the halo (centre voxels from shared memory, w-1 / w+1
-//                 neighbours by warp shuffles) and writes it into a tensor-
-//                 memory A buffer with tcgen05.st (lane = voxel);
+//                 (W*C, H, D, N): 4 planes x 18 lines x (8 + 2*margin) voxels,
+//                 zero outside the volume) into a ring;
+//   warps 2..5  : builders: each thread gathers the im2col rows of its (line,
+//                 voxel) for both planes from the halo (centre voxels from
+//                 shared memory, w-1 / w+1 neighbours by warp shuffles) and
+//                 writes them into a tensor-memory A buffer with tcgen05.st;
 //   warp 1      : tcgen05.mma with A from tensor memory and the filter
 //                 (resident in shared memory, K-major SW128) as B;
-//   warps 6..9  : the same epilogues as the generic kernel (fused bias +
-//                 leaky ReLU + 2x2x2 max-pool with argmax, or plain bf16).
+//   warps 6..9  : the epilogues of halo_common.cuh (fused bias + leaky ReLU +
+//                 2x2x2 max-pool with argmax by warp shuffles, or plain bf16).
+#include "halo_common.cuh"
 #include "smallc_common.cuh"
 
 namespace cf {
@@ -27,42 +30,110 @@ template <int CIN, int BN, int EPI>
 struct SmallTmCfg {
     static constexpr int KREAL = 27 * CIN;
     static constexpr int KP = (KREAL + 15) / 16 * 16;  // 112 or 32
-    static constexpr int KCOLS = CIN == 4 ? 56 : 16;   // TMEM columns of one A row (bf16 pairs)
-    static constexpr int KSTRIDE = CIN == 4 ? 64 : 16; // TMEM columns between A stages
     static constexpr int KSTEPS = KP / 16;
+    static constexpr int PCOLS = CIN == 4 ? 64 : 16;   // TMEM columns per plane's A rows (56 / 16 used)
+    static constexpr int ASTRIDE = 2 * PCOLS;          // TMEM columns per A stage (two planes)
     static constexpr int ATOMS = (KP + 63) / 64;
     static constexpr uint32_t B_BYTES = BN * 128 * ATOMS;
-    static constexpr uint32_t HALO_MAX = 4096 + 1024;  // >= halo_bytes() of every tile shape, 1 KB aligned
-    static constexpr int HS = 4;                       // halo ring stages
-    static constexpr int AST = 4;                      // TMEM A stages
-    static constexpr int NACC = (2 * BN + AST * KSTRIDE <= 512) ? 2 : 1;
-    static constexpr uint32_t STG_BYTES = EPI == EPI_POOL ? 128 * 33 * 4 : 0;
+    static constexpr int HALO_BYTES = 4 * 18 * (8 + 2 * (16 / (2 * CIN))) * CIN * 2;  // 6912 or 3456
+    static constexpr uint32_t HALO_STRIDE = (HALO_BYTES + 1023) / 1024 * 1024;
+    static constexpr int HS = 4;
+    static constexpr int NACC = (4 * BN + 2 * ASTRIDE <= 512) ? 2 : 1;
+    static constexpr int AST_RAW = (512 - 2 * NACC * BN) / ASTRIDE;
+    static constexpr int AST = AST_RAW > 4 ? 4 : AST_RAW;
     static constexpr uint32_t BAR_BYTES = 256;
-    static constexpr uint32_t SMEM = 1024 + B_BYTES + HS * HALO_MAX + STG_BYTES + BAR_BYTES;
+    static constexpr uint32_t SMEM = 1024 + B_BYTES + HS * HALO_STRIDE + BAR_BYTES;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t ACOL0 = NACC * BN;
+    static constexpr uint32_t ACOL0 = 2 * NACC * BN;
     static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
-    static_assert(NACC * BN + AST * KSTRIDE <= 512, "tensor memory budget");
+    static_assert(AST >= 2, "tensor memory budget");
 };
 
 struct SmallTmParams {
-    ConvGeom g;
+    HaloParams hp;
     const uint16_t* w;  // [Cout][27*CIN]
-    EpiArgs ea;
-    int* status;
-    uint64_t wait_ns;
 };
+
+// Gathers, for the thread's (line j, voxel l), the 12 halo values of planes
+// 0..3 x rows j..j+2 at voxel l-1, l, l+1 (c_in = 4: 8 bytes each) and packs
+// the im2col rows of plane 0 (planes 0..2) and plane 1 (planes 1..3).
+__device__ __forceinline__ void gather_two_planes_c4(const uint8_t* halo, int j, int l, uint32_t (&r0)[56],
+                                                     uint32_t (&r1)[56]) {
+    constexpr int PITCH = 12 * 8;  // (8 + 2*2) voxels x 8 bytes
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+#pragma unroll
+        for (int kh = 0; kh < 3; ++kh) {
+            const uint8_t* line = halo + (P * 18 + j + kh) * PITCH;
+            const uint2 mid = *reinterpret_cast<const uint2*>(line + (l + 2) * 8);
+            uint2 left, right;
+            left.x = __shfl_up_sync(0xffffffffu, mid.x, 1);
+            left.y = __shfl_up_sync(0xffffffffu, mid.y, 1);
+            right.x = __shfl_down_sync(0xffffffffu, mid.x, 1);
+            right.y = __shfl_down_sync(0xffffffffu, mid.y, 1);
+            if (l == 0) left = *reinterpret_cast<const uint2*>(line + (l + 1) * 8);
+            if (l == 7) right = *reinterpret_cast<const uint2*>(line + (l + 3) * 8);
+            // plane 0 uses kd = P (P <= 2), plane 1 uses kd = P - 1 (P >= 1)
+            if (P <= 2) {
+                const int t0 = P * 9 + kh * 3;
+                r0[2 * t0 + 0] = left.x;
+                r0[2 * t0 + 1] = left.y;
+                r0[2 * t0 + 2] = mid.x;
+                r0[2 * t0 + 3] = mid.y;
+                r0[2 * t0 + 4] = right.x;
+                r0[2 * t0 + 5] = right.y;
+            }
+            if (P >= 1) {
+                const int t0 = (P - 1) * 9 + kh * 3;
+                r1[2 * t0 + 0] = left.x;
+                r1[2 * t0 + 1] = left.y;
+                r1[2 * t0 + 2] = mid.x;
+                r1[2 * t0 + 3] = mid.y;
+                r1[2 * t0 + 4] = right.x;
+                r1[2 * t0 + 5] = right.y;
+            }
+        }
+    }
+    r0[54] = r0[55] = 0u;
+    r1[54] = r1[55] = 0u;
+}
+
+// c_in = 1: 27 taps padded to 32 per plane (16 words).
+__device__ __forceinline__ void gather_two_planes_c1(const uint8_t* halo, int j, int l, uint32_t (&r0)[56],
+                                                     uint32_t (&r1)[56]) {
+    constexpr int PITCH = 24 * 2;  // (8 + 2*8) voxels x 2 bytes
+    uint32_t v0[32], v1[32];
+#pragma unroll
+    for (int t = 27; t < 32; ++t) v0[t] = v1[t] = 0u;
+#pragma unroll
+    for (int P = 0; P < 4; ++P)
+#pragma unroll
+        for (int kh = 0; kh < 3; ++kh) {
+            const uint16_t* line = reinterpret_cast<const uint16_t*>(halo + (P * 18 + j + kh) * PITCH);
+#pragma unroll
+            for (int kw = 0; kw < 3; ++kw) {
+                const uint32_t val = line[l + 8 + kw - 1];
+                if (P <= 2) v0[P * 9 + kh * 3 + kw] = val;
+                if (P >= 1) v1[(P - 1) * 9 + kh * 3 + kw] = val;
+            }
+        }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        r0[q] = v0[2 * q] | (v0[2 * q + 1] << 16);
+        r1[q] = v1[2 * q] | (v1[2 * q + 1] << 16);
+    }
+}
 
 template <int CIN, int BN, int EPI>
 __global__ void __launch_bounds__(320, 1)
-    conv_smallc_kernel(const __grid_constant__ CUtensorMap tmH, const SmallTmParams p) {
+    conv_smallc_kernel(const __grid_constant__ CUtensorMap tmH, const SmallTmParams sp) {
     using C = SmallTmCfg<CIN, BN, EPI>;
+    const HaloParams& p = sp.hp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* bsm = smem;
     uint8_t* hring = smem + C::B_BYTES;
-    float* stg = reinterpret_cast<float*>(hring + C::HS * C::HALO_MAX);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(hring + C::HS * C::HALO_MAX + C::STG_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(hring + C::HS * C::HALO_STRIDE);
     uint64_t* hfull = bars;
     uint64_t* hempty = hfull + C::HS;
     uint64_t* afull = hempty + C::HS;
@@ -75,8 +146,6 @@ __global__ void __launch_bounds__(320, 1)
     volatile int* epi_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const ConvGeom& g = p.g;
-    const uint32_t halo_tx = (uint32_t)halo_bytes(g.tw, g.th, g.td, CIN);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::HS; ++s) {
@@ -96,23 +165,28 @@ __global__ void __launch_bounds__(320, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmH);
     }
-    // resident filter: rows co < BN (zero at and above Cout), K padded with zeros,
-    // SW128 K-major atoms of 64 K-elements (atom a at a * BN * 128 bytes)
-    for (int e = threadIdx.x; e < BN * (C::ATOMS * 8); e += blockDim.x) {
-        const int r = e / (C::ATOMS * 8), c = e % (C::ATOMS * 8);
-        uint32_t v[4] = {0u, 0u, 0u, 0u};
+    // resident filter of the CTA's N tile: rows co0 .. co0+BN-1 (zero at and
+    // above Cout), K padded with zeros, SW128 K-major atoms of 64 K-elements.
+    // Tiles are dealt with stride gridDim.x and the launch makes gridDim.x a
+    // multiple of n_ntiles, so every tile of this CTA has the same N tile.
+    {
+        const int co0 = (blockIdx.x % p.n_ntiles) * BN;
+        for (int e = threadIdx.x; e < BN * (C::ATOMS * 8); e += blockDim.x) {
+            const int r = e / (C::ATOMS * 8), c = e % (C::ATOMS * 8);
+            uint32_t v[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int k8 = 0; k8 < 8; ++k8) {
-            const int k = c * 8 + k8;
-            uint32_t bits = 0;
-            if (r < g.Cout && k < C::KREAL) bits = p.w[(int64_t)r * C::KREAL + k];
-            v[k8 >> 1] |= bits << (16 * (k8 & 1));
+            for (int k8 = 0; k8 < 8; ++k8) {
+                const int k = c * 8 + k8;
+                uint32_t bits = 0;
+                if (co0 + r < p.Cout && k < C::KREAL) bits = sp.w[(int64_t)(co0 + r) * C::KREAL + k];
+                v[k8 >> 1] |= bits << (16 * (k8 & 1));
+            }
+            const int atom = c >> 3, cin_atom = c & 7;
+            *reinterpret_cast<uint4*>(bsm + atom * (BN * 128) + r * 128 + ((cin_atom ^ (r & 7)) << 4)) =
+                make_uint4(v[0], v[1], v[2], v[3]);
         }
-        const int atom = c >> 3, cin_atom = c & 7;
-        *reinterpret_cast<uint4*>(bsm + atom * (BN * 128) + r * 128 + ((cin_atom ^ (r & 7)) << 4)) =
-            make_uint4(v[0], v[1], v[2], v[3]);
+        fence_proxy_async_smem();
     }
-    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(tmem_holder, C::TMEM_COLS);
         tmem_relinquish();
@@ -128,14 +202,14 @@ __global__ void __launch_bounds__(320, 1)
             int hs = 0;
             uint32_t hph = 0, issued = 0, par = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
-                const TileCoord tc = decode_tile(g, tile, BN);
+            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+                const HTile t = halo_decode(p, tile, BN);
                 if (!mbar_wait(&hempty[hs], hph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&hfull[hs], halo_tx);
-                load_halo<CIN>(hring + hs * C::HALO_MAX, &tmH, &hfull[hs], tc.n, tc.d0, tc.h0, tc.w0);
+                mbar_arrive_expect_tx(&hfull[hs], (uint32_t)C::HALO_BYTES);
+                load_halo<CIN>(hring + hs * C::HALO_STRIDE, &tmH, &hfull[hs], t.n, t.d0, t.h0, t.w0);
                 issued |= 1u << hs;
                 par = (par & ~(1u << hs)) | (hph << hs);
                 if (++hs == C::HS) {
@@ -155,7 +229,7 @@ __global__ void __launch_bounds__(320, 1)
             uint32_t aph = 0, local = 0;
             bool ok = true;
             const uint32_t b_addr = smem_u32(bsm);
-            for (int tile = blockIdx.x; tile < g.num_tiles && ok; tile += gridDim.x, ++local) {
+            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++local) {
                 const uint32_t acc = C::NACC == 2 ? (local & 1) : 0u;
                 const uint32_t use = C::NACC == 2 ? (local >> 1) : local;
                 if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_TMEM_EMPTY)) {
@@ -167,13 +241,15 @@ __global__ void __launch_bounds__(320, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
-                const uint32_t a_tmem = tmem_base + C::ACOL0 + as * C::KSTRIDE;
+                const uint32_t d_tmem = tmem_base + acc * 2 * BN;
+                const uint32_t a_tmem = tmem_base + C::ACOL0 + as * C::ASTRIDE;
 #pragma unroll
                 for (int k = 0; k < C::KSTEPS; ++k) {
                     const uint32_t atom = k >> 2, koff = (k & 3) * 32;
                     const uint64_t bd = sdesc(b_addr + atom * (BN * 128) + koff, 16, 1024, SWZ_128B);
-                    umma_bf16_tmem_a(d_tmem, a_tmem + 8 * k, bd, C::IDESC, k != 0);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        umma_bf16_tmem_a(d_tmem + i * BN, a_tmem + i * C::PCOLS + 8 * k, bd, C::IDESC, k != 0);
                 }
                 umma_commit(&aempty[as]);
                 umma_commit(&tfull[acc]);
@@ -188,36 +264,40 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
     } else if (warp < 6) {
-        // ---------------- builders: one voxel row per thread, TMEM lanes 32*q ..
+        // ---------------- builders: rows of both planes for (line j, voxel l)
         const int q = warp & 3;
-        const int row = q * 32 + lane;
-        const int l = row % g.tw, j = (row / g.tw) % g.th, i = row / (g.tw * g.th);
+        const int r = q * 32 + lane;
+        const int j = r >> 3, l = r & 7;
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + C::ACOL0;
         int hs = 0, as = 0;
         uint32_t hph = 0, aph = 0;
-        for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
             // every lane waits, and the warp leaves together if any lane gave up, so
             // the shuffles and .sync.aligned tensor-memory stores below always see
             // the full warp
             if (!__all_sync(0xffffffffu, mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)))
                 break;
-            uint32_t wd[56];
+            uint32_t r0[56], r1[56];
             if (CIN == 4)
-                gather_row_c4(hring + hs * C::HALO_MAX, g.tw, g.th, i, j, l, wd);
+                gather_two_planes_c4(hring + hs * C::HALO_STRIDE, j, l, r0, r1);
             else
-                gather_row_c1(hring + hs * C::HALO_MAX, g.tw, g.th, i, j, l, wd);
+                gather_two_planes_c1(hring + hs * C::HALO_STRIDE, j, l, r0, r1);
             mbar_arrive(&hempty[hs]);
             if (!__all_sync(0xffffffffu,
                             mbar_wait(&aempty[as], aph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)))
                 break;
             tc_fence_after();
-            const uint32_t ta = lane_addr + as * C::KSTRIDE;
+            const uint32_t ta = lane_addr + as * C::ASTRIDE;
             if (CIN == 4) {
-                tmem_st32(ta, wd);
-                tmem_st16(ta + 32, wd + 32);
-                tmem_st8(ta + 48, wd + 48);
+                tmem_st32(ta, r0);
+                tmem_st16(ta + 32, r0 + 32);
+                tmem_st8(ta + 48, r0 + 48);
+                tmem_st32(ta + C::PCOLS, r1);
+                tmem_st16(ta + C::PCOLS + 32, r1 + 32);
+                tmem_st8(ta + C::PCOLS + 48, r1 + 48);
             } else {
-                tmem_st16(ta, wd);
+                tmem_st16(ta, r0);
+                tmem_st16(ta + C::PCOLS, r1);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -236,13 +316,13 @@ __global__ void __launch_bounds__(320, 1)
         const int q = warp & 3;
         const int et = threadIdx.x - 192;
         uint32_t local = 0;
-        for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x, ++local) {
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const uint32_t acc = C::NACC == 2 ? (local & 1) : 0u;
             const uint32_t use = C::NACC == 2 ? (local >> 1) : local;
             if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
             tc_fence_after();
-            const TileCoord tc = decode_tile(g, tile, BN);
-            conv_epilogue<BN, EPI>(g, tc, p.ea, tmem_base, acc * BN, q, lane, et, stg);
+            const HTile t = halo_decode(p, tile, BN);
+            halo_epilogue<BN, EPI>(p, t, tmem_base, acc * 2 * BN, q, lane);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
@@ -267,31 +347,25 @@ bool make_halo_map(CUtensorMap* m, const uint16_t* x, int n, int d, int h, int w
 }
 
 template <int CIN, int BN, int EPI>
-static cf_status run_smallc(const LaunchCtx& ctx, const ConvGeom& g, const uint16_t* x, const uint16_t* wk,
-                            const EpiArgs& ea) {
+static cf_status run_smallc(const LaunchCtx& ctx, const HaloParams& hp, const uint16_t* x, const uint16_t* wk) {
     using C = SmallTmCfg<CIN, BN, EPI>;
-    if (halo_bytes(g.tw, g.th, g.td, CIN) > (int)C::HALO_MAX) return CF_ERR_UNSUPPORTED;
     CUtensorMap th;
-    if (!make_halo_map(&th, x, g.N, g.D, g.H, g.W, CIN, g.tw, g.th, g.td)) return CF_ERR_CUDA;
-    SmallTmParams p;
-    p.g = g;
-    p.w = wk;
-    p.ea = ea;
-    p.status = ctx.status;
-    p.wait_ns = ctx.wait_ns;
+    if (!make_halo_map(&th, x, hp.N, hp.D, hp.H, hp.W, CIN, HT_W, HT_H, HT_D)) return CF_ERR_CUDA;
+    SmallTmParams sp{hp, wk};
     auto kern = conv_smallc_kernel<CIN, BN, EPI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return CF_ERR_CUDA;
-    const int grid = grid_for(kern, C::SMEM, 320, ctx.num_sms, g.num_tiles, C::TMEM_COLS);
-    kern<<<grid, 320, C::SMEM, ctx.stream>>>(th, p);
+    int grid = grid_for(kern, C::SMEM, 320, ctx.num_sms, hp.num_tiles, C::TMEM_COLS);
+    grid = std::max(hp.n_ntiles, grid / hp.n_ntiles * hp.n_ntiles);  // each CTA keeps one N tile
+    kern<<<grid, 320, C::SMEM, ctx.stream>>>(th, sp);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
 template <int CIN, int BN>
-static cf_status smallc_epi(const LaunchCtx& ctx, const ConvGeom& g, const uint16_t* x, const uint16_t* wk, int epi,
-                            const EpiArgs& ea) {
-    if (epi == EPI_POOL) return run_smallc<CIN, BN, EPI_POOL>(ctx, g, x, wk, ea);
-    if (epi == EPI_PLAIN) return run_smallc<CIN, BN, EPI_PLAIN>(ctx, g, x, wk, ea);
+static cf_status smallc_epi(const LaunchCtx& ctx, const HaloParams& hp, const uint16_t* x, const uint16_t* wk,
+                            int epi) {
+    if (epi == EPI_POOL) return run_smallc<CIN, BN, EPI_POOL>(ctx, hp, x, wk);
+    if (epi == EPI_PLAIN) return run_smallc<CIN, BN, EPI_PLAIN>(ctx, hp, x, wk);
     return CF_ERR_UNSUPPORTED;
 }
 
@@ -301,21 +375,37 @@ cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t
     if (c_out % 8 != 0 || c_out > 256) return CF_ERR_UNSUPPORTED;
     if (c_in != 1 && c_in != 4) return CF_ERR_UNSUPPORTED;
     if ((w * c_in) % 8 != 0) return CF_ERR_UNSUPPORTED;  // halo rows must be 16-byte multiples
-    const int bn = (c_out + 15) / 16 * 16;
-    EpiArgs ea{y, idx, bias, nullptr, slope};
-    ConvGeom g = make_geom(n, d, h, w, c_in, c_out, bn);
-    g.n_ntiles = 1;
-    g.num_tiles = (int)(n * g.tiles_d * g.tiles_h * g.tiles_w);
-#define CF_SC_CASE(B)                                                              \
-    case B:                                                                        \
-        return c_in == 4 ? smallc_epi<4, B>(ctx, g, x, wk, epi, ea)                \
-                         : smallc_epi<1, B>(ctx, g, x, wk, epi, ea);
+    // N tile: c_out rounded up to 16, at most 128 (two N tiles above that)
+    const int bn = c_out <= 128 ? (c_out + 15) / 16 * 16 : 128;
+    HaloParams hp;
+    hp.N = (int)n;
+    hp.D = (int)d;
+    hp.H = (int)h;
+    hp.W = (int)w;
+    hp.Cin = c_in;
+    hp.Cout = c_out;
+    hp.tiles_w = (int)((w + HT_W - 1) / HT_W);
+    hp.tiles_h = (int)((h + HT_H - 1) / HT_H);
+    hp.tiles_d = (int)((d + HT_D - 1) / HT_D);
+    hp.n_ntiles = (c_out + bn - 1) / bn;
+    hp.num_tiles = (int)(n * hp.tiles_d * hp.tiles_h * hp.tiles_w * hp.n_ntiles);
+    hp.n_chunks = 1;
+    hp.ea = EpiArgs{y, idx, bias, nullptr, slope};
+    hp.status = ctx.status;
+    hp.wait_ns = ctx.wait_ns;
+#define CF_SC_CASE(B)                                                        \
+    case B:                                                                  \
+        return c_in == 4 ? smallc_epi<4, B>(ctx, hp, x, wk, epi)             \
+                         : smallc_epi<1, B>(ctx, hp, x, wk, epi);
     switch (bn) {
         CF_SC_CASE(16)
         CF_SC_CASE(32)
+        CF_SC_CASE(48)
         CF_SC_CASE(64)
+        CF_SC_CASE(80)
+        CF_SC_CASE(96)
+        CF_SC_CASE(112)
         CF_SC_CASE(128)
-        CF_SC_CASE(256)
         default: return CF_ERR_UNSUPPORTED;
     }
 #undef CF_SC_CASE

@@ -1,0 +1,146 @@
+// halo_common.cuh -- output-tile shape and epilogue shared by the kernels
+// that compute a 2 x 16 x 8 voxel tile as two M=128 accumulators (one per
+// plane, row r = 8*line + voxel): the halo-tile implicit GEMM (conv_halo.cu)
+// and the small-channel first layer (conv_smallc.cu).
+#pragma once
+
+#include "conv_common.cuh"
+
+namespace cf {
+
+constexpr int HT_W = 8, HT_H = 16, HT_D = 2;                 // output tile
+constexpr int HH_W = HT_W + 2, HH_H = HT_H + 2, HH_D = HT_D + 2;  // halo box
+constexpr int H_ROWS = HH_W * HH_H * HH_D;                   // 720
+
+struct HaloParams {
+    int N, D, H, W, Cin, Cout;
+    int tiles_w, tiles_h, tiles_d, n_ntiles, num_tiles, n_chunks;
+    EpiArgs ea;
+    int* status;
+    uint64_t wait_ns;
+};
+
+struct HTile {
+    int n, d0, h0, w0, co0;
+};
+
+__device__ __forceinline__ HTile halo_decode(const HaloParams& p, int tile, int bn) {
+    HTile t;
+    const int nt = tile % p.n_ntiles;
+    int m = tile / p.n_ntiles;
+    const int tw = m % p.tiles_w;
+    m /= p.tiles_w;
+    const int th = m % p.tiles_h;
+    m /= p.tiles_h;
+    const int td = m % p.tiles_d;
+    t.n = m / p.tiles_d;
+    t.w0 = tw * HT_W;
+    t.h0 = th * HT_H;
+    t.d0 = td * HT_D;
+    t.co0 = nt * bn;
+    return t;
+}
+
+// (value, code) pair of the first maximum: larger value wins, equal values
+// keep the smaller code.
+__device__ __forceinline__ void pool_combine(float& v, int& k, float v2, int k2) {
+    if (v2 > v || (v2 == v && k2 < k)) {
+        v = v2;
+        k = k2;
+    }
+}
+
+template <int BN, int EPI>
+__device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& t, uint32_t tmem_base,
+                                              uint32_t acc_col, int q, int lane) {
+    constexpr int CH = BN >= 32 ? 32 : 16;  // accumulator columns per pass
+    const int r = q * 32 + lane;
+    const int j = r >> 3, l = r & 7;
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
+    const int h = t.h0 + j, w = t.w0 + l;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += CH) {
+        uint32_t a0[32], a1[32];
+        if (CH == 32) {
+            tmem_ld32(lane_addr + c, a0);
+            tmem_ld32(lane_addr + BN + c, a1);
+        } else {
+            tmem_ld16(lane_addr + c, a0);
+            tmem_ld16(lane_addr + BN + c, a1);
+        }
+        tmem_ld_wait();
+        // channels of this pass that exist (c_out is a multiple of 8)
+        const int nvalid = min(CH, p.Cout - (t.co0 + c));
+        if (EPI == EPI_POOL) {
+            const int D2 = p.D >> 1, H2 = p.H >> 1, W2 = p.W >> 1;
+            const int pd = t.d0 >> 1, ph = h >> 1, pw = w >> 1;
+            const bool writer = ((j | l) & 1) == 0 && pd < D2 && ph < H2 && pw < W2;
+            const int kbase = (j & 1) * 2 + (l & 1);
+            uint32_t ybits[CH / 2];
+            uint32_t codes[CH / 4];
+#pragma unroll
+            for (int cc = 0; cc < CH; ++cc) {
+                float v = __uint_as_float(a0[cc]);
+                int k = kbase;
+                pool_combine(v, k, __uint_as_float(a1[cc]), kbase + 4);
+                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 1), __shfl_xor_sync(0xffffffffu, k, 1));
+                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 8), __shfl_xor_sync(0xffffffffu, k, 8));
+                const int co = t.co0 + c + cc;
+                const float s = v + ((p.ea.bias != nullptr && co < p.Cout) ? p.ea.bias[co] : 0.f);
+                const float y = s > 0.f ? s : p.ea.slope * s;
+                const uint32_t yb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y));
+                if (cc & 1)
+                    ybits[cc >> 1] |= yb << 16;
+                else
+                    ybits[cc >> 1] = yb;
+                if ((cc & 3) == 0) codes[cc >> 2] = 0;
+                codes[cc >> 2] |= (uint32_t)k << (8 * (cc & 3));
+            }
+            if (writer) {
+                const int64_t po = ((((int64_t)t.n * D2 + pd) * H2 + ph) * W2 + pw) * p.Cout + t.co0 + c;
+#pragma unroll
+                for (int g8 = 0; g8 < CH / 8; ++g8) {
+                    if (g8 * 8 >= nvalid) break;
+                    *reinterpret_cast<uint4*>(p.ea.y + po + 8 * g8) =
+                        make_uint4(ybits[4 * g8], ybits[4 * g8 + 1], ybits[4 * g8 + 2], ybits[4 * g8 + 3]);
+                    if (p.ea.idx)
+                        *reinterpret_cast<uint2*>(p.ea.idx + po + 8 * g8) = make_uint2(codes[2 * g8], codes[2 * g8 + 1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int d = t.d0 + i;
+                if (d >= p.D || h >= p.H || w >= p.W) continue;
+                const int64_t o = ((((int64_t)t.n * p.D + d) * p.H + h) * p.W + w) * p.Cout + t.co0 + c;
+                const uint32_t* a = i == 0 ? a0 : a1;
+#pragma unroll
+                for (int q8 = 0; q8 < CH / 8; ++q8) {
+                    if (q8 * 8 >= nvalid) break;
+                    float v[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(a[q8 * 8 + k]);
+                    if (EPI == EPI_DGRAD) {
+                        const uint4 xa = *reinterpret_cast<const uint4*>(p.ea.x_act + o + q8 * 8);
+                        const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float lo = __uint_as_float(xw[k] << 16);
+                            const float hi = __uint_as_float(xw[k] & 0xFFFF0000u);
+                            v[2 * k] *= (lo > 0.f ? 1.f : p.ea.slope);
+                            v[2 * k + 1] *= (hi > 0.f ? 1.f : p.ea.slope);
+                        }
+                    }
+                    uint4 pk;
+                    pk.x = pack_bf16x2(v[0], v[1]);
+                    pk.y = pack_bf16x2(v[2], v[3]);
+                    pk.z = pack_bf16x2(v[4], v[5]);
+                    pk.w = pack_bf16x2(v[6], v[7]);
+                    *reinterpret_cast<uint4*>(p.ea.y + o + q8 * 8) = pk;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace cf
