@@ -62,6 +62,14 @@ cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t
                              int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
                              uint8_t* idx, const float* bias, float slope);
 
+// conv_wgrad_halo.cu: backward weight reading the input once per K block as a
+// halo tile (c_in 32 with c_out 32/64/128, c_in 64 with c_out 64/128); writes
+// split-K partials [n_splits][c_out][27*c_in].
+bool wgrad_halo_supported(int c_in, int c_out);
+size_t wgrad_halo_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out);
+cf_status launch_wgrad_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
+                            int c_out, const uint16_t* x, const uint16_t* dz, float* part, int* n_splits);
+
 // conv_wgrad.cu -------------------------------------------------------------
 size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out);
 cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,

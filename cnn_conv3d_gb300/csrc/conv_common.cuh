@@ -46,9 +46,9 @@ __device__ __forceinline__ TileCoord decode_tile(const ConvGeom& g, int tile, in
 // then releases the other 127 with a named barrier: a wait that gives up is
 // thus seen by all of them, and none is left behind at a later named barrier.
 __device__ __forceinline__ bool epi_wait(uint64_t* bar, uint32_t parity, int et, volatile int* flag,
-                                         volatile int* abort, uint64_t limit_ns, int* status) {
+                                         volatile int* abort, uint64_t limit_ns, int* status, int nthreads = 128) {
     if (et == 0) *flag = mbar_wait(bar, parity, abort, limit_ns, status, WAIT_EPI_TMEM_FULL) ? 1 : 0;
-    named_bar_sync(2, 128);
+    named_bar_sync(2, nthreads);
     return *flag != 0;
 }
 

@@ -13,14 +13,18 @@
 //   warp 0      : TMA of the tile's input halo (one box of the input viewed as
 //                 (W*C, H, D, N): 4 planes x 18 lines x (8 + 2*margin) voxels,
 //                 zero outside the volume) into a ring;
-//   warps 2..5  : builders: each thread gathers the im2col rows of its (line,
-//                 voxel) for both planes from the halo (centre voxels from
-//                 shared memory, w-1 / w+1 neighbours by warp shuffles) and
-//                 writes them into a tensor-memory A buffer with tcgen05.st;
+//   warps 2..9  : builders (plane 0: warps 2..5, plane 1: warps 6..9): each
+//                 thread gathers the im2col row of its (line, voxel) from the
+//                 halo (centre voxels from shared memory, w-1 / w+1 neighbours
+//                 by warp shuffles) and writes it into a tensor-memory A
+//                 buffer with tcgen05.st;
 //   warp 1      : tcgen05.mma with A from tensor memory and the filter
 //                 (resident in shared memory, K-major SW128) as B;
-//   warps 6..9  : the epilogues of halo_common.cuh (fused bias + leaky ReLU +
-//                 2x2x2 max-pool with argmax by warp shuffles, or plain bf16).
+//   warps 10..17: the epilogues of halo_common.cuh (fused bias + leaky ReLU +
+//                 2x2x2 max-pool with argmax by warp shuffles, or plain bf16),
+//                 two warps per TMEM lane quarter splitting the channels.
+// Every per-tile chain (gather, pooling) is latency-bound, so each role has
+// two warps per SM sub-partition.
 #include "halo_common.cuh"
 #include "smallc_common.cuh"
 
@@ -37,11 +41,11 @@ struct SmallTmCfg {
     static constexpr uint32_t B_BYTES = BN * 128 * ATOMS;
     static constexpr int HALO_BYTES = 4 * 18 * (8 + 2 * (16 / (2 * CIN))) * CIN * 2;  // 6912 or 3456
     static constexpr uint32_t HALO_STRIDE = (HALO_BYTES + 1023) / 1024 * 1024;
-    static constexpr int HS = 4;
+    static constexpr int HS = 12;  // halo stages in flight (TMA latency)
     static constexpr int NACC = (4 * BN + 2 * ASTRIDE <= 512) ? 2 : 1;
     static constexpr int AST_RAW = (512 - 2 * NACC * BN) / ASTRIDE;
     static constexpr int AST = AST_RAW > 4 ? 4 : AST_RAW;
-    static constexpr uint32_t BAR_BYTES = 256;
+    static constexpr uint32_t BAR_BYTES = 8 * (2 * HS + 2 * 4 + 5) + 16;
     static constexpr uint32_t SMEM = 1024 + B_BYTES + HS * HALO_STRIDE + BAR_BYTES;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t ACOL0 = 2 * NACC * BN;
@@ -54,78 +58,48 @@ struct SmallTmParams {
     const uint16_t* w;  // [Cout][27*CIN]
 };
 
-// Gathers, for the thread's (line j, voxel l), the 12 halo values of planes
-// 0..3 x rows j..j+2 at voxel l-1, l, l+1 (c_in = 4: 8 bytes each) and packs
-// the im2col rows of plane 0 (planes 0..2) and plane 1 (planes 1..3).
-__device__ __forceinline__ void gather_two_planes_c4(const uint8_t* halo, int j, int l, uint32_t (&r0)[56],
-                                                     uint32_t (&r1)[56]) {
+// Gathers the im2col row of (plane i, line j, voxel l) from the halo tile:
+// for c_in = 4 the 9 (kd, kh) halo lines at voxel l-1, l, l+1 (8 bytes each),
+// K index k = 4*t + ci, t = 9*kd + 3*kh + kw (54 words + 2 zero words).  The
+// 27 shared-memory loads are independent (no shuffles, no divergent edge
+// cases), so a warp keeps them all in flight.
+__device__ __forceinline__ void gather_plane_c4(const uint8_t* halo, int i, int j, int l, uint32_t (&wd)[56]) {
     constexpr int PITCH = 12 * 8;  // (8 + 2*2) voxels x 8 bytes
+    const uint8_t* base = halo + (i * 18 + j) * PITCH + (l + 1) * 8;
 #pragma unroll
-    for (int P = 0; P < 4; ++P) {
+    for (int kd = 0; kd < 3; ++kd)
 #pragma unroll
-        for (int kh = 0; kh < 3; ++kh) {
-            const uint8_t* line = halo + (P * 18 + j + kh) * PITCH;
-            const uint2 mid = *reinterpret_cast<const uint2*>(line + (l + 2) * 8);
-            uint2 left, right;
-            left.x = __shfl_up_sync(0xffffffffu, mid.x, 1);
-            left.y = __shfl_up_sync(0xffffffffu, mid.y, 1);
-            right.x = __shfl_down_sync(0xffffffffu, mid.x, 1);
-            right.y = __shfl_down_sync(0xffffffffu, mid.y, 1);
-            if (l == 0) left = *reinterpret_cast<const uint2*>(line + (l + 1) * 8);
-            if (l == 7) right = *reinterpret_cast<const uint2*>(line + (l + 3) * 8);
-            // plane 0 uses kd = P (P <= 2), plane 1 uses kd = P - 1 (P >= 1)
-            if (P <= 2) {
-                const int t0 = P * 9 + kh * 3;
-                r0[2 * t0 + 0] = left.x;
-                r0[2 * t0 + 1] = left.y;
-                r0[2 * t0 + 2] = mid.x;
-                r0[2 * t0 + 3] = mid.y;
-                r0[2 * t0 + 4] = right.x;
-                r0[2 * t0 + 5] = right.y;
-            }
-            if (P >= 1) {
-                const int t0 = (P - 1) * 9 + kh * 3;
-                r1[2 * t0 + 0] = left.x;
-                r1[2 * t0 + 1] = left.y;
-                r1[2 * t0 + 2] = mid.x;
-                r1[2 * t0 + 3] = mid.y;
-                r1[2 * t0 + 4] = right.x;
-                r1[2 * t0 + 5] = right.y;
-            }
-        }
-    }
-    r0[54] = r0[55] = 0u;
-    r1[54] = r1[55] = 0u;
-}
-
-// c_in = 1: 27 taps padded to 32 per plane (16 words).
-__device__ __forceinline__ void gather_two_planes_c1(const uint8_t* halo, int j, int l, uint32_t (&r0)[56],
-                                                     uint32_t (&r1)[56]) {
-    constexpr int PITCH = 24 * 2;  // (8 + 2*8) voxels x 2 bytes
-    uint32_t v0[32], v1[32];
-#pragma unroll
-    for (int t = 27; t < 32; ++t) v0[t] = v1[t] = 0u;
-#pragma unroll
-    for (int P = 0; P < 4; ++P)
-#pragma unroll
-        for (int kh = 0; kh < 3; ++kh) {
-            const uint16_t* line = reinterpret_cast<const uint16_t*>(halo + (P * 18 + j + kh) * PITCH);
+        for (int kh = 0; kh < 3; ++kh)
 #pragma unroll
             for (int kw = 0; kw < 3; ++kw) {
-                const uint32_t val = line[l + 8 + kw - 1];
-                if (P <= 2) v0[P * 9 + kh * 3 + kw] = val;
-                if (P >= 1) v1[(P - 1) * 9 + kh * 3 + kw] = val;
+                const uint2 v = *reinterpret_cast<const uint2*>(base + (kd * 18 + kh) * PITCH + kw * 8);
+                const int t = kd * 9 + kh * 3 + kw;
+                wd[2 * t] = v.x;
+                wd[2 * t + 1] = v.y;
             }
+    wd[54] = wd[55] = 0u;
+}
+
+// c_in = 1: 27 taps padded to 32 (16 words).
+__device__ __forceinline__ void gather_plane_c1(const uint8_t* halo, int i, int j, int l, uint32_t (&wd)[56]) {
+    constexpr int PITCH = 24 * 2;  // (8 + 2*8) voxels x 2 bytes
+    uint32_t v[32];
+#pragma unroll
+    for (int t = 27; t < 32; ++t) v[t] = 0u;
+#pragma unroll
+    for (int kd = 0; kd < 3; ++kd)
+#pragma unroll
+        for (int kh = 0; kh < 3; ++kh) {
+            const uint16_t* line = reinterpret_cast<const uint16_t*>(halo + ((i + kd) * 18 + j + kh) * PITCH);
+#pragma unroll
+            for (int kw = 0; kw < 3; ++kw) v[kd * 9 + kh * 3 + kw] = line[l + 8 + kw - 1];
         }
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        r0[q] = v0[2 * q] | (v0[2 * q + 1] << 16);
-        r1[q] = v1[2 * q] | (v1[2 * q + 1] << 16);
-    }
+    for (int q = 0; q < 16; ++q) wd[q] = v[2 * q] | (v[2 * q + 1] << 16);
 }
 
 template <int CIN, int BN, int EPI>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(576, 1)
     conv_smallc_kernel(const __grid_constant__ CUtensorMap tmH, const SmallTmParams sp) {
     using C = SmallTmCfg<CIN, BN, EPI>;
     const HaloParams& p = sp.hp;
@@ -150,15 +124,15 @@ __global__ void __launch_bounds__(320, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::HS; ++s) {
             mbar_init(&hfull[s], 1);
-            mbar_init(&hempty[s], 128);
+            mbar_init(&hempty[s], 256);
         }
         for (int s = 0; s < C::AST; ++s) {
-            mbar_init(&afull[s], 128);
+            mbar_init(&afull[s], 256);
             mbar_init(&aempty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
+            mbar_init(&tempty[a], 256);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -263,12 +237,13 @@ __global__ void __launch_bounds__(320, 1)
                 mbar_wait_timed(drain, 0, p.wait_ns);
             }
         }
-    } else if (warp < 6) {
-        // ---------------- builders: rows of both planes for (line j, voxel l)
+    } else if (warp < 10) {
+        // ---------------- builders: warps 2..5 plane 0, 6..9 plane 1; one row each
         const int q = warp & 3;
+        const int plane = (warp - 2) >> 2;
         const int r = q * 32 + lane;
         const int j = r >> 3, l = r & 7;
-        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + C::ACOL0;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + C::ACOL0 + plane * C::PCOLS;
         int hs = 0, as = 0;
         uint32_t hph = 0, aph = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
@@ -277,11 +252,11 @@ __global__ void __launch_bounds__(320, 1)
             // the full warp
             if (!__all_sync(0xffffffffu, mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)))
                 break;
-            uint32_t r0[56], r1[56];
+            uint32_t wd[56];
             if (CIN == 4)
-                gather_two_planes_c4(hring + hs * C::HALO_STRIDE, j, l, r0, r1);
+                gather_plane_c4(hring + hs * C::HALO_STRIDE, plane, j, l, wd);
             else
-                gather_two_planes_c1(hring + hs * C::HALO_STRIDE, j, l, r0, r1);
+                gather_plane_c1(hring + hs * C::HALO_STRIDE, plane, j, l, wd);
             mbar_arrive(&hempty[hs]);
             if (!__all_sync(0xffffffffu,
                             mbar_wait(&aempty[as], aph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)))
@@ -289,15 +264,11 @@ __global__ void __launch_bounds__(320, 1)
             tc_fence_after();
             const uint32_t ta = lane_addr + as * C::ASTRIDE;
             if (CIN == 4) {
-                tmem_st32(ta, r0);
-                tmem_st16(ta + 32, r0 + 32);
-                tmem_st8(ta + 48, r0 + 48);
-                tmem_st32(ta + C::PCOLS, r1);
-                tmem_st16(ta + C::PCOLS + 32, r1 + 32);
-                tmem_st8(ta + C::PCOLS + 48, r1 + 48);
+                tmem_st32(ta, wd);
+                tmem_st16(ta + 32, wd + 32);
+                tmem_st8(ta + 48, wd + 48);
             } else {
-                tmem_st16(ta, r0);
-                tmem_st16(ta + C::PCOLS, r1);
+                tmem_st16(ta, wd);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -312,17 +283,19 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
     } else {
-        // ---------------- epilogue warps 6..9
+        // ---------------- epilogue warps 10..17: two per lane quarter, each taking
+        // half of every 32-channel group (16 channels when BN is 16: one warp idles)
         const int q = warp & 3;
-        const int et = threadIdx.x - 192;
+        const int half = (warp - 10) >> 2;
+        const int et = threadIdx.x - 320;
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const uint32_t acc = C::NACC == 2 ? (local & 1) : 0u;
             const uint32_t use = C::NACC == 2 ? (local >> 1) : local;
-            if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
+            if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status, 256)) break;
             tc_fence_after();
             const HTile t = halo_decode(p, tile, BN);
-            halo_epilogue<BN, EPI>(p, t, tmem_base, acc * 2 * BN, q, lane);
+            halo_epilogue<BN, EPI, 16>(p, t, tmem_base, acc * 2 * BN, q, lane, 16 * half, 32);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
@@ -355,9 +328,9 @@ static cf_status run_smallc(const LaunchCtx& ctx, const HaloParams& hp, const ui
     auto kern = conv_smallc_kernel<CIN, BN, EPI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return CF_ERR_CUDA;
-    int grid = grid_for(kern, C::SMEM, 320, ctx.num_sms, hp.num_tiles, C::TMEM_COLS);
+    int grid = grid_for(kern, C::SMEM, 576, ctx.num_sms, hp.num_tiles, C::TMEM_COLS);
     grid = std::max(hp.n_ntiles, grid / hp.n_ntiles * hp.n_ntiles);  // each CTA keeps one N tile
-    kern<<<grid, 320, C::SMEM, ctx.stream>>>(th, sp);
+    kern<<<grid, 576, C::SMEM, ctx.stream>>>(th, sp);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 

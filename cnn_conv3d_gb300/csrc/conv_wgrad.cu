@@ -554,6 +554,8 @@ static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_
 }
 
 size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out) {
+    if (wgrad_halo_supported(c_in, c_out))
+        return wgrad_halo_workspace_bytes(num_sms, n, d, h, w, c_in, c_out);
     WgradGeom g = wgrad_geom(num_sms, n, d, h, w, c_in, c_out);
     return (size_t)g.n_splits * c_out * 27 * c_in * sizeof(float);
 }
@@ -621,16 +623,31 @@ static cf_status wgrad_bn(const LaunchCtx& ctx, const WgradGeom& g, const uint16
     return run_wgrad<BN, 32, SUBB>(ctx, g, x, dz, part);
 }
 
+static cf_status launch_splitk_reduce(const LaunchCtx& ctx, const float* part, float* dw, int64_t count, int splits,
+                                      int accumulate) {
+    const int threads = 256;
+    const int blocks = (int)std::min<int64_t>((count + threads - 1) / threads, 4 * (int64_t)ctx.num_sms);
+    splitk_reduce_kernel<<<blocks, threads, 0, ctx.stream>>>(part, dw, count, splits, accumulate);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
 cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                        const uint16_t* x, const uint16_t* dz, float* dw, int accumulate, void* ws, size_t ws_bytes) {
     if (!(c_in == 1 || c_in == 4 || c_in % 32 == 0)) return CF_ERR_UNSUPPORTED;
     if (!(c_out == 16 || c_out == 32 || c_out % 64 == 0) || c_out > 256) return CF_ERR_UNSUPPORTED;
     if ((c_in == 1 || c_in == 4) && (w * c_in) % 8 != 0) return CF_ERR_UNSUPPORTED;
-    WgradGeom g = wgrad_geom(ctx.num_sms, n, d, h, w, c_in, c_out);
-    const size_t need = (size_t)g.n_splits * c_out * 27 * c_in * sizeof(float);
+    const size_t need = wgrad_workspace_bytes(ctx.num_sms, n, d, h, w, c_in, c_out);
     if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
     float* part = static_cast<float*>(ws);
+    int n_splits = 0;
     cf_status st;
+    if (wgrad_halo_supported(c_in, c_out)) {
+        st = launch_wgrad_halo(ctx, n, d, h, w, c_in, c_out, x, dz, part, &n_splits);
+        if (st != CF_OK) return st;
+        return launch_splitk_reduce(ctx, part, dw, (int64_t)c_out * 27 * c_in, n_splits, accumulate);
+    }
+    WgradGeom g = wgrad_geom(ctx.num_sms, n, d, h, w, c_in, c_out);
+    n_splits = g.n_splits;
     switch (c_out) {
         case 16: st = wgrad_bn<16>(ctx, g, x, dz, part); break;
         case 32: st = wgrad_bn<32>(ctx, g, x, dz, part); break;
@@ -641,11 +658,7 @@ cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, in
         default: return CF_ERR_UNSUPPORTED;
     }
     if (st != CF_OK) return st;
-    const int64_t count = (int64_t)c_out * 27 * c_in;
-    const int threads = 256;
-    const int blocks = (int)std::min<int64_t>((count + threads - 1) / threads, 4 * (int64_t)ctx.num_sms);
-    splitk_reduce_kernel<<<blocks, threads, 0, ctx.stream>>>(part, dw, count, g.n_splits, accumulate);
-    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+    return launch_splitk_reduce(ctx, part, dw, (int64_t)c_out * 27 * c_in, n_splits, accumulate);
 }
 
 }  // namespace cf

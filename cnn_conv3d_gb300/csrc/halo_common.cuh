@@ -50,16 +50,21 @@ __device__ __forceinline__ void pool_combine(float& v, int& k, float v2, int k2)
     }
 }
 
-template <int BN, int EPI>
+// Epilogue of one tile for the accumulator columns c_begin, c_begin + step,
+// ... (CH columns per pass); CH = 0 picks min(BN, 32) and step CH.  Several
+// warps per TMEM lane quarter can thus split the channels of a tile.
+template <int BN, int EPI, int CH_ = 0>
 __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& t, uint32_t tmem_base,
-                                              uint32_t acc_col, int q, int lane) {
-    constexpr int CH = BN >= 32 ? 32 : 16;  // accumulator columns per pass
+                                              uint32_t acc_col, int q, int lane, int c_begin = 0,
+                                              int c_step = 0) {
+    constexpr int CH = CH_ != 0 ? CH_ : (BN >= 32 ? 32 : 16);  // accumulator columns per pass
     const int r = q * 32 + lane;
     const int j = r >> 3, l = r & 7;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
     const int h = t.h0 + j, w = t.w0 + l;
+    const int step = c_step != 0 ? c_step : CH;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += CH) {
+    for (int c = c_begin; c < BN; c += step) {
         uint32_t a0[32], a1[32];
         if (CH == 32) {
             tmem_ld32(lane_addr + c, a0);

@@ -265,6 +265,9 @@ WGRAD_SHAPES = [
     (1, 4, 8, 16, 4, 16),
     (1, 8, 8, 8, 1, 16),
     (1, 2, 4, 8, 32, 192),
+    (2, 2, 8, 16, 32, 32),     # halo-tile wgrad variants: 32 -> 32, 32 -> 128, 64 -> 64
+    (1, 4, 20, 8, 32, 128),
+    (1, 2, 4, 24, 64, 64),
 ]
 
 
