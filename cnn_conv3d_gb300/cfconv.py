@@ -52,6 +52,8 @@ _SIGS = {
     "cf_bias_lrelu_pool_fwd": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _f32, _vp, _vp, _vp], ctypes.c_int),
     "cf_bias_lrelu_pool_bwd": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _sz, _vp],
                                ctypes.c_int),
+    "cf_bias_lrelu_pool_bwd_noalloc": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp],
+                                       ctypes.c_int),
     "cf_workspace_size": ([ctypes.c_int, _DP], _sz),
     "cf_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "cf_last_device_status": ([_vp], ctypes.c_int),
@@ -144,6 +146,12 @@ def cf_bias_lrelu_pool_bwd(n, d, h, w, c, dy, y, idx, slope, dz, dy_pre, dbias, 
     st = _lib.cf_bias_lrelu_pool_bwd(n, d, h, w, c, _ptr(dy), _ptr(y), _ptr(idx), float(slope), _ptr(dz),
                                      _ptr(dy_pre), _ptr(dbias), _ptr(ws), ws_bytes, _stream(stream))
     return _check(st, "cf_bias_lrelu_pool_bwd") if check else st
+
+
+def cf_bias_lrelu_pool_bwd_noalloc(n, d, h, w, c, dy, y, idx, slope, dz, dy_pre, dbias, stream=None, check=True):
+    st = _lib.cf_bias_lrelu_pool_bwd_noalloc(n, d, h, w, c, _ptr(dy), _ptr(y), _ptr(idx), float(slope), _ptr(dz),
+                                             _ptr(dy_pre), _ptr(dbias), _stream(stream))
+    return _check(st, "cf_bias_lrelu_pool_bwd_noalloc") if check else st
 
 
 def cf_last_device_status(stream=None) -> int:

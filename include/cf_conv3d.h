@@ -145,6 +145,30 @@ cf_status cf_bias_lrelu_pool_bwd(int64_t n, int64_t d, int64_t h, int64_t w, int
                                  float slope, uint16_t* dz, uint16_t* dy_pre, float* dbias,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * cf_bias_lrelu_pool_bwd without a workspace argument, for callers that
+ * cannot allocate device memory (for example an operator plugged into a host
+ * framework that owns all device allocations and hands its plug-ins neither
+ * an allocator nor a workspace).  The CosmoFlow pages have no counterpart:
+ * this is an interface variant, not part of the method.
+ *   Arguments, layouts and results: as cf_bias_lrelu_pool_bwd.
+ *   Scratch: the bias-gradient partial sums live in a 1 MiB array inside the
+ *   library (one per device, held until the process exits).  It holds
+ *   4 * SM-count * c floats, so c <= 65536 / SM-count (442 on a 148-SM GPU)
+ *   when dbias is requested; larger c returns CF_ERR_WORKSPACE before
+ *   anything is launched.
+ *   The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ *   Every call shares the array (it keeps the last call's contents; this
+ *   operation overwrites every partial it reads, so nothing needs clearing):
+ *   calls whose work overlaps on the GPU race on it.
+ *   Calls no allocating routine.
+ */
+cf_status cf_bias_lrelu_pool_bwd_noalloc(int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                                         const uint16_t* dy, const uint16_t* y, const uint8_t* idx,
+                                         float slope, uint16_t* dz, uint16_t* dy_pre, float* dbias,
+                                         void* stream);
+
 /* Workspace bytes the operation `op` (CF_OP_*) needs for `desc` (for
  * CF_OP_POOL_BWD desc->c_out is the channel count).  0 if none. */
 size_t cf_workspace_size(int op, const cf_conv_desc* desc);
