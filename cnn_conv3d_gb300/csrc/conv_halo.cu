@@ -190,6 +190,9 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     const uint64_t ah = adesc0 + ((hs * C::HALO_STRIDE) >> 4);
+                    // taps in groups of TPS = 3 (one kw line: kd, kh fixed); inside a group every
+                    // descriptor offset is a compile-time constant
+#pragma unroll 1
                     for (int g = 0; g < 27 / C::TPS; ++g) {
                         uint64_t bg;
                         if (RES) {
@@ -202,18 +205,20 @@ __global__ void __launch_bounds__(192, 1)
                             bg = bdesc0 + ((ws * C::TPS * C::W_BYTES) >> 4);
                         }
                         tc_fence_after();
+                        const int kd = g / 3, kh = g % 3;
+                        const uint64_t ag = ah + (((uint32_t)((kd * HH_H + kh) * HH_W) * C::ROW) >> 4);
+                        const uint32_t first = (ch | g) != 0;
 #pragma unroll
-                        for (int u = 0; u < C::TPS; ++u) {
-                            const int tap = g * C::TPS + u;
-                            const int kd = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
-                            const uint64_t bw = bg + ((u * C::W_BYTES) >> 4);
+                        for (int kw = 0; kw < 3; ++kw) {
+                            const uint64_t bw = bg + ((kw * C::W_BYTES) >> 4);
 #pragma unroll
                             for (int k = 0; k < KC / 16; ++k) {
 #pragma unroll
                                 for (int i = 0; i < 2; ++i) {
-                                    const uint32_t row = ((i + kd) * HH_H + kh) * HH_W + kw;
-                                    const uint64_t ad = ah + ((row * C::ROW + k * 32) >> 4);
-                                    umma_bf16(d0 + i * BN, ad, bw + ((k * 32) >> 4), C::IDESC, (ch | tap | k) != 0);
+                                    constexpr uint32_t plane_rows = HH_H * HH_W;
+                                    const uint64_t ad = ag + (((i * plane_rows + kw) * C::ROW + k * 32) >> 4);
+                                    umma_bf16(d0 + i * BN, ad, bw + ((k * 32) >> 4), C::IDESC,
+                                              (first | kw | k) != 0);
                                 }
                             }
                         }

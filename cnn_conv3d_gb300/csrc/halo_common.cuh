@@ -77,6 +77,12 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
         // channels of this pass that exist (c_out is a multiple of 8)
         const int nvalid = min(CH, p.Cout - (t.co0 + c));
         if (EPI == EPI_POOL) {
+            float bias[CH];  // the pass's bias values, loaded before the reduction chain
+#pragma unroll
+            for (int cc = 0; cc < CH; ++cc) {
+                const int co = t.co0 + c + cc;
+                bias[cc] = (p.ea.bias != nullptr && co < p.Cout) ? __ldg(p.ea.bias + co) : 0.f;
+            }
             const int D2 = p.D >> 1, H2 = p.H >> 1, W2 = p.W >> 1;
             const int pd = t.d0 >> 1, ph = h >> 1, pw = w >> 1;
             const bool writer = ((j | l) & 1) == 0 && pd < D2 && ph < H2 && pw < W2;
@@ -90,8 +96,7 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
                 pool_combine(v, k, __uint_as_float(a1[cc]), kbase + 4);
                 pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 1), __shfl_xor_sync(0xffffffffu, k, 1));
                 pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 8), __shfl_xor_sync(0xffffffffu, k, 8));
-                const int co = t.co0 + c + cc;
-                const float s = v + ((p.ea.bias != nullptr && co < p.Cout) ? p.ea.bias[co] : 0.f);
+                const float s = v + bias[cc];
                 const float y = s > 0.f ? s : p.ea.slope * s;
                 const uint32_t yb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y));
                 if (cc & 1)
