@@ -101,7 +101,8 @@ def traffic_for(key):
 
 
 class Clocks:
-    """Samples nvidia-smi every 200 ms while the timed region runs."""
+    """Samples nvidia-smi every 50 ms from the warm-up to the end of the timed
+    and end-to-end regions."""
 
     def __init__(self, index):
         self.index = index
@@ -116,7 +117,7 @@ class Clocks:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -198,6 +199,23 @@ def cpu_sample_step(n_threads=None, budget_s=20.0):
     return total / est_time / 1e12, sampled
 
 
+def max_over_ranks(value, world, device=None):
+    """Largest value of `value` over all ranks (each rank times its own replica;
+    the job takes as long as the slowest).  Identity on one rank."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank, world, max_ms):
+    """Throughput of the whole job: every rank's work over the slowest rank's time."""
+    return world * work_per_rank / (max_ms * 1e-3)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -257,6 +275,7 @@ def run_ours(args, rank, world, local_rank):
                                    st.g[l - 1], st.ws, wsb, stream)
         mark("end")
 
+    clk = Clocks(local_rank).__enter__()
     for _ in range(args.warmup):
         st.step(dy, stream)
     torch.cuda.synchronize(dev)
@@ -269,7 +288,7 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize(dev)
     step_ms, per_op = [], {}
-    with Clocks(local_rank) as clk:
+    if True:
         for _ in range(args.steps):
             flush.zero_()  # evict L2 between steps (outside the timed events)
             evs = []
@@ -284,11 +303,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     if cf.cf_last_device_status(stream) != cf.CF_OK:
         raise RuntimeError("device status word set during the timed steps")
-    ms = float(np.mean(step_ms))
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.mean(step_ms)), world, dev)
 
     # end-to-end through host buffers: H2D of the step inputs (pinned), the
     # step, D2H of its results (all weight and bias gradients)
@@ -322,14 +337,11 @@ def run_ours(args, rank, world, local_rank):
             e1.record(stream)
             torch.cuda.synchronize(dev)
             e_ms.append(e0.elapsed_time(e1))
-        em = float(np.mean(e_ms))
-        if world > 1:
-            t = torch.tensor([em], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            em = float(t.item())
-        e2e = {"value": round(world * total_flops / (em * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        em = max_over_ranks(float(np.mean(e_ms)), world, dev)
+        e2e = {"value": round(whole_job_rate(total_flops, world, em) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(em, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    clk.__exit__(None, None, None)
     # dominant conv op: largest mean time
     op_ms = {k: float(np.mean(v)) for k, v in per_op.items()}
     conv_ops = {o[0]: o for o in ops}
@@ -343,12 +355,12 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / pk["bf16_tflops_sustained"], 4), "traffic": tr,
                 "peak_kind": f"bf16 sustained ({pk['source']})"}
 
-    value = world * total_flops / (ms * 1e-3) / 1e12
+    value = whole_job_rate(total_flops, world, ms) / 1e12
     res = {
         "metric": METRIC,
         "value": round(value, 3),
         "unit": "TFLOP/s",
-        "samples_per_s": round(world * n / (ms * 1e-3), 1),
+        "samples_per_s": round(whole_job_rate(n, world, ms), 1),
         "pct_of_bf16_peak": {"measured_burst": round(100 * value / world / pk["bf16_tflops"], 2),
                              "measured_sustained": round(100 * value / world / pk["bf16_tflops_sustained"], 2),
                              "nominal_2250": round(100 * value / world / 2250.0, 2)},

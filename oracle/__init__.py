@@ -148,15 +148,16 @@ def pool_fwd(z: np.ndarray, bias, slope: float):
     return y, idx
 
 
-def pool_bwd(dy: np.ndarray, y, idx: np.ndarray, slope: float):
+def pool_bwd(dy: np.ndarray, y, idx: np.ndarray, slope: float, want_dz: bool = True):
     """(dz, dy_pre, db) of the pool/LReLU stage; y=None means dy is already the
-    gradient w.r.t. the pooled pre-activation."""
+    gradient w.r.t. the pooled pre-activation.  want_dz=False skips the
+    full-resolution dz (returned as None)."""
     lib = _load()
     dy = _f64(dy)
     N, D2, H2, W2, C = dy.shape
     yy = None if y is None else _f64(y)
     idx = np.ascontiguousarray(idx, dtype=np.uint8)
-    dz = np.empty((N, 2 * D2, 2 * H2, 2 * W2, C), np.float64)
+    dz = np.empty((N, 2 * D2, 2 * H2, 2 * W2, C), np.float64) if want_dz else None
     dyp = np.empty_like(dy)
     db = np.empty((C,), np.float64)
     lib.oracle_pool_bwd(N, 2 * D2, 2 * H2, 2 * W2, C, _p(dy, _D), _p(yy, _D), _p(idx, _U8), slope,
