@@ -53,10 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // non-zero (another role gave up) or after `limit_ns`; in the latter case it
 // raises `*abort` and records `code` in the device status word `status`.
 // Returns true when the phase completed.
+// sleep_cap_ns > 0 adds an exponential back-off (__nanosleep, doubling up to
+// the cap) between polls: for roles whose waits are long and not on the
+// critical path (builders, epilogue), so that waiting warps leave the issue
+// slots to the warps that work.  The TMA producer and the MMA issuer poll
+// without sleeping.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns, int* status, int code) {
+                                          uint64_t limit_ns, int* status, int code, uint32_t sleep_cap_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
+    uint32_t nap = 32;
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 4; ++i)
@@ -67,8 +73,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             atomicCAS(status, 0, code);
             return false;
         }
+        if (sleep_cap_ns != 0) {
+            __nanosleep(nap);
+            if (nap < sleep_cap_ns) nap <<= 1;
+        }
     }
 }
+
+constexpr uint32_t kNapNs = 512;  // back-off cap for builder and epilogue waits
 
 // Bounded wait that ignores the abort flag (used to drain copies and MMAs
 // already in flight before a CTA that gave up exits).

@@ -5,7 +5,8 @@
 // GEMM view: D[m, co] = sum_k A[m, k] * W[co, k] with k = 4*t + ci
 // (t = 9*kd + 3*kh + kw), K = 27*c_in padded to 112 (c_in 4) or 32 (c_in 1).
 // Output tile: 2 planes x 16 lines x 8 voxels, two M=128 accumulators (one
-// per plane, row r = 8*line + voxel), as in conv_halo.cu.
+// per plane), as in conv_halo.cu, but with the interleaved row order of
+// tile_line() so that the gathers are free of shared-memory bank conflicts.
 //
 // With only 8 (or 2) bytes per voxel, an im2col tile in shared memory would
 // be written and read once per tap and bound the kernel by shared-memory
@@ -241,8 +242,7 @@ __global__ void __launch_bounds__(576, 1)
         // ---------------- builders: warps 2..5 plane 0, 6..9 plane 1; one row each
         const int q = warp & 3;
         const int plane = (warp - 2) >> 2;
-        const int r = q * 32 + lane;
-        const int j = r >> 3, l = r & 7;
+        const int j = tile_line<true>(q, lane), l = lane & 7;
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + C::ACOL0 + plane * C::PCOLS;
         int hs = 0, as = 0;
         uint32_t hph = 0, aph = 0;
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(576, 1)
             // every lane waits, and the warp leaves together if any lane gave up, so
             // the shuffles and .sync.aligned tensor-memory stores below always see
             // the full warp
-            if (!__all_sync(0xffffffffu, mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)))
+            if (!__all_sync(0xffffffffu, mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL, kNapNs)))
                 break;
             uint32_t wd[56];
             if (CIN == 4)
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(576, 1)
                 gather_plane_c1(hring + hs * C::HALO_STRIDE, plane, j, l, wd);
             mbar_arrive(&hempty[hs]);
             if (!__all_sync(0xffffffffu,
-                            mbar_wait(&aempty[as], aph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)))
+                            mbar_wait(&aempty[as], aph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY, kNapNs)))
                 break;
             tc_fence_after();
             const uint32_t ta = lane_addr + as * C::ASTRIDE;
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(576, 1)
             if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status, 256)) break;
             tc_fence_after();
             const HTile t = halo_decode(p, tile, BN);
-            halo_epilogue<BN, EPI, 16>(p, t, tmem_base, acc * 2 * BN, q, lane, 16 * half, 32);
+            halo_epilogue<BN, EPI, 16, true>(p, t, tmem_base, acc * 2 * BN, q, lane, 16 * half, 32);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }

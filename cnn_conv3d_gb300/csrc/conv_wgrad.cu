@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int64_t b = b0; b < b1; ++b) {
                 // all lanes wait; the warp leaves together (shuffles need the full warp)
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait(&loaded[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL))) {
+                                mbar_wait(&loaded[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL, kNapNs))) {
                     ok = false;
                     break;
                 }
