@@ -4,54 +4,62 @@
 //
 // GEMM view: D[m, co] = sum_k A[m, k] * W[co, k] with k = 4*t + ci
 // (t = 9*kd + 3*kh + kw), K = 27*c_in padded to 112 (c_in 4) or 32 (c_in 1).
-// Output tile: 2 planes x 16 lines x 8 voxels, two M=128 accumulators (one
-// per plane), as in conv_halo.cu, but with the interleaved row order of
-// tile_line() so that the gathers are free of shared-memory bank conflicts.
+//
+// Output tile: 2 planes x 16 lines x 16 voxels (512 voxels), computed as four
+// M=128 row blocks, one per (plane, line parity); row r of a block is voxel
+// r % 16 of line pair r / 16.  The four (plane, line) members of a 2x2x2
+// pooling window are thus the same TMEM lane of the four blocks and its two
+// voxels are adjacent lanes: the pooling is a per-thread reduction plus one
+// exchange between lane pairs, which also splits the finalisation (bias,
+// activation, stores) of the window's channels between the two lanes.
 //
 // With only 8 (or 2) bytes per voxel, an im2col tile in shared memory would
 // be written and read once per tap and bound the kernel by shared-memory
 // bandwidth.  Instead:
 //   warp 0      : TMA of the tile's input halo (one box of the input viewed as
-//                 (W*C, H, D, N): 4 planes x 18 lines x (8 + 2*margin) voxels,
+//                 (W*C, H, D, N): 4 planes x 18 lines x (16 + 2*margin) voxels,
 //                 zero outside the volume) into a ring;
-//   warps 2..9  : builders (plane 0: warps 2..5, plane 1: warps 6..9): each
-//                 thread gathers the im2col row of its (line, voxel) from the
-//                 halo (centre voxels from shared memory, w-1 / w+1 neighbours
-//                 by warp shuffles) and writes it into a tensor-memory A
-//                 buffer with tcgen05.st;
+//   warps 2..9  : builders, two groups of four warps (one per TMEM lane
+//                 quarter); group g fills row blocks g and g + 2 of every tile.
+//                 Each thread gathers the im2col row of its voxel from the halo
+//                 (27 independent 8-byte loads; a half-warp reads 16
+//                 consecutive voxels of one halo line, 128 contiguous bytes, so
+//                 the loads are free of bank conflicts) and writes it into the
+//                 block's tensor-memory A buffer with tcgen05.st;
 //   warp 1      : tcgen05.mma with A from tensor memory and the filter
 //                 (resident in shared memory, K-major SW128) as B;
-//   warps 10..17: the epilogues of halo_common.cuh (fused bias + leaky ReLU +
-//                 2x2x2 max-pool with argmax by warp shuffles, or plain bf16),
-//                 two warps per TMEM lane quarter splitting the channels.
-// Every per-tile chain (gather, pooling) is latency-bound, so each role has
-// two warps per SM sub-partition.
+//   warps 10..17: epilogue (fused bias + leaky ReLU + 2x2x2 max-pool with
+//                 argmax, or plain bf16), two warps per TMEM lane quarter
+//                 splitting the channels.
 #include "halo_common.cuh"
 #include "smallc_common.cuh"
 
 namespace cf {
+
+constexpr int SC_W = 16, SC_H = 16, SC_D = 2;  // output tile (voxels, lines, planes)
+constexpr int SC_BLOCKS = 4;                   // M=128 row blocks per tile: (plane, line parity)
 
 template <int CIN, int BN, int EPI>
 struct SmallTmCfg {
     static constexpr int KREAL = 27 * CIN;
     static constexpr int KP = (KREAL + 15) / 16 * 16;  // 112 or 32
     static constexpr int KSTEPS = KP / 16;
-    static constexpr int PCOLS = CIN == 4 ? 64 : 16;   // TMEM columns per plane's A rows (56 / 16 used)
-    static constexpr int ASTRIDE = 2 * PCOLS;          // TMEM columns per A stage (two planes)
+    static constexpr int PCOLS = CIN == 4 ? 64 : 16;   // TMEM columns per A block (56 / 16 used)
     static constexpr int ATOMS = (KP + 63) / 64;
     static constexpr uint32_t B_BYTES = BN * 128 * ATOMS;
-    static constexpr int HALO_BYTES = 4 * 18 * (8 + 2 * (16 / (2 * CIN))) * CIN * 2;  // 6912 or 3456
+    static constexpr int MARGIN = 16 / (2 * CIN);       // halo voxels left of the tile (16-byte start)
+    static constexpr int PITCH = (SC_W + 2 * MARGIN) * CIN * 2;  // bytes per halo line: 160 or 64
+    static constexpr int HALO_BYTES = (SC_D + 2) * (SC_H + 2) * PITCH;  // 11520 or 4608
     static constexpr uint32_t HALO_STRIDE = (HALO_BYTES + 1023) / 1024 * 1024;
-    static constexpr int HS = 12;  // halo stages in flight (TMA latency)
-    static constexpr int NACC = (4 * BN + 2 * ASTRIDE <= 512) ? 2 : 1;
-    static constexpr int AST_RAW = (512 - 2 * NACC * BN) / ASTRIDE;
-    static constexpr int AST = AST_RAW > 4 ? 4 : AST_RAW;
-    static constexpr uint32_t BAR_BYTES = 8 * (2 * HS + 2 * 4 + 5) + 16;
+    static constexpr int HS = CIN == 4 ? 8 : 12;        // halo stages in flight (TMA latency)
+    static constexpr int ACC_COLS = SC_BLOCKS * BN;      // accumulator columns of one tile
+    static constexpr int NACC = (2 * ACC_COLS + SC_BLOCKS * PCOLS <= 512) ? 2 : 1;
+    static constexpr uint32_t ACOL0 = NACC * ACC_COLS;   // first A column
+    static constexpr uint32_t BAR_BYTES = 8 * (2 * HS + 2 * SC_BLOCKS + 2 * 2 + 1) + 16;
     static constexpr uint32_t SMEM = 1024 + B_BYTES + HS * HALO_STRIDE + BAR_BYTES;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t ACOL0 = 2 * NACC * BN;
     static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
-    static_assert(AST >= 2, "tensor memory budget");
+    static_assert(ACOL0 + SC_BLOCKS * PCOLS <= TMEM_COLS, "tensor memory budget");
 };
 
 struct SmallTmParams {
@@ -59,44 +67,63 @@ struct SmallTmParams {
     const uint16_t* w;  // [Cout][27*CIN]
 };
 
-// Gathers the im2col row of (plane i, line j, voxel l) from the halo tile:
-// for c_in = 4 the 9 (kd, kh) halo lines at voxel l-1, l, l+1 (8 bytes each),
-// K index k = 4*t + ci, t = 9*kd + 3*kh + kw (54 words + 2 zero words).  The
-// 27 shared-memory loads are independent (no shuffles, no divergent edge
-// cases), so a warp keeps them all in flight.
-__device__ __forceinline__ void gather_plane_c4(const uint8_t* halo, int i, int j, int l, uint32_t (&wd)[56]) {
-    constexpr int PITCH = 12 * 8;  // (8 + 2*2) voxels x 8 bytes
-    const uint8_t* base = halo + (i * 18 + j) * PITCH + (l + 1) * 8;
-#pragma unroll
-    for (int kd = 0; kd < 3; ++kd)
-#pragma unroll
-        for (int kh = 0; kh < 3; ++kh)
-#pragma unroll
-            for (int kw = 0; kw < 3; ++kw) {
-                const uint2 v = *reinterpret_cast<const uint2*>(base + (kd * 18 + kh) * PITCH + kw * 8);
-                const int t = kd * 9 + kh * 3 + kw;
-                wd[2 * t] = v.x;
-                wd[2 * t + 1] = v.y;
-            }
-    wd[54] = wd[55] = 0u;
+struct SmallTile {
+    int n, d0, h0, w0;
+};
+
+// Tiles are numbered N tile fastest, then w, h, d, n.
+__device__ __forceinline__ SmallTile small_decode(const HaloParams& p, int tile) {
+    SmallTile t;
+    int m = tile / p.n_ntiles;
+    const int tw = m % p.tiles_w;
+    m /= p.tiles_w;
+    const int th = m % p.tiles_h;
+    m /= p.tiles_h;
+    const int td = m % p.tiles_d;
+    t.n = m / p.tiles_d;
+    t.w0 = tw * SC_W;
+    t.h0 = th * SC_H;
+    t.d0 = td * SC_D;
+    return t;
 }
 
-// c_in = 1: 27 taps padded to 32 (16 words).
-__device__ __forceinline__ void gather_plane_c1(const uint8_t* halo, int i, int j, int l, uint32_t (&wd)[56]) {
-    constexpr int PITCH = 24 * 2;  // (8 + 2*8) voxels x 2 bytes
-    uint32_t v[32];
+// im2col row of the voxel (plane pl, line ln, voxel v) of the tile, from its
+// halo.  c_in = 4: tap t = 9*kd + 3*kh + kw is halo voxel v + kw of halo line
+// (pl + kd, ln + kh), K index 4*t + ci (54 words + 2 zero words).  c_in = 1:
+// 27 taps padded to 32 (16 words).
+template <int CIN>
+__device__ __forceinline__ void gather_row(const uint8_t* halo, int pl, int ln, int v, uint32_t (&wd)[56]) {
+    using C = SmallTmCfg<CIN, 16, EPI_PLAIN>;
+    if (CIN == 4) {
+        const uint8_t* base = halo + (pl * (SC_H + 2) + ln) * C::PITCH + (v + C::MARGIN - 1) * 8;
 #pragma unroll
-    for (int t = 27; t < 32; ++t) v[t] = 0u;
+        for (int kd = 0; kd < 3; ++kd)
 #pragma unroll
-    for (int kd = 0; kd < 3; ++kd)
+            for (int kh = 0; kh < 3; ++kh)
 #pragma unroll
-        for (int kh = 0; kh < 3; ++kh) {
-            const uint16_t* line = reinterpret_cast<const uint16_t*>(halo + ((i + kd) * 18 + j + kh) * PITCH);
+                for (int kw = 0; kw < 3; ++kw) {
+                    const uint2 x = *reinterpret_cast<const uint2*>(base + (kd * (SC_H + 2) + kh) * C::PITCH + kw * 8);
+                    const int t = kd * 9 + kh * 3 + kw;
+                    wd[2 * t] = x.x;
+                    wd[2 * t + 1] = x.y;
+                }
+        wd[54] = wd[55] = 0u;
+    } else {
+        uint32_t e[32];
 #pragma unroll
-            for (int kw = 0; kw < 3; ++kw) v[kd * 9 + kh * 3 + kw] = line[l + 8 + kw - 1];
-        }
+        for (int t = 27; t < 32; ++t) e[t] = 0u;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) wd[q] = v[2 * q] | (v[2 * q + 1] << 16);
+        for (int kd = 0; kd < 3; ++kd)
+#pragma unroll
+            for (int kh = 0; kh < 3; ++kh) {
+                const uint16_t* line =
+                    reinterpret_cast<const uint16_t*>(halo + ((pl + kd) * (SC_H + 2) + ln + kh) * C::PITCH);
+#pragma unroll
+                for (int kw = 0; kw < 3; ++kw) e[kd * 9 + kh * 3 + kw] = line[v + C::MARGIN - 1 + kw];
+            }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) wd[q] = e[2 * q] | (e[2 * q + 1] << 16);
+    }
 }
 
 template <int CIN, int BN, int EPI>
@@ -112,8 +139,8 @@ __global__ void __launch_bounds__(576, 1)
     uint64_t* hfull = bars;
     uint64_t* hempty = hfull + C::HS;
     uint64_t* afull = hempty + C::HS;
-    uint64_t* aempty = afull + C::AST;
-    uint64_t* tfull = aempty + C::AST;
+    uint64_t* aempty = afull + SC_BLOCKS;
+    uint64_t* tfull = aempty + SC_BLOCKS;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -121,15 +148,16 @@ __global__ void __launch_bounds__(576, 1)
     volatile int* epi_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int co0 = (blockIdx.x % p.n_ntiles) * BN;  // the CTA's N tile (see the launch)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::HS; ++s) {
             mbar_init(&hfull[s], 1);
             mbar_init(&hempty[s], 256);
         }
-        for (int s = 0; s < C::AST; ++s) {
-            mbar_init(&afull[s], 256);
-            mbar_init(&aempty[s], 1);
+        for (int b = 0; b < SC_BLOCKS; ++b) {
+            mbar_init(&afull[b], 128);
+            mbar_init(&aempty[b], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -145,7 +173,6 @@ __global__ void __launch_bounds__(576, 1)
     // Tiles are dealt with stride gridDim.x and the launch makes gridDim.x a
     // multiple of n_ntiles, so every tile of this CTA has the same N tile.
     {
-        const int co0 = (blockIdx.x % p.n_ntiles) * BN;
         for (int e = threadIdx.x; e < BN * (C::ATOMS * 8); e += blockDim.x) {
             const int r = e / (C::ATOMS * 8), c = e % (C::ATOMS * 8);
             uint32_t v[4] = {0u, 0u, 0u, 0u};
@@ -178,7 +205,7 @@ __global__ void __launch_bounds__(576, 1)
             uint32_t hph = 0, issued = 0, par = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-                const HTile t = halo_decode(p, tile, BN);
+                const SmallTile t = small_decode(p, tile);
                 if (!mbar_wait(&hempty[hs], hph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
                     ok = false;
                     break;
@@ -199,8 +226,7 @@ __global__ void __launch_bounds__(576, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---------------- MMA issuer
-            int as = 0;
+            // ---------------- MMA issuer: per tile, the four row blocks in order
             uint32_t aph = 0, local = 0;
             bool ok = true;
             const uint32_t b_addr = smem_u32(bsm);
@@ -211,27 +237,26 @@ __global__ void __launch_bounds__(576, 1)
                     ok = false;
                     break;
                 }
-                if (!mbar_wait(&afull[as], aph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * 2 * BN;
-                const uint32_t a_tmem = tmem_base + C::ACOL0 + as * C::ASTRIDE;
+#pragma unroll 1
+                for (int blk = 0; blk < SC_BLOCKS; ++blk) {
+                    if (!mbar_wait(&afull[blk], aph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS + blk * BN;
+                    const uint32_t a_tmem = tmem_base + C::ACOL0 + blk * C::PCOLS;
 #pragma unroll
-                for (int k = 0; k < C::KSTEPS; ++k) {
-                    const uint32_t atom = k >> 2, koff = (k & 3) * 32;
-                    const uint64_t bd = sdesc(b_addr + atom * (BN * 128) + koff, 16, 1024, SWZ_128B);
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-                        umma_bf16_tmem_a(d_tmem + i * BN, a_tmem + i * C::PCOLS + 8 * k, bd, C::IDESC, k != 0);
+                    for (int k = 0; k < C::KSTEPS; ++k) {
+                        const uint32_t atom = k >> 2, koff = (k & 3) * 32;
+                        const uint64_t bd = sdesc(b_addr + atom * (BN * 128) + koff, 16, 1024, SWZ_128B);
+                        umma_bf16_tmem_a(d_tmem, a_tmem + 8 * k, bd, C::IDESC, k != 0);
+                    }
+                    umma_commit(&aempty[blk]);
                 }
-                umma_commit(&aempty[as]);
+                if (!ok) break;
                 umma_commit(&tfull[acc]);
-                if (++as == C::AST) {
-                    as = 0;
-                    aph ^= 1;
-                }
+                aph ^= 1;
             }
             if (!ok) {
                 umma_commit(drain);
@@ -239,63 +264,167 @@ __global__ void __launch_bounds__(576, 1)
             }
         }
     } else if (warp < 10) {
-        // ---------------- builders: warps 2..5 plane 0, 6..9 plane 1; one row each
+        // ---------------- builders: group g (warps 2..5 / 6..9) fills blocks g and g + 2
         const int q = warp & 3;
-        const int plane = (warp - 2) >> 2;
-        const int j = tile_line<true>(q, lane), l = lane & 7;
-        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + C::ACOL0 + plane * C::PCOLS;
-        int hs = 0, as = 0;
+        const int g = (warp - 2) >> 2;
+        const int lp = 2 * q + (lane >> 4), v = lane & 15;  // row 32q + lane: line pair, voxel
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + C::ACOL0;
+        int hs = 0;
         uint32_t hph = 0, aph = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
             // every lane waits, and the warp leaves together if any lane gave up, so
-            // the shuffles and .sync.aligned tensor-memory stores below always see
-            // the full warp
-            if (!__all_sync(0xffffffffu, mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL, kNapNs)))
-                break;
-            uint32_t wd[56];
-            if (CIN == 4)
-                gather_plane_c4(hring + hs * C::HALO_STRIDE, plane, j, l, wd);
-            else
-                gather_plane_c1(hring + hs * C::HALO_STRIDE, plane, j, l, wd);
-            mbar_arrive(&hempty[hs]);
+            // the .sync.aligned tensor-memory stores below always see the full warp
             if (!__all_sync(0xffffffffu,
-                            mbar_wait(&aempty[as], aph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY, kNapNs)))
+                            mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL, kNapNs)))
                 break;
-            tc_fence_after();
-            const uint32_t ta = lane_addr + as * C::ASTRIDE;
-            if (CIN == 4) {
-                tmem_st32(ta, wd);
-                tmem_st16(ta + 32, wd + 32);
-                tmem_st8(ta + 48, wd + 48);
-            } else {
-                tmem_st16(ta, wd);
+            const uint8_t* halo = hring + hs * C::HALO_STRIDE;
+#pragma unroll 1
+            for (int b2 = 0; b2 < 2; ++b2) {
+                const int blk = g + 2 * b2;
+                uint32_t wd[56];
+                gather_row<CIN>(halo, blk >> 1, 2 * lp + (blk & 1), v, wd);
+                if (b2 == 1) mbar_arrive(&hempty[hs]);
+                if (!__all_sync(0xffffffffu, mbar_wait(&aempty[blk], aph ^ 1, abort_flag, p.wait_ns, p.status,
+                                                       WAIT_PRODUCER_EMPTY, kNapNs))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ta = lane_addr + blk * C::PCOLS;
+                if (CIN == 4) {
+                    tmem_st32(ta, wd);
+                    tmem_st16(ta + 32, wd + 32);
+                    tmem_st8(ta + 48, wd + 48);
+                } else {
+                    tmem_st16(ta, wd);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&afull[blk]);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&afull[as]);
             if (++hs == C::HS) {
                 hs = 0;
                 hph ^= 1;
             }
-            if (++as == C::AST) {
-                as = 0;
-                aph ^= 1;
-            }
+            aph ^= 1;
         }
     } else {
         // ---------------- epilogue warps 10..17: two per lane quarter, each taking
-        // half of every 32-channel group (16 channels when BN is 16: one warp idles)
+        // 16 of every 32 channels (when BN is 16, the second warp of a quarter idles)
         const int q = warp & 3;
         const int half = (warp - 10) >> 2;
         const int et = threadIdx.x - 320;
+        const int lp = 2 * q + (lane >> 4), v = lane & 15, dw = v & 1;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+        constexpr int NPASS = (BN + 31) / 32;
+        // bias of the 8 channels this lane finalises in each pass
+        float bias[NPASS][8];
+#pragma unroll
+        for (int ps = 0; ps < NPASS; ++ps)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int co = co0 + 32 * ps + 16 * half + 8 * dw + i;
+                bias[ps][i] = (EPI == EPI_POOL && p.ea.bias != nullptr && co < p.Cout) ? __ldg(p.ea.bias + co) : 0.f;
+            }
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const uint32_t acc = C::NACC == 2 ? (local & 1) : 0u;
             const uint32_t use = C::NACC == 2 ? (local >> 1) : local;
             if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status, 256)) break;
             tc_fence_after();
-            const HTile t = halo_decode(p, tile, BN);
-            halo_epilogue<BN, EPI, 16, true>(p, t, tmem_base, acc * 2 * BN, q, lane, 16 * half, 32);
+            const SmallTile t = small_decode(p, tile);
+            const uint32_t acol = lane_addr + acc * C::ACC_COLS;
+#pragma unroll
+            for (int ps = 0; ps < NPASS; ++ps) {
+                const int c = 32 * ps + 16 * half;  // first of the warp's 16 accumulator columns
+                if (c >= BN) break;
+                if (EPI == EPI_POOL) {
+                    // per channel: first maximum over the lane's four (plane, line) values,
+                    // in the window's scan order (code dd*4 + dh*2 + dw)
+                    uint32_t r0[32], r1[32];
+                    float m[16];
+                    int k[16];
+                    tmem_ld16(acol + 0 * BN + c, r0);
+                    tmem_ld16(acol + 1 * BN + c, r1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) {
+                        m[cc] = __uint_as_float(r0[cc]);
+                        k[cc] = dw;
+                        const float b = __uint_as_float(r1[cc]);
+                        if (b > m[cc]) {
+                            m[cc] = b;
+                            k[cc] = 2 + dw;
+                        }
+                    }
+                    tmem_ld16(acol + 2 * BN + c, r0);
+                    tmem_ld16(acol + 3 * BN + c, r1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) {
+                        const float a = __uint_as_float(r0[cc]), b = __uint_as_float(r1[cc]);
+                        if (a > m[cc]) {
+                            m[cc] = a;
+                            k[cc] = 4 + dw;
+                        }
+                        if (b > m[cc]) {
+                            m[cc] = b;
+                            k[cc] = 6 + dw;
+                        }
+                    }
+                    // lane pair (dw = 0, 1): each keeps 8 channels and takes the
+                    // partner's values for them; larger value wins, ties keep the
+                    // smaller code
+                    float y[8];
+                    uint32_t codes[2] = {0u, 0u};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float kv = dw ? m[8 + i] : m[i];
+                        int kk = dw ? k[8 + i] : k[i];
+                        const float sv = dw ? m[i] : m[8 + i];
+                        const int sk = dw ? k[i] : k[8 + i];
+                        const float ov = __shfl_xor_sync(0xffffffffu, sv, 1);
+                        const int ok2 = __shfl_xor_sync(0xffffffffu, sk, 1);
+                        if (ov > kv || (ov == kv && ok2 < kk)) {
+                            kv = ov;
+                            kk = ok2;
+                        }
+                        const float s = kv + bias[ps][i];
+                        y[i] = s > 0.f ? s : p.ea.slope * s;
+                        codes[i >> 2] |= (uint32_t)kk << (8 * (i & 3));
+                    }
+                    const int D2 = p.D >> 1, H2 = p.H >> 1, W2 = p.W >> 1;
+                    const int pd = t.d0 >> 1, ph = (t.h0 >> 1) + lp, pw = (t.w0 + v) >> 1;
+                    if (pd < D2 && ph < H2 && pw < W2 && co0 + c + 8 * dw < p.Cout) {
+                        const int64_t po =
+                            ((((int64_t)t.n * D2 + pd) * H2 + ph) * W2 + pw) * p.Cout + co0 + c + 8 * dw;
+                        *reinterpret_cast<uint4*>(p.ea.y + po) =
+                            make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                       pack_bf16x2(y[6], y[7]));
+                        if (p.ea.idx) *reinterpret_cast<uint2*>(p.ea.idx + po) = make_uint2(codes[0], codes[1]);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int blk = 0; blk < SC_BLOCKS; ++blk) {
+                        uint32_t r[32];
+                        tmem_ld16(acol + blk * BN + c, r);
+                        tmem_ld_wait();
+                        const int d = t.d0 + (blk >> 1), h = t.h0 + 2 * lp + (blk & 1), w = t.w0 + v;
+                        if (d >= p.D || h >= p.H || w >= p.W) continue;
+                        const int64_t o = ((((int64_t)t.n * p.D + d) * p.H + h) * p.W + w) * p.Cout + co0 + c;
+#pragma unroll
+                        for (int q8 = 0; q8 < 2; ++q8) {
+                            if (co0 + c + 8 * q8 >= p.Cout) break;
+                            *reinterpret_cast<uint4*>(p.ea.y + o + 8 * q8) = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[8 * q8 + 0]), __uint_as_float(r[8 * q8 + 1])),
+                                pack_bf16x2(__uint_as_float(r[8 * q8 + 2]), __uint_as_float(r[8 * q8 + 3])),
+                                pack_bf16x2(__uint_as_float(r[8 * q8 + 4]), __uint_as_float(r[8 * q8 + 5])),
+                                pack_bf16x2(__uint_as_float(r[8 * q8 + 6]), __uint_as_float(r[8 * q8 + 7])));
+                        }
+                    }
+                }
+            }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
@@ -322,8 +451,9 @@ bool make_halo_map(CUtensorMap* m, const uint16_t* x, int n, int d, int h, int w
 template <int CIN, int BN, int EPI>
 static cf_status run_smallc(const LaunchCtx& ctx, const HaloParams& hp, const uint16_t* x, const uint16_t* wk) {
     using C = SmallTmCfg<CIN, BN, EPI>;
+    static_assert(halo_bytes(SC_W, SC_H, SC_D, CIN) == C::HALO_BYTES, "halo box and ring stage disagree");
     CUtensorMap th;
-    if (!make_halo_map(&th, x, hp.N, hp.D, hp.H, hp.W, CIN, HT_W, HT_H, HT_D)) return CF_ERR_CUDA;
+    if (!make_halo_map(&th, x, hp.N, hp.D, hp.H, hp.W, CIN, SC_W, SC_H, SC_D)) return CF_ERR_CUDA;
     SmallTmParams sp{hp, wk};
     auto kern = conv_smallc_kernel<CIN, BN, EPI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
@@ -348,8 +478,9 @@ cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t
     if (c_out % 8 != 0 || c_out > 256) return CF_ERR_UNSUPPORTED;
     if (c_in != 1 && c_in != 4) return CF_ERR_UNSUPPORTED;
     if ((w * c_in) % 8 != 0) return CF_ERR_UNSUPPORTED;  // halo rows must be 16-byte multiples
-    // N tile: c_out rounded up to 16, at most 128 (two N tiles above that)
-    const int bn = c_out <= 128 ? (c_out + 15) / 16 * 16 : 128;
+    // N tile: c_out rounded up to 16, at most 64 (four accumulators of a tile
+    // and the four A blocks share the 512 tensor-memory columns)
+    const int bn = c_out <= 64 ? (c_out + 15) / 16 * 16 : 64;
     HaloParams hp;
     hp.N = (int)n;
     hp.D = (int)d;
@@ -357,9 +488,9 @@ cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t
     hp.W = (int)w;
     hp.Cin = c_in;
     hp.Cout = c_out;
-    hp.tiles_w = (int)((w + HT_W - 1) / HT_W);
-    hp.tiles_h = (int)((h + HT_H - 1) / HT_H);
-    hp.tiles_d = (int)((d + HT_D - 1) / HT_D);
+    hp.tiles_w = (int)((w + SC_W - 1) / SC_W);
+    hp.tiles_h = (int)((h + SC_H - 1) / SC_H);
+    hp.tiles_d = (int)((d + SC_D - 1) / SC_D);
     hp.n_ntiles = (c_out + bn - 1) / bn;
     hp.num_tiles = (int)(n * hp.tiles_d * hp.tiles_h * hp.tiles_w * hp.n_ntiles);
     hp.n_chunks = 1;
@@ -375,10 +506,6 @@ cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t
         CF_SC_CASE(32)
         CF_SC_CASE(48)
         CF_SC_CASE(64)
-        CF_SC_CASE(80)
-        CF_SC_CASE(96)
-        CF_SC_CASE(112)
-        CF_SC_CASE(128)
         default: return CF_ERR_UNSUPPORTED;
     }
 #undef CF_SC_CASE

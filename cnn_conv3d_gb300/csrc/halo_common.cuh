@@ -1,7 +1,7 @@
 // halo_common.cuh -- output-tile shape and epilogue shared by the kernels
 // that compute a 2 x 16 x 8 voxel tile as two M=128 accumulators (one per
-// plane, row r = 8*line + voxel): the halo-tile implicit GEMM (conv_halo.cu)
-// and the small-channel first layer (conv_smallc.cu).
+// plane, row r = 8*line + voxel): the halo-tile implicit GEMM (conv_halo.cu).
+// The small-channel first layer (conv_smallc.cu) shares the parameter block.
 #pragma once
 
 #include "conv_common.cuh"
@@ -50,30 +50,16 @@ __device__ __forceinline__ void pool_combine(float& v, int& k, float v2, int k2)
     }
 }
 
-// Line of the tile held by row `lane` of TMEM lane quarter q.  Plain order:
-// row r = 8*line + voxel.  Interleaved order (kernels whose rows are written
-// by threads, not by descriptors): the four 8-row groups of a quarter hold
-// lines 0, 2, 1, 3 (of the quarter's 4 lines), so that a half-warp's two
-// lines lie 2 halo lines apart -- for a 96-byte halo line pitch, 192 bytes,
-// which puts their 64-byte segments in complementary shared-memory banks.
-// Vertical pool neighbours are then 16 lanes apart instead of 8.
-template <bool ILV>
-__device__ __forceinline__ int tile_line(int q, int lane) {
-    const int g = lane >> 3;
-    return q * 4 + (ILV ? (((g & 1) << 1) | (g >> 1)) : g);
-}
-
 // Epilogue of one tile for the accumulator columns c_begin, c_begin + step,
 // ... (CH columns per pass); CH = 0 picks min(BN, 32) and step CH.  Several
-// warps per TMEM lane quarter can thus split the channels of a tile.  ILV:
-// interleaved row order (tile_line).
-template <int BN, int EPI, int CH_ = 0, bool ILV = false>
+// warps per TMEM lane quarter can thus split the channels of a tile.
+template <int BN, int EPI, int CH_ = 0>
 __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& t, uint32_t tmem_base,
                                               uint32_t acc_col, int q, int lane, int c_begin = 0,
                                               int c_step = 0) {
     constexpr int CH = CH_ != 0 ? CH_ : (BN >= 32 ? 32 : 16);  // accumulator columns per pass
-    constexpr int HPAIR = ILV ? 16 : 8;                          // lane distance of vertical neighbours
-    const int j = tile_line<ILV>(q, lane), l = lane & 7;
+    const int r = q * 32 + lane;
+    const int j = r >> 3, l = r & 7;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
     const int h = t.h0 + j, w = t.w0 + l;
     const int step = c_step != 0 ? c_step : CH;
@@ -109,7 +95,7 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
                 int k = kbase;
                 pool_combine(v, k, __uint_as_float(a1[cc]), kbase + 4);
                 pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 1), __shfl_xor_sync(0xffffffffu, k, 1));
-                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, HPAIR), __shfl_xor_sync(0xffffffffu, k, HPAIR));
+                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 8), __shfl_xor_sync(0xffffffffu, k, 8));
                 const float s = v + bias[cc];
                 const float y = s > 0.f ? s : p.ea.slope * s;
                 const uint32_t yb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y));
