@@ -251,28 +251,9 @@ def run_ours(args, rank, world, local_rank):
             e = torch.cuda.Event(enable_timing=True)
             e.record(stream)
             evs.append((key, e))
-        for l in range(st.L):
-            mark(f"fwd{l + 1}")
-            cf.cf_conv3d_fwd(st.desc(l), st.block_input(l), st.w[l], (st.b[l], st.slope, st.idx[l]),
-                             st.y[l], None, 0, stream)
+        st.forward(stream, mark)
         mark("fwd_end")
-        wsb = st.ws.numel()
-        for l in range(st.L - 1, -1, -1):
-            nn, d, h, w = st.dims[l]
-            co = ch[l + 1]
-            mark(f"poolbwd{l + 1}")
-            if l == st.L - 1:
-                cf.cf_bias_lrelu_pool_bwd(nn, d, h, w, co, dy, st.y[l], st.idx[l], st.slope, st.dz[l], None,
-                                          st.db[l], st.ws, wsb, stream)
-            else:
-                cf.cf_bias_lrelu_pool_bwd(nn, d, h, w, co, st.g[l], None, st.idx[l], st.slope, st.dz[l], None,
-                                          st.db[l], st.ws, wsb, stream)
-            mark(f"wgrad{l + 1}")
-            cf.cf_conv3d_wgrad(st.desc(l), st.block_input(l), st.dz[l], None, st.dw[l], 0, st.ws, wsb, stream)
-            if l > 0:
-                mark(f"dgrad{l + 1}")
-                cf.cf_conv3d_dgrad(st.desc(l), st.dz[l], None, st.w[l], st.block_input(l), st.slope,
-                                   st.g[l - 1], st.ws, wsb, stream)
+        st.backward(dy, stream, mark)
         mark("end")
 
     clk = Clocks(local_rank).__enter__()

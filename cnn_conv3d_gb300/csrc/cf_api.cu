@@ -146,7 +146,7 @@ size_t cf_workspace_size(int op, const cf_conv_desc* desc) {
         case CF_OP_DGRAD: return wt;
         case CF_OP_DGRAD_ROUTED: return wt + dense;
         case CF_OP_WGRAD: return part;
-        case CF_OP_WGRAD_ROUTED: return part + dense;
+        case CF_OP_WGRAD_ROUTED: return part + (wgrad_routed_fused(desc->c_in) ? 0 : dense);
         case CF_OP_POOL_BWD: return round_up(pool_bwd_workspace_bytes(ctx.num_sms, desc->c_out), 256);
     }
     return 0;
@@ -224,8 +224,12 @@ cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uin
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
     const size_t part = round_up(
         wgrad_workspace_bytes(ctx.num_sms, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out), 256);
-    const size_t need = part + (idx ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0);
+    const bool fused = idx && wgrad_routed_fused(desc->c_in);
+    const size_t need = part + (idx && !fused ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0);
     if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
+    if (fused)
+        return launch_wgrad(ctx, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out, x, dz, idx, dw,
+                            accumulate, ws, part);
     const uint16_t* dz_dense = dz;
     if (idx) {
         uint16_t* buf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + part);
@@ -234,7 +238,7 @@ cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uin
         if (st != CF_OK) return st;
         dz_dense = buf;
     }
-    return launch_wgrad(ctx, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out, x, dz_dense, dw,
+    return launch_wgrad(ctx, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out, x, dz_dense, nullptr, dw,
                         accumulate, ws, part);
 }
 

@@ -72,9 +72,12 @@ cf_status launch_wgrad_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
 
 // conv_wgrad.cu -------------------------------------------------------------
 size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out);
+// true when launch_wgrad takes the routed form (idx != NULL: dz pooled, the
+// dense dZ expanded on chip) for this c_in
+bool wgrad_routed_fused(int c_in);
 cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
-                       const uint16_t* x, const uint16_t* dz, float* dw, int accumulate, void* ws,
-                       size_t ws_bytes);
+                       const uint16_t* x, const uint16_t* dz, const uint8_t* idx, float* dw, int accumulate,
+                       void* ws, size_t ws_bytes);
 
 // elementwise.cu ------------------------------------------------------------
 cf_status launch_pool_fwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,

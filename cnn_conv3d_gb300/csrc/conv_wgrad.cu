@@ -13,73 +13,15 @@
 // fp32 accumulator (TMEM) is written to a partial buffer [split][co][27*c_in],
 // and a second kernel sums the splits in a fixed order into dW.
 //
-// The small-channel variant (c_in = 1 or 4) builds the A tile with producer
-// threads (im2col rows = voxels, 27*c_in columns padded to 128) because TMA
-// cannot address 2- or 8-byte channel rows; its K block is the 128-voxel box.
+// The small-channel variant (c_in = 1 or 4, conv_wgrad_smallc.cu) builds the
+// A tile with builder warps (im2col rows = voxels, 27*c_in columns padded to
+// 128) because TMA cannot address 2- or 8-byte channel rows.
 #include <algorithm>
 
 #include "smallc_common.cuh"
+#include "wgrad_common.cuh"
 
 namespace cf {
-
-struct WgradGeom {
-    int N, D, H, W, Cin, Cout;
-    int vw, vh, vd;           // voxel box (K block)
-    int nb_w, nb_h, nb_d;     // boxes per dimension
-    int64_t total_boxes;      // N * nb_d * nb_h * nb_w
-    int n_mblocks;            // ceil(27*Cin / 128)
-    int n_splits;
-    int64_t boxes_per_split;
-    int num_units;            // n_mblocks * n_splits
-};
-
-// Box cursor: decodes a linear box index once, then steps through the boxes
-// with carries (no divisions on the per-stage path).
-struct BoxCursor {
-    int n, bd, bh, bw;
-    __device__ __forceinline__ void init(const WgradGeom& g, int64_t b) {
-        bw = (int)(b % g.nb_w);
-        b /= g.nb_w;
-        bh = (int)(b % g.nb_h);
-        b /= g.nb_h;
-        bd = (int)(b % g.nb_d);
-        n = (int)(b / g.nb_d);
-    }
-    __device__ __forceinline__ void next(const WgradGeom& g) {
-        if (++bw == g.nb_w) {
-            bw = 0;
-            if (++bh == g.nb_h) {
-                bh = 0;
-                if (++bd == g.nb_d) {
-                    bd = 0;
-                    ++n;
-                }
-            }
-        }
-    }
-};
-
-// Writes the unit's accumulator rows (t,ci) < 27*Cin into part[split][co][row].
-template <int BN>
-__device__ __forceinline__ void wgrad_store_partial(const WgradGeom& g, float* part, int mb, int split,
-                                                    uint32_t tmem_base, int q, int lane) {
-    const int row = q * 32 + lane;
-    const int mrow = mb * 128 + row;
-    const int KK = 27 * g.Cin;
-    const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
-    float* base = part + (int64_t)split * g.Cout * KK + mrow;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-        uint32_t r[32];
-        tmem_ld16(lane_addr + c, r);
-        tmem_ld_wait();
-        if (mrow < KK) {
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                if (c + k < g.Cout) base[(int64_t)(c + k) * KK] = __uint_as_float(r[k]);
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------
 // generic: c_in a multiple of 32
@@ -280,232 +222,6 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-// ---------------------------------------------------------------------------
-// small channel count: c_in in {1, 4}; one M block (27*c_in <= 128 rows);
-// K block = one 128-voxel box (2 x th x tw).  A TMA producer loads the box's
-// input halo and its dZ rows; four builder warps gather each voxel's im2col
-// row from the halo (warp shuffles for the w neighbours) and store it into the
-// MN-major SW128 A tile (row = voxel, 128 (t,ci) columns in two 64-wide atoms).
-
-template <int CIN, int BN, int SUBB>
-struct WgSmallCfg {
-    static constexpr uint32_t A_BYTES = 128 * 128 * 2;  // 128 voxels x 128 (t,ci)
-    static constexpr uint32_t B_BYTES = BN * 128 * 2;   // 128 voxels x BN
-    static constexpr uint32_t HALO_MAX = 4096 + 1024;
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + HALO_MAX;
-    static constexpr uint32_t B_SUB_BYTES = 128 * SUBB * 2;
-    static constexpr uint32_t BAR_BYTES = 256;
-    static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - BAR_BYTES;
-    static constexpr int STAGES_RAW = (int)(BUDGET / STAGE_BYTES);
-    static constexpr int STAGES = STAGES_RAW > 4 ? 4 : STAGES_RAW;
-    static constexpr uint32_t SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
-    static constexpr uint32_t SWZ_B = SUBB == 64 ? SWZ_128B : (SUBB == 32 ? SWZ_64B : SWZ_32B);
-    static constexpr uint32_t SBO_B = 8 * SUBB * 2;
-    static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
-    static constexpr uint32_t IDESC = idesc_bf16(128, BN, 1, 1);
-    static_assert(STAGES >= 2, "not enough shared memory");
-};
-
-struct WgSmallParams {
-    WgradGeom g;  // vw,vh,vd = the 128-voxel box (2 x th x tw)
-    float* part;
-    int* status;
-    uint64_t wait_ns;
-};
-
-template <int CIN, int BN, int SUBB>
-__global__ void __launch_bounds__(320, 1)
-    wgrad_smallc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmG,
-                        const WgSmallParams p) {
-    using C = WgSmallCfg<CIN, BN, SUBB>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* ring = smem;  // stage: [A 32 KB][B][halo]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-    uint64_t* loaded = bars;               // TMA halo + dZ landed (tx)
-    uint64_t* built = bars + C::STAGES;    // A tile written (128 builders)
-    uint64_t* empty = bars + 2 * C::STAGES;  // MMAs of the stage done
-    uint64_t* tfull = bars + 3 * C::STAGES;
-    uint64_t* tempty = tfull + 1;
-    uint64_t* drain = tempty + 1;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    volatile int* epi_flag = abort_flag + 1;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const WgradGeom& g = p.g;
-    const uint32_t halo_tx = (uint32_t)halo_bytes(g.vw, g.vh, g.vd, CIN);
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&loaded[s], 1);
-            mbar_init(&built[s], 128);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_init(tfull, 1);
-        mbar_init(tempty, 128);
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-        tma_prefetch_desc(&tmH);
-        tma_prefetch_desc(&tmG);
-    }
-    // the A columns the builders never write (k >= 8 * words) stay zero
-    for (int e = threadIdx.x; e < C::STAGES * (int)(C::A_BYTES / 16); e += blockDim.x) {
-        const int s = e / (C::A_BYTES / 16), o = e % (C::A_BYTES / 16);
-        *reinterpret_cast<uint4*>(ring + s * C::STAGE_BYTES + o * 16) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();
-    if (warp == 5) {
-        tmem_alloc(tmem_holder, C::TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_holder;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer: halo of the box + its dZ rows
-            int stage = 0;
-            uint32_t phase = 0, issued = 0, par = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
-                const int64_t b0 = (int64_t)u * g.boxes_per_split;
-                const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
-                BoxCursor cur;
-                cur.init(g, b0);
-                for (int64_t b = b0; b < b1; ++b, cur.next(g)) {
-                    const int n = cur.n, d0 = cur.bd * g.vd, h0 = cur.bh * g.vh, w0 = cur.bw * g.vw;
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* st = ring + stage * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&loaded[stage], halo_tx + C::B_BYTES);
-                    load_halo<CIN>(st + C::A_BYTES + C::B_BYTES, &tmH, &loaded[stage], n, d0, h0, w0);
-#pragma unroll
-                    for (int s = 0; s < BN / SUBB; ++s)
-                        tma_load_5d(st + C::A_BYTES + s * C::B_SUB_BYTES, &tmG, &loaded[stage], s * SUBB, w0, h0, d0,
-                                    n);
-                    issued |= 1u << stage;
-                    par = (par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-            if (!ok) {
-                for (int s = 0; s < C::STAGES; ++s)
-                    if (issued & (1u << s)) mbar_wait_timed(&loaded[s], (par >> s) & 1, p.wait_ns);
-            }
-        }
-    } else if (warp < 5) {
-        // ---------------- builders (warps 1..4): one voxel row each
-        const int row = threadIdx.x - 32;
-        const int l = row % g.vw, j = (row / g.vw) % g.vh, i = row / (g.vw * g.vh);
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
-            const int64_t b0 = (int64_t)u * g.boxes_per_split;
-            const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
-            for (int64_t b = b0; b < b1; ++b) {
-                // all lanes wait; the warp leaves together (shuffles need the full warp)
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&loaded[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL, kNapNs))) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* st = ring + stage * C::STAGE_BYTES;
-                uint32_t wd[56];
-                if (CIN == 4)
-                    gather_row_c4(st + C::A_BYTES + C::B_BYTES, g.vw, g.vh, i, j, l, wd);
-                else
-                    gather_row_c1(st + C::A_BYTES + C::B_BYTES, g.vw, g.vh, i, j, l, wd);
-                constexpr int NCH = CIN == 4 ? 14 : 4;  // 16-byte chunks holding real (t,ci) columns
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    const int atom = c >> 3, cin_atom = c & 7;
-                    *reinterpret_cast<uint4*>(st + atom * (128 * 128) + row * 128 + ((cin_atom ^ (row & 7)) << 4)) =
-                        make_uint4(wd[4 * c], wd[4 * c + 1], wd[4 * c + 2], wd[4 * c + 3]);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&built[stage]);
-                if (++stage == C::STAGES) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-        }
-    } else if (warp == 5) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            int stage = 0;
-            uint32_t phase = 0, local = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x, ++local) {
-                const int64_t b0 = (int64_t)u * g.boxes_per_split;
-                const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
-                if (!mbar_wait(tempty, (local & 1) ^ 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_TMEM_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                bool first = true;
-                for (int64_t b = b0; b < b1; ++b) {
-                    if (!mbar_wait(&built[stage], phase, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(ring + stage * C::STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + C::A_BYTES;
-#pragma unroll
-                    for (int k = 0; k < 128 / 16; ++k) {
-                        const uint64_t ad = sdesc(a_addr + k * 16 * 128, 128 * 128, 1024, SWZ_128B);
-                        const uint64_t bd = sdesc(b_addr + k * 16 * SUBB * 2, C::B_SUB_BYTES, C::SBO_B, C::SWZ_B);
-                        umma_bf16(tmem_base, ad, bd, C::IDESC, first ? 0u : 1u);
-                        first = false;
-                    }
-                    umma_commit(&empty[stage]);
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-                if (!ok) break;
-                umma_commit(tfull);
-            }
-            if (!ok) {
-                umma_commit(drain);
-                mbar_wait_timed(drain, 0, p.wait_ns);
-            }
-        }
-    } else {
-        // ---------------- epilogue warps 6..9
-        const int q = warp & 3;
-        const int et = threadIdx.x - 192;
-        uint32_t local = 0;
-        for (int u = blockIdx.x; u < g.num_units; u += gridDim.x, ++local) {
-            if (!epi_wait(tfull, local & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
-            tc_fence_after();
-            wgrad_store_partial<BN>(g, p.part, 0, u, tmem_base, q, lane);
-            tc_fence_before();
-            mbar_arrive(tempty);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 5) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
-    }
-}
-
 // dW[i] = (accumulate ? dW[i] : 0) + sum_{s < splits} part[s][i], s ascending.
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw, int64_t count,
                                      int splits, int accumulate) {
@@ -529,10 +245,9 @@ static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_
     g.Cout = c_out;
     const bool small = c_in == 1 || c_in == 4;
     if (small) {
-        TileGeom t = choose_tile(d, h, w);
-        g.vw = t.tw;
-        g.vh = t.th;
-        g.vd = t.td;
+        g.vw = 16;  // the small-channel kernel's box: 2 planes x 4 lines x 16 voxels
+        g.vh = 4;
+        g.vd = 2;
         g.n_mblocks = 1;
     } else {
         g.vw = w >= 64 ? 64 : (w >= 32 ? 32 : (w >= 16 ? 16 : 8));
@@ -552,6 +267,8 @@ static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_
     g.num_units = g.n_mblocks * g.n_splits;
     return g;
 }
+
+bool wgrad_routed_fused(int c_in) { return c_in == 1 || c_in == 4; }
 
 size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out) {
     if (wgrad_halo_supported(c_in, c_out))
@@ -596,29 +313,10 @@ static cf_status run_wgrad(const LaunchCtx& ctx, const WgradGeom& g, const uint1
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
-template <int CIN, int BN, int SUBB>
-static cf_status run_wgrad_small(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
-                                 float* part) {
-    using C = WgSmallCfg<CIN, BN, SUBB>;
-    if (halo_bytes(g.vw, g.vh, g.vd, CIN) > (int)C::HALO_MAX) return CF_ERR_UNSUPPORTED;
-    CUtensorMap th, tg;
-    if (!make_halo_map(&th, x, g.N, g.D, g.H, g.W, CIN, g.vw, g.vh, g.vd)) return CF_ERR_CUDA;
-    if (!make_act_map(&tg, dz, g, g.Cout, SUBB)) return CF_ERR_CUDA;
-    WgSmallParams p{g, part, ctx.status, ctx.wait_ns};
-    auto kern = wgrad_smallc_kernel<CIN, BN, SUBB>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-        return CF_ERR_CUDA;
-    const int grid = wg_grid(kern, C::SMEM, 320, ctx.num_sms, g.num_units, C::TMEM_COLS);
-    kern<<<grid, 320, C::SMEM, ctx.stream>>>(th, tg, p);
-    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
-}
-
 template <int BN>
 static cf_status wgrad_bn(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
                           float* part) {
     constexpr int SUBB = BN >= 64 ? 64 : BN;
-    if (g.Cin == 4) return run_wgrad_small<4, BN, SUBB>(ctx, g, x, dz, part);
-    if (g.Cin == 1) return run_wgrad_small<1, BN, SUBB>(ctx, g, x, dz, part);
     if (g.Cin % 64 == 0) return run_wgrad<BN, 64, SUBB>(ctx, g, x, dz, part);
     return run_wgrad<BN, 32, SUBB>(ctx, g, x, dz, part);
 }
@@ -632,8 +330,10 @@ static cf_status launch_splitk_reduce(const LaunchCtx& ctx, const float* part, f
 }
 
 cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
-                       const uint16_t* x, const uint16_t* dz, float* dw, int accumulate, void* ws, size_t ws_bytes) {
+                       const uint16_t* x, const uint16_t* dz, const uint8_t* idx, float* dw, int accumulate, void* ws,
+                       size_t ws_bytes) {
     if (!(c_in == 1 || c_in == 4 || c_in % 32 == 0)) return CF_ERR_UNSUPPORTED;
+    if (idx && !wgrad_routed_fused(c_in)) return CF_ERR_UNSUPPORTED;
     if (!(c_out == 16 || c_out == 32 || c_out % 64 == 0) || c_out > 256) return CF_ERR_UNSUPPORTED;
     if ((c_in == 1 || c_in == 4) && (w * c_in) % 8 != 0) return CF_ERR_UNSUPPORTED;
     const size_t need = wgrad_workspace_bytes(ctx.num_sms, n, d, h, w, c_in, c_out);
@@ -648,6 +348,11 @@ cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, in
     }
     WgradGeom g = wgrad_geom(ctx.num_sms, n, d, h, w, c_in, c_out);
     n_splits = g.n_splits;
+    if (c_in == 1 || c_in == 4) {
+        st = launch_wgrad_smallc(ctx, g, x, dz, idx, part);
+        if (st != CF_OK) return st;
+        return launch_splitk_reduce(ctx, part, dw, (int64_t)c_out * 27 * c_in, n_splits, accumulate);
+    }
     switch (c_out) {
         case 16: st = wgrad_bn<16>(ctx, g, x, dz, part); break;
         case 32: st = wgrad_bn<32>(ctx, g, x, dz, part); break;

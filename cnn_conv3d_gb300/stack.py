@@ -14,6 +14,10 @@ One training step of the stack (forward + backward):
             l > 0: cf_conv3d_dgrad(dZ_l, W_l, x_act = x_l) -> g_{l-1}
             (g_{l-1} already carries the leaky-ReLU derivative of block l-1;
             the first block's input gradient has no consumer and is skipped)
+  The first block, when its input has 1 or 4 channels, needs dZ only for its
+  weight gradient: the pool backward then computes db alone and
+  cf_conv3d_wgrad takes the pooled gradient with the argmax codes (routed
+  form), expanding dZ on chip; its dense dZ is never allocated.
 """
 from __future__ import annotations
 
@@ -48,19 +52,25 @@ class CosmoStack:
             for l in range(self.L):
                 n_, d, h, w = self.dims[l]
                 co = channels[l + 1]
-                self.dz.append(torch.empty((n_, d, h, w, co), dtype=bf, device=device))
+                self.dz.append(None if self.routed(l) else torch.empty((n_, d, h, w, co), dtype=bf, device=device))
                 self.dw.append(torch.empty((co, 3, 3, 3, channels[l]), dtype=f32, device=device))
                 self.db.append(torch.empty((co,), dtype=f32, device=device))
                 # g[l]: gradient w.r.t. block l's pooled pre-activation (dgrad output of block l+1)
+                # (for a routed top block: its pooled pre-activation gradient)
                 self.g.append(torch.empty((n_, d // 2, h // 2, w // 2, co), dtype=bf, device=device)
-                              if l < self.L - 1 else None)
+                              if l < self.L - 1 or self.routed(l) else None)
             for l in range(self.L):
                 desc = self.desc(l)
-                ws = max(ws, cf.cf_workspace_size(cf.CF_OP_WGRAD, desc))
+                ws = max(ws, cf.cf_workspace_size(cf.CF_OP_WGRAD_ROUTED if self.routed(l) else cf.CF_OP_WGRAD,
+                                                  desc))
                 ws = max(ws, cf.cf_workspace_size(cf.CF_OP_POOL_BWD, desc))
                 if l > 0:
                     ws = max(ws, cf.cf_workspace_size(cf.CF_OP_DGRAD, desc))
         self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=device)
+
+    def routed(self, l) -> bool:
+        """Block l's weight gradient takes the pooled gradient + argmax codes."""
+        return l == 0 and self.channels[0] in (1, 4)
 
     def desc(self, l):
         n, d, h, w = self.dims[l]
@@ -81,25 +91,40 @@ class CosmoStack:
             up(self.w[l], ws_u16[l])
             self.b[l].copy_(torch.from_numpy(np.ascontiguousarray(bs_f32[l], dtype=np.float32)))
 
-    def forward(self, stream=None):
+    def forward(self, stream=None, mark=None):
+        """mark(key), if given, is called before each launch (key "fwd<l+1>")."""
         for l in range(self.L):
+            if mark:
+                mark(f"fwd{l + 1}")
             cf.cf_conv3d_fwd(self.desc(l), self.block_input(l), self.w[l], (self.b[l], self.slope, self.idx[l]),
                              self.y[l], None, 0, stream)
 
-    def backward(self, dy, stream=None):
+    def backward(self, dy, stream=None, mark=None):
+        """mark(key), if given, is called before each op ("poolbwd<l+1>",
+        "wgrad<l+1>", "dgrad<l+1>")."""
         ws, wsb = self.ws, self.ws.numel()
         for l in range(self.L - 1, -1, -1):
             n, d, h, w = self.dims[l]
             co = self.channels[l + 1]
+            routed = self.routed(l)
+            if mark:
+                mark(f"poolbwd{l + 1}")
             if l == self.L - 1:
                 cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope, self.dz[l],
-                                          None, self.db[l], ws, wsb, stream)
+                                          self.g[l] if routed else None, self.db[l], ws, wsb, stream)
             else:
                 cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope, self.dz[l],
                                           None, self.db[l], ws, wsb, stream)
             desc = self.desc(l)
-            cf.cf_conv3d_wgrad(desc, self.block_input(l), self.dz[l], None, self.dw[l], 0, ws, wsb, stream)
+            if mark:
+                mark(f"wgrad{l + 1}")
+            if routed:
+                cf.cf_conv3d_wgrad(desc, self.block_input(l), self.g[l], self.idx[l], self.dw[l], 0, ws, wsb, stream)
+            else:
+                cf.cf_conv3d_wgrad(desc, self.block_input(l), self.dz[l], None, self.dw[l], 0, ws, wsb, stream)
             if l > 0:
+                if mark:
+                    mark(f"dgrad{l + 1}")
                 cf.cf_conv3d_dgrad(desc, self.dz[l], None, self.w[l], self.block_input(l), self.slope,
                                    self.g[l - 1], ws, wsb, stream)
 

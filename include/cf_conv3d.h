@@ -108,7 +108,11 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
  * split over voxels):
  *   dW[co,t,ci] = sum_{n,v} dZ[n,v,co] * X[n, v+(t-1), ci]   (X zero-padded)
  * accumulated in fp32 (split-K over n*d*h*w with a fixed-order reduction).
- *   dz/idx : as in cf_conv3d_dgrad.
+ *   dz/idx : as in cf_conv3d_dgrad.  For c_in 1 or 4 the routed form is fused:
+ *        the kernel expands each K block of dZ in shared memory from the pooled
+ *        gradient and the codes (no dense dZ, no workspace beyond the split-K
+ *        partials); d, h, w must be even.  Other c_in expand dZ into the
+ *        workspace first.  cf_workspace_size(CF_OP_WGRAD_ROUTED) covers both.
  *   dw : [c_out][3][3][3][c_in] fp32; accumulate != 0 adds to it, else overwrites.
  * Supported: c_in in {1, 4} (w * c_in a multiple of 8) or a multiple of 32;
  * c_out 16, 32 or a multiple of 64, <= 256.

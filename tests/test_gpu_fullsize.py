@@ -106,9 +106,19 @@ def _check_forward(oracle_mod, st, inp, rng, k):
                            rng, k, f"block {l + 1} forward")
 
 
+def _routed_dz_channel(oracle_mod, g16, y16, idx, co):
+    """Dense dZ of channel co (bf16 bits, [n][d][h][w][1]) routed by the oracle
+    from the pooled gradient and the argmax codes."""
+    f = oracle_mod.bf16_bits_to_f64
+    gy = None if y16 is None else f(y16[..., co:co + 1])
+    dz, _, _ = oracle_mod.pool_bwd(f(g16[..., co:co + 1]), gy, np.ascontiguousarray(idx[..., co:co + 1]), SLOPE)
+    return synthdata.to_bf16_bits(dz)
+
+
 def _pool_bwd_checks(oracle_mod, g16, y16, idx, gdb, dz16, rng, what):
-    """Bias gradient (oracle over slabs of the pooled tensor) and the routed
-    dZ at sampled windows (oracle on the extracted windows)."""
+    """Bias gradient (oracle over slabs of the pooled tensor) and, when the
+    dense dZ was written (dz16 not None), the routed dZ at sampled windows
+    (oracle on the extracted windows)."""
     f = oracle_mod.bf16_bits_to_f64
     C = g16.shape[-1]
     db = np.zeros(C)
@@ -121,6 +131,8 @@ def _pool_bwd_checks(oracle_mod, g16, y16, idx, gdb, dz16, rng, what):
             db += part
             sabs += np.abs(gp).reshape(-1, C).sum(0)
     assert_close(gdb, db, sabs, f"db {what}")
+    if dz16 is None:
+        return
     # K sampled windows as K one-channel 2x2x2 windows
     K = 2048
     pw = rand_pts(rng, g16.shape, K)
@@ -142,14 +154,26 @@ def _check_backward(oracle_mod, st, inp, dy, rng, k_dx, k_dw):
         g16 = u16(dy) if l == L - 1 else u16(st.g[l])
         y16 = u16(st.y[l]) if l == L - 1 else None
         idx = st.idx[l].cpu().numpy()
-        dz16 = u16(st.dz[l])
+        dz16 = None if st.routed(l) else u16(st.dz[l])
         _pool_bwd_checks(oracle_mod, g16, y16, idx, st.db[l].cpu().numpy().astype(np.float64), dz16, rng,
                          f"block {l + 1}")
         # weight gradient at sampled filter taps (sum over every sample and voxel)
         x16 = u16(st.block_input(l))
         pts = rand_pts(rng, st.dw[l].shape, k_dw)
+        got = st.dw[l].cpu().numpy()[tuple(pts.T)].astype(np.float64)
+        if dz16 is None:
+            # routed weight gradient: the oracle routes dZ of each sampled channel
+            ref, S = np.zeros(len(pts)), np.zeros(len(pts))
+            for co in np.unique(pts[:, 0]):
+                sel = np.nonzero(pts[:, 0] == co)[0]
+                dzc = _routed_dz_channel(oracle_mod, g16, y16, idx, int(co))
+                p1 = pts[sel].copy()
+                p1[:, 0] = 0
+                ref[sel], S[sel] = oracle_mod.conv3d_wgrad_pts(x16, dzc, p1)
+            assert_close(got, ref, S, f"dW{l + 1} (routed)")
+            continue
         ref, S = oracle_mod.conv3d_wgrad_pts(x16, dz16, pts)
-        assert_close(st.dw[l].cpu().numpy()[tuple(pts.T)].astype(np.float64), ref, S, f"dW{l + 1}")
+        assert_close(got, ref, S, f"dW{l + 1}")
         if l > 0:
             # input gradient times the previous block's leaky-ReLU derivative
             pts = rand_pts(rng, x16.shape, k_dx)

@@ -292,7 +292,17 @@ def test_conv_wgrad(cf, oracle_mod, shape):
 
 # ----------------------------------------------------------------------------- argmax-routed inputs
 
-@pytest.mark.parametrize("shape", [(2, 4, 6, 40, 32, 64), (1, 4, 4, 16, 4, 32)])
+ROUTED_SHAPES = [
+    (2, 4, 6, 40, 32, 64),
+    (1, 4, 4, 16, 4, 32),      # small c_in: dZ expanded on chip by the weight-gradient kernel
+    (2, 4, 6, 40, 4, 32),      # ragged box in w (40 = 2.5 boxes of 16)
+    (1, 2, 8, 24, 1, 16),
+    (1, 2, 4, 16, 4, 64),
+    (1, 2, 4, 16, 4, 256),
+]
+
+
+@pytest.mark.parametrize("shape", ROUTED_SHAPES)
 def test_routed_gradients_match_dense(cf, oracle_mod, shape):
     import torch
     N, D, H, W, Ci, Co = shape
@@ -311,6 +321,8 @@ def test_routed_gradients_match_dense(cf, oracle_mod, shape):
     ref = oracle_mod.conv3d_wgrad(x, rdz)
     S = oracle_mod.conv3d_wgrad(np.abs(x), np.abs(rdz))
     assert_close(dw.cpu().numpy().astype(np.float64), ref, S, "routed wgrad")
+    cf.cf_conv3d_wgrad(desc, dev_bf16(c["x"]), dev_bf16(g16), dev(ridx), dw, 1, ws, wsb)
+    assert_close(dw.cpu().numpy().astype(np.float64), 2 * ref, 2 * S, "routed wgrad acc")
     if Ci % 16 == 0 and Co % 32 == 0:
         ws, wsb = _ws(cf, cf.CF_OP_DGRAD_ROUTED, desc)
         dx = empty_bf16((N, D, H, W, Ci))
