@@ -54,7 +54,7 @@ struct HaloCfg {
 };
 
 template <int BN, int KC, int EPI, bool RES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     conv_halo_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const HaloParams p) {
     using C = HaloCfg<BN, KC, EPI, RES>;
@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* wempty = wfull + C::WS;
     uint64_t* tfull = wempty + C::WS;
     uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
-    uint64_t* wres = drain + 1;
+    uint64_t* drain = tempty + 2;  // [2]
+    uint64_t* wres = drain + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(wres + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* epi_flag = abort_flag + 1;
@@ -79,19 +79,20 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        // stages are released and accumulators completed by both MMA issuers
         for (int s = 0; s < C::HS; ++s) {
             mbar_init(&hfull[s], 1);
-            mbar_init(&hempty[s], 1);
+            mbar_init(&hempty[s], 2);
         }
         for (int s = 0; s < C::WS; ++s) {
             mbar_init(&wfull[s], 1);
-            mbar_init(&wempty[s], 1);
+            mbar_init(&wempty[s], 2);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
+            mbar_init(&tfull[a], 2);
             mbar_init(&tempty[a], 128);
+            mbar_init(&drain[a], 1);
         }
-        mbar_init(drain, 1);
         mbar_init(wres, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -166,9 +167,11 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 6) {
         if (lane == 0) {
-            // ---------------- MMA issuer
+            // ---------------- MMA issuers: warp 1 for plane 0, warp 6 for plane 1 (one
+            // thread's issue rate bounds narrow-N MMAs; the planes' accumulators are disjoint)
+            const int i = warp == 1 ? 0 : 1;
             int hs = 0, ws = 0;
             uint32_t hph = 0, wph = 0, local = 0;
             bool ok = true;
@@ -213,13 +216,9 @@ __global__ void __launch_bounds__(192, 1)
                             const uint64_t bw = bg + ((kw * C::W_BYTES) >> 4);
 #pragma unroll
                             for (int k = 0; k < KC / 16; ++k) {
-#pragma unroll
-                                for (int i = 0; i < 2; ++i) {
-                                    constexpr uint32_t plane_rows = HH_H * HH_W;
-                                    const uint64_t ad = ag + (((i * plane_rows + kw) * C::ROW + k * 32) >> 4);
-                                    umma_bf16(d0 + i * BN, ad, bw + ((k * 32) >> 4), C::IDESC,
-                                              (first | kw | k) != 0);
-                                }
+                                constexpr uint32_t plane_rows = HH_H * HH_W;
+                                const uint64_t ad = ag + (((i * plane_rows + kw) * C::ROW + k * 32) >> 4);
+                                umma_bf16(d0 + i * BN, ad, bw + ((k * 32) >> 4), C::IDESC, (first | kw | k) != 0);
                             }
                         }
                         if (!RES) {
@@ -241,8 +240,8 @@ __global__ void __launch_bounds__(192, 1)
                 umma_commit(&tfull[acc]);
             }
             if (!ok) {
-                umma_commit(drain);
-                mbar_wait_timed(drain, 0, p.wait_ns);
+                umma_commit(&drain[i]);
+                mbar_wait_timed(&drain[i], 0, p.wait_ns);
             }
         }
     } else {
@@ -292,8 +291,8 @@ static cf_status run_halo(const LaunchCtx& ctx, HaloParams p, const uint16_t* x,
     auto kern = conv_halo_kernel<BN, KC, EPI, RES>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return CF_ERR_CUDA;
-    const int grid = grid_for(kern, smem, 192, ctx.num_sms, p.num_tiles, C::TMEM_COLS);
-    kern<<<grid, 192, smem, ctx.stream>>>(tx, tw, p);
+    const int grid = grid_for(kern, smem, 224, ctx.num_sms, p.num_tiles, C::TMEM_COLS);
+    kern<<<grid, 224, smem, ctx.stream>>>(tx, tw, p);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
