@@ -90,7 +90,7 @@ __device__ __forceinline__ void wh_block_taps(int b, int& t_first, int& lbo_rows
 }
 
 template <int KC, int BN, int PLANES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     wgrad_halo_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                       const WhParams p) {
     using C = WhCfg<KC, BN, PLANES>;
@@ -102,8 +102,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* empty = bars + C::STAGES;
     uint64_t* tfull = bars + 2 * C::STAGES;
     uint64_t* tempty = tfull + 1;
-    uint64_t* drain = tempty + 1;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* drain = tempty + 1;  // [2]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* epi_flag = abort_flag + 1;
 
@@ -111,13 +111,15 @@ __global__ void __launch_bounds__(192, 1)
     const WhGeom& g = p.g;
 
     if (threadIdx.x == 0) {
+        // stages are released and the accumulators completed by both MMA issuers
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);
         }
-        mbar_init(tfull, 1);
+        mbar_init(tfull, 2);
         mbar_init(tempty, 128);
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmX);
@@ -186,9 +188,11 @@ __global__ void __launch_bounds__(192, 1)
                     if (issued & (1u << s)) mbar_wait_timed(&full[s], (par >> s) & 1, p.wait_ns);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 6) {
         if (lane == 0) {
-            // ---------------- MMA issuer
+            // ---------------- MMA issuers: warp 1 takes the even M blocks of the set,
+            // warp 6 the odd ones (one thread's issue rate bounds narrow-N MMAs)
+            const int mi = warp == 1 ? 0 : 1;
             int stage = 0;
             uint32_t phase = 0, local = 0;
             bool ok = true;
@@ -214,7 +218,7 @@ __global__ void __launch_bounds__(192, 1)
                     tc_fence_after();
                     const uint64_t a_st = adesc_base + ((stage * C::STAGE_BYTES) >> 4);
                     const uint64_t b_st = bdesc_base + ((stage * C::STAGE_BYTES) >> 4);
-                    for (int m = 0; m < nmb; ++m) {
+                    for (int m = mi; m < nmb; m += 2) {
                         int t1, lbo_rows, nreal;
                         wh_block_taps<KC>(mb0 + m, t1, lbo_rows, nreal);
                         const uint64_t a_m = (a_st + ((uint32_t)(wh_tap_offset(t1) * C::ROW) >> 4)) |
@@ -239,12 +243,12 @@ __global__ void __launch_bounds__(192, 1)
                 umma_commit(tfull);
             }
             if (!ok) {
-                umma_commit(drain);
-                mbar_wait_timed(drain, 0, p.wait_ns);
+                umma_commit(&drain[mi]);
+                mbar_wait_timed(&drain[mi], 0, p.wait_ns);
             }
         }
     } else {
-        // ---------------- epilogue: accumulator rows (atom, ci) -> partial[split][co][t*Cin + ci]
+        // ---------------- epilogue (warps 2..5): accumulator rows (atom, ci) -> partial[split][co][t*Cin + ci]
         const int q = warp & 3;
         const int et = threadIdx.x - 64;
         const int r = q * 32 + lane;
@@ -369,7 +373,7 @@ static cf_status run_wgrad_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int6
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return CF_ERR_CUDA;
     const int grid = std::max(1, std::min(g.num_units, ctx.num_sms));
-    kern<<<grid, 192, C::SMEM, ctx.stream>>>(tx, tg, p);
+    kern<<<grid, 224, C::SMEM, ctx.stream>>>(tx, tg, p);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
