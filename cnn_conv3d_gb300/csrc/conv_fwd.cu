@@ -288,8 +288,9 @@ cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
     if (c_in % 32 != 0 || c_out % 16 != 0) return CF_ERR_UNSUPPORTED;
     int bn = c_out <= 256 ? c_out : 256;
     if (c_out > 256 && c_out % 256 != 0) return CF_ERR_UNSUPPORTED;
-    // Small grids: narrower N tiles when that shortens the critical path.  Cost
-    // of a CTA's share = waves x cycles per K step of one MMA 128 x bn x 16,
+    // Small grids: narrower N tiles when that clearly shortens the critical
+    // path (by 20%: narrower tiles re-fetch A once more per N tile).  Cost of a
+    // CTA's share = waves x cycles per K step of one MMA 128 x bn x 16,
     // max(issue ~52, shared-memory operand reads 32 + bn/4, tensor bn/2).
     if (bn >= 128 && bn % 64 == 0 && c_out % 64 == 0) {
         const int64_t tiles_m = make_geom(n, d, h, w, c_in, c_out, bn).num_tiles / ((c_out + bn - 1) / bn);
@@ -300,7 +301,7 @@ cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
         };
         int best = bn;
         for (int b = bn / 2; b >= 64; b /= 2)
-            if (c_out % b == 0 && cost(b) < cost(best)) best = b;
+            if (c_out % b == 0 && 5 * cost(b) < 4 * cost(best)) best = b;
         bn = best;
     }
     const int kc = (c_in % 64 == 0) ? 64 : 32;

@@ -306,11 +306,11 @@ static cf_status halo_epi(const LaunchCtx& ctx, const HaloParams& p, const uint1
     return CF_ERR_INVALID_ARG;
 }
 
-// The halo tile pays off where the per-tap A re-fetch dominates the L2->SM
-// traffic, i.e. for narrow GEMM N; at N = 128 the per-tap kernel with
-// 64-channel chunks is as fast.
+// The halo tile pays off wherever the per-tap A re-fetch of the per-tap
+// kernel would load L2 (it reads each input row once per tap); c_out up to
+// 128 fits two double-buffered accumulator pairs in tensor memory.
 bool halo_path_supported(int c_in, int c_out) {
-    return (c_in % 32 == 0) && (c_out == 32 || c_out == 64);
+    return (c_in % 32 == 0) && (c_out == 32 || c_out == 64 || c_out == 128);
 }
 
 cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
@@ -339,6 +339,7 @@ cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
     switch (c_out) {
         case 32: return resident ? halo_epi<32, 32, true>(ctx, p, x, wk, epi) : halo_epi<32, 32, false>(ctx, p, x, wk, epi);
         case 64: return resident ? halo_epi<64, 32, true>(ctx, p, x, wk, epi) : halo_epi<64, 32, false>(ctx, p, x, wk, epi);
+        case 128: return halo_epi<128, 32, false>(ctx, p, x, wk, epi);
     }
     return CF_ERR_UNSUPPORTED;
 }

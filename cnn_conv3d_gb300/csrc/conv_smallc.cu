@@ -26,8 +26,10 @@
 //                 consecutive voxels of one halo line, 128 contiguous bytes, so
 //                 the loads are free of bank conflicts) and writes it into the
 //                 block's tensor-memory A buffer with tcgen05.st;
-//   warp 1      : tcgen05.mma with A from tensor memory and the filter
-//                 (resident in shared memory, K-major SW128) as B;
+//   warps 1, 18 : tcgen05.mma with A from tensor memory and the filter
+//                 (resident in shared memory, K-major SW128) as B; warp 1
+//                 issues row blocks 0 and 1, warp 18 blocks 2 and 3 (one
+//                 thread's issue rate would bound these N = 32 MMAs);
 //   warps 10..17: epilogue (fused bias + leaky ReLU + 2x2x2 max-pool with
 //                 argmax, or plain bf16), two warps per TMEM lane quarter
 //                 splitting the channels.
@@ -55,7 +57,7 @@ struct SmallTmCfg {
     static constexpr int ACC_COLS = SC_BLOCKS * BN;      // accumulator columns of one tile
     static constexpr int NACC = (2 * ACC_COLS + SC_BLOCKS * PCOLS <= 512) ? 2 : 1;
     static constexpr uint32_t ACOL0 = NACC * ACC_COLS;   // first A column
-    static constexpr uint32_t BAR_BYTES = 8 * (2 * HS + 2 * SC_BLOCKS + 2 * 2 + 1) + 16;
+    static constexpr uint32_t BAR_BYTES = 8 * (2 * HS + 2 * SC_BLOCKS + 2 * 2 + 2) + 16;
     static constexpr uint32_t SMEM = 1024 + B_BYTES + HS * HALO_STRIDE + BAR_BYTES;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
@@ -127,7 +129,7 @@ __device__ __forceinline__ void gather_row(const uint8_t* halo, int pl, int ln, 
 }
 
 template <int CIN, int BN, int EPI>
-__global__ void __launch_bounds__(576, 1)
+__global__ void __launch_bounds__(608, 1)
     conv_smallc_kernel(const __grid_constant__ CUtensorMap tmH, const SmallTmParams sp) {
     using C = SmallTmCfg<CIN, BN, EPI>;
     const HaloParams& p = sp.hp;
@@ -142,8 +144,8 @@ __global__ void __launch_bounds__(576, 1)
     uint64_t* aempty = afull + SC_BLOCKS;
     uint64_t* tfull = aempty + SC_BLOCKS;
     uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* drain = tempty + 2;  // [2]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* epi_flag = abort_flag + 1;
 
@@ -153,17 +155,17 @@ __global__ void __launch_bounds__(576, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::HS; ++s) {
             mbar_init(&hfull[s], 1);
-            mbar_init(&hempty[s], 256);
+            mbar_init(&hempty[s], 8);  // one arrival per builder warp
         }
         for (int b = 0; b < SC_BLOCKS; ++b) {
-            mbar_init(&afull[b], 128);
+            mbar_init(&afull[b], 4);   // one arrival per builder warp of the group
             mbar_init(&aempty[b], 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 256);
+            mbar_init(&tfull[a], 2);  // both MMA issuers
+            mbar_init(&tempty[a], 8);  // one arrival per epilogue warp
+            mbar_init(&drain[a], 1);
         }
-        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmH);
@@ -224,9 +226,10 @@ __global__ void __launch_bounds__(576, 1)
                     if (issued & (1u << s)) mbar_wait_timed(&hfull[s], (par >> s) & 1, p.wait_ns);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 18) {
         if (lane == 0) {
-            // ---------------- MMA issuer: per tile, the four row blocks in order
+            // ---------------- MMA issuers: per tile, row blocks 0, 1 (warp 1) or 2, 3 (warp 18)
+            const int bi = warp == 1 ? 0 : 1;
             uint32_t aph = 0, local = 0;
             bool ok = true;
             const uint32_t b_addr = smem_u32(bsm);
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(576, 1)
                     break;
                 }
 #pragma unroll 1
-                for (int blk = 0; blk < SC_BLOCKS; ++blk) {
+                for (int blk = 2 * bi; blk < 2 * bi + 2; ++blk) {
                     if (!mbar_wait(&afull[blk], aph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
                         ok = false;
                         break;
@@ -259,8 +262,8 @@ __global__ void __launch_bounds__(576, 1)
                 aph ^= 1;
             }
             if (!ok) {
-                umma_commit(drain);
-                mbar_wait_timed(drain, 0, p.wait_ns);
+                umma_commit(&drain[bi]);
+                mbar_wait_timed(&drain[bi], 0, p.wait_ns);
             }
         }
     } else if (warp < 10) {
@@ -284,7 +287,10 @@ __global__ void __launch_bounds__(576, 1)
                 const int blk = g + 2 * b2;
                 uint32_t wd[56];
                 gather_row<CIN>(halo, blk >> 1, 2 * lp + (blk & 1), v, wd);
-                if (b2 == 1) mbar_arrive(&hempty[hs]);
+                if (b2 == 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&hempty[hs]);
+                }
                 if (!__all_sync(0xffffffffu, mbar_wait(&aempty[blk], aph ^ 1, abort_flag, p.wait_ns, p.status,
                                                        WAIT_PRODUCER_EMPTY, kNapNs))) {
                     ok = false;
@@ -301,7 +307,8 @@ __global__ void __launch_bounds__(576, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&afull[blk]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[blk]);
             }
             if (++hs == C::HS) {
                 hs = 0;
@@ -309,7 +316,7 @@ __global__ void __launch_bounds__(576, 1)
             }
             aph ^= 1;
         }
-    } else {
+    } else if (warp < 18) {
         // ---------------- epilogue warps 10..17: two per lane quarter, each taking
         // 16 of every 32 channels (when BN is 16, the second warp of a quarter idles)
         const int q = warp & 3;
@@ -426,7 +433,8 @@ __global__ void __launch_bounds__(576, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
         }
     }
 
@@ -458,9 +466,9 @@ static cf_status run_smallc(const LaunchCtx& ctx, const HaloParams& hp, const ui
     auto kern = conv_smallc_kernel<CIN, BN, EPI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return CF_ERR_CUDA;
-    int grid = grid_for(kern, C::SMEM, 576, ctx.num_sms, hp.num_tiles, C::TMEM_COLS);
+    int grid = grid_for(kern, C::SMEM, 608, ctx.num_sms, hp.num_tiles, C::TMEM_COLS);
     grid = std::max(hp.n_ntiles, grid / hp.n_ntiles * hp.n_ntiles);  // each CTA keeps one N tile
-    kern<<<grid, 576, C::SMEM, ctx.stream>>>(th, sp);
+    kern<<<grid, 608, C::SMEM, ctx.stream>>>(th, sp);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
