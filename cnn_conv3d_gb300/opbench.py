@@ -1,7 +1,7 @@
 """Per-operation benchmark of the conv3d library (single-layer sweep).
 
 python -m cnn_conv3d_gb300.opbench [--ops fwd,dgrad,wgrad] [--shapes S1,S2,...]
-        [--n-scale F] [--pool] [--warmup W] [--iters K] [--json]
+        [--n-scale F] [--pool] [--routed] [--warmup W] [--iters K] [--json]
 
 Shapes S1..S5 are the single-layer sweep (C_in -> C_out, spatial^3, N):
 S1 4->32 @128^3 N=8, S2 32->64 @64^3 N=16, S3 64->128 @32^3 N=32,
@@ -43,6 +43,8 @@ def main(argv=None):
     ap.add_argument("--shapes", default="S1,S2,S3,S4,S5")
     ap.add_argument("--n-scale", type=float, default=1.0)
     ap.add_argument("--pool", action="store_true", help="forward with the fused bias/LReLU/max-pool epilogue")
+    ap.add_argument("--routed", action="store_true",
+                    help="wgrad from the pooled gradient + argmax codes (the fused max-pool backward)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--iters", type=int, default=10)
     ap.add_argument("--json", action="store_true")
@@ -69,7 +71,8 @@ def main(argv=None):
         w = (torch.randn((co, 3, 3, 3, ci), device=dev) * np.sqrt(2.0 / (27 * ci))).to(torch.bfloat16)
         dz = torch.randn((n, sp, sp, sp, co), device=dev).to(torch.bfloat16)
         b = torch.zeros((co,), device=dev)
-        ws_n = max(cf.cf_workspace_size(cf.CF_OP_WGRAD, desc), cf.cf_workspace_size(cf.CF_OP_DGRAD, desc), 256)
+        ws_n = max(cf.cf_workspace_size(cf.CF_OP_WGRAD, desc), cf.cf_workspace_size(cf.CF_OP_DGRAD, desc),
+                   cf.cf_workspace_size(cf.CF_OP_WGRAD_ROUTED, desc) if a.routed else 0, 256)
         ws = torch.empty((ws_n,), dtype=torch.uint8, device=dev)
         flops = 2.0 * co * ci * 27 * n * sp ** 3
         for op in a.ops.split(","):
@@ -91,8 +94,14 @@ def main(argv=None):
                 nbytes = dz.numel() * 2 + w.numel() * 2 + 2 * dx.numel() * 2
             elif op == "wgrad":
                 dw = torch.empty((co, 3, 3, 3, ci), dtype=torch.float32, device=dev)
-                fn = lambda: cf.cf_conv3d_wgrad(desc, x, dz, None, dw, 0, ws, ws_n, stream)
-                nbytes = x.numel() * 2 + dz.numel() * 2 + dw.numel() * 4
+                if a.routed:
+                    gp = torch.randn((n, sp // 2, sp // 2, sp // 2, co), device=dev).to(torch.bfloat16)
+                    gi = torch.randint(0, 8, gp.shape, dtype=torch.uint8, device=dev)
+                    fn = lambda: cf.cf_conv3d_wgrad(desc, x, gp, gi, dw, 0, ws, ws_n, stream)
+                    nbytes = x.numel() * 2 + gp.numel() * 3 + dw.numel() * 4
+                else:
+                    fn = lambda: cf.cf_conv3d_wgrad(desc, x, dz, None, dw, 0, ws, ws_n, stream)
+                    nbytes = x.numel() * 2 + dz.numel() * 2 + dw.numel() * 4
             else:
                 raise SystemExit(f"unknown op {op}")
             for _ in range(a.warmup):
@@ -111,7 +120,8 @@ def main(argv=None):
                 raise SystemExit("device status word set")
             ms = float(np.median(ts))
             tf = flops / (ms * 1e-3) / 1e12
-            rec = {"shape": label, "op": op + ("+pool" if (op == "fwd" and a.pool) else ""), "n": n, "c_in": ci,
+            tag = "+pool" if (op == "fwd" and a.pool) else ("+routed" if (op == "wgrad" and a.routed) else "")
+            rec = {"shape": label, "op": op + tag, "n": n, "c_in": ci,
                    "c_out": co, "spatial": sp, "ms": round(ms, 4), "tflops": round(tf, 1),
                    "frac_bf16_peak": round(tf / peak, 3), "min_bytes_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
                    "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 3)}
