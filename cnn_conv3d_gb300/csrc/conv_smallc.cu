@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(608, 1)
             tc_fence_after();
             const SmallTile t = small_decode(p, tile);
             const uint32_t acol = lane_addr + acc * C::ACC_COLS;
+            bool released = false;
 #pragma unroll
             for (int ps = 0; ps < NPASS; ++ps) {
                 const int c = 32 * ps + 16 * half;  // first of the warp's 16 accumulator columns
@@ -349,34 +350,38 @@ __global__ void __launch_bounds__(608, 1)
                 if (EPI == EPI_POOL) {
                     // per channel: first maximum over the lane's four (plane, line) values,
                     // in the window's scan order (code dd*4 + dh*2 + dw)
-                    uint32_t r0[32], r1[32];
+                    uint32_t r0[32], r1[32], r2[32], r3[32];
                     float m[16];
                     int k[16];
                     tmem_ld16(acol + 0 * BN + c, r0);
                     tmem_ld16(acol + 1 * BN + c, r1);
+                    tmem_ld16(acol + 2 * BN + c, r2);
+                    tmem_ld16(acol + 3 * BN + c, r3);
                     tmem_ld_wait();
+                    if (ps == NPASS - 1 || c + 32 >= BN) {
+                        // the tile's accumulator is in registers: hand it back to the MMA
+                        // before the pooling arithmetic and the stores
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[acc]);
+                        released = true;
+                    }
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
-                        m[cc] = __uint_as_float(r0[cc]);
+                        const float v0 = __uint_as_float(r0[cc]), v1 = __uint_as_float(r1[cc]);
+                        const float v2 = __uint_as_float(r2[cc]), v3 = __uint_as_float(r3[cc]);
+                        m[cc] = v0;
                         k[cc] = dw;
-                        const float b = __uint_as_float(r1[cc]);
-                        if (b > m[cc]) {
-                            m[cc] = b;
+                        if (v1 > m[cc]) {
+                            m[cc] = v1;
                             k[cc] = 2 + dw;
                         }
-                    }
-                    tmem_ld16(acol + 2 * BN + c, r0);
-                    tmem_ld16(acol + 3 * BN + c, r1);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int cc = 0; cc < 16; ++cc) {
-                        const float a = __uint_as_float(r0[cc]), b = __uint_as_float(r1[cc]);
-                        if (a > m[cc]) {
-                            m[cc] = a;
+                        if (v2 > m[cc]) {
+                            m[cc] = v2;
                             k[cc] = 4 + dw;
                         }
-                        if (b > m[cc]) {
-                            m[cc] = b;
+                        if (v3 > m[cc]) {
+                            m[cc] = v3;
                             k[cc] = 6 + dw;
                         }
                     }
@@ -432,9 +437,11 @@ __global__ void __launch_bounds__(608, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (!released) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
         }
     }
 
