@@ -222,13 +222,39 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-// dW[i] = (accumulate ? dW[i] : 0) + sum_{s < splits} part[s][i], s ascending.
-__global__ void splitk_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw, int64_t count,
-                                     int splits, int accumulate) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
-        float s = accumulate ? dw[i] : 0.f;
-        for (int k = 0; k < splits; ++k) s += part[(int64_t)k * count + i];
-        dw[i] = s;
+// dW[i] = (accumulate ? dW[i] : 0) + sum over the splits of part[s][i], in a
+// fixed order: G groups of consecutive splits per column (each group summed
+// ascending in four interleaved partial sums), then the groups in order.
+// A block covers 256 / G columns; its threads read a split's columns
+// contiguously.
+template <int G>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
+                                                            int64_t count, int splits, int accumulate) {
+    constexpr int COLS = 256 / G;
+    __shared__ float red[G][COLS];
+    const int col = threadIdx.x % COLS, grp = threadIdx.x / COLS;
+    const int per = (splits + G - 1) / G;
+    const int s0 = min(splits, grp * per), s1 = min(splits, s0 + per);
+    for (int64_t c0 = (int64_t)blockIdx.x * COLS; c0 < count; c0 += (int64_t)gridDim.x * COLS) {
+        const int64_t i = c0 + col;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        if (i < count) {
+            int k = s0;
+            for (; k + 4 <= s1; k += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) a[u] += __ldg(part + (int64_t)(k + u) * count + i);
+            }
+            for (; k < s1; ++k) a[0] += __ldg(part + (int64_t)k * count + i);
+        }
+        red[grp][col] = (a[0] + a[1]) + (a[2] + a[3]);
+        __syncthreads();
+        if (grp == 0 && i < count) {
+            float t = accumulate ? dw[i] : 0.f;
+#pragma unroll
+            for (int g = 0; g < G; ++g) t += red[g][col];
+            dw[i] = t;
+        }
+        __syncthreads();
     }
 }
 
@@ -323,9 +349,15 @@ static cf_status wgrad_bn(const LaunchCtx& ctx, const WgradGeom& g, const uint16
 
 static cf_status launch_splitk_reduce(const LaunchCtx& ctx, const float* part, float* dw, int64_t count, int splits,
                                       int accumulate) {
-    const int threads = 256;
-    const int blocks = (int)std::min<int64_t>((count + threads - 1) / threads, 4 * (int64_t)ctx.num_sms);
-    splitk_reduce_kernel<<<blocks, threads, 0, ctx.stream>>>(part, dw, count, splits, accumulate);
+    // many splits of few columns (small-channel layers): split groups per block;
+    // few splits of many columns: one group, 256 columns per block
+    auto launch = [&](auto kern, int cols) {
+        const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((count + cols - 1) / cols, 8LL * ctx.num_sms));
+        kern<<<blocks, 256, 0, ctx.stream>>>(part, dw, count, splits, accumulate);
+    };
+    if (splits >= 64) launch(splitk_reduce_kernel<8>, 32);
+    else if (splits >= 16) launch(splitk_reduce_kernel<4>, 64);
+    else launch(splitk_reduce_kernel<1>, 256);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 

@@ -161,16 +161,64 @@ __global__ void colsum_kernel(const float* __restrict__ partial, int rows, int C
 }
 
 // W'[ci][t'][co] = W[co][26 - t'][ci]: the filter of the backward-data
-// convolution written as a forward convolution.
+// convolution written as a forward convolution.  One 32 x 32 (co, ci) tile
+// of one tap per block iteration, transposed through shared memory so both
+// the reads (ci contiguous) and the writes (co contiguous) are coalesced.
 __global__ void flip_transpose_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ wt, int Cout, int Cin) {
-    const int64_t total = (int64_t)Cout * 27 * Cin;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int co = (int)(i % Cout);
-        const int64_t r = i / Cout;
-        const int tp = (int)(r % 27);
-        const int ci = (int)(r / 27);
-        wt[i] = w[((int64_t)co * 27 + (26 - tp)) * Cin + ci];
+    __shared__ uint16_t tile[32][33];
+    const int tiles_co = (Cout + 31) / 32, tiles_ci = (Cin + 31) / 32;
+    const int ntiles = 27 * tiles_co * tiles_ci;
+    for (int b = blockIdx.x; b < ntiles; b += gridDim.x) {
+        const int tci = b % tiles_ci;
+        const int r = b / tiles_ci;
+        const int tco = r % tiles_co;
+        const int tp = r / tiles_co;  // output tap t'
+        for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
+            const int co = tco * 32 + ty, ci = tci * 32 + threadIdx.x;
+            tile[ty][threadIdx.x] = (co < Cout && ci < Cin) ? w[((int64_t)co * 27 + (26 - tp)) * Cin + ci] : 0;
+        }
+        __syncthreads();
+        for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
+            const int ci = tci * 32 + ty, co = tco * 32 + threadIdx.x;
+            if (ci < Cin && co < Cout) wt[((int64_t)ci * 27 + tp) * Cout + co] = tile[threadIdx.x][ty];
+        }
+        __syncthreads();
+    }
+}
+
+// Bias gradient alone (no dZ, no dYpre, dy already the pre-activation
+// gradient): per-thread sums of one 8-channel group over the rows i, i +
+// stride, ... in increasing order -- the order pool_bwd_kernel uses -- with
+// four rows loaded per iteration; partial[block][C] as pool_bwd_kernel.
+__global__ void pool_bwd_dbias_kernel(const uint16_t* __restrict__ dy, float* __restrict__ partial, int64_t total8,
+                                      int C) {
+    extern __shared__ float red[];  // [blockDim][8]
+    const int C8 = C / 8;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < total8; i0 += 4 * stride) {
+        uint4 gv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            gv[u] = i < total8 ? __ldg(reinterpret_cast<const uint4*>(dy) + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float g[8];
+            unpack8(gv[u], g);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] += g[c];
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) red[threadIdx.x * 8 + c] = acc[c];
+    __syncthreads();
+    for (int ch = threadIdx.x; ch < C; ch += blockDim.x) {
+        const int c8 = ch / 8, c = ch % 8;
+        float s = 0.f;
+        for (int t = c8; t < (int)blockDim.x; t += C8) s += red[t * 8 + c];
+        partial[(int64_t)blockIdx.x * C + ch] = s;
     }
 }
 
@@ -218,8 +266,14 @@ cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
         if (ws == nullptr || ws_bytes < pool_bwd_workspace_bytes(ctx.num_sms, c)) return CF_ERR_WORKSPACE;
         partial = static_cast<float*>(ws);
     }
-    pool_bwd_kernel<<<blocks, threads, threads * 8 * sizeof(float), ctx.stream>>>(
-        dy, y, idx, slope, dz, dy_pre, partial, n, (int)d, (int)h, (int)w, c);
+    if (y == nullptr && dz == nullptr && dy_pre == nullptr) {
+        if (partial == nullptr) return CF_OK;  // nothing requested
+        pool_bwd_dbias_kernel<<<blocks, threads, threads * 8 * sizeof(float), ctx.stream>>>(
+            dy, partial, n * (d / 2) * (h / 2) * (w / 2) * (c / 8), c);
+    } else {
+        pool_bwd_kernel<<<blocks, threads, threads * 8 * sizeof(float), ctx.stream>>>(
+            dy, y, idx, slope, dz, dy_pre, partial, n, (int)d, (int)h, (int)w, c);
+    }
     if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
     if (dbias) {
         colsum_kernel<<<c, 256, 0, ctx.stream>>>(partial, blocks, c, dbias);
@@ -229,10 +283,9 @@ cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
 }
 
 cf_status launch_flip_transpose(const LaunchCtx& ctx, int c_out, int c_in, const uint16_t* w, uint16_t* wt) {
-    const int64_t total = (int64_t)c_out * 27 * c_in;
-    const int threads = 256;
-    const int blocks = (int)std::min<int64_t>((total + threads - 1) / threads, 8LL * ctx.num_sms);
-    flip_transpose_kernel<<<blocks, threads, 0, ctx.stream>>>(w, wt, c_out, c_in);
+    const int64_t ntiles = 27LL * ((c_out + 31) / 32) * ((c_in + 31) / 32);
+    const int blocks = (int)std::min<int64_t>(ntiles, 8LL * ctx.num_sms);
+    flip_transpose_kernel<<<blocks, dim3(32, 8), 0, ctx.stream>>>(w, wt, c_out, c_in);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
