@@ -245,16 +245,16 @@ def run_ours(args, rank, world, local_rank):
     ops = op_table(n, s, ch)
     total_flops = sum(o[3] for o in ops)
 
-    # instrumented step: events around every conv op (same stream)
+    # instrumented step: events around the step on the main stream and around
+    # every op on the stream it is launched on (the weight gradients run on
+    # the stack's second stream, joined before the step's end event)
     def step_with_events(evs):
-        def mark(key):
-            e = torch.cuda.Event(enable_timing=True)
-            e.record(stream)
-            evs.append((key, e))
-        st.forward(stream, mark)
-        mark("fwd_end")
-        st.backward(dy, stream, mark)
-        mark("end")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st.forward(stream, evs)
+        st.backward(dy, stream, evs)
+        e1.record(stream)
+        return e0, e1
 
     clk = Clocks(local_rank).__enter__()
     for _ in range(args.warmup):
@@ -273,12 +273,11 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(args.steps):
             flush.zero_()  # evict L2 between steps (outside the timed events)
             evs = []
-            step_with_events(evs)
+            s0, s1 = step_with_events(evs)
             torch.cuda.synchronize(dev)
-            step_ms.append(evs[0][1].elapsed_time(evs[-1][1]))
-            for (k, e0), (_, e1) in zip(evs[:-1], evs[1:]):
-                if k != "fwd_end":
-                    per_op.setdefault(k, []).append(e0.elapsed_time(e1))
+            step_ms.append(s0.elapsed_time(s1))
+            for k, e0, e1 in evs:
+                per_op.setdefault(k, []).append(e0.elapsed_time(e1))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)

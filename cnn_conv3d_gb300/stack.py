@@ -18,6 +18,11 @@ One training step of the stack (forward + backward):
   weight gradient: the pool backward then computes db alone and
   cf_conv3d_wgrad takes the pooled gradient with the argmax codes (routed
   form), expanding dZ on chip; its dense dZ is never allocated.
+  The weight gradients are off the backward critical path (nothing in the
+  step reads dW), so by default they run on a second stream, each after its
+  block's pool backward (event), with their own workspace; the step ends by
+  joining that stream.  Kernels of the two chains overlap where one leaves
+  SMs idle (the small deep layers, grid tails).
 """
 from __future__ import annotations
 
@@ -28,7 +33,7 @@ from . import cfconv as cf
 
 class CosmoStack:
     def __init__(self, n: int, spatial: int, channels, slope: float = 0.3, device: str = "cuda",
-                 backward: bool = True):
+                 backward: bool = True, overlap: bool = True):
         self.n, self.spatial, self.channels, self.slope = n, spatial, tuple(channels), float(slope)
         self.L = len(channels) - 1
         self.device = device
@@ -46,7 +51,8 @@ class CosmoStack:
             self.idx.append(torch.empty((n, s // 2, s // 2, s // 2, co), dtype=u8, device=device))
             s //= 2
         self.backward_enabled = backward
-        ws = 0
+        self.side = torch.cuda.Stream(device=device) if (backward and overlap) else None
+        ws = ws_w = 0
         if backward:
             self.dz, self.dw, self.db, self.g = [], [], [], []
             for l in range(self.L):
@@ -61,12 +67,16 @@ class CosmoStack:
                               if l < self.L - 1 or self.routed(l) else None)
             for l in range(self.L):
                 desc = self.desc(l)
-                ws = max(ws, cf.cf_workspace_size(cf.CF_OP_WGRAD_ROUTED if self.routed(l) else cf.CF_OP_WGRAD,
-                                                  desc))
+                ws_w = max(ws_w, cf.cf_workspace_size(
+                    cf.CF_OP_WGRAD_ROUTED if self.routed(l) else cf.CF_OP_WGRAD, desc))
                 ws = max(ws, cf.cf_workspace_size(cf.CF_OP_POOL_BWD, desc))
                 if l > 0:
                     ws = max(ws, cf.cf_workspace_size(cf.CF_OP_DGRAD, desc))
+        if self.side is None:
+            ws = max(ws, ws_w)
         self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=device)
+        # the weight gradients' workspace (the main one when they share the stream)
+        self.ws_w = torch.empty((max(ws_w, 256),), dtype=torch.uint8, device=device) if self.side else self.ws
 
     def routed(self, l) -> bool:
         """Block l's weight gradient takes the pooled gradient + argmax codes."""
@@ -91,42 +101,68 @@ class CosmoStack:
             up(self.w[l], ws_u16[l])
             self.b[l].copy_(torch.from_numpy(np.ascontiguousarray(bs_f32[l], dtype=np.float32)))
 
-    def forward(self, stream=None, mark=None):
-        """mark(key), if given, is called before each launch (key "fwd<l+1>")."""
-        for l in range(self.L):
-            if mark:
-                mark(f"fwd{l + 1}")
-            cf.cf_conv3d_fwd(self.desc(l), self.block_input(l), self.w[l], (self.b[l], self.slope, self.idx[l]),
-                             self.y[l], None, 0, stream)
+    def _main(self, stream):
+        return stream if stream is not None else torch.cuda.current_stream(self.device)
 
-    def backward(self, dy, stream=None, mark=None):
-        """mark(key), if given, is called before each op ("poolbwd<l+1>",
-        "wgrad<l+1>", "dgrad<l+1>")."""
+    @staticmethod
+    def _run(key, stream, fn, timer):
+        """fn(); with a timer list, CUDA events around it on `stream` are appended
+        as (key, start, end)."""
+        if timer is None:
+            fn()
+            return
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        timer.append((key, e0, e1))
+
+    def forward(self, stream=None, timer=None):
+        """timer: optional list receiving (key, start event, end event) per launch."""
+        main = self._main(stream)
+        for l in range(self.L):
+            self._run(f"fwd{l + 1}", main, lambda l=l: cf.cf_conv3d_fwd(
+                self.desc(l), self.block_input(l), self.w[l], (self.b[l], self.slope, self.idx[l]), self.y[l],
+                None, 0, main), timer)
+
+    def backward(self, dy, stream=None, timer=None):
+        """timer: as in forward (keys "poolbwd<l+1>", "wgrad<l+1>", "dgrad<l+1>")."""
+        main = self._main(stream)
+        side = self.side if self.side is not None else main
         ws, wsb = self.ws, self.ws.numel()
+        wsw, wswb = self.ws_w, self.ws_w.numel()
         for l in range(self.L - 1, -1, -1):
             n, d, h, w = self.dims[l]
             co = self.channels[l + 1]
             routed = self.routed(l)
-            if mark:
-                mark(f"poolbwd{l + 1}")
             if l == self.L - 1:
-                cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope, self.dz[l],
-                                          self.g[l] if routed else None, self.db[l], ws, wsb, stream)
+                fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope,
+                                                       self.dz[l], self.g[l] if routed else None, self.db[l], ws,
+                                                       wsb, main)
             else:
-                cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope, self.dz[l],
-                                          None, self.db[l], ws, wsb, stream)
+                fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope,
+                                                       self.dz[l], None, self.db[l], ws, wsb, main)
+            self._run(f"poolbwd{l + 1}", main, fn, timer)
             desc = self.desc(l)
-            if mark:
-                mark(f"wgrad{l + 1}")
+            if side is not main:
+                ev = torch.cuda.Event()
+                ev.record(main)
+                side.wait_event(ev)
             if routed:
-                cf.cf_conv3d_wgrad(desc, self.block_input(l), self.g[l], self.idx[l], self.dw[l], 0, ws, wsb, stream)
+                fn = lambda: cf.cf_conv3d_wgrad(desc, self.block_input(l), self.g[l], self.idx[l], self.dw[l], 0,
+                                                wsw, wswb, side)
             else:
-                cf.cf_conv3d_wgrad(desc, self.block_input(l), self.dz[l], None, self.dw[l], 0, ws, wsb, stream)
+                fn = lambda: cf.cf_conv3d_wgrad(desc, self.block_input(l), self.dz[l], None, self.dw[l], 0, wsw,
+                                                wswb, side)
+            self._run(f"wgrad{l + 1}", side, fn, timer)
             if l > 0:
-                if mark:
-                    mark(f"dgrad{l + 1}")
-                cf.cf_conv3d_dgrad(desc, self.dz[l], None, self.w[l], self.block_input(l), self.slope,
-                                   self.g[l - 1], ws, wsb, stream)
+                self._run(f"dgrad{l + 1}", main, lambda: cf.cf_conv3d_dgrad(
+                    desc, self.dz[l], None, self.w[l], self.block_input(l), self.slope, self.g[l - 1], ws, wsb,
+                    main), timer)
+        if side is not main:
+            ev = torch.cuda.Event()
+            ev.record(side)
+            main.wait_event(ev)
 
     def step(self, dy, stream=None):
         self.forward(stream)
