@@ -104,14 +104,17 @@ class CosmoStack:
     def _main(self, stream):
         return stream if stream is not None else torch.cuda.current_stream(self.device)
 
-    @staticmethod
-    def _run(key, stream, fn, timer):
+    _capturing = False
+    timer_keys = None  # when set, only these ops get events
+
+    def _run(self, key, stream, fn, timer):
         """fn(); with a timer list, CUDA events around it on `stream` are appended
-        as (key, start, end)."""
-        if timer is None:
+        as (key, start, end) (recorded as graph nodes while capturing)."""
+        if timer is None or (self.timer_keys is not None and key not in self.timer_keys):
             fn()
             return
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        kw = {"external": True} if self._capturing else {}
+        e0, e1 = torch.cuda.Event(enable_timing=True, **kw), torch.cuda.Event(enable_timing=True, **kw)
         e0.record(stream)
         fn()
         e1.record(stream)
@@ -164,10 +167,29 @@ class CosmoStack:
             ev.record(side)
             main.wait_event(ev)
 
-    def step(self, dy, stream=None):
-        self.forward(stream)
+    def step(self, dy, stream=None, timer=None):
+        self.forward(stream, timer)
         if self.backward_enabled:
-            self.backward(dy, stream)
+            self.backward(dy, stream, timer)
+
+    def capture(self, dy, timer=None, keys=None):
+        """Records one step into a CUDA graph (replay() then re-runs it with no
+        per-launch host work).  The buffers, dy included, are bound at capture.
+        With a timer list, the events of the ops in `keys` (all if None) become
+        event-record nodes."""
+        g = torch.cuda.CUDAGraph()
+        cur = torch.cuda.current_stream(self.device)
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(cur)
+        self._capturing, self.timer_keys = True, keys
+        try:
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    self.step(dy, s, timer)
+        finally:
+            self._capturing, self.timer_keys = False, None
+        cur.wait_stream(s)
+        return g
 
     def launches_per_step(self) -> int:
         """Kernels one step enqueues: fwd 1 per block; pool-bwd 2 (scatter +
