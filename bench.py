@@ -247,12 +247,13 @@ def run_ours(args, rank, world, local_rank):
 
     # instrumented step: events around the step on the main stream and around
     # every op on the stream it is launched on (the weight gradients run on
-    # the stack's second stream, joined before the step's end event)
-    def step_with_events(evs):
+    # the stack's second stream, joined before the step's end event); serial:
+    # all ops on one stream, so that each op's events time it alone
+    def step_with_events(evs, serial=False):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         st.forward(stream, evs)
-        st.backward(dy, stream, evs)
+        st.backward(dy, stream, evs, serial)
         e1.record(stream)
         return e0, e1
 
@@ -262,13 +263,13 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     if cf.cf_last_device_status(stream) != cf.CF_OK:
         raise RuntimeError("device status word set during warm-up")
-    # per-op durations: instrumented eager steps (events around every op on its
-    # stream), outside the timed region; they pick the dominant op
+    # per-op durations of each op alone: instrumented serial eager steps,
+    # outside the timed region; they pick the dominant op
     inst = {}
     for _ in range(3):
         flush.zero_()
         evs = []
-        step_with_events(evs)
+        step_with_events(evs, serial=True)
         torch.cuda.synchronize(dev)
         for k, e0, e1 in evs:
             inst.setdefault(k, []).append(e0.elapsed_time(e1))
@@ -391,7 +392,7 @@ def run_ours(args, rank, world, local_rank):
                                  + ", weight gradients on a second stream",
                    "parallelism": f"replicas x{world}"},
         "per_op_ms": {k: round(v, 4) for k, v in sorted(op_ms.items())},
-        "per_op_source": "instrumented eager steps before the timed ones (ops of the two streams overlap); "
+        "per_op_source": "each op alone (instrumented serial eager steps before the timed ones); "
                          "the dominant op's from the timed steps",
         "roofline": roofline,
         "e2e": e2e,

@@ -51,7 +51,10 @@ class CosmoStack:
             self.idx.append(torch.empty((n, s // 2, s // 2, s // 2, co), dtype=u8, device=device))
             s //= 2
         self.backward_enabled = backward
+        # with overlap: the backward-data chain on a high-priority stream (it is the
+        # step's critical path), the weight gradients on a normal-priority one
         self.side = torch.cuda.Stream(device=device) if (backward and overlap) else None
+        self.crit = torch.cuda.Stream(device=device, priority=-1) if (backward and overlap) else None
         ws = ws_w = 0
         if backward:
             self.dz, self.dw, self.db, self.g = [], [], [], []
@@ -128,10 +131,17 @@ class CosmoStack:
                 self.desc(l), self.block_input(l), self.w[l], (self.b[l], self.slope, self.idx[l]), self.y[l],
                 None, 0, main), timer)
 
-    def backward(self, dy, stream=None, timer=None):
-        """timer: as in forward (keys "poolbwd<l+1>", "wgrad<l+1>", "dgrad<l+1>")."""
-        main = self._main(stream)
-        side = self.side if self.side is not None else main
+    def backward(self, dy, stream=None, timer=None, serial=False):
+        """timer: as in forward (keys "poolbwd<l+1>", "wgrad<l+1>", "dgrad<l+1>").
+        serial: every op on the caller's stream (each op's events then time it
+        alone)."""
+        caller = self._main(stream)
+        main = self.crit if (self.crit is not None and not serial) else caller
+        side = self.side if (self.side is not None and not serial) else caller
+        if main is not caller:
+            ev = torch.cuda.Event()
+            ev.record(caller)
+            main.wait_event(ev)
         ws, wsb = self.ws, self.ws.numel()
         wsw, wswb = self.ws_w, self.ws_w.numel()
         for l in range(self.L - 1, -1, -1):
@@ -162,15 +172,16 @@ class CosmoStack:
                 self._run(f"dgrad{l + 1}", main, lambda: cf.cf_conv3d_dgrad(
                     desc, self.dz[l], None, self.w[l], self.block_input(l), self.slope, self.g[l - 1], ws, wsb,
                     main), timer)
-        if side is not main:
-            ev = torch.cuda.Event()
-            ev.record(side)
-            main.wait_event(ev)
+        for s in (main, side):
+            if s is not caller:
+                ev = torch.cuda.Event()
+                ev.record(s)
+                caller.wait_event(ev)
 
-    def step(self, dy, stream=None, timer=None):
+    def step(self, dy, stream=None, timer=None, serial=False):
         self.forward(stream, timer)
         if self.backward_enabled:
-            self.backward(dy, stream, timer)
+            self.backward(dy, stream, timer, serial)
 
     def capture(self, dy, timer=None, keys=None):
         """Records one step into a CUDA graph (replay() then re-runs it with no
