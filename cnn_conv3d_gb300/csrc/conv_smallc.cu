@@ -233,6 +233,10 @@ __global__ void __launch_bounds__(608, 1)
             uint32_t aph = 0, local = 0;
             bool ok = true;
             const uint32_t b_addr = smem_u32(bsm);
+            uint64_t bdk[C::KSTEPS];  // the filter's K-step descriptors (fixed)
+#pragma unroll
+            for (int k = 0; k < C::KSTEPS; ++k)
+                bdk[k] = sdesc(b_addr + (k >> 2) * (BN * 128) + (k & 3) * 32, 16, 1024, SWZ_128B);
             for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++local) {
                 const uint32_t acc = C::NACC == 2 ? (local & 1) : 0u;
                 const uint32_t use = C::NACC == 2 ? (local >> 1) : local;
@@ -250,11 +254,8 @@ __global__ void __launch_bounds__(608, 1)
                     const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS + blk * BN;
                     const uint32_t a_tmem = tmem_base + C::ACOL0 + blk * C::PCOLS;
 #pragma unroll
-                    for (int k = 0; k < C::KSTEPS; ++k) {
-                        const uint32_t atom = k >> 2, koff = (k & 3) * 32;
-                        const uint64_t bd = sdesc(b_addr + atom * (BN * 128) + koff, 16, 1024, SWZ_128B);
-                        umma_bf16_tmem_a(d_tmem, a_tmem + 8 * k, bd, C::IDESC, k != 0);
-                    }
+                    for (int k = 0; k < C::KSTEPS; ++k)
+                        umma_bf16_tmem_a(d_tmem, a_tmem + 8 * k, bdk[k], C::IDESC, k != 0);
                     umma_commit(&aempty[blk]);
                 }
                 if (!ok) break;

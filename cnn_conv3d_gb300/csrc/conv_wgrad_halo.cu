@@ -89,6 +89,21 @@ __device__ __forceinline__ void wh_block_taps(int b, int& t_first, int& lbo_rows
     }
 }
 
+// Unit u of the CTA grid (size G) -> (M-block set, K split).  With two sets,
+// the CTAs pair up on a split in every round (b and b^1 read the same K
+// blocks, so the second read hits L2) and alternate sets between rounds, so
+// that a CTA's units are not all of the larger set.
+__device__ __forceinline__ void wh_unit(const WhGeom& g, int u, int G, int& set, int& split) {
+    if (g.n_sets == 2 && (G & 1) == 0) {
+        const int r = u / G, b = u - r * G;
+        split = r * (G / 2) + (b >> 1);
+        set = (b + r) & 1;
+    } else {
+        set = u % g.n_sets;
+        split = u / g.n_sets;
+    }
+}
+
 template <int KC, int BN, int PLANES>
 __global__ void __launch_bounds__(224, 1)
     wgrad_halo_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
@@ -141,7 +156,8 @@ __global__ void __launch_bounds__(224, 1)
             uint32_t phase = 0, issued = 0, par = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
-                const int set = u % g.n_sets, split = u / g.n_sets;
+                int set, split;
+                wh_unit(g, u, (int)gridDim.x, set, split);
                 const int chunk = set / g.sets_per_chunk;
                 const int64_t k0 = (int64_t)split * g.kb_per_split;
                 const int64_t k1 = k0 + g.kb_per_split < g.total_kb ? k0 + g.kb_per_split : g.total_kb;
@@ -199,7 +215,8 @@ __global__ void __launch_bounds__(224, 1)
             const uint64_t adesc_base = sdesc(smem_u32(ring), 0, C::SBO_A, C::SWZ_A);
             const uint64_t bdesc_base = sdesc(smem_u32(ring) + C::HALO_STRIDE, C::B_SUB_BYTES, C::SBO_B, C::SWZ_B);
             for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x, ++local) {
-                const int set = u % g.n_sets, split = u / g.n_sets;
+                int set, split;
+                wh_unit(g, u, (int)gridDim.x, set, split);
                 const int sub = set % g.sets_per_chunk;
                 const int mb0 = sub * g.g_per_set;
                 const int nmb = min(g.g_per_set, g.blocks_per_chunk - mb0);
@@ -255,7 +272,8 @@ __global__ void __launch_bounds__(224, 1)
         const int KK = 27 * g.Cin;
         uint32_t local = 0;
         for (int u = blockIdx.x; u < g.num_units; u += gridDim.x, ++local) {
-            const int set = u % g.n_sets, split = u / g.n_sets;
+            int set, split;
+            wh_unit(g, u, (int)gridDim.x, set, split);
             const int chunk = set / g.sets_per_chunk, sub = set % g.sets_per_chunk;
             const int mb0 = sub * g.g_per_set;
             const int nmb = min(g.g_per_set, g.blocks_per_chunk - mb0);
