@@ -47,7 +47,7 @@ _EP = ctypes.POINTER(cf_pool_epi)
 
 _SIGS = {
     "cf_conv3d_fwd": ([_DP, _vp, _vp, _EP, _vp, _vp, _sz, _vp], ctypes.c_int),
-    "cf_conv3d_dgrad": ([_DP, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "cf_conv3d_dgrad": ([_DP, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_conv3d_wgrad": ([_DP, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _sz, _vp], ctypes.c_int),
     "cf_bias_lrelu_pool_fwd": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _f32, _vp, _vp, _vp], ctypes.c_int),
     "cf_bias_lrelu_pool_bwd": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _sz, _vp],
@@ -123,9 +123,9 @@ def cf_conv3d_fwd(desc, x, w, epi, y, ws=None, ws_bytes=0, stream=None, check=Tr
     return _check(st, "cf_conv3d_fwd") if check else st
 
 
-def cf_conv3d_dgrad(desc, dz, idx, w, x_act, slope, dx, ws=None, ws_bytes=0, stream=None, check=True):
+def cf_conv3d_dgrad(desc, dz, idx, w, x_act, slope, dx, ws=None, ws_bytes=0, stream=None, check=True, dsum=None):
     st = _lib.cf_conv3d_dgrad(ctypes.byref(_desc(desc)), _ptr(dz), _ptr(idx), _ptr(w), _ptr(x_act), float(slope),
-                              _ptr(dx), _ptr(ws), ws_bytes, _stream(stream))
+                              _ptr(dx), _ptr(dsum), _ptr(ws), ws_bytes, _stream(stream))
     return _check(st, "cf_conv3d_dgrad") if check else st
 
 

@@ -2,6 +2,7 @@
 // argument validation, workspace layout, per-device context (SM count,
 // device status word, tensor-map encoder) and the launch sequence of each
 // operation.  No entry point allocates or frees device memory.
+#include <algorithm>
 #include <mutex>
 
 #include "cf_internal.h"
@@ -133,6 +134,13 @@ cf_status cf_debug_wait_timeout_probe(void* stream) {
     return launch_timeout_probe(ctx);
 }
 
+// Workspace of cf_conv3d_dgrad after the flipped filter: the channel-sum
+// partials (whichever of the fused rows or the separate pass is larger).
+static size_t dgrad_sum_bytes(int num_sms, int c_in) {
+    return round_up(std::max((size_t)num_sms * c_in * sizeof(float), channel_sums_workspace_bytes(num_sms, c_in)),
+                    256);
+}
+
 size_t cf_workspace_size(int op, const cf_conv_desc* desc) {
     if (!desc_ok(desc)) return 0;
     LaunchCtx ctx;
@@ -143,8 +151,8 @@ size_t cf_workspace_size(int op, const cf_conv_desc* desc) {
         wgrad_workspace_bytes(ctx.num_sms, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out), 256);
     switch (op) {
         case CF_OP_FWD: return 0;
-        case CF_OP_DGRAD: return wt;
-        case CF_OP_DGRAD_ROUTED: return wt + dense;
+        case CF_OP_DGRAD: return wt + dgrad_sum_bytes(ctx.num_sms, desc->c_in);
+        case CF_OP_DGRAD_ROUTED: return wt + dgrad_sum_bytes(ctx.num_sms, desc->c_in) + dense;
         case CF_OP_WGRAD: return part;
         case CF_OP_WGRAD_ROUTED: return part + (wgrad_routed_fused(desc->c_in) ? 0 : dense);
         case CF_OP_POOL_BWD: return round_up(pool_bwd_workspace_bytes(ctx.num_sms, desc->c_out), 256);
@@ -180,38 +188,52 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
 }
 
 cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx, const uint16_t* w,
-                          const uint16_t* x_act, float slope, uint16_t* dx, void* ws, size_t ws_bytes,
-                          void* stream) {
+                          const uint16_t* x_act, float slope, uint16_t* dx, float* dsum, void* ws,
+                          size_t ws_bytes, void* stream) {
     if (!desc_ok(desc) || dz == nullptr || w == nullptr || dx == nullptr) return CF_ERR_INVALID_ARG;
     if (!aligned16(dz) || !aligned16(w) || !aligned16(dx) || (x_act && !aligned16(x_act)) ||
-        (idx && !aligned16(idx)) || (ws && !aligned16(ws)))
+        (idx && !aligned16(idx)) || (ws && !aligned16(ws)) || (dsum && !aligned16(dsum)))
         return CF_ERR_INVALID_ARG;
     const int ci = desc->c_in, co = desc->c_out;
     if (co % 32 != 0 || ci % 16 != 0) return CF_ERR_UNSUPPORTED;
     if (idx && ((desc->d | desc->h | desc->w) & 1)) return CF_ERR_UNSUPPORTED;
-    const size_t wt_bytes = round_up((size_t)co * 27 * ci * 2, 256);
-    const size_t need = wt_bytes + (idx ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0);
-    if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
     LaunchCtx ctx;
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    const size_t wt_bytes = round_up((size_t)co * 27 * ci * 2, 256);
+    const size_t sum_bytes = dgrad_sum_bytes(ctx.num_sms, ci);
+    const size_t need = wt_bytes + sum_bytes + (idx ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0);
+    if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
     uint16_t* wt = static_cast<uint16_t*>(ws);
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wt_bytes);
     cf_status st = launch_flip_transpose(ctx, co, ci, w, wt);
     if (st != CF_OK) return st;
     const uint16_t* dz_dense = dz;
     if (idx) {
-        uint16_t* buf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + wt_bytes);
+        uint16_t* buf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + wt_bytes + sum_bytes);
         st = launch_pool_bwd(ctx, desc->n, desc->d, desc->h, desc->w, co, dz, nullptr, idx, 1.f, buf, nullptr,
                              nullptr, nullptr, 0);
         if (st != CF_OK) return st;
         dz_dense = buf;
     }
     // backward data = forward conv of dZ with the flipped, transposed filter:
-    // GEMM input channels c_out, output channels c_in
-    if (halo_path_supported(co, ci))
-        return launch_conv_halo(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt,
-                                x_act ? EPI_DGRAD : EPI_PLAIN, dx, nullptr, nullptr, x_act, slope);
-    return launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt,
-                             x_act ? EPI_DGRAD : EPI_PLAIN, dx, nullptr, nullptr, x_act, slope);
+    // GEMM input channels c_out, output channels c_in.  Channel sums of dx: in
+    // the halo kernel's epilogue when c_in <= 32 (one row of partials per CTA,
+    // rows of CTAs that get no tile stay zero), else a separate pass over dx.
+    const int epi = x_act ? EPI_DGRAD : EPI_PLAIN;
+    if (halo_path_supported(co, ci)) {
+        const bool fused = dsum != nullptr && ci <= 32;
+        if (fused && cudaMemsetAsync(part, 0, (size_t)ctx.num_sms * ci * sizeof(float), ctx.stream) != cudaSuccess)
+            return CF_ERR_CUDA;
+        st = launch_conv_halo(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt, epi, dx, nullptr,
+                              nullptr, x_act, slope, fused ? part : nullptr);
+        if (st != CF_OK || dsum == nullptr) return st;
+        if (fused) return launch_colsum(ctx, part, ctx.num_sms, ci, dsum);
+    } else {
+        st = launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt, epi, dx, nullptr,
+                               nullptr, x_act, slope);
+        if (st != CF_OK || dsum == nullptr) return st;
+    }
+    return launch_channel_sums(ctx, dx, desc->n * desc->d * desc->h * desc->w, ci, part, dsum);
 }
 
 cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* dz, const uint8_t* idx,

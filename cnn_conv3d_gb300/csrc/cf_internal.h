@@ -53,9 +53,12 @@ cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
 // conv_halo.cu: same contract as launch_conv_igemm for c_in % 32 == 0 and
 // c_out in {32, 64, 128}, reading A from one halo tile per channel chunk.
 bool halo_path_supported(int c_in, int c_out);
+// colsum_part (unpooled epilogues, c_out <= 32): [grid][c_out] channel sums of
+// the stored outputs, one row per CTA (grid <= SM count), or NULL.
 cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                            int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
-                           uint8_t* idx, const float* bias, const uint16_t* x_act, float slope);
+                           uint8_t* idx, const float* bias, const uint16_t* x_act, float slope,
+                           float* colsum_part = nullptr);
 
 // conv_smallc.cu: forward conv for c_in in {1,4} (im2col operand in tensor memory).
 cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
@@ -87,6 +90,13 @@ cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
                           const uint16_t* dy, const uint16_t* y, const uint8_t* idx, float slope, uint16_t* dz,
                           uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes);
 cf_status launch_flip_transpose(const LaunchCtx& ctx, int c_out, int c_in, const uint16_t* w, uint16_t* wt);
+// out[ch] = sum over `rows` of partial[row][ch] (fixed order)
+cf_status launch_colsum(const LaunchCtx& ctx, const float* partial, int rows, int c, float* out);
+// out[ch] = sum over the rows of x [rows][c] bf16 (fixed order); partial holds
+// channel_sums_workspace_bytes
+size_t channel_sums_workspace_bytes(int num_sms, int c);
+cf_status launch_channel_sums(const LaunchCtx& ctx, const uint16_t* x, int64_t rows, int c, float* partial,
+                              float* out);
 cf_status launch_timeout_probe(const LaunchCtx& ctx);
 
 }  // namespace cf

@@ -58,6 +58,9 @@ struct EpiArgs {
     const float* bias;
     const uint16_t* x_act;
     float slope;
+    // backward-data only: per-CTA channel sums of the stored outputs,
+    // [gridDim.x][C] fp32 (rows of CTAs without tiles stay as they were), or NULL
+    float* colsum_part = nullptr;
 };
 
 // Epilogue of one tile, executed by the 128 epilogue threads (4 warps whose

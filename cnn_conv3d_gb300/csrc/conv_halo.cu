@@ -248,15 +248,37 @@ __global__ void __launch_bounds__(224, 1)
         // ---------------- epilogue warps 2..5
         const int q = warp & 3;
         const int et = threadIdx.x - 64;
+        // unpooled outputs with BN <= 32, on request: channel sums of the stored
+        // outputs (in backward data, the bias gradient of the previous block), per
+        // thread over its tiles, then over the CTA
+        constexpr bool DSUM = EPI != EPI_POOL && BN <= 32;
+        const bool dsum_on = DSUM && p.ea.colsum_part != nullptr;
+        float dsum[DSUM ? BN : 1];
+#pragma unroll
+        for (int c = 0; c < (DSUM ? BN : 1); ++c) dsum[c] = 0.f;
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const uint32_t acc = local & 1, use = local >> 1;
             if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
             tc_fence_after();
             const HTile t = halo_decode(p, tile, BN);
-            halo_epilogue<BN, EPI>(p, t, tmem_base, acc * 2 * BN, q, lane);
+            halo_epilogue<BN, EPI>(p, t, tmem_base, acc * 2 * BN, q, lane, 0, 0, dsum_on ? dsum : nullptr);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
+        }
+        if (dsum_on) {
+            // the last tile's MMAs are complete, so the halo ring is idle: reduce
+            // the 128 threads' sums through it (thread order, then one row per CTA)
+            float* red = reinterpret_cast<float*>(hring);
+            named_bar_sync(2, 128);
+#pragma unroll
+            for (int c = 0; c < (DSUM ? BN : 1); ++c) red[et * (BN + 1) + c] = dsum[c];
+            named_bar_sync(2, 128);
+            if (et < BN && et < p.Cout) {
+                float s = 0.f;
+                for (int r = 0; r < 128; ++r) s += red[r * (BN + 1) + et];
+                p.ea.colsum_part[(int64_t)blockIdx.x * p.Cout + et] = s;
+            }
         }
     }
 
@@ -315,8 +337,9 @@ bool halo_path_supported(int c_in, int c_out) {
 
 cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                            const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
-                           const float* bias, const uint16_t* x_act, float slope) {
+                           const float* bias, const uint16_t* x_act, float slope, float* colsum_part) {
     if (!halo_path_supported(c_in, c_out)) return CF_ERR_UNSUPPORTED;
+    if (colsum_part && (epi == EPI_POOL || c_out > 32)) return CF_ERR_UNSUPPORTED;
     HaloParams p;
     p.N = (int)n;
     p.D = (int)d;
@@ -330,7 +353,7 @@ cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
     p.n_ntiles = 1;
     p.num_tiles = (int)(n * p.tiles_d * p.tiles_h * p.tiles_w);
     p.n_chunks = 0;
-    p.ea = EpiArgs{y, idx, bias, x_act, slope};
+    p.ea = EpiArgs{y, idx, bias, x_act, slope, colsum_part};
     p.status = ctx.status;
     p.wait_ns = ctx.wait_ns;
     // The whole filter stays in shared memory when it fits beside two halo

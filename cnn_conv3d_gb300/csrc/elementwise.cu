@@ -282,6 +282,26 @@ cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
     return CF_OK;
 }
 
+size_t channel_sums_workspace_bytes(int num_sms, int c) { return pool_bwd_workspace_bytes(num_sms, c); }
+
+cf_status launch_colsum(const LaunchCtx& ctx, const float* partial, int rows, int c, float* out);
+
+cf_status launch_channel_sums(const LaunchCtx& ctx, const uint16_t* x, int64_t rows, int c, float* partial,
+                              float* out) {
+    if (c % 8 != 0 || c / 8 > 256) return CF_ERR_UNSUPPORTED;
+    const int threads = pool_bwd_block(c);
+    const int blocks = pool_bwd_grid(ctx.num_sms);
+    pool_bwd_dbias_kernel<<<blocks, threads, threads * 8 * sizeof(float), ctx.stream>>>(x, partial, rows * (c / 8),
+                                                                                         c);
+    if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+    return launch_colsum(ctx, partial, blocks, c, out);
+}
+
+cf_status launch_colsum(const LaunchCtx& ctx, const float* partial, int rows, int c, float* out) {
+    colsum_kernel<<<c, 256, 0, ctx.stream>>>(partial, rows, c, out);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
 cf_status launch_flip_transpose(const LaunchCtx& ctx, int c_out, int c_in, const uint16_t* w, uint16_t* wt) {
     const int64_t ntiles = 27LL * ((c_out + 31) / 32) * ((c_in + 31) / 32);
     const int blocks = (int)std::min<int64_t>(ntiles, 8LL * ctx.num_sms);

@@ -53,10 +53,12 @@ __device__ __forceinline__ void pool_combine(float& v, int& k, float v2, int k2)
 // Epilogue of one tile for the accumulator columns c_begin, c_begin + step,
 // ... (CH columns per pass); CH = 0 picks min(BN, 32) and step CH.  Several
 // warps per TMEM lane quarter can thus split the channels of a tile.
+// dsum (backward-data, BN <= 32): per-channel running sums of the stored
+// bf16 outputs of this thread's voxels, or NULL.
 template <int BN, int EPI, int CH_ = 0>
 __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& t, uint32_t tmem_base,
                                               uint32_t acc_col, int q, int lane, int c_begin = 0,
-                                              int c_step = 0) {
+                                              int c_step = 0, float* dsum = nullptr) {
     constexpr int CH = CH_ != 0 ? CH_ : (BN >= 32 ? 32 : 16);  // accumulator columns per pass
     const int r = q * 32 + lane;
     const int j = r >> 3, l = r & 7;
@@ -147,6 +149,14 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
                     pk.z = pack_bf16x2(v[4], v[5]);
                     pk.w = pack_bf16x2(v[6], v[7]);
                     *reinterpret_cast<uint4*>(p.ea.y + o + q8 * 8) = pk;
+                    if (BN <= 32 && dsum != nullptr) {
+                        const uint32_t pw[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            dsum[c + q8 * 8 + 2 * k] += __uint_as_float(pw[k] << 16);
+                            dsum[c + q8 * 8 + 2 * k + 1] += __uint_as_float(pw[k] & 0xFFFF0000u);
+                        }
+                    }
                 }
             }
         }

@@ -15,9 +15,11 @@ One training step of the stack (forward + backward):
             (g_{l-1} already carries the leaky-ReLU derivative of block l-1;
             the first block's input gradient has no consumer and is skipped)
   The first block, when its input has 1 or 4 channels, needs dZ only for its
-  weight gradient: the pool backward then computes db alone and
-  cf_conv3d_wgrad takes the pooled gradient with the argmax codes (routed
-  form), expanding dZ on chip; its dense dZ is never allocated.
+  weight gradient: cf_conv3d_wgrad takes the pooled gradient with the argmax
+  codes (routed form), expanding dZ on chip, so its dense dZ is never
+  allocated, and its bias gradient (the channel sums of that pooled gradient)
+  comes from the epilogue of block 2's backward-data conv (dsum): block 1 has
+  no pool-backward launch.
   The weight gradients are off the backward critical path (nothing in the
   step reads dW), so by default they run on a second stream, each after its
   block's pool backward (event), with their own workspace; the step ends by
@@ -152,10 +154,12 @@ class CosmoStack:
                 fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope,
                                                        self.dz[l], self.g[l] if routed else None, self.db[l], ws,
                                                        wsb, main)
-            else:
+                self._run(f"poolbwd{l + 1}", main, fn, timer)
+            elif not routed:
                 fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope,
                                                        self.dz[l], None, self.db[l], ws, wsb, main)
-            self._run(f"poolbwd{l + 1}", main, fn, timer)
+                self._run(f"poolbwd{l + 1}", main, fn, timer)
+            # (a routed block below the top: db[l] came with g[l] from block l+1's dgrad)
             desc = self.desc(l)
             if side is not main:
                 ev = torch.cuda.Event()
@@ -169,9 +173,10 @@ class CosmoStack:
                                                 wswb, side)
             self._run(f"wgrad{l + 1}", side, fn, timer)
             if l > 0:
+                dsum = self.db[l - 1] if self.routed(l - 1) else None
                 self._run(f"dgrad{l + 1}", main, lambda: cf.cf_conv3d_dgrad(
                     desc, self.dz[l], None, self.w[l], self.block_input(l), self.slope, self.g[l - 1], ws, wsb,
-                    main), timer)
+                    main, dsum=dsum), timer)
         for s in (main, side):
             if s is not caller:
                 ev = torch.cuda.Event()
@@ -204,9 +209,20 @@ class CosmoStack:
 
     def launches_per_step(self) -> int:
         """Kernels one step enqueues: fwd 1 per block; pool-bwd 2 (scatter +
-        bias sum), wgrad 2 (split-K + reduce) per block; dgrad 2 (filter
-        flip + conv) for blocks 1..L-1."""
+        bias sum) per block except a routed block below the top; wgrad 2
+        (split-K + reduce) per block; dgrad 2 (filter flip + conv) for blocks
+        1..L-1, plus the channel sums for a routed block below: 1 (partials
+        reduction) when fused in the halo-tile epilogue, else 2."""
         n = self.L
         if self.backward_enabled:
-            n += 2 * self.L + 2 * self.L + 2 * (self.L - 1)
+            ch = self.channels
+            for l in range(self.L):
+                n += 2  # wgrad
+                if l == self.L - 1 or not self.routed(l):
+                    n += 2  # pool backward
+                if l > 0:
+                    n += 2  # dgrad
+                    if self.routed(l - 1):
+                        fused = ch[l] <= 32 and ch[l + 1] % 32 == 0 and ch[l] in (32, 64, 128)
+                        n += 1 if fused else 2
         return n

@@ -97,11 +97,15 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
  *        (written to the workspace first; needs cf_workspace_size(CF_OP_DGRAD_ROUTED)).
  *   w  : the forward filter [c_out][3][3][3][c_in] (flipped and transposed
  *        internally into the workspace).
+ *   dsum : NULL, or [c_in] fp32 receiving sum over n and all voxels of the
+ *        stored dx (fixed order).  In a block stack dx is the previous block's
+ *        pooled pre-activation gradient and dsum its bias gradient (fused into
+ *        the epilogue for c_in <= 32, a separate pass over dx otherwise).
  * Supported: c_out a multiple of 32, c_in a multiple of 16.
  */
 cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx,
                           const uint16_t* w, const uint16_t* x_act, float slope, uint16_t* dx,
-                          void* ws, size_t ws_bytes, void* stream);
+                          float* dsum, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Backward weight (CosmoFlow page, section III-C "backward weights", work

@@ -242,9 +242,16 @@ def test_conv_dgrad(cf, oracle_mod, shape, with_act):
     c = _case(shape, 400 + Ci + Co)
     desc = cf.cf_conv_desc(*shape)
     ws, wsb = _ws(cf, cf.CF_OP_DGRAD, desc)
+    import torch
     dx = empty_bf16((N, D, H, W, Ci), fill=float("nan"))
     x_act = dev_bf16(c["x"]) if with_act else None
-    cf.cf_conv3d_dgrad(desc, dev_bf16(c["dz"]), None, dev_bf16(c["w"]), x_act, SLOPE, dx, ws, wsb)
+    dsum = torch.full((Ci,), float("nan"), dtype=torch.float32, device="cuda")
+    cf.cf_conv3d_dgrad(desc, dev_bf16(c["dz"]), None, dev_bf16(c["w"]), x_act, SLOPE, dx, ws, wsb, dsum=dsum)
+    # dsum: channel sums of the stored dx (fused in the epilogue for c_in <= 32)
+    got_dx = host_bf16_f64(dx)
+    ref_sum = got_dx.reshape(-1, Ci).sum(0)
+    np.testing.assert_allclose(dsum.cpu().numpy().astype(np.float64), ref_sum,
+                               rtol=1e-5, atol=1e-5 * np.abs(got_dx).reshape(-1, Ci).sum(0).max())
     dz, w = _f64(oracle_mod, c["dz"]), _f64(oracle_mod, c["w"])
     ref = oracle_mod.conv3d_dgrad(dz, w)
     S = oracle_mod.conv3d_dgrad(np.abs(dz), np.abs(w))
