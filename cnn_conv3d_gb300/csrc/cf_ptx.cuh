@@ -52,17 +52,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on phase `parity` of `bar`.  Gives up when `*abort` becomes
 // non-zero (another role gave up) or after `limit_ns`; in the latter case it
 // raises `*abort` and records `code` in the device status word `status`.
-// Returns true when the phase completed.
-// sleep_cap_ns > 0 adds an exponential back-off (__nanosleep, doubling up to
-// the cap) between polls: for roles whose waits are long and not on the
-// critical path (builders, epilogue), so that waiting warps leave the issue
-// slots to the warps that work.  The TMA producer and the MMA issuer poll
-// without sleeping.
+// Returns true when the phase completed.  Polls with the suspending try_wait
+// and no sleep: a nanosleep back-off measured slower for every role.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns, int* status, int code, uint32_t sleep_cap_ns = 0) {
+                                          uint64_t limit_ns, int* status, int code) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    uint32_t nap = 32;
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 4; ++i)
@@ -73,14 +68,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             atomicCAS(status, 0, code);
             return false;
         }
-        if (sleep_cap_ns != 0) {
-            __nanosleep(nap);
-            if (nap < sleep_cap_ns) nap <<= 1;
-        }
     }
 }
 
-constexpr uint32_t kNapNs = 512;  // back-off cap for builder and epilogue waits
+// Warp-wide bounded wait: lane 0 polls the barrier and the warp takes its
+// result; the __syncwarp orders the other lanes' later accesses after lane 0's
+// observation of the phase.  Must be called by all 32 lanes.  (Measured: a
+// help where a warp waits on several barriers per item and the shared-memory
+// pipe is busy, e.g. the small-channel weight-gradient builders; slower for
+// the small-channel forward builders, which keep all-lane waits.)
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns, int* status, int code) {
+    uint32_t ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns, status, code) ? 1u : 0u;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
 
 // Bounded wait that ignores the abort flag (used to drain copies and MMAs
 // already in flight before a CTA that gave up exits).

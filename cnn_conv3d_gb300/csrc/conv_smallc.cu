@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(608, 1)
             // every lane waits, and the warp leaves together if any lane gave up, so
             // the .sync.aligned tensor-memory stores below always see the full warp
             if (!__all_sync(0xffffffffu,
-                            mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL, kNapNs)))
+                            mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)))
                 break;
             const uint8_t* halo = hring + hs * C::HALO_STRIDE;
 #pragma unroll 1
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(608, 1)
                     if (lane == 0) mbar_arrive(&hempty[hs]);
                 }
                 if (!__all_sync(0xffffffffu, mbar_wait(&aempty[blk], aph ^ 1, abort_flag, p.wait_ns, p.status,
-                                                       WAIT_PRODUCER_EMPTY, kNapNs))) {
+                                                       WAIT_PRODUCER_EMPTY))) {
                     ok = false;
                     break;
                 }

@@ -272,6 +272,8 @@ WGRAD_SHAPES = [
     (1, 4, 8, 16, 4, 16),
     (1, 8, 8, 8, 1, 16),
     (1, 2, 4, 8, 32, 192),
+    (1, 2, 4, 16, 4, 128),     # small c_in with A in tensor memory, one accumulator per issuer
+    (1, 2, 8, 24, 1, 64),
     (2, 2, 8, 16, 32, 32),     # halo-tile wgrad variants: 32 -> 32, 32 -> 128, 64 -> 64
     (1, 4, 20, 8, 32, 128),
     (1, 2, 4, 24, 64, 64),
@@ -305,6 +307,7 @@ ROUTED_SHAPES = [
     (2, 4, 6, 40, 4, 32),      # ragged box in w (40 = 2.5 boxes of 16)
     (1, 2, 8, 24, 1, 16),
     (1, 2, 4, 16, 4, 64),
+    (1, 2, 4, 16, 4, 128),
     (1, 2, 4, 16, 4, 256),
 ]
 
