@@ -52,8 +52,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on phase `parity` of `bar`.  Gives up when `*abort` becomes
 // non-zero (another role gave up) or after `limit_ns`; in the latter case it
 // raises `*abort` and records `code` in the device status word `status`.
-// Returns true when the phase completed.  Polls with the suspending try_wait
-// and no sleep: a nanosleep back-off measured slower for every role.
+// Returns true when the phase completed.  Every waiting lane polls with the
+// suspending try_wait and no sleep (measured: a nanosleep back-off gains
+// nothing, and a lane-0 wait broadcast to the warp is slower than every lane
+// polling).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns, int* status, int code) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -69,21 +71,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             return false;
         }
     }
-}
-
-// Warp-wide bounded wait: lane 0 polls the barrier and the warp takes its
-// result; the __syncwarp orders the other lanes' later accesses after lane 0's
-// observation of the phase.  Must be called by all 32 lanes.  (Measured: a
-// help where a warp waits on several barriers per item and the shared-memory
-// pipe is busy, e.g. the small-channel weight-gradient builders; slower for
-// the small-channel forward builders, which keep all-lane waits.)
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                               uint64_t limit_ns, int* status, int code) {
-    uint32_t ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns, status, code) ? 1u : 0u;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
 }
 
 // Bounded wait that ignores the abort flag (used to drain copies and MMAs

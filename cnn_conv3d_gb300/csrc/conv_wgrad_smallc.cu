@@ -284,9 +284,11 @@ __global__ void __launch_bounds__(480, 1)
             const int64_t b1 = std::min<int64_t>(b0 + g.boxes_per_split, g.total_boxes);
             for (int64_t b = b0; b < b1; ++b, ++lb) {
                 if ((int)(lb & 1) == grp) {
-                    // lane 0 waits for the warp; the warp leaves together
-                    if (!mbar_wait_warp(&lfull[ls], lph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL) ||
-                        !mbar_wait_warp(&bempty[bs], bph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
+                    // all lanes wait; the warp leaves together
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&lfull[ls], lph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL) &&
+                                        mbar_wait(&bempty[bs], bph ^ 1, abort_flag, p.wait_ns, p.status,
+                                                  WAIT_PRODUCER_EMPTY))) {
                         ok = false;
                         break;
                     }
