@@ -352,6 +352,7 @@ cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
     p.tiles_d = (int)((d + HT_D - 1) / HT_D);
     p.n_ntiles = 1;
     p.num_tiles = (int)(n * p.tiles_d * p.tiles_h * p.tiles_w);
+    set_tile_dividers(p);
     p.n_chunks = 0;
     p.ea = EpiArgs{y, idx, bias, x_act, slope, colsum_part};
     p.status = ctx.status;

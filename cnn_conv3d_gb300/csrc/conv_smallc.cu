@@ -76,16 +76,11 @@ struct SmallTile {
 // Tiles are numbered N tile fastest, then w, h, d, n.
 __device__ __forceinline__ SmallTile small_decode(const HaloParams& p, int tile) {
     SmallTile t;
-    int m = tile / p.n_ntiles;
-    const int tw = m % p.tiles_w;
-    m /= p.tiles_w;
-    const int th = m % p.tiles_h;
-    m /= p.tiles_h;
-    const int td = m % p.tiles_d;
-    t.n = m / p.tiles_d;
-    t.w0 = tw * SC_W;
-    t.h0 = th * SC_H;
-    t.d0 = td * SC_D;
+    const TileIdx r = tile_index(p, tile);
+    t.n = r.n;
+    t.w0 = r.tw * SC_W;
+    t.h0 = r.th * SC_H;
+    t.d0 = r.td * SC_D;
     return t;
 }
 
@@ -509,6 +504,7 @@ cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t
     hp.tiles_d = (int)((d + SC_D - 1) / SC_D);
     hp.n_ntiles = (c_out + bn - 1) / bn;
     hp.num_tiles = (int)(n * hp.tiles_d * hp.tiles_h * hp.tiles_w * hp.n_ntiles);
+    set_tile_dividers(hp);
     hp.n_chunks = 1;
     hp.ea = EpiArgs{y, idx, bias, nullptr, slope};
     hp.status = ctx.status;

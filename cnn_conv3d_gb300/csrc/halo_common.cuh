@@ -15,10 +15,40 @@ constexpr int H_ROWS = HH_W * HH_H * HH_D;                   // 720
 struct HaloParams {
     int N, D, H, W, Cin, Cout;
     int tiles_w, tiles_h, tiles_d, n_ntiles, num_tiles, n_chunks;
+    FastDiv fd_nt, fd_w, fd_h, fd_d;  // dividers by n_ntiles, tiles_w, tiles_h, tiles_d
     EpiArgs ea;
     int* status;
     uint64_t wait_ns;
 };
+
+// Host: the tile-decode dividers of p (after its tile counts are set).
+inline void set_tile_dividers(HaloParams& p) {
+    p.fd_nt = FastDiv::make((uint32_t)p.n_ntiles);
+    p.fd_w = FastDiv::make((uint32_t)p.tiles_w);
+    p.fd_h = FastDiv::make((uint32_t)p.tiles_h);
+    p.fd_d = FastDiv::make((uint32_t)p.tiles_d);
+}
+
+// Tile index -> (N tile, w, h, d, n) tile coordinates, N tile fastest.
+struct TileIdx {
+    int nt, tw, th, td, n;
+};
+__device__ __forceinline__ TileIdx tile_index(const HaloParams& p, int tile) {
+    TileIdx r;
+    uint32_t m = (uint32_t)tile, q = p.fd_nt.div(m);
+    r.nt = (int)(m - q * p.fd_nt.d);
+    m = q;
+    q = p.fd_w.div(m);
+    r.tw = (int)(m - q * p.fd_w.d);
+    m = q;
+    q = p.fd_h.div(m);
+    r.th = (int)(m - q * p.fd_h.d);
+    m = q;
+    q = p.fd_d.div(m);
+    r.td = (int)(m - q * p.fd_d.d);
+    r.n = (int)q;
+    return r;
+}
 
 struct HTile {
     int n, d0, h0, w0, co0;
@@ -26,14 +56,10 @@ struct HTile {
 
 __device__ __forceinline__ HTile halo_decode(const HaloParams& p, int tile, int bn) {
     HTile t;
-    const int nt = tile % p.n_ntiles;
-    int m = tile / p.n_ntiles;
-    const int tw = m % p.tiles_w;
-    m /= p.tiles_w;
-    const int th = m % p.tiles_h;
-    m /= p.tiles_h;
-    const int td = m % p.tiles_d;
-    t.n = m / p.tiles_d;
+    const TileIdx r = tile_index(p, tile);
+    const int nt = r.nt, tw = r.tw, th = r.th;
+    t.n = r.n;
+    const int td = r.td;
     t.w0 = tw * HT_W;
     t.h0 = th * HT_H;
     t.d0 = td * HT_D;

@@ -54,3 +54,36 @@ def test_unsupported_shapes(cf):
                                      check=False) == cf.CF_ERR_UNSUPPORTED
     assert cf.cf_bias_lrelu_pool_fwd(1, 4, 4, 4, 12, 16, None, 0.3, 32, None,
                                      check=False) == cf.CF_ERR_UNSUPPORTED
+
+
+def test_tile_divider_method():
+    """The tile decoders divide by launch-time constants with the unsigned
+    multiply-and-shift method of Granlund and Montgomery ("Division by
+    Invariant Integers using Multiplication", figure 4.1, N = 32).  The
+    method, as the kernels write it, equals floor division for every divisor
+    and numerator checked here (all divisors up to 4096 plus large ones, with
+    numerators at 0, around multiples of d and at the 32-bit edge)."""
+    import random
+
+    def make(d):
+        l = 0
+        while l < 32 and (1 << l) < d:
+            l += 1
+        m = ((1 << 32) * ((1 << l) - d)) // d + 1
+        assert 0 < m < (1 << 32)
+        return m, (1 if l else 0), (l - 1 if l else 0)
+
+    def div(x, mss):
+        m, s1, s2 = mss
+        t = (x * m) >> 32
+        return (t + ((x - t) >> s1)) >> s2
+
+    rng = random.Random(5)
+    divisors = list(range(1, 4097)) + [rng.randrange(4097, 1 << 31) for _ in range(200)] + [(1 << 31) - 1]
+    for d in divisors:
+        mss = make(d)
+        xs = [0, 1, d - 1, d, d + 1, 2 * d - 1, 2 * d, (1 << 32) - 1, (1 << 31) - 1]
+        xs += [rng.randrange(0, 1 << 32) for _ in range(40)]
+        for x in xs:
+            if 0 <= x < (1 << 32):
+                assert div(x, mss) == x // d, (x, d)
