@@ -7,37 +7,12 @@
 
 #include "cf_internal.h"
 #include "cf_ptx.cuh"
+#include "fastdiv.cuh"
 
 namespace cf {
 
 // Output tile of 128 voxels: box (TD=2) x th x tw starting at (d0,h0,w0) of
 // sample n, and output channels [co0, co0 + BN).
-// Division by a divisor fixed at launch, by multiply and shifts (Granlund and
-// Montgomery, "Division by Invariant Integers using Multiplication", 1994,
-// the unsigned N-bit algorithm of their figure 4.1 with N = 32): with
-// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
-//   q = (t + ((x - t) >> min(l, 1))) >> max(l - 1, 0),  t = mulhi(m, x),
-// equals floor(x / d) for every 32-bit x.  Tile decoders run it once per
-// tile in every epilogue thread, where an integer division costs about 20
-// instructions.
-struct FastDiv {
-    uint32_t d, m, s1, s2;
-    static FastDiv make(uint32_t d) {
-        uint32_t l = 0;
-        while (l < 32 && (1ull << l) < d) ++l;
-        FastDiv f;
-        f.d = d;
-        f.m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
-        f.s1 = l ? 1u : 0u;
-        f.s2 = l ? l - 1 : 0u;
-        return f;
-    }
-    __device__ __forceinline__ uint32_t div(uint32_t x) const {
-        const uint32_t t = __umulhi(x, m);
-        return (t + ((x - t) >> s1)) >> s2;
-    }
-};
-
 struct TileCoord {
     int n, d0, h0, w0, co0;
 };
@@ -46,21 +21,27 @@ struct ConvGeom {
     int N, D, H, W;
     int Cin, Cout;  // GEMM view: K = 27 * Cin, N-dimension = Cout
     int tw, th, td;
+    int lw, lh;  // log2(tw), log2(th): the tile extents are powers of two
     int tiles_w, tiles_h, tiles_d;
     int n_ntiles;
     int num_tiles;
+    FastDiv fd_nt, fd_w, fd_h, fd_d;  // dividers by n_ntiles, tiles_w, tiles_h, tiles_d
 };
 
 __device__ __forceinline__ TileCoord decode_tile(const ConvGeom& g, int tile, int bn) {
     TileCoord c;
-    int nt = tile % g.n_ntiles;
-    int mt = tile / g.n_ntiles;
-    int tw = mt % g.tiles_w;
-    mt /= g.tiles_w;
-    int th = mt % g.tiles_h;
-    mt /= g.tiles_h;
-    int td = mt % g.tiles_d;
-    c.n = mt / g.tiles_d;
+    uint32_t m = (uint32_t)tile, q = g.fd_nt.div(m);
+    const int nt = (int)(m - q * g.fd_nt.d);
+    m = q;
+    q = g.fd_w.div(m);
+    const int tw = (int)(m - q * g.fd_w.d);
+    m = q;
+    q = g.fd_h.div(m);
+    const int th = (int)(m - q * g.fd_h.d);
+    m = q;
+    q = g.fd_d.div(m);
+    const int td = (int)(m - q * g.fd_d.d);
+    c.n = (int)q;
     c.w0 = tw * g.tw;
     c.h0 = th * g.th;
     c.d0 = td * g.td;
@@ -101,7 +82,7 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
     constexpr int CH = BN >= 32 ? 32 : 16;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
-    const int l = row % g.tw, j = (row / g.tw) % g.th, i = row / (g.tw * g.th);
+    const int l = row & (g.tw - 1), j = (row >> g.lw) & (g.th - 1), i = row >> (g.lw + g.lh);
     const int d = tc.d0 + i, h = tc.h0 + j, w = tc.w0 + l;
     const bool valid = d < g.D && h < g.H && w < g.W;
     const int64_t vox = (((int64_t)tc.n * g.D + d) * g.H + h) * g.W + w;
@@ -206,11 +187,19 @@ inline ConvGeom make_geom(int64_t n, int64_t d, int64_t h, int64_t w, int cin, i
     g.tw = t.tw;
     g.th = t.th;
     g.td = t.td;
+    g.lw = 0;
+    while ((1 << g.lw) < g.tw) ++g.lw;
+    g.lh = 0;
+    while ((1 << g.lh) < g.th) ++g.lh;
     g.tiles_w = (int)((w + t.tw - 1) / t.tw);
     g.tiles_h = (int)((h + t.th - 1) / t.th);
     g.tiles_d = (int)((d + t.td - 1) / t.td);
     g.n_ntiles = (cout + bn - 1) / bn;
     g.num_tiles = (int)(n * g.tiles_d * g.tiles_h * g.tiles_w * g.n_ntiles);
+    g.fd_nt = FastDiv::make((uint32_t)g.n_ntiles);
+    g.fd_w = FastDiv::make((uint32_t)g.tiles_w);
+    g.fd_h = FastDiv::make((uint32_t)g.tiles_h);
+    g.fd_d = FastDiv::make((uint32_t)g.tiles_d);
     return g;
 }
 

@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------
 // host side
 
+// Tile extents are powers of two (the epilogue decodes rows with shifts).
 TileGeom choose_tile(int64_t d, int64_t h, int64_t w) {
     (void)d;
     TileGeom t;

@@ -11,6 +11,7 @@
 
 #include "cf_internal.h"
 #include "cf_ptx.cuh"
+#include "fastdiv.cuh"
 
 namespace cf {
 
@@ -31,22 +32,50 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return v;
 }
 
+// Pooled voxel index -> (n, pd, ph, pw) of the pooled grid [N][D2][H2][W2]:
+// multiply-shift division by the launch-time extents while the index fits 32
+// bits (every realistic case), 64-bit division beyond.
+struct PoolGrid {
+    FastDiv w2, h2, d2;
+};
+__device__ __forceinline__ void pool_decode(const PoolGrid& g, int64_t pvox, int64_t& n, int& pd, int& ph, int& pw) {
+    if (pvox < (int64_t)0xFFFFFFFF) {
+        uint32_t m = (uint32_t)pvox, q = g.w2.div(m);
+        pw = (int)(m - q * g.w2.d);
+        m = q;
+        q = g.h2.div(m);
+        ph = (int)(m - q * g.h2.d);
+        m = q;
+        q = g.d2.div(m);
+        pd = (int)(m - q * g.d2.d);
+        n = q;
+    } else {
+        pw = (int)(pvox % g.w2.d);
+        int64_t r = pvox / g.w2.d;
+        ph = (int)(r % g.h2.d);
+        r /= g.h2.d;
+        pd = (int)(r % g.d2.d);
+        n = r / g.d2.d;
+    }
+}
+
+static PoolGrid pool_grid(int64_t d, int64_t h, int64_t w) {
+    return PoolGrid{FastDiv::make((uint32_t)(w / 2)), FastDiv::make((uint32_t)(h / 2)), FastDiv::make((uint32_t)(d / 2))};
+}
+
 // one thread = one pooled voxel x 8 channels
 __global__ void pool_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ bias, float slope,
                                 uint16_t* __restrict__ y, uint8_t* __restrict__ idx, int64_t N, int D, int H, int W,
-                                int C) {
+                                int C, PoolGrid pg) {
     const int C8 = C / 8, D2 = D / 2, H2 = H / 2, W2 = W / 2;
     const int64_t total = N * D2 * H2 * W2 * C8;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int c8 = (int)(i % C8);
         int64_t pvox = i / C8;
-        const int pw = (int)(pvox % W2);
-        int64_t r = pvox / W2;
-        const int ph = (int)(r % H2);
-        r /= H2;
-        const int pd = (int)(r % D2);
-        const int64_t n = r / D2;
+        int64_t n;
+        int pd, ph, pw;
+        pool_decode(pg, pvox, n, pd, ph, pw);
         float m[8];
         uint32_t code[8];
 #pragma unroll
@@ -87,15 +116,18 @@ __global__ void pool_fwd_kernel(const uint16_t* __restrict__ z, const float* __r
 __global__ void pool_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ y,
                                 const uint8_t* __restrict__ idx, float slope, uint16_t* __restrict__ dz,
                                 uint16_t* __restrict__ dy_pre, float* __restrict__ partial, int64_t N, int D, int H,
-                                int W, int C) {
+                                int W, int C, PoolGrid pg) {
     extern __shared__ float red[];  // [blockDim][8]
     const int C8 = C / 8, D2 = D / 2, H2 = H / 2, W2 = W / 2;
     const int64_t total = N * D2 * H2 * W2 * C8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int c8 = (int)(i % C8);
-        const int64_t pvox = i / C8;
+    // blockDim and the grid stride are multiples of C8: the thread's channel
+    // group is fixed and its pooled voxel advances by a fixed step
+    const int c8 = (int)(threadIdx.x % C8);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t pstep = stride / C8;
+    int64_t pvox = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / C8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += stride, pvox += pstep) {
         const int64_t po = pvox * C + 8 * c8;
         float g[8];
         unpack8(__ldg(reinterpret_cast<const uint4*>(dy + po)), g);
@@ -114,12 +146,9 @@ __global__ void pool_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t*
         if (dz) {
             const uint2 cv = __ldg(reinterpret_cast<const uint2*>(idx + po));
             const uint32_t codes[2] = {cv.x, cv.y};
-            const int pw = (int)(pvox % W2);
-            int64_t r = pvox / W2;
-            const int ph = (int)(r % H2);
-            r /= H2;
-            const int pd = (int)(r % D2);
-            const int64_t n = r / D2;
+            int64_t n;
+            int pd, ph, pw;
+            pool_decode(pg, pvox, n, pd, ph, pw);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
@@ -251,7 +280,8 @@ cf_status launch_pool_fwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
     const int64_t total = n * (d / 2) * (h / 2) * (w / 2) * (c / 8);
     const int threads = 256;
     const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads, 16LL * ctx.num_sms));
-    pool_fwd_kernel<<<blocks, threads, 0, ctx.stream>>>(z, bias, slope, y, idx, n, (int)d, (int)h, (int)w, c);
+    pool_fwd_kernel<<<blocks, threads, 0, ctx.stream>>>(z, bias, slope, y, idx, n, (int)d, (int)h, (int)w, c,
+                                                        pool_grid(d, h, w));
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
@@ -272,7 +302,7 @@ cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
             dy, partial, n * (d / 2) * (h / 2) * (w / 2) * (c / 8), c);
     } else {
         pool_bwd_kernel<<<blocks, threads, threads * 8 * sizeof(float), ctx.stream>>>(
-            dy, y, idx, slope, dz, dy_pre, partial, n, (int)d, (int)h, (int)w, c);
+            dy, y, idx, slope, dz, dy_pre, partial, n, (int)d, (int)h, (int)w, c, pool_grid(d, h, w));
     }
     if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
     if (dbias) {
