@@ -142,7 +142,6 @@ __global__ void __launch_bounds__(608, 1)
     uint64_t* drain = tempty + 2;  // [2]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    volatile int* epi_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int co0 = (blockIdx.x % p.n_ntiles) * BN;  // the CTA's N tile (see the launch)
@@ -317,7 +316,6 @@ __global__ void __launch_bounds__(608, 1)
         // 16 of every 32 channels (when BN is 16, the second warp of a quarter idles)
         const int q = warp & 3;
         const int half = (warp - 10) >> 2;
-        const int et = threadIdx.x - 320;
         const int lp = 2 * q + (lane >> 4), v = lane & 15, dw = v & 1;
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
         constexpr int NPASS = (BN + 31) / 32;
@@ -334,7 +332,12 @@ __global__ void __launch_bounds__(608, 1)
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const uint32_t acc = C::NACC == 2 ? (local & 1) : 0u;
             const uint32_t use = C::NACC == 2 ? (local >> 1) : local;
-            if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status, 256)) break;
+            // each warp waits on its own (no barrier across the eight warps: the
+            // slowest warp of a tile would hold the others and the accumulator's
+            // release); a warp that gives up raises the abort flag for all
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&tfull[acc], use & 1, abort_flag, p.wait_ns, p.status, WAIT_EPI_TMEM_FULL)))
+                break;
             tc_fence_after();
             const SmallTile t = small_decode(p, tile);
             const uint32_t acol = lane_addr + acc * C::ACC_COLS;
