@@ -30,8 +30,9 @@
 //                 accumulator (two per issuer when tensor memory allows);
 //   warps 10..13: at the end of a unit of boxes, the sum of the two issuers'
 //                 accumulators to the split-K partials.
-// The load ring (about 12 boxes) hides the TMA latency, the build ring the
-// MMA-completion latency; each box's load stage is released by the MMA commit.
+// The load ring (as many boxes as shared memory leaves, up to 12) hides the
+// TMA latency, the build ring the MMA-completion latency; each box's load
+// stage is released by the MMA commit.
 #include <algorithm>
 
 #include "smallc_common.cuh"
