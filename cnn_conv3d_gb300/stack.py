@@ -125,18 +125,32 @@ class CosmoStack:
         e1.record(stream)
         timer.append((key, e0, e1))
 
-    def forward(self, stream=None, timer=None):
-        """timer: optional list receiving (key, start event, end event) per launch."""
+    def forward(self, stream=None, timer=None, x_chunks=None):
+        """timer: optional list receiving (key, start event, end event) per launch.
+        x_chunks: optional [(n0, n1, event)]: the first block runs per sample range
+        [n0, n1), each after its event (the range's input has landed); a
+        sample's output does not depend on the others, so the results are the
+        same bits as one launch over the batch."""
         main = self._main(stream)
         for l in range(self.L):
+            if l == 0 and x_chunks is not None:
+                _, d, h, w = self.dims[0]
+                for n0, n1, ev in x_chunks:
+                    main.wait_event(ev)
+                    cf.cf_conv3d_fwd(cf.cf_conv_desc(n1 - n0, d, h, w, self.channels[0], self.channels[1]),
+                                     self.x[n0:n1], self.w[0], (self.b[0], self.slope, self.idx[0][n0:n1]),
+                                     self.y[0][n0:n1], None, 0, main)
+                continue
             self._run(f"fwd{l + 1}", main, lambda l=l: cf.cf_conv3d_fwd(
                 self.desc(l), self.block_input(l), self.w[l], (self.b[l], self.slope, self.idx[l]), self.y[l],
                 None, 0, main), timer)
 
-    def backward(self, dy, stream=None, timer=None, serial=False):
+    def backward(self, dy, stream=None, timer=None, serial=False, host_out=None):
         """timer: as in forward (keys "poolbwd<l+1>", "wgrad<l+1>", "dgrad<l+1>").
         serial: every op on the caller's stream (each op's events then time it
-        alone)."""
+        alone).  host_out: optional (dw_host, db_host, copy_stream): each dW and
+        db is copied to its host tensor on the copy stream as soon as the
+        launch that completes it has run (the caller joins the copy stream)."""
         caller = self._main(stream)
         main = self.crit if (self.crit is not None and not serial) else caller
         side = self.side if (self.side is not None and not serial) else caller
@@ -146,6 +160,17 @@ class CosmoStack:
             main.wait_event(ev)
         ws, wsb = self.ws, self.ws.numel()
         wsw, wswb = self.ws_w, self.ws_w.numel()
+
+        def to_host(src_stream, dst, src):
+            if host_out is None:
+                return
+            cp = host_out[2]
+            ev = torch.cuda.Event()
+            ev.record(src_stream)
+            cp.wait_event(ev)
+            with torch.cuda.stream(cp):
+                dst.copy_(src, non_blocking=True)
+
         for l in range(self.L - 1, -1, -1):
             n, d, h, w = self.dims[l]
             co = self.channels[l + 1]
@@ -155,10 +180,12 @@ class CosmoStack:
                                                        self.dz[l], self.g[l] if routed else None, self.db[l], ws,
                                                        wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
+                to_host(main, host_out and host_out[1][l], self.db[l])
             elif not routed:
                 fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope,
                                                        self.dz[l], None, self.db[l], ws, wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
+                to_host(main, host_out and host_out[1][l], self.db[l])
             # (a routed block below the top: db[l] came with g[l] from block l+1's dgrad)
             desc = self.desc(l)
             if side is not main:
@@ -172,12 +199,15 @@ class CosmoStack:
                 fn = lambda: cf.cf_conv3d_wgrad(desc, self.block_input(l), self.dz[l], None, self.dw[l], 0, wsw,
                                                 wswb, side)
             self._run(f"wgrad{l + 1}", side, fn, timer)
+            to_host(side, host_out and host_out[0][l], self.dw[l])
             if l > 0:
                 dsum = self.db[l - 1] if self.routed(l - 1) else None
                 self._run(f"dgrad{l + 1}", main, lambda: cf.cf_conv3d_dgrad(
                     desc, self.dz[l], None, self.w[l], self.block_input(l), self.slope, self.g[l - 1], ws, wsb,
                     main, dsum=dsum), timer)
-        for s in (main, side):
+                if dsum is not None:
+                    to_host(main, host_out and host_out[1][l - 1], dsum)
+        for s in (main, side) + ((host_out[2],) if host_out is not None else ()):
             if s is not caller:
                 ev = torch.cuda.Event()
                 ev.record(s)
@@ -188,11 +218,65 @@ class CosmoStack:
         if self.backward_enabled:
             self.backward(dy, stream, timer, serial)
 
-    def capture(self, dy, timer=None, keys=None):
+    def _copy_stream(self):
+        if getattr(self, "_cp", None) is None:
+            self._cp = torch.cuda.Stream(device=self.device)
+        return self._cp
+
+    def step_host(self, x_host, dy_host, dw_host, db_host, stream=None, chunks=None):
+        """One training step from host inputs to host results: x_host (the batch,
+        [n][d][h][w][c0] bf16) and dy_host (the gradient at the top output) in
+        pinned host memory are copied in, every dW[l] and db[l] is copied out to
+        the pinned host tensors dw_host[l] / db_host[l].  The copies overlap the
+        compute: the input goes over in `chunks` sample ranges (default: one per
+        sample, at most 8), the first block starting on each range as it lands,
+        and each gradient leaves as soon as it is final.  Same results, bit for
+        bit, as load + step + copy-back.  The host tensors must stay untouched
+        until the caller's stream has passed the step."""
+        main = self._main(stream)
+        cp = self._copy_stream()
+        ev = torch.cuda.Event()
+        ev.record(main)
+        cp.wait_event(ev)  # after the previous work on the caller's stream (buffer reuse)
+        n = self.n
+        k = max(1, min(n, chunks if chunks else 8))
+        bounds = [(i * n // k, (i + 1) * n // k) for i in range(k)]
+        x_chunks = []
+        with torch.cuda.stream(cp):
+            for n0, n1 in bounds:
+                if n1 <= n0:
+                    continue
+                self.x[n0:n1].copy_(x_host.view(self.x.shape)[n0:n1], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(cp)
+                x_chunks.append((n0, n1, e))
+            dy_dev = self._dy_buffer(dy_host)
+            dy_dev.copy_(dy_host.view(dy_dev.shape), non_blocking=True)
+            e_dy = torch.cuda.Event()
+            e_dy.record(cp)
+        self.forward(main, None, x_chunks)
+        if self.backward_enabled:
+            main.wait_event(e_dy)
+            self.backward(dy_dev, main, host_out=(dw_host, db_host, cp))
+        else:
+            ev = torch.cuda.Event()
+            ev.record(cp)
+            main.wait_event(ev)
+
+    def _dy_buffer(self, dy_host):
+        """Device buffer of the top-output gradient for step_host."""
+        if getattr(self, "_dy", None) is None:
+            n, d, h, w = self.dims[self.L - 1]
+            self._dy = torch.empty((n, d // 2, h // 2, w // 2, self.channels[self.L]), dtype=torch.bfloat16,
+                                   device=self.device)
+        return self._dy
+
+    def capture(self, dy, timer=None, keys=None, host=None):
         """Records one step into a CUDA graph (replay() then re-runs it with no
         per-launch host work).  The buffers, dy included, are bound at capture.
         With a timer list, the events of the ops in `keys` (all if None) become
-        event-record nodes."""
+        event-record nodes.  host: (x_host, dy_host, dw_host, db_host) records
+        step_host instead (its copies become graph nodes; dy is unused)."""
         g = torch.cuda.CUDAGraph()
         cur = torch.cuda.current_stream(self.device)
         s = torch.cuda.Stream(device=self.device)
@@ -201,7 +285,10 @@ class CosmoStack:
         try:
             with torch.cuda.stream(s):
                 with torch.cuda.graph(g, stream=s):
-                    self.step(dy, s, timer)
+                    if host is not None:
+                        self.step_host(*host, stream=s)
+                    else:
+                        self.step(dy, s, timer)
         finally:
             self._capturing, self.timer_keys = False, None
         cur.wait_stream(s)

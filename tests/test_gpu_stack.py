@@ -54,3 +54,42 @@ def test_schedules_agree(torch_cuda, shape):
     for a, b, c in zip(ref, two, graph):
         assert torch.equal(a, b)
         assert torch.equal(a, c)
+
+
+@pytest.mark.parametrize("shape", [(3, 32, (4, 32, 64, 128))])
+def test_host_step_matches(torch_cuda, shape):
+    """step_host (input copied in per sample range, overlapped with the first
+    block; gradients copied out as each is final), eager and as a CUDA graph,
+    gives the bits of load + step + copy-back."""
+    torch = torch_cuda
+    from cnn_conv3d_gb300 import cfconv as cf
+    from cnn_conv3d_gb300.stack import CosmoStack
+    n, s, ch = shape
+    inp = synthdata.stack_inputs(n, s, ch, seed=4343, with_dy=True)
+    dy = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).cuda()
+    st = CosmoStack(n, s, ch, 0.3, backward=True)
+    st.load(inp["x"], inp["w"], inp["b"])
+    st.step(dy)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in st.y + st.idx] + [t.cpu() for t in st.dw + st.db]
+    x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    dy_host = dy.cpu().pin_memory()
+    dw_host = [torch.full(t.shape, float("nan"), dtype=t.dtype).pin_memory() for t in st.dw]
+    db_host = [torch.full(t.shape, float("nan"), dtype=t.dtype).pin_memory() for t in st.db]
+    st.x.zero_()
+    for t in st.y + st.dw + st.db:
+        t.zero_()
+    st.step_host(x_host, dy_host, dw_host, db_host, chunks=2)
+    torch.cuda.synchronize()
+    got = [t.clone() for t in st.y + st.idx] + [t.clone() for t in dw_host + db_host]
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+    for t in dw_host + db_host:
+        t.fill_(float("nan"))
+    g = st.capture(None, host=(x_host, dy_host, dw_host, db_host))
+    g.replay()
+    torch.cuda.synchronize()
+    got = [t.clone() for t in st.y + st.idx] + [t.clone() for t in dw_host + db_host]
+    assert cf.cf_last_device_status() == cf.CF_OK
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
