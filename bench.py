@@ -329,7 +329,7 @@ def run_ours(args, rank, world, local_rank):
         d2h = sum(t.numel() * 4 for t in dw_host) + sum(t.numel() * 4 for t in db_host)
 
         # the public host-buffer step: the input goes over per sample, each
-        # sample's first block starting as it lands; each dW / db leaves as
+        # sample's leading blocks starting as it lands; each dW / db leaves as
         # soon as it is final (a CUDA graph of it when the step is graphed)
         host = (x_host, dy_host, dw_host, db_host)
         st.step_host(*host, stream=stream)
@@ -362,8 +362,8 @@ def run_ours(args, rank, world, local_rank):
         em = max_over_ranks(float(np.mean(e_ms)), world, dev)
         e2e = {"value": round(whole_job_rate(total_flops, world, em) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(em, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "api": "CosmoStack.step_host (pinned host buffers; input per sample overlapped with the first "
-                      "block, gradients copied out as each is final)"
+               "api": "CosmoStack.step_host (pinned host buffers; input per sample overlapped with the leading "
+                      "blocks, gradients copied out as each is final)"
                       + (", CUDA graph" if e2e_graph is not None else ", eager")}
 
     clk.__exit__(None, None, None)

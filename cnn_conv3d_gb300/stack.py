@@ -125,22 +125,29 @@ class CosmoStack:
         e1.record(stream)
         timer.append((key, e0, e1))
 
+    # blocks run per sample range by step_host while the input is still arriving
+    # (those whose per-sample volume is at least 32^3 voxels: enough tiles)
+    def _chunked_blocks(self) -> int:
+        return sum(1 for l in range(self.L) if self.dims[l][1] >= 32)
+
     def forward(self, stream=None, timer=None, x_chunks=None):
         """timer: optional list receiving (key, start event, end event) per launch.
-        x_chunks: optional [(n0, n1, event)]: the first block runs per sample range
-        [n0, n1), each after its event (the range's input has landed); a
-        sample's output does not depend on the others, so the results are the
-        same bits as one launch over the batch."""
+        x_chunks: optional [(n0, n1, event)]: the leading blocks (those of
+        _chunked_blocks) run per sample range [n0, n1), each range after its
+        event (its input has landed); a sample's outputs do not depend on the
+        others, so the results are the same bits as launches over the batch."""
         main = self._main(stream)
-        for l in range(self.L):
-            if l == 0 and x_chunks is not None:
-                _, d, h, w = self.dims[0]
-                for n0, n1, ev in x_chunks:
-                    main.wait_event(ev)
-                    cf.cf_conv3d_fwd(cf.cf_conv_desc(n1 - n0, d, h, w, self.channels[0], self.channels[1]),
-                                     self.x[n0:n1], self.w[0], (self.b[0], self.slope, self.idx[0][n0:n1]),
-                                     self.y[0][n0:n1], None, 0, main)
-                continue
+        first = 0
+        if x_chunks is not None:
+            first = max(1, self._chunked_blocks())
+            for n0, n1, ev in x_chunks:
+                main.wait_event(ev)
+                for l in range(first):
+                    _, d, h, w = self.dims[l]
+                    cf.cf_conv3d_fwd(cf.cf_conv_desc(n1 - n0, d, h, w, self.channels[l], self.channels[l + 1]),
+                                     self.block_input(l)[n0:n1], self.w[l],
+                                     (self.b[l], self.slope, self.idx[l][n0:n1]), self.y[l][n0:n1], None, 0, main)
+        for l in range(first, self.L):
             self._run(f"fwd{l + 1}", main, lambda l=l: cf.cf_conv3d_fwd(
                 self.desc(l), self.block_input(l), self.w[l], (self.b[l], self.slope, self.idx[l]), self.y[l],
                 None, 0, main), timer)
@@ -229,8 +236,8 @@ class CosmoStack:
         pinned host memory are copied in, every dW[l] and db[l] is copied out to
         the pinned host tensors dw_host[l] / db_host[l].  The copies overlap the
         compute: the input goes over in `chunks` sample ranges (default: one per
-        sample, at most 8), the first block starting on each range as it lands,
-        and each gradient leaves as soon as it is final.  Same results, bit for
+        sample, at most 8), the leading blocks running on each range as it
+        lands, and each gradient leaves as soon as it is final.  Same results, bit for
         bit, as load + step + copy-back.  The host tensors must stay untouched
         until the caller's stream has passed the step."""
         main = self._main(stream)

@@ -56,7 +56,7 @@ def test_schedules_agree(torch_cuda, shape):
         assert torch.equal(a, c)
 
 
-@pytest.mark.parametrize("shape", [(3, 32, (4, 32, 64, 128))])
+@pytest.mark.parametrize("shape", [(3, 64, (4, 32, 64, 128))])
 def test_host_step_matches(torch_cuda, shape):
     """step_host (input copied in per sample range, overlapped with the first
     block; gradients copied out as each is final), eager and as a CUDA graph,
