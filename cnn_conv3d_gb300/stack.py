@@ -33,6 +33,13 @@ import torch
 from . import cfconv as cf
 
 
+def sample_ranges(n: int, chunks: int):
+    """[n0, n1) sample ranges splitting n samples into min(n, chunks) nearly
+    equal, non-empty, ascending pieces (at least one)."""
+    k = max(1, min(n, chunks))
+    return [(i * n // k, (i + 1) * n // k) for i in range(k) if (i + 1) * n // k > i * n // k]
+
+
 class CosmoStack:
     def __init__(self, n: int, spatial: int, channels, slope: float = 0.3, device: str = "cuda",
                  backward: bool = True, overlap: bool = True):
@@ -245,14 +252,9 @@ class CosmoStack:
         ev = torch.cuda.Event()
         ev.record(main)
         cp.wait_event(ev)  # after the previous work on the caller's stream (buffer reuse)
-        n = self.n
-        k = max(1, min(n, chunks if chunks else 8))
-        bounds = [(i * n // k, (i + 1) * n // k) for i in range(k)]
         x_chunks = []
         with torch.cuda.stream(cp):
-            for n0, n1 in bounds:
-                if n1 <= n0:
-                    continue
+            for n0, n1 in sample_ranges(self.n, chunks if chunks else 8):
                 self.x[n0:n1].copy_(x_host.view(self.x.shape)[n0:n1], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(cp)

@@ -56,3 +56,18 @@ def test_max_over_ranks_gloo_two_processes():
         res = dict(out)
     assert res[0][0] == res[1][0] == 4.0
     assert res[0][1] == pytest.approx(2 * 8 / 4e-3)
+
+
+def test_host_step_sample_ranges():
+    """The host-buffer step's input split: contiguous, non-empty, covering
+    every sample once, at most `chunks` pieces whose sizes differ by <= 1."""
+    from cnn_conv3d_gb300.stack import sample_ranges
+    for n in range(1, 20):
+        for chunks in range(1, 12):
+            r = sample_ranges(n, chunks)
+            assert 1 <= len(r) <= min(n, chunks)
+            assert r[0][0] == 0 and r[-1][1] == n
+            assert all(a < b for a, b in r)
+            assert all(r[i][1] == r[i + 1][0] for i in range(len(r) - 1))
+            sizes = [b - a for a, b in r]
+            assert max(sizes) - min(sizes) <= 1
