@@ -63,10 +63,11 @@ def _load():
         lib.oracle_conv3d_wgrad_pts_bf16.argtypes = dims + [_U16, _U16] + pts
         lib.oracle_block_fwd_pts_bf16.argtypes = dims + [_U16, _U16, _F32, ctypes.c_double,
                                                          _i64, _I64, _D, _U8, _D, _D]
+        lib.oracle_conv3d_wgrad_routed_pts_bf16.argtypes = dims + [_U16, _U16, _U8] + pts
         for f in (lib.oracle_conv3d_fwd, lib.oracle_conv3d_dgrad, lib.oracle_conv3d_wgrad,
                   lib.oracle_pool_fwd, lib.oracle_pool_bwd, lib.oracle_conv3d_fwd_pts_bf16,
                   lib.oracle_conv3d_dgrad_pts_bf16, lib.oracle_conv3d_wgrad_pts_bf16,
-                  lib.oracle_block_fwd_pts_bf16):
+                  lib.oracle_block_fwd_pts_bf16, lib.oracle_conv3d_wgrad_routed_pts_bf16):
             f.restype = None
         _lib = lib
     return _lib
@@ -209,6 +210,47 @@ def conv3d_wgrad_pts(x16, dz16, pts):
     lib.oracle_conv3d_wgrad_pts_bf16(N, D, H, W, Ci, Co, _p(x16, _U16), _p(dz16, _U16), len(pts),
                                      _p(pts, _I64), _p(out, _D), _p(s, _D))
     return out, s
+
+
+def conv3d_wgrad_routed_pts(x16, g16, idx, pts):
+    """Exact dW and S at points (co,kd,kh,kw,ci) when dZ is the argmax-routed
+    expansion of the pooled gradient g16 [n][d/2][h/2][w/2][co] by the codes idx."""
+    lib = _load()
+    x16, g16 = _u16(x16), _u16(g16)
+    idx = np.ascontiguousarray(idx, dtype=np.uint8)
+    N, D, H, W, Ci = x16.shape
+    Co = g16.shape[4]
+    assert g16.shape == (N, D // 2, H // 2, W // 2, Co) and idx.shape == g16.shape
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 5)
+    out = np.empty(len(pts)); s = np.empty(len(pts))
+    lib.oracle_conv3d_wgrad_routed_pts_bf16(N, D, H, W, Ci, Co, _p(x16, _U16), _p(g16, _U16), _p(idx, _U8),
+                                            len(pts), _p(pts, _I64), _p(out, _D), _p(s, _D))
+    return out, s
+
+
+def conv3d_wgrad_mm(x, dz, x_below=None, x_above=None):
+    """dW [Co,3,3,3,Ci] = sum over n and voxels of dz[n,v,co] * x[n,v+t-1,ci],
+    one matrix product per tap t (numpy matmul of the flattened dz with the
+    tap-shifted x; x zero outside the volume).  x_below / x_above: the plane
+    of a taller volume just below / above the d-range of x and dz ([N,H,W,Ci]),
+    zero when None, so that slabs of a volume can be summed one at a time."""
+    x, dz = _f64(x), _f64(dz)
+    N, D, H, W, Ci = x.shape
+    Co = dz.shape[4]
+    xp = np.zeros((N, D + 2, H + 2, W + 2, Ci))
+    xp[:, 1:D + 1, 1:H + 1, 1:W + 1, :] = x
+    if x_below is not None:
+        xp[:, 0, 1:H + 1, 1:W + 1, :] = x_below
+    if x_above is not None:
+        xp[:, D + 1, 1:H + 1, 1:W + 1, :] = x_above
+    g = dz.reshape(-1, Co).T
+    dw = np.empty((Co, 3, 3, 3, Ci))
+    for kd in range(3):
+        for kh in range(3):
+            for kw in range(3):
+                xs = np.ascontiguousarray(xp[:, kd:kd + D, kh:kh + H, kw:kw + W, :]).reshape(-1, Ci)
+                dw[:, kd, kh, kw, :] = g @ xs
+    return dw
 
 
 def block_fwd_pts(x16, w16, bias, slope, pts):

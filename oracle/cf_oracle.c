@@ -399,3 +399,42 @@ void oracle_block_fwd_pts_bf16(int64_t N, int64_t D, int64_t H, int64_t W, int32
     (void)N;
     (void)Co;
 }
+
+/* Backward weight at sampled filter elements when dZ is the argmax-routed
+ * expansion of a pooled gradient (the max-pool backward): dz[n,v,co] equals
+ * g[n,p,co] at the voxel v = 2p + (dd,dh,dw) whose code dd*4+dh*2+dw is
+ * idx[n,p,co], and 0 at the other seven voxels of the window.  The sum
+ *   dW[co,t,ci] = sum_{n,v} dz[n,v,co] * x[n, v+(t-1), ci]
+ * therefore runs over the pooled voxels p, one routed voxel each.
+ * g, idx: [N][D/2][H/2][W/2][Co]; x: [N][D][H][W][Ci]; D, H, W even.
+ * pts: npts x (co,kd,kh,kw,ci). */
+void oracle_conv3d_wgrad_routed_pts_bf16(int64_t N, int64_t D, int64_t H, int64_t W, int32_t Ci, int32_t Co,
+                                         const uint16_t* x, const uint16_t* g, const uint8_t* idx,
+                                         int64_t npts, const int64_t* pts, double* out, double* sabs)
+{
+    int64_t D2 = D / 2, H2 = H / 2, W2 = W / 2;
+    for (int64_t p = 0; p < npts; ++p) {
+        int32_t co = (int32_t)pts[5 * p];
+        int kd = (int)pts[5 * p + 1], kh = (int)pts[5 * p + 2], kw = (int)pts[5 * p + 3];
+        int32_t ci = (int32_t)pts[5 * p + 4];
+        double acc = 0.0, sa = 0.0;
+        int64_t planes = N * D2;
+#pragma omp parallel for schedule(static) reduction(+ : acc, sa)
+        for (int64_t np = 0; np < planes; ++np) {
+            int64_t n = np / D2, pd = np % D2;
+            for (int64_t ph = 0; ph < H2; ++ph)
+                for (int64_t pw = 0; pw < W2; ++pw) {
+                    int64_t o = I5(n, pd, ph, pw, co, D2, H2, W2, Co);
+                    int code = idx[o];
+                    int64_t d = 2 * pd + ((code >> 2) & 1), h = 2 * ph + ((code >> 1) & 1), w = 2 * pw + (code & 1);
+                    int64_t id = d + kd - 1, ih = h + kh - 1, iw = w + kw - 1;
+                    if (id < 0 || id >= D || ih < 0 || ih >= H || iw < 0 || iw >= W) continue;
+                    double t = bf16_to_double(g[o]) * bf16_to_double(x[I5(n, id, ih, iw, ci, D, H, W, Ci)]);
+                    acc += t;
+                    sa += dabs(t);
+                }
+        }
+        out[p] = acc;
+        if (sabs) sabs[p] = sa;
+    }
+}

@@ -1,9 +1,13 @@
 """Parity at the full sizes of the benchmark configurations, in the launch
 configuration bench.py times (the CosmoStack sequence of C-ABI calls).
 
-The fp64 oracle evaluates sampled output elements one by one (its point
-routines), each on the GPU's own bf16 input of that layer, so every check
-isolates one kernel.  Tolerance as elsewhere: |err| <= 1e-2 * S per element
+The fp64 oracle evaluates output elements on the GPU's own bf16 input of
+that layer, so every check isolates one kernel: sampled activations and
+input gradients (its point routines), and every element of the weight
+gradients of the benchmark stack (its per-tap matrix-product form, and for
+the first block the routed sum over pooled voxels); the 512^3 pair and the
+sweep check at least one weight-gradient element in every (64 output
+channels x tap x 32 input channels) tile, 512 or more in all.  Tolerance as elsewhere: |err| <= 1e-2 * S per element
 (S = sum of |product| terms) and relative L2 <= 5e-3 over the sample; argmax
 codes bit-exact where the window's top-two gap exceeds the tolerance.
 
@@ -18,7 +22,7 @@ import numpy as np
 import pytest
 
 import synthdata
-from tests.gpu_util import assert_close, dev, dev_bf16, empty_bf16
+from tests.gpu_util import assert_close, dev, dev_bf16, empty_bf16, tile_cover_pts
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -106,15 +110,6 @@ def _check_forward(oracle_mod, st, inp, rng, k):
                            rng, k, f"block {l + 1} forward")
 
 
-def _routed_dz_channel(oracle_mod, g16, y16, idx, co):
-    """Dense dZ of channel co (bf16 bits, [n][d][h][w][1]) routed by the oracle
-    from the pooled gradient and the argmax codes."""
-    f = oracle_mod.bf16_bits_to_f64
-    gy = None if y16 is None else f(y16[..., co:co + 1])
-    dz, _, _ = oracle_mod.pool_bwd(f(g16[..., co:co + 1]), gy, np.ascontiguousarray(idx[..., co:co + 1]), SLOPE)
-    return synthdata.to_bf16_bits(dz)
-
-
 def _pool_bwd_checks(oracle_mod, g16, y16, idx, gdb, dz16, rng, what):
     """Bias gradient (oracle over slabs of the pooled tensor) and, when the
     dense dZ was written (dz16 not None), the routed dZ at sampled windows
@@ -146,7 +141,36 @@ def _pool_bwd_checks(oracle_mod, g16, y16, idx, gdb, dz16, rng, what):
         np.testing.assert_allclose(got, dzw[:, dd, dh, dw, 0], rtol=2 ** -8, atol=0, err_msg=f"dZ routing {what}")
 
 
-def _check_backward(oracle_mod, st, inp, dy, rng, k_dx, k_dw):
+def _check_dw_dense_full(oracle_mod, x16, dz16, gdw, what, slab=16):
+    """The whole weight gradient of one layer, from the GPU's own bf16 input and
+    dense dZ: the oracle's per-tap matrix-product form, sample by sample in
+    d-slabs (neighbouring planes passed in)."""
+    f = oracle_mod.bf16_bits_to_f64
+    N, D = x16.shape[:2]
+    ref = np.zeros(gdw.shape)
+    S = np.zeros(gdw.shape)
+    for n in range(N):
+        for d0 in range(0, D, slab):
+            d1 = min(D, d0 + slab)
+            xs, dzs = f(x16[n:n + 1, d0:d1]), f(dz16[n:n + 1, d0:d1])
+            below = f(x16[n:n + 1, d0 - 1]) if d0 > 0 else None
+            above = f(x16[n:n + 1, d1]) if d1 < D else None
+            ref += oracle_mod.conv3d_wgrad_mm(xs, dzs, below, above)
+            S += oracle_mod.conv3d_wgrad_mm(np.abs(xs), np.abs(dzs), None if below is None else np.abs(below),
+                                            None if above is None else np.abs(above))
+    assert_close(gdw, ref, S, what)
+
+
+def _all_filter_pts(c_out, c_in):
+    return np.array([(co, t // 9, (t // 3) % 3, t % 3, ci) for co in range(c_out) for t in range(27)
+                     for ci in range(c_in)], dtype=np.int64)
+
+
+def _check_backward(oracle_mod, st, inp, dy, rng, k_dx, dw_full=True):
+    """Every block: bias gradient (full), routed dZ at sampled windows, the
+    weight gradient (every element when dw_full, else at least one element per
+    split-K / accumulator tile and >= 512 in all), input gradient at k_dx
+    sampled elements."""
     L = st.L
     f = oracle_mod.bf16_bits_to_f64
     for l in range(L - 1, -1, -1):
@@ -157,23 +181,23 @@ def _check_backward(oracle_mod, st, inp, dy, rng, k_dx, k_dw):
         dz16 = None if st.routed(l) else u16(st.dz[l])
         _pool_bwd_checks(oracle_mod, g16, y16, idx, st.db[l].cpu().numpy().astype(np.float64), dz16, rng,
                          f"block {l + 1}")
-        # weight gradient at sampled filter taps (sum over every sample and voxel)
         x16 = u16(st.block_input(l))
-        pts = rand_pts(rng, st.dw[l].shape, k_dw)
-        got = st.dw[l].cpu().numpy()[tuple(pts.T)].astype(np.float64)
+        gdw = st.dw[l].cpu().numpy().astype(np.float64)
+        co, ci = gdw.shape[0], gdw.shape[4]
         if dz16 is None:
-            # routed weight gradient: the oracle routes dZ of each sampled channel
-            ref, S = np.zeros(len(pts)), np.zeros(len(pts))
-            for co in np.unique(pts[:, 0]):
-                sel = np.nonzero(pts[:, 0] == co)[0]
-                dzc = _routed_dz_channel(oracle_mod, g16, y16, idx, int(co))
-                p1 = pts[sel].copy()
-                p1[:, 0] = 0
-                ref[sel], S[sel] = oracle_mod.conv3d_wgrad_pts(x16, dzc, p1)
-            assert_close(got, ref, S, f"dW{l + 1} (routed)")
+            # routed weight gradient (the first block: g is already the pre-activation
+            # gradient): every filter element, summed over the pooled voxels
+            assert y16 is None
+            pts = _all_filter_pts(co, ci) if dw_full else tile_cover_pts(rng, co, ci)
+            ref, S = oracle_mod.conv3d_wgrad_routed_pts(x16, g16, idx, pts)
+            assert_close(gdw[tuple(pts.T)], ref, S, f"dW{l + 1} (routed, {len(pts)} elements)")
             continue
-        ref, S = oracle_mod.conv3d_wgrad_pts(x16, dz16, pts)
-        assert_close(got, ref, S, f"dW{l + 1}")
+        if dw_full:
+            _check_dw_dense_full(oracle_mod, x16, dz16, gdw, f"dW{l + 1} (all elements)")
+        else:
+            pts = tile_cover_pts(rng, co, ci)
+            ref, S = oracle_mod.conv3d_wgrad_pts(x16, dz16, pts)
+            assert_close(gdw[tuple(pts.T)], ref, S, f"dW{l + 1} ({len(pts)} tile-covering elements)")
         if l > 0:
             # input gradient times the previous block's leaky-ReLU derivative
             pts = rand_pts(rng, x16.shape, k_dx)
@@ -193,14 +217,14 @@ def test_stack_train_step_n8(cf, oracle_mod):
     st, inp, dy = _stack(cf, 8, 128, synthdata.STACK_CHANNELS, 20260003, backward=True)
     rng = np.random.default_rng(3)
     _check_forward(oracle_mod, st, inp, rng, 2048)
-    _check_backward(oracle_mod, st, inp, dy, rng, k_dx=2048, k_dw=24)
+    _check_backward(oracle_mod, st, inp, dy, rng, k_dx=2048, dw_full=True)
 
 
 def test_large_sample_pair_512(cf, oracle_mod):
     st, inp, dy = _stack(cf, 1, 512, (4, 32, 64), 20260004, backward=True)
     rng = np.random.default_rng(4)
     _check_forward(oracle_mod, st, inp, rng, 2048)
-    _check_backward(oracle_mod, st, inp, dy, rng, k_dx=1024, k_dw=8)
+    _check_backward(oracle_mod, st, inp, dy, rng, k_dx=1024, dw_full=False)
 
 
 @pytest.mark.parametrize("shape", list(synthdata.SWEEP_SHAPES))
@@ -226,8 +250,9 @@ def test_sweep_layer(cf, oracle_mod, shape):
     ws = torch.empty((max(cf.cf_workspace_size(cf.CF_OP_WGRAD, desc), 256),), dtype=torch.uint8, device="cuda")
     dw = torch.empty((co, 3, 3, 3, ci), dtype=torch.float32, device="cuda")
     cf.cf_conv3d_wgrad(desc, x, dz, None, dw, 0, ws, ws.numel())
-    pts = rand_pts(rng, dw.shape, 16)
+    pts = tile_cover_pts(rng, co, ci)
     ref, S = oracle_mod.conv3d_wgrad_pts(inp["x"], inp["dz"], pts)
-    assert_close(dw.cpu().numpy()[tuple(pts.T)].astype(np.float64), ref, S, f"sweep wgrad {shape}")
+    assert_close(dw.cpu().numpy()[tuple(pts.T)].astype(np.float64), ref, S,
+                 f"sweep wgrad {shape} ({len(pts)} tile-covering elements)")
     torch.cuda.synchronize()
     assert cf.cf_last_device_status() == cf.CF_OK

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import synthdata
-from tests.gpu_util import assert_close, dev, dev_bf16, empty_bf16, host_bf16_f64
+from tests.gpu_util import assert_close, dev, dev_bf16, empty_bf16, guarded, host_bf16_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -82,10 +82,12 @@ def test_pool_fwd_standalone(cf, oracle_mod):
     z16[0, 0:2, 0:2, 0:2, 3] = z16[0, 0, 0, 0, 3]
     z16[1, 2:4, 2:4, 4:6, 5] = synthdata.to_bf16_bits(np.array([1.5]))[0]
     b = rng.normal(0, 0.1, size=C).astype(np.float32)
-    y = empty_bf16((N, D // 2, H // 2, W // 2, C))
     import torch
-    idx = torch.empty(y.shape, dtype=torch.uint8, device="cuda")
+    y, ycheck = guarded((N, D // 2, H // 2, W // 2, C), torch.bfloat16)
+    idx, icheck = guarded(y.shape, torch.uint8)
     cf.cf_bias_lrelu_pool_fwd(N, D, H, W, C, dev_bf16(z16), dev(b), SLOPE, y, idx)
+    ycheck("y")
+    icheck("idx")
     ry, ridx = oracle_mod.pool_fwd(_f64(oracle_mod, z16), b.astype(np.float64), SLOPE)
     np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
     gy = host_bf16_f64(y)
@@ -101,11 +103,14 @@ def test_pool_bwd_standalone(cf, oracle_mod):
     ry, ridx = oracle_mod.pool_fwd(z, b, SLOPE)
     y16 = synthdata.to_bf16_bits(ry)
     dy16 = synthdata.to_bf16_bits(rng.normal(size=ry.shape))
-    dz = empty_bf16((N, D, H, W, C), fill=7.0)
-    dyp = empty_bf16(ry.shape)
-    db = torch.empty(C, dtype=torch.float32, device="cuda")
+    dz, dzcheck = guarded((N, D, H, W, C), torch.bfloat16, fill=7.0)
+    dyp, dypcheck = guarded(ry.shape, torch.bfloat16)
+    db, dbcheck = guarded((C,), torch.float32)
     ws, wsb = _ws(cf, cf.CF_OP_POOL_BWD, cf.cf_conv_desc(N, D, H, W, C, C))
     cf.cf_bias_lrelu_pool_bwd(N, D, H, W, C, dev_bf16(dy16), dev_bf16(y16), dev(ridx), SLOPE, dz, dyp, db, ws, wsb)
+    dzcheck("dz")
+    dypcheck("dy_pre")
+    dbcheck("db")
     rdz, rdyp, rdb = oracle_mod.pool_bwd(_f64(oracle_mod, dy16), _f64(oracle_mod, y16), ridx, SLOPE)
     gdz = host_bf16_f64(dz)
     # same nonzero pattern (zeros everywhere but the argmax), values = bf16(g)
@@ -143,8 +148,10 @@ def _case(shape, seed):
 def test_conv_fwd_plain(cf, oracle_mod, shape):
     N, D, H, W, Ci, Co = shape
     c = _case(shape, 100 + Ci + Co)
-    y = empty_bf16((N, D, H, W, Co), fill=float("nan"))
+    import torch
+    y, check = guarded((N, D, H, W, Co), torch.bfloat16, fill=float("nan"))
     cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), None, y)
+    check(f"fwd {shape}")
     x, w = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["w"])
     ref = oracle_mod.conv3d_fwd(x, w)
     S = oracle_mod.conv3d_fwd(np.abs(x), np.abs(w))
@@ -176,9 +183,11 @@ def test_conv_fwd_pooled(cf, oracle_mod, shape):
     import torch
     N, D, H, W, Ci, Co = shape
     c = _case(shape, 200 + Ci + Co)
-    y = empty_bf16((N, D // 2, H // 2, W // 2, Co), fill=float("nan"))
-    idx = torch.full(y.shape, 255, dtype=torch.uint8, device="cuda")
+    y, ycheck = guarded((N, D // 2, H // 2, W // 2, Co), torch.bfloat16, fill=float("nan"))
+    idx, icheck = guarded(y.shape, torch.uint8, fill=255)
     cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), (dev(c["b"]), SLOPE, idx), y)
+    ycheck(f"pooled y {shape}")
+    icheck(f"pooled idx {shape}")
     x, w = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["w"])
     _check_pooled(oracle_mod, x, w, c["b"].astype(np.float64), host_bf16_f64(y), idx.cpu().numpy(),
                   f"pooled {shape}")
@@ -211,15 +220,18 @@ def test_conv_fwd_smallc(cf, oracle_mod, shape, pooled):
     c = _case(shape, 300 + Ci + Co)
     x, w = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["w"])
     if not pooled:
-        y = empty_bf16((N, D, H, W, Co), fill=float("nan"))
+        y, check = guarded((N, D, H, W, Co), torch.bfloat16, fill=float("nan"))
         cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), None, y)
+        check(f"smallc fwd {shape}")
         ref = oracle_mod.conv3d_fwd(x, w)
         S = oracle_mod.conv3d_fwd(np.abs(x), np.abs(w))
         assert_close(host_bf16_f64(y), ref, S, f"smallc fwd {shape}")
     else:
-        y = empty_bf16((N, D // 2, H // 2, W // 2, Co), fill=float("nan"))
-        idx = torch.full(y.shape, 255, dtype=torch.uint8, device="cuda")
+        y, ycheck = guarded((N, D // 2, H // 2, W // 2, Co), torch.bfloat16, fill=float("nan"))
+        idx, icheck = guarded(y.shape, torch.uint8, fill=255)
         cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), (dev(c["b"]), SLOPE, idx), y)
+        ycheck(f"smallc pooled y {shape}")
+        icheck(f"smallc pooled idx {shape}")
         _check_pooled(oracle_mod, x, w, c["b"].astype(np.float64), host_bf16_f64(y), idx.cpu().numpy(),
                       f"smallc pooled {shape}")
 
@@ -243,10 +255,12 @@ def test_conv_dgrad(cf, oracle_mod, shape, with_act):
     desc = cf.cf_conv_desc(*shape)
     ws, wsb = _ws(cf, cf.CF_OP_DGRAD, desc)
     import torch
-    dx = empty_bf16((N, D, H, W, Ci), fill=float("nan"))
+    dx, dxcheck = guarded((N, D, H, W, Ci), torch.bfloat16, fill=float("nan"))
     x_act = dev_bf16(c["x"]) if with_act else None
-    dsum = torch.full((Ci,), float("nan"), dtype=torch.float32, device="cuda")
+    dsum, scheck = guarded((Ci,), torch.float32, fill=float("nan"))
     cf.cf_conv3d_dgrad(desc, dev_bf16(c["dz"]), None, dev_bf16(c["w"]), x_act, SLOPE, dx, ws, wsb, dsum=dsum)
+    dxcheck(f"dgrad dx {shape}")
+    scheck(f"dgrad dsum {shape}")
     # dsum: channel sums of the stored dx (fused in the epilogue for c_in <= 32)
     got_dx = host_bf16_f64(dx)
     ref_sum = got_dx.reshape(-1, Ci).sum(0)
@@ -259,6 +273,10 @@ def test_conv_dgrad(cf, oracle_mod, shape, with_act):
         f = np.where(_f64(oracle_mod, c["x"]) > 0, 1.0, SLOPE)
         ref, S = ref * f, S * f
     assert_close(host_bf16_f64(dx), ref, S, f"dgrad {shape} act={with_act}")
+    # dsum against the oracle: channel sums of the exact dx (each stored element
+    # is within 1e-2*S of it, so the sums are within 1e-2 * sum(S))
+    assert_close(dsum.cpu().numpy().astype(np.float64), ref.reshape(-1, Ci).sum(0), S.reshape(-1, Ci).sum(0),
+                 f"dgrad dsum vs oracle {shape}")
 
 
 # ----------------------------------------------------------------------------- backward weight
@@ -287,8 +305,9 @@ def test_conv_wgrad(cf, oracle_mod, shape):
     c = _case(shape, 500 + Ci + Co)
     desc = cf.cf_conv_desc(*shape)
     ws, wsb = _ws(cf, cf.CF_OP_WGRAD, desc)
-    dw = torch.full((Co, 3, 3, 3, Ci), float("nan"), dtype=torch.float32, device="cuda")
+    dw, check = guarded((Co, 3, 3, 3, Ci), torch.float32, fill=float("nan"))
     cf.cf_conv3d_wgrad(desc, dev_bf16(c["x"]), dev_bf16(c["dz"]), None, dw, 0, ws, wsb)
+    check(f"wgrad {shape}")
     x, dz = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["dz"])
     ref = oracle_mod.conv3d_wgrad(x, dz)
     S = oracle_mod.conv3d_wgrad(np.abs(x), np.abs(dz))
@@ -325,8 +344,9 @@ def test_routed_gradients_match_dense(cf, oracle_mod, shape):
     rdz, _, _ = oracle_mod.pool_bwd(_f64(oracle_mod, g16), None, ridx, SLOPE)
     # wgrad from (g, idx)
     ws, wsb = _ws(cf, cf.CF_OP_WGRAD_ROUTED, desc)
-    dw = torch.empty((Co, 3, 3, 3, Ci), dtype=torch.float32, device="cuda")
+    dw, check = guarded((Co, 3, 3, 3, Ci), torch.float32, fill=float("nan"))
     cf.cf_conv3d_wgrad(desc, dev_bf16(c["x"]), dev_bf16(g16), dev(ridx), dw, 0, ws, wsb)
+    check("routed wgrad")
     x = _f64(oracle_mod, c["x"])
     ref = oracle_mod.conv3d_wgrad(x, rdz)
     S = oracle_mod.conv3d_wgrad(np.abs(x), np.abs(rdz))
@@ -335,8 +355,9 @@ def test_routed_gradients_match_dense(cf, oracle_mod, shape):
     assert_close(dw.cpu().numpy().astype(np.float64), 2 * ref, 2 * S, "routed wgrad acc")
     if Ci % 16 == 0 and Co % 32 == 0:
         ws, wsb = _ws(cf, cf.CF_OP_DGRAD_ROUTED, desc)
-        dx = empty_bf16((N, D, H, W, Ci))
+        dx, check = guarded((N, D, H, W, Ci), torch.bfloat16, fill=float("nan"))
         cf.cf_conv3d_dgrad(desc, dev_bf16(g16), dev(ridx), dev_bf16(c["w"]), None, SLOPE, dx, ws, wsb)
+        check("routed dgrad")
         w = _f64(oracle_mod, c["w"])
         ref = oracle_mod.conv3d_dgrad(rdz, w)
         S = oracle_mod.conv3d_dgrad(np.abs(rdz), np.abs(w))

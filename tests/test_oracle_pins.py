@@ -307,3 +307,164 @@ def test_flop_convention_reproduces_table1(row):
     assert abs(f - fwd) <= 0.5 * 10 ** (np.floor(np.log10(fwd)) - 3) + 1e-9, (f, fwd)
     assert abs(3 * f - ops) <= 0.5 * 10 ** (np.floor(np.log10(ops)) - 3) + 1e-9, (3 * f, ops)
     assert round(flops.p3_table1_params() / 1e6, 2) == params
+
+
+def _window_view(a):
+    """[N,D,H,W,C] -> [N,D/2,H/2,W/2,C,8], window members in (dd,dh,dw) order."""
+    N, D, H, W, C = a.shape
+    return a.reshape(N, D // 2, 2, H // 2, 2, W // 2, 2, C).transpose(0, 1, 3, 5, 7, 2, 4, 6).reshape(
+        N, D // 2, H // 2, W // 2, C, 8)
+
+
+def test_stack_chain_finite_differences(oracle_mod):
+    """Two chained blocks through oracle.stack_fwd / stack_bwd (exact mode):
+    the weight and bias gradients of both blocks against central differences
+    of L = <g, y_top>.  This pins the chaining itself -- the top block's
+    gradient through its stored output, the lower block's leaky-ReLU
+    derivative taken from its pooled output (the next block's input) -- and
+    not only one block."""
+    slope = 0.3
+    rng = np.random.default_rng(21)
+    ch = (2, 3, 2)
+    for _ in range(500):
+        x = rng.normal(size=(1, 4, 4, 4, ch[0]))
+        ws = [rng.normal(size=(ch[l + 1], 3, 3, 3, ch[l])) for l in range(2)]
+        # biases that put about half of each block's pooled pre-activations below
+        # zero, so that both branches of the leaky-ReLU derivative are exercised
+        bs = []
+        cur = x
+        for l in range(2):
+            m = _window_view(oracle_mod.conv3d_fwd(cur, ws[l])).max(axis=-1)
+            bs.append(-np.median(m.reshape(-1, ch[l + 1]), axis=0) + rng.choice([-0.5, 0.5], ch[l + 1]))
+            cur = oracle_mod.pool_fwd(oracle_mod.conv3d_fwd(cur, ws[l]), bs[l], slope)[0]
+        xs, zs, ys, idxs = oracle_mod.stack_fwd(x, ws, bs, slope, mirrored=False)
+        ok = True
+        for l in range(2):
+            srt = np.sort(_window_view(zs[l]), axis=-1)
+            pre = srt[..., -1] + bs[l]
+            ok &= np.min(srt[..., -1] - srt[..., -2]) > 1e-3 and np.min(np.abs(pre)) > 1e-3
+            ok &= np.any(pre < 0) and np.any(pre > 0)
+        if ok:
+            break
+    else:
+        pytest.fail("could not draw a kink-free case")
+    g = rng.normal(size=ys[-1].shape)
+    dws, dbs, _, dxs = oracle_mod.stack_bwd(xs, ys, idxs, ws, g, slope, mirrored=False)
+    assert dxs[0] is None and dxs[1].shape == ys[0].shape
+
+    def loss(ws_, bs_):
+        return np.vdot(g, oracle_mod.stack_fwd(x, ws_, bs_, slope, mirrored=False)[2][-1])
+
+    h = 1e-6
+    for l in range(2):
+        for _ in range(5):
+            pos = tuple(rng.integers(0, s) for s in ws[l].shape)
+            wp = [w.copy() for w in ws]
+            wm = [w.copy() for w in ws]
+            wp[l][pos] += h
+            wm[l][pos] -= h
+            num = (loss(wp, bs) - loss(wm, bs)) / (2 * h)
+            assert abs(num - dws[l][pos]) <= 1e-5 * max(1.0, abs(num)), (l, pos, num, dws[l][pos])
+        for c in range(ch[l + 1]):
+            bp = [b.copy() for b in bs]
+            bm = [b.copy() for b in bs]
+            bp[l][c] += h
+            bm[l][c] -= h
+            num = (loss(ws, bp) - loss(ws, bm)) / (2 * h)
+            assert abs(num - dbs[l][c]) <= 1e-5 * max(1.0, abs(num)), (l, c, num, dbs[l][c])
+    # the gradient at the lower block's pooled pre-activation, g1 = dL/d(m1 + b1):
+    # shifting b1 by h moves every m1 + b1 of that channel, so its channel sums
+    # are db1, already checked above; check them against dxs[1] directly
+    np.testing.assert_allclose(dxs[1].reshape(-1, ch[1]).sum(0), dbs[0], rtol=1e-12, atol=1e-12)
+
+
+def test_stack_mirrored_rounds_at_block_boundaries(oracle_mod):
+    """Mirrored mode stores each block output as bf16 (exactly representable)
+    and stays within bf16 rounding of the exact chain."""
+    rng = np.random.default_rng(22)
+    x = oracle_mod.round_to_bf16(rng.normal(size=(1, 8, 8, 8, 4)))
+    ws = [oracle_mod.round_to_bf16(rng.normal(0, 0.2, size=(8, 3, 3, 3, 4))),
+          oracle_mod.round_to_bf16(rng.normal(0, 0.1, size=(8, 3, 3, 3, 8)))]
+    bs = [np.zeros(8), np.zeros(8)]
+    xs, _, ys, _ = oracle_mod.stack_fwd(x, ws, bs, 0.3, mirrored=True)
+    _, _, ye, _ = oracle_mod.stack_fwd(x, ws, bs, 0.3, mirrored=False)
+    for l in range(2):
+        np.testing.assert_array_equal(oracle_mod.round_to_bf16(ys[l]), ys[l])
+    np.testing.assert_array_equal(xs[1], ys[0])
+    assert np.linalg.norm(ys[-1] - ye[-1]) <= 2e-2 * np.linalg.norm(ye[-1])
+
+
+def test_point_routine_scales_and_gaps(oracle_mod):
+    """S (sum of |products|) and the top-two gap returned by the point
+    routines, against the full routines on |x|, |w|, |dz| and a numpy sort of
+    each window's eight values.  These two numbers set the tolerance and the
+    no-tie selection of every full-size GPU check."""
+    c = synthdata.random_case(12, 2, 4, 6, 8, 16, 8)
+    f = oracle_mod.bf16_bits_to_f64
+    x, w, dz = f(c["x"]), f(c["w"]), f(c["dz"])
+    rng = np.random.default_rng(4)
+    Sf = oracle_mod.conv3d_fwd(np.abs(x), np.abs(w))
+    pts = np.stack([rng.integers(0, s, 60) for s in Sf.shape], 1)
+    _, s = oracle_mod.conv3d_fwd_pts(c["x"], c["w"], pts)
+    np.testing.assert_allclose(s, Sf[tuple(pts.T)], rtol=1e-13)
+    Sd = oracle_mod.conv3d_dgrad(np.abs(dz), np.abs(w))
+    pts = np.stack([rng.integers(0, s, 60) for s in Sd.shape], 1)
+    _, s = oracle_mod.conv3d_dgrad_pts(c["dz"], c["w"], pts)
+    np.testing.assert_allclose(s, Sd[tuple(pts.T)], rtol=1e-13)
+    Sw = oracle_mod.conv3d_wgrad(np.abs(x), np.abs(dz))
+    pts = np.stack([rng.integers(0, s, 60) for s in Sw.shape], 1)
+    _, s = oracle_mod.conv3d_wgrad_pts(c["x"], c["dz"], pts)
+    np.testing.assert_allclose(s, Sw[tuple(pts.T)], rtol=1e-12)
+    # fused block: S at the argmax voxel plus |b|, gap = largest - second largest
+    z = oracle_mod.conv3d_fwd(x, w)
+    b = c["b"].astype(np.float64)
+    zw, sw = _window_view(z), _window_view(Sf)
+    pts = np.stack([rng.integers(0, s, 60) for s in zw.shape[:5]], 1)
+    _, iv, sv, gap = oracle_mod.block_fwd_pts(c["x"], c["w"], c["b"], 0.3, pts)
+    win = zw[tuple(pts.T)]
+    srt = np.sort(win, axis=-1)
+    np.testing.assert_allclose(gap, srt[:, -1] - srt[:, -2], rtol=1e-12, atol=1e-14)
+    s_at = sw[tuple(pts.T)][np.arange(len(pts)), iv.astype(np.int64)] + np.abs(b[pts[:, 4]])
+    np.testing.assert_allclose(sv, s_at, rtol=1e-13)
+    # an all-zero input: every window is a tie, gap 0 and code 0 (first maximum)
+    x0 = np.zeros_like(c["x"])
+    _, iv, sv, gap = oracle_mod.block_fwd_pts(x0, c["w"], c["b"], 0.3, pts)
+    assert np.all(gap == 0) and np.all(iv == 0)
+    np.testing.assert_array_equal(sv, np.abs(b[pts[:, 4]]))
+
+
+def test_wgrad_matmul_form_and_slabs(oracle_mod):
+    """The per-tap matrix-product form of the weight gradient equals the direct
+    loops, and summing it over d-slabs (with the neighbouring planes passed in)
+    equals the whole volume."""
+    rng = np.random.default_rng(31)
+    x = rng.normal(size=(2, 6, 5, 4, 3))
+    dz = rng.normal(size=(2, 6, 5, 4, 5))
+    ref = oracle_mod.conv3d_wgrad(x, dz)
+    np.testing.assert_allclose(oracle_mod.conv3d_wgrad_mm(x, dz), ref, rtol=1e-12, atol=1e-12)
+    acc = np.zeros_like(ref)
+    for d0, d1 in ((0, 2), (2, 5), (5, 6)):
+        below = x[:, d0 - 1] if d0 > 0 else None
+        above = x[:, d1] if d1 < 6 else None
+        acc += oracle_mod.conv3d_wgrad_mm(x[:, d0:d1], dz[:, d0:d1], below, above)
+    np.testing.assert_allclose(acc, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_routed_wgrad_points_match_dense(oracle_mod):
+    """Weight gradient from the pooled gradient + argmax codes (summed over
+    pooled voxels) equals the weight gradient of the dense routed dZ."""
+    rng = np.random.default_rng(32)
+    N, D, H, W, Ci, Co = 2, 4, 6, 8, 4, 5
+    z = rng.normal(size=(N, D, H, W, Co))
+    _, idx = oracle_mod.pool_fwd(z, None, 0.3)
+    g16 = synthdata.to_bf16_bits(rng.normal(size=idx.shape))
+    x16 = synthdata.to_bf16_bits(rng.normal(size=(N, D, H, W, Ci)))
+    f = oracle_mod.bf16_bits_to_f64
+    dz, _, _ = oracle_mod.pool_bwd(f(g16), None, idx, 0.3)
+    ref = oracle_mod.conv3d_wgrad(f(x16), dz)
+    S = oracle_mod.conv3d_wgrad(np.abs(f(x16)), np.abs(dz))
+    pts = np.array([[co, kd, kh, kw, ci] for co in range(Co) for kd in range(3) for kh in range(3)
+                    for kw in range(3) for ci in range(Ci)])
+    v, s = oracle_mod.conv3d_wgrad_routed_pts(x16, g16, idx, pts)
+    np.testing.assert_allclose(v, ref[tuple(pts.T)], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s, S[tuple(pts.T)], rtol=1e-12, atol=1e-12)
