@@ -56,3 +56,24 @@ def p3_table1_params() -> int:
     conv = sum(ch[l] * ch[l + 1] * 27 for l in range(7))
     fc = 2048 * 2048 + 2048 * 256 + 256 * 4
     return conv + fc
+
+
+def op_min_bytes(kind: str, n: int, spatial: int, c_in: int, c_out: int, routed: bool = False) -> int:
+    """Minimum HBM bytes of one conv op of the pooled stack (every input read
+    once, every output written once, bf16 activations, uint8 argmax codes,
+    fp32 weight gradients), for the roofline of the op:
+      fwd   : x, w, pooled y, codes, bias
+      wgrad : x, dense dZ (or, routed, the pooled gradient and the codes), dW
+      dgrad : dense dZ, w, the block input (leaky-ReLU derivative), dX
+    """
+    v = n * spatial ** 3
+    p = v // 8
+    w = c_out * 27 * c_in * 2
+    if kind == "fwd":
+        return v * c_in * 2 + w + p * c_out * 3 + c_out * 4
+    if kind == "wgrad":
+        dz = p * c_out * 3 if routed else v * c_out * 2
+        return v * c_in * 2 + dz + c_out * 27 * c_in * 4
+    if kind == "dgrad":
+        return v * c_out * 2 + w + 2 * v * c_in * 2
+    raise ValueError(kind)

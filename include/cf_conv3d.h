@@ -162,11 +162,16 @@ cf_status cf_bias_lrelu_pool_bwd(int64_t n, int64_t d, int64_t h, int64_t w, int
  *   Arguments, layouts and results: as cf_bias_lrelu_pool_bwd.
  *   Scratch: the bias-gradient partial sums live in a 1 MiB array inside the
  *   library (one per device, held until the process exits).  It holds
- *   4 * SM-count * c floats, so c <= 65536 / SM-count (442 on a 148-SM GPU)
- *   when dbias is requested; larger c returns CF_ERR_WORKSPACE before
- *   anything is launched.
+ *   4 * SM-count * c floats, so when dbias is requested c may be at most the
+ *   largest multiple of 8 not above 65536 / SM-count (424 on a 152-SM GB300,
+ *   440 on a 148-SM GPU); a larger c returns CF_ERR_WORKSPACE before anything
+ *   is launched.
  *   The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ *   device current; make that first call before any stream capture.  The
+ *   address is kept for the life of the process (as is the device status
+ *   word's, for every entry point): after a cudaDeviceReset the kept
+ *   addresses are stale, so the library must not be used across a device
+ *   reset.
  *   Every call shares the array (it keeps the last call's contents; this
  *   operation overwrites every partial it reads, so nothing needs clearing):
  *   calls whose work overlaps on the GPU race on it.
