@@ -173,7 +173,7 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
     }
     const int ci = desc->c_in, co = desc->c_out;
     const bool small = ci == 1 || ci == 4;
-    if (!small && ci % 32 != 0) return CF_ERR_UNSUPPORTED;
+    if (!small && ci % 16 != 0) return CF_ERR_UNSUPPORTED;
     LaunchCtx ctx;
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
     const int mode = epi ? EPI_POOL : EPI_PLAIN;
@@ -195,7 +195,7 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
         (idx && !aligned16(idx)) || (ws && !aligned16(ws)) || (dsum && !aligned16(dsum)))
         return CF_ERR_INVALID_ARG;
     const int ci = desc->c_in, co = desc->c_out;
-    if (co % 32 != 0 || ci % 16 != 0) return CF_ERR_UNSUPPORTED;
+    if (co % 16 != 0 || ci % 16 != 0) return CF_ERR_UNSUPPORTED;
     if (idx && ((desc->d | desc->h | desc->w) & 1)) return CF_ERR_UNSUPPORTED;
     LaunchCtx ctx;
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;

@@ -9,7 +9,7 @@
 //   B[co,(t,ci)] = W[co][t][ci] (the filter is already K-major).
 //
 // Kernel structure (one persistent CTA per SM, 6 warps):
-//   warp 0      : TMA producer.  For each tap and 32/64-channel chunk it loads
+//   warp 0      : TMA producer.  For each tap and 16/32/64-channel chunk it loads
 //                 the shifted activation box (the A tile, 128 rows) and the
 //                 matching filter slab (B tile) into a multi-stage ring.
 //   warp 1      : TMEM allocator and single-thread tcgen05.mma issuer, M=128,
@@ -30,7 +30,8 @@
 namespace cf {
 
 // ---------------------------------------------------------------------------
-// generic kernel: c_in a multiple of KC (32 or 64)
+// generic kernel: c_in a multiple of KC (16, 32 or 64 channels per K chunk;
+// the A and B rows are KC * 2 bytes, swizzled 32, 64 or 128 bytes)
 
 template <int BN, int KC, int EPI>
 struct IgemmCfg {
@@ -42,10 +43,11 @@ struct IgemmCfg {
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - STG_BYTES - BAR_BYTES;
     static constexpr int STAGES_RAW = (int)(BUDGET / STAGE_BYTES);
-    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int STAGE_CAP = KC == 16 ? 16 : 8;  // K steps in flight: 16-channel stages are small
+    static constexpr int STAGES = STAGES_RAW > STAGE_CAP ? STAGE_CAP : STAGES_RAW;
     static constexpr uint32_t SMEM = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES;
     static constexpr uint32_t ROW_BYTES = KC * 2;
-    static constexpr uint32_t SWZ = KC == 64 ? SWZ_128B : SWZ_64B;
+    static constexpr uint32_t SWZ = KC == 64 ? SWZ_128B : (KC == 32 ? SWZ_64B : SWZ_32B);
     static constexpr uint32_t SBO = 8 * ROW_BYTES;
     static constexpr uint32_t TMEM_COLS = (2 * BN) <= 32 ? 32 : (2 * BN) <= 64 ? 64 : (2 * BN) <= 128 ? 128
                                                                                  : (2 * BN) <= 256 ? 256 : 512;
@@ -251,7 +253,9 @@ static cf_status run_igemm(const LaunchCtx& ctx, const ConvGeom& g, const uint16
     const uint64_t sa[4] = {(uint64_t)g.Cin * 2, (uint64_t)g.W * g.Cin * 2, (uint64_t)g.H * g.W * g.Cin * 2,
                             (uint64_t)g.D * g.H * g.W * g.Cin * 2};
     const uint32_t ba[5] = {(uint32_t)KC, (uint32_t)g.tw, (uint32_t)g.th, (uint32_t)g.td, 1u};
-    const CUtensorMapSwizzle swz = KC == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle swz = KC == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : KC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
     if (!encode_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, da, sa, ba, swz)) return CF_ERR_CUDA;
     const uint64_t db[2] = {(uint64_t)27 * g.Cin, (uint64_t)g.Cout};
     const uint64_t sb[1] = {(uint64_t)27 * g.Cin * 2};
@@ -286,7 +290,7 @@ static cf_status dispatch_epi(const LaunchCtx& ctx, const ConvGeom& g, const uin
 cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                             const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
                             const float* bias, const uint16_t* x_act, float slope) {
-    if (c_in % 32 != 0 || c_out % 16 != 0) return CF_ERR_UNSUPPORTED;
+    if (c_in % 16 != 0 || c_out % 16 != 0) return CF_ERR_UNSUPPORTED;
     int bn = c_out <= 256 ? c_out : 256;
     if (c_out > 256 && c_out % 256 != 0) return CF_ERR_UNSUPPORTED;
     // Small grids: narrower N tiles when that clearly shortens the critical
@@ -305,13 +309,14 @@ cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
             if (c_out % b == 0 && 5 * cost(b) < 4 * cost(best)) best = b;
         bn = best;
     }
-    const int kc = (c_in % 64 == 0) ? 64 : 32;
+    const int kc = (c_in % 64 == 0) ? 64 : (c_in % 32 == 0 ? 32 : 16);
     EpiArgs ea{y, idx, bias, x_act, slope};
     ConvGeom g = make_geom(n, d, h, w, c_in, c_out, bn);
 #define CF_BN_CASE(B)                                                                       \
     case B:                                                                                 \
-        return kc == 64 ? dispatch_epi<B, 64>(ctx, g, x, wk, epi, ea)                       \
-                        : dispatch_epi<B, 32>(ctx, g, x, wk, epi, ea);
+        return kc == 64   ? dispatch_epi<B, 64>(ctx, g, x, wk, epi, ea)                     \
+               : kc == 32 ? dispatch_epi<B, 32>(ctx, g, x, wk, epi, ea)                     \
+                          : dispatch_epi<B, 16>(ctx, g, x, wk, epi, ea);
     switch (bn) {
         CF_BN_CASE(16)
         CF_BN_CASE(32)

@@ -4,7 +4,7 @@
 //
 // Output tile: 2 planes x 16 lines x 8 voxels (256 voxels) of sample n,
 // computed as two M=128 accumulators (plane 0, plane 1); accumulator row
-// r = 8*j + l is line j, voxel l.  For each chunk of KC input channels the
+// r = 8*j + l is line j, voxel l.  For each chunk of KC (16 or 32) input channels the
 // producer loads the halo box (KC, 10, 18, 4) -- voxels w0-1..w0+8, lines
 // h0-1..h0+16, planes d0-1..d0+2, zero outside the volume -- into shared
 // memory with TMA (row R = (dd*18 + hh)*10 + ww, KC*2 bytes per row, swizzled).
@@ -29,7 +29,7 @@ namespace cf {
 template <int BN, int KC, int EPI, bool RES>
 struct HaloCfg {
     static constexpr uint32_t ROW = KC * 2;
-    static constexpr uint32_t HALO_BYTES = H_ROWS * ROW;  // 46080 or 92160
+    static constexpr uint32_t HALO_BYTES = H_ROWS * ROW;  // 23040, 46080 or 92160
     static constexpr uint32_t HALO_STRIDE = (HALO_BYTES + 1023) / 1024 * 1024;
     static constexpr uint32_t W_BYTES = BN * KC * 2;      // one tap's filter slab
     static constexpr int TPS = 3;                         // taps per streamed filter stage
@@ -38,7 +38,7 @@ struct HaloCfg {
     static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - BAR_BYTES - HS * HALO_STRIDE;
     static constexpr int WS_RAW = (int)(BUDGET / (TPS * W_BYTES));
     static constexpr int WS = WS_RAW > 12 ? 12 : WS_RAW;
-    static constexpr uint32_t SWZ = KC == 64 ? SWZ_128B : SWZ_64B;
+    static constexpr uint32_t SWZ = KC == 64 ? SWZ_128B : (KC == 32 ? SWZ_64B : SWZ_32B);
     static constexpr uint32_t SBO_A = HH_W * ROW;  // one halo line
     static constexpr uint32_t SBO_B = 8 * ROW;
     static constexpr uint32_t TMEM_COLS = 4 * BN <= 128 ? 128 : (4 * BN <= 256 ? 256 : 512);
@@ -301,7 +301,9 @@ static cf_status run_halo(const LaunchCtx& ctx, HaloParams p, const uint16_t* x,
     const uint64_t sx[4] = {(uint64_t)p.Cin * 2, (uint64_t)p.W * p.Cin * 2, (uint64_t)p.H * p.W * p.Cin * 2,
                             (uint64_t)p.D * p.H * p.W * p.Cin * 2};
     const uint32_t bx[5] = {(uint32_t)KC, (uint32_t)HH_W, (uint32_t)HH_H, (uint32_t)HH_D, 1u};
-    const CUtensorMapSwizzle swz = KC == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle swz = KC == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : KC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
     if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, dx, sx, bx, swz)) return CF_ERR_CUDA;
     const uint64_t dw[2] = {(uint64_t)27 * p.Cin, (uint64_t)p.Cout};
     const uint64_t sw[1] = {(uint64_t)27 * p.Cin * 2};
@@ -330,9 +332,11 @@ static cf_status halo_epi(const LaunchCtx& ctx, const HaloParams& p, const uint1
 
 // The halo tile pays off wherever the per-tap A re-fetch of the per-tap
 // kernel would load L2 (it reads each input row once per tap); c_out up to
-// 128 fits two double-buffered accumulator pairs in tensor memory.
+// 128 fits two double-buffered accumulator pairs in tensor memory.  Input
+// channels go in chunks of 32 (64-byte rows), or of 16 (32-byte rows) when
+// c_in is an odd multiple of 16.
 bool halo_path_supported(int c_in, int c_out) {
-    return (c_in % 32 == 0) && (c_out == 32 || c_out == 64 || c_out == 128);
+    return (c_in % 16 == 0) && (c_out == 32 || c_out == 64 || c_out == 128);
 }
 
 cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
@@ -358,8 +362,17 @@ cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
     p.status = ctx.status;
     p.wait_ns = ctx.wait_ns;
     // The whole filter stays in shared memory when it fits beside two halo
-    // stages of 32-channel chunks; otherwise it streams 3 taps per stage.
-    const bool resident = (size_t)27 * c_in * c_out * 2 + 2 * 46080 + 4096 <= (size_t)227 * 1024;
+    // stages; otherwise it streams 3 taps per stage.
+    const int kc = c_in % 32 == 0 ? 32 : 16;
+    const bool resident = (size_t)27 * c_in * c_out * 2 + 2 * (size_t)H_ROWS * kc * 2 + 4096 <= (size_t)227 * 1024;
+    if (kc == 16) {
+        switch (c_out) {
+            case 32: return resident ? halo_epi<32, 16, true>(ctx, p, x, wk, epi) : halo_epi<32, 16, false>(ctx, p, x, wk, epi);
+            case 64: return resident ? halo_epi<64, 16, true>(ctx, p, x, wk, epi) : halo_epi<64, 16, false>(ctx, p, x, wk, epi);
+            case 128: return halo_epi<128, 16, false>(ctx, p, x, wk, epi);
+        }
+        return CF_ERR_UNSUPPORTED;
+    }
     switch (c_out) {
         case 32: return resident ? halo_epi<32, 32, true>(ctx, p, x, wk, epi) : halo_epi<32, 32, false>(ctx, p, x, wk, epi);
         case 64: return resident ? halo_epi<64, 32, true>(ctx, p, x, wk, epi) : halo_epi<64, 32, false>(ctx, p, x, wk, epi);

@@ -4,14 +4,17 @@
 // (CosmoFlow page, section III-C "backward weights": the weight-gradient work
 // is divided over voxels.)
 //   dW[co, t, ci] = sum_{n,v} dZ[n,v,co] * X[n, v + t - 1, ci]
-// GEMM view: M = (t, ci) rows (128 per CTA tile), N = co (the whole c_out,
-// <= 256), K = voxels.  Both operands are MN-major in shared memory:
+// GEMM view: M = (t, ci) rows (128 per CTA tile), N = co (tiles of BN <= 256
+// channels), K = voxels.  Both operands are MN-major in shared memory:
 //   A[(t,ci), v] = X[v + t - 1, ci]  -- TMA box of the tap-shifted activation
-//                  (zero fill outside the volume), channel rows of 32 or 64
-//   B[co, v]     = dZ[v, co]         -- TMA box of the output gradient
-// Each CTA unit = one M block x one contiguous range of 64-voxel boxes; its
-// fp32 accumulator (TMEM) is written to a partial buffer [split][co][27*c_in],
-// and a second kernel sums the splits in a fixed order into dW.
+//                  (zero fill outside the volume), channel rows of 16, 32 or 64
+//   B[co, v]     = dZ[v, co]         -- TMA box of the output gradient; channels
+//                  at and beyond c_out read as zero (out-of-bounds fill), so an
+//                  N tile may be wider than what is left of c_out
+// Each CTA unit = one M block x one N tile x one contiguous range of 64-voxel
+// boxes; its fp32 accumulator (TMEM) is written to a partial buffer
+// [split][co][27*c_in], and a second kernel sums the splits in a fixed order
+// into dW.
 //
 // The small-channel variant (c_in = 1 or 4, conv_wgrad_smallc.cu) builds the
 // A tile with builder warps (im2col rows = voxels, 27*c_in columns padded to
@@ -24,7 +27,7 @@
 namespace cf {
 
 // ---------------------------------------------------------------------------
-// generic: c_in a multiple of 32
+// generic: c_in a multiple of 16
 
 template <int BN, int SUBA, int SUBB>
 struct WgCfg {
@@ -106,7 +109,8 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0, issued = 0, par = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x) {
-                const int mb = u % g.n_mblocks, split = u / g.n_mblocks;
+                const int mb = u % g.n_mblocks, rest = u / g.n_mblocks;
+                const int co0 = (rest % g.n_ntiles) * BN, split = rest / g.n_ntiles;
                 const int64_t b0 = (int64_t)split * g.boxes_per_split;
                 const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
                 // A sub-blocks of this M block that hold real rows, and their taps
@@ -141,7 +145,8 @@ __global__ void __launch_bounds__(192, 1)
                                         d0 + sdd[s], n);
 #pragma unroll
                     for (int s = 0; s < BN / SUBB; ++s)
-                        tma_load_5d(sa + C::A_BYTES + s * C::B_SUB_BYTES, &tmG, &full[stage], s * SUBB, w0, h0, d0, n);
+                        tma_load_5d(sa + C::A_BYTES + s * C::B_SUB_BYTES, &tmG, &full[stage], co0 + s * SUBB, w0, h0,
+                                    d0, n);
                     issued |= 1u << stage;
                     par = (par & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -161,7 +166,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0, local = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x, ++local) {
-                const int split = u / g.n_mblocks;
+                const int split = u / g.n_mblocks / g.n_ntiles;
                 const int64_t b0 = (int64_t)split * g.boxes_per_split;
                 const int64_t b1 = b0 + g.boxes_per_split < g.total_boxes ? b0 + g.boxes_per_split : g.total_boxes;
                 if (!mbar_wait(tempty, (local & 1) ^ 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_TMEM_EMPTY)) {
@@ -205,10 +210,11 @@ __global__ void __launch_bounds__(192, 1)
         const int et = threadIdx.x - 64;
         uint32_t local = 0;
         for (int u = blockIdx.x; u < g.num_units; u += gridDim.x, ++local) {
-            const int mb = u % g.n_mblocks, split = u / g.n_mblocks;
+            const int mb = u % g.n_mblocks, rest = u / g.n_mblocks;
+            const int co0 = (rest % g.n_ntiles) * BN, split = rest / g.n_ntiles;
             if (!epi_wait(tfull, local & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
             tc_fence_after();
-            wgrad_store_partial<BN>(g, p.part, mb, split, tmem_base, q, lane);
+            wgrad_store_partial<BN>(g, p.part, mb, split, co0, tmem_base, q, lane);
             tc_fence_before();
             mbar_arrive(tempty);
         }
@@ -261,6 +267,20 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 // ---------------------------------------------------------------------------
 // host side
 
+// N tile of the weight-gradient GEMM for c_out (a multiple of 16): the smallest
+// of the compiled widths that holds it, 256-wide tiles above that (c_in 1 or 4:
+// at most 256 channels, one tile).
+static int wgrad_tile_n(int c_in, int c_out) {
+    const bool small = c_in == 1 || c_in == 4;
+    static const int generic[] = {16, 32, 48, 64, 96, 128, 192, 256};
+    static const int smallc[] = {16, 32, 64, 128, 192, 256};
+    const int* t = small ? smallc : generic;
+    const int nt = small ? 6 : 8;
+    for (int i = 0; i < nt; ++i)
+        if (c_out <= t[i]) return t[i];
+    return 256;
+}
+
 static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out) {
     WgradGeom g;
     g.N = (int)n;
@@ -270,6 +290,8 @@ static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_
     g.Cin = c_in;
     g.Cout = c_out;
     const bool small = c_in == 1 || c_in == 4;
+    g.bn = wgrad_tile_n(c_in, c_out);
+    g.n_ntiles = (c_out + g.bn - 1) / g.bn;
     if (small) {
         g.vw = 16;  // the small-channel kernel's box: 2 planes x 4 lines x 16 voxels
         g.vh = 4;
@@ -286,11 +308,12 @@ static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_
     g.nb_d = (int)((d + g.vd - 1) / g.vd);
     g.total_boxes = n * g.nb_d * g.nb_h * g.nb_w;
     // about two units per SM, each unit at least 8 boxes long
-    int64_t target = std::max<int64_t>(1, (2 * (int64_t)num_sms + g.n_mblocks - 1) / g.n_mblocks);
+    const int tiles = g.n_mblocks * g.n_ntiles;
+    int64_t target = std::max<int64_t>(1, (2 * (int64_t)num_sms + tiles - 1) / tiles);
     target = std::min<int64_t>(target, std::max<int64_t>(1, g.total_boxes / 8));
     g.boxes_per_split = (g.total_boxes + target - 1) / target;
     g.n_splits = (int)((g.total_boxes + g.boxes_per_split - 1) / g.boxes_per_split);
-    g.num_units = g.n_mblocks * g.n_splits;
+    g.num_units = tiles * g.n_splits;
     return g;
 }
 
@@ -342,9 +365,11 @@ static cf_status run_wgrad(const LaunchCtx& ctx, const WgradGeom& g, const uint1
 template <int BN>
 static cf_status wgrad_bn(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
                           float* part) {
-    constexpr int SUBB = BN >= 64 ? 64 : BN;
+    // dZ sub-blocks: the widest of 64 / 32 / 16 channels that divides the tile
+    constexpr int SUBB = BN % 64 == 0 ? 64 : (BN % 32 == 0 ? 32 : 16);
     if (g.Cin % 64 == 0) return run_wgrad<BN, 64, SUBB>(ctx, g, x, dz, part);
-    return run_wgrad<BN, 32, SUBB>(ctx, g, x, dz, part);
+    if (g.Cin % 32 == 0) return run_wgrad<BN, 32, SUBB>(ctx, g, x, dz, part);
+    return run_wgrad<BN, 16, SUBB>(ctx, g, x, dz, part);
 }
 
 static cf_status launch_splitk_reduce(const LaunchCtx& ctx, const float* part, float* dw, int64_t count, int splits,
@@ -364,9 +389,10 @@ static cf_status launch_splitk_reduce(const LaunchCtx& ctx, const float* part, f
 cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                        const uint16_t* x, const uint16_t* dz, const uint8_t* idx, float* dw, int accumulate, void* ws,
                        size_t ws_bytes) {
-    if (!(c_in == 1 || c_in == 4 || c_in % 32 == 0)) return CF_ERR_UNSUPPORTED;
+    if (!(c_in == 1 || c_in == 4 || c_in % 16 == 0)) return CF_ERR_UNSUPPORTED;
     if (idx && !wgrad_routed_fused(c_in)) return CF_ERR_UNSUPPORTED;
-    if (!(c_out == 16 || c_out == 32 || c_out % 64 == 0) || c_out > 256) return CF_ERR_UNSUPPORTED;
+    if (c_out % 16 != 0) return CF_ERR_UNSUPPORTED;
+    if ((c_in == 1 || c_in == 4) && c_out > 256) return CF_ERR_UNSUPPORTED;
     if ((c_in == 1 || c_in == 4) && (w * c_in) % 8 != 0) return CF_ERR_UNSUPPORTED;
     const size_t need = wgrad_workspace_bytes(ctx.num_sms, n, d, h, w, c_in, c_out);
     if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
@@ -385,10 +411,12 @@ cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, in
         if (st != CF_OK) return st;
         return launch_splitk_reduce(ctx, part, dw, (int64_t)c_out * 27 * c_in, n_splits, accumulate);
     }
-    switch (c_out) {
+    switch (g.bn) {
         case 16: st = wgrad_bn<16>(ctx, g, x, dz, part); break;
         case 32: st = wgrad_bn<32>(ctx, g, x, dz, part); break;
+        case 48: st = wgrad_bn<48>(ctx, g, x, dz, part); break;
         case 64: st = wgrad_bn<64>(ctx, g, x, dz, part); break;
+        case 96: st = wgrad_bn<96>(ctx, g, x, dz, part); break;
         case 128: st = wgrad_bn<128>(ctx, g, x, dz, part); break;
         case 192: st = wgrad_bn<192>(ctx, g, x, dz, part); break;
         case 256: st = wgrad_bn<256>(ctx, g, x, dz, part); break;

@@ -488,7 +488,7 @@ static cf_status wgrad_smallc_route(const LaunchCtx& ctx, const WgradGeom& g, co
 template <int CIN>
 static cf_status wgrad_smallc_cin(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
                                   const uint8_t* idx, float* part) {
-    switch (g.Cout) {
+    switch (g.bn) {  // c_out rounded up to a compiled width (extra channels read as zero)
         case 16: return wgrad_smallc_route<CIN, 16>(ctx, g, x, dz, idx, part);
         case 32: return wgrad_smallc_route<CIN, 32>(ctx, g, x, dz, idx, part);
         case 64: return wgrad_smallc_route<CIN, 64>(ctx, g, x, dz, idx, part);
@@ -501,7 +501,8 @@ static cf_status wgrad_smallc_cin(const LaunchCtx& ctx, const WgradGeom& g, cons
 
 cf_status launch_wgrad_smallc(const LaunchCtx& ctx, const WgradGeom& g, const uint16_t* x, const uint16_t* dz,
                               const uint8_t* idx, float* part) {
-    if (g.vw != WS_VW || g.vh != WS_VH || g.vd != WS_VD || g.n_mblocks != 1) return CF_ERR_UNSUPPORTED;
+    if (g.vw != WS_VW || g.vh != WS_VH || g.vd != WS_VD || g.n_mblocks != 1 || g.n_ntiles != 1)
+        return CF_ERR_UNSUPPORTED;
     if (idx && ((g.D | g.H | g.W) & 1)) return CF_ERR_UNSUPPORTED;
     if (g.Cin == 4) return wgrad_smallc_cin<4>(ctx, g, x, dz, idx, part);
     if (g.Cin == 1) return wgrad_smallc_cin<1>(ctx, g, x, dz, idx, part);

@@ -14,9 +14,11 @@ struct WgradGeom {
     int nb_w, nb_h, nb_d;     // boxes per dimension
     int64_t total_boxes;      // N * nb_d * nb_h * nb_w
     int n_mblocks;            // ceil(27*Cin / 128)
+    int n_ntiles;             // output-channel tiles of bn channels (the last may be partly beyond Cout)
+    int bn;                   // channels per N tile
     int n_splits;
     int64_t boxes_per_split;
-    int num_units;            // n_mblocks * n_splits
+    int num_units;            // n_mblocks * n_ntiles * n_splits
 };
 
 // Box cursor: decodes a linear box index once, then steps through the boxes
@@ -45,15 +47,16 @@ struct BoxCursor {
     }
 };
 
-// Writes the unit's accumulator rows (t,ci) < 27*Cin into part[split][co][row].
+// Writes the unit's accumulator rows (t,ci) < 27*Cin, channels co0 + c < Cout,
+// into part[split][co][row].
 template <int BN>
-__device__ __forceinline__ void wgrad_store_partial(const WgradGeom& g, float* part, int mb, int split,
+__device__ __forceinline__ void wgrad_store_partial(const WgradGeom& g, float* part, int mb, int split, int co0,
                                                     uint32_t tmem_base, int q, int lane) {
     const int row = q * 32 + lane;
     const int mrow = mb * 128 + row;
     const int KK = 27 * g.Cin;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
-    float* base = part + (int64_t)split * g.Cout * KK + mrow;
+    float* base = part + ((int64_t)split * g.Cout + co0) * KK + mrow;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 16) {
         uint32_t r[32];
@@ -62,7 +65,7 @@ __device__ __forceinline__ void wgrad_store_partial(const WgradGeom& g, float* p
         if (mrow < KK) {
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-                if (c + k < g.Cout) base[(int64_t)(c + k) * KK] = __uint_as_float(r[k]);
+                if (co0 + c + k < g.Cout) base[(int64_t)(c + k) * KK] = __uint_as_float(r[k]);
         }
     }
 }

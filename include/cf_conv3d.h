@@ -76,7 +76,8 @@ enum { CF_OP_FWD = 0, CF_OP_DGRAD = 1, CF_OP_WGRAD = 2, CF_OP_DGRAD_ROUTED = 3,
  *        else y is the pooled block output Y, [n][d/2][h/2][w/2][c_out], and
  *        epi->argmax (if not NULL) receives the window codes.
  *   ws : unused (pass NULL, 0).
- * Supported: c_in in {1, 4} or a multiple of 32; c_out a multiple of 16 and
+ * Supported: c_in in {1, 4} or a multiple of 16 (the CosmoFlow page's rule of
+ * channel counts in multiples of 16, section III-A); c_out a multiple of 16 and
  * <= 256 per kernel tile (multiples of 256 above that), or c_out a multiple of 8
  * (<= 256) when c_in is 1 or 4; w * c_in a multiple of 8 when c_in is 1 or 4;
  * d, h, w even when pooling.
@@ -101,7 +102,7 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
  *        stored dx (fixed order).  In a block stack dx is the previous block's
  *        pooled pre-activation gradient and dsum its bias gradient (fused into
  *        the epilogue for c_in <= 32, a separate pass over dx otherwise).
- * Supported: c_out a multiple of 32, c_in a multiple of 16.
+ * Supported: c_out and c_in multiples of 16.
  */
 cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx,
                           const uint16_t* w, const uint16_t* x_act, float slope, uint16_t* dx,
@@ -118,8 +119,8 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
  *        partials); d, h, w must be even.  Other c_in expand dZ into the
  *        workspace first.  cf_workspace_size(CF_OP_WGRAD_ROUTED) covers both.
  *   dw : [c_out][3][3][3][c_in] fp32; accumulate != 0 adds to it, else overwrites.
- * Supported: c_in in {1, 4} (w * c_in a multiple of 8) or a multiple of 32;
- * c_out 16, 32 or a multiple of 64, <= 256.
+ * Supported: c_in in {1, 4} (w * c_in a multiple of 8) or a multiple of 16;
+ * c_out a multiple of 16 (at most 256 when c_in is 1 or 4).
  */
 cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* dz,
                           const uint8_t* idx, float* dw, int accumulate, void* ws,

@@ -62,8 +62,11 @@ def test_invalid_arguments_return_codes(cf):
     x = torch.empty(1 * 4 * 4 * 4 * 48, dtype=torch.bfloat16, device="cuda")
     w = torch.empty(64 * 27 * 48, dtype=torch.bfloat16, device="cuda")
     y = torch.empty(4 * 4 * 4 * 64, dtype=torch.bfloat16, device="cuda")
-    bad = cf.cf_conv_desc(1, 4, 4, 4, 48, 64)  # c_in 48: not a multiple of 32
+    bad = cf.cf_conv_desc(1, 4, 4, 4, 40, 64)  # c_in 40: not 1, 4 or a multiple of 16
     assert cf.cf_conv3d_fwd(bad, x, w, None, y, check=False) == cf.CF_ERR_UNSUPPORTED
+    bad = cf.cf_conv_desc(1, 4, 4, 4, 32, 72)  # c_out 72: not a multiple of 16
+    assert cf.cf_conv3d_fwd(bad, x, w, None, y, check=False) == cf.CF_ERR_UNSUPPORTED
+    assert cf.cf_conv3d_wgrad(bad, x, y, None, w, 0, x, 16, check=False) == cf.CF_ERR_UNSUPPORTED
     # misaligned pointer
     assert cf.cf_conv3d_fwd(desc, x.data_ptr() + 2, w, None, y, check=False) == cf.CF_ERR_INVALID_ARG
     # workspace too small
@@ -136,6 +139,10 @@ FWD_SHAPES = [
     (1, 2, 2, 8, 64, 16),
     (1, 2, 4, 8, 96, 96),      # three 32-channel K chunks, N tile 96
     (1, 2, 4, 8, 64, 512),     # two N tiles of 256
+    (1, 4, 6, 16, 16, 32),     # 16-channel input (Table I c2: 16 -> 32): halo tile, 16-channel chunks
+    (1, 2, 4, 24, 16, 48),     # 16-channel chunks, per-tap engine, N tile 48
+    (1, 2, 6, 8, 48, 64),      # three 16-channel chunks, halo tile
+    (2, 2, 4, 8, 32, 80),      # N tile 80
 ]
 
 
@@ -178,7 +185,7 @@ def _check_pooled(oracle_mod, x, w, b, gy, gidx, what):
     return int((~notie).sum())
 
 
-@pytest.mark.parametrize("shape", FWD_SHAPES[:6])
+@pytest.mark.parametrize("shape", FWD_SHAPES[:6] + FWD_SHAPES[8:])
 def test_conv_fwd_pooled(cf, oracle_mod, shape):
     import torch
     N, D, H, W, Ci, Co = shape
@@ -244,6 +251,9 @@ DGRAD_SHAPES = [
     (1, 2, 8, 8, 128, 256),
     (1, 2, 8, 8, 256, 256),
     (1, 2, 4, 8, 16, 32),
+    (1, 4, 6, 16, 16, 32),     # the Table I c2 layer: dX has 16 channels
+    (1, 2, 4, 8, 48, 16),      # dZ has 16 channels: 16-channel K chunks
+    (1, 2, 4, 16, 32, 80),     # dZ has 80 channels: five 16-channel chunks, halo tile
 ]
 
 
@@ -295,6 +305,12 @@ WGRAD_SHAPES = [
     (2, 2, 8, 16, 32, 32),     # halo-tile wgrad variants: 32 -> 32, 32 -> 128, 64 -> 64
     (1, 4, 20, 8, 32, 128),
     (1, 2, 4, 24, 64, 64),
+    (1, 4, 6, 16, 16, 32),     # 16-channel input rows (Table I c2)
+    (1, 2, 4, 8, 48, 48),      # N tile 48
+    (1, 2, 4, 16, 32, 80),     # c_out 80 in a 96-wide tile (channels past c_out read as zero)
+    (1, 2, 4, 8, 64, 320),     # two N tiles, the second mostly beyond c_out
+    (1, 2, 4, 8, 32, 512),     # two full N tiles
+    (1, 2, 4, 16, 4, 80),      # small c_in, c_out 80 in a 128-wide tile
 ]
 
 
@@ -328,6 +344,8 @@ ROUTED_SHAPES = [
     (1, 2, 4, 16, 4, 64),
     (1, 2, 4, 16, 4, 128),
     (1, 2, 4, 16, 4, 256),
+    (1, 2, 4, 16, 4, 48),      # routed small c_in with a padded N tile
+    (1, 2, 4, 16, 16, 32),     # 16-channel input, dZ expanded in the workspace
 ]
 
 
