@@ -64,6 +64,16 @@ def _load():
         lib.oracle_block_fwd_pts_bf16.argtypes = dims + [_U16, _U16, _F32, ctypes.c_double,
                                                          _i64, _I64, _D, _U8, _D, _D]
         lib.oracle_conv3d_wgrad_routed_pts_bf16.argtypes = dims + [_U16, _U16, _U8] + pts
+        lib.oracle_avgpool_fwd.argtypes = pdims + [_D, _D, ctypes.c_double, _D, _U8]
+        lib.oracle_avgpool_bwd.argtypes = pdims + [_D, _U8, ctypes.c_double, _D, _D]
+        lib.oracle_act_fwd.argtypes = [_i64, _i32, _D, _D, ctypes.c_double, _D]
+        lib.oracle_act_bwd.argtypes = [_i64, _i32, _D, _D, ctypes.c_double, _D, _D]
+        lib.oracle_conv3d_fwd_s2.argtypes = dims + [_D, _D, _D]
+        lib.oracle_conv3d_dgrad_s2.argtypes = dims + [_D, _D, _D]
+        lib.oracle_conv3d_wgrad_s2.argtypes = dims + [_D, _D, _D]
+        for f in (lib.oracle_avgpool_fwd, lib.oracle_avgpool_bwd, lib.oracle_act_fwd, lib.oracle_act_bwd,
+                  lib.oracle_conv3d_fwd_s2, lib.oracle_conv3d_dgrad_s2, lib.oracle_conv3d_wgrad_s2):
+            f.restype = None
         for f in (lib.oracle_conv3d_fwd, lib.oracle_conv3d_dgrad, lib.oracle_conv3d_wgrad,
                   lib.oracle_pool_fwd, lib.oracle_pool_bwd, lib.oracle_conv3d_fwd_pts_bf16,
                   lib.oracle_conv3d_dgrad_pts_bf16, lib.oracle_conv3d_wgrad_pts_bf16,
@@ -164,6 +174,87 @@ def pool_bwd(dy: np.ndarray, y, idx: np.ndarray, slope: float, want_dz: bool = T
     lib.oracle_pool_bwd(N, 2 * D2, 2 * H2, 2 * W2, C, _p(dy, _D), _p(yy, _D), _p(idx, _U8), slope,
                         _p(dz, _D), _p(dyp, _D), _p(db, _D))
     return dz, dyp, db
+
+
+def avgpool_fwd(z: np.ndarray, bias, slope: float):
+    """(y, mask) = 2x2x2 average of LReLU(z + b) and the per-window bits of
+    z + b > 0 (bit dd*4+dh*2+dw)."""
+    lib = _load()
+    z = _f64(z)
+    N, D, H, W, C = z.shape
+    b = None if bias is None else _f64(bias)
+    y = np.empty((N, D // 2, H // 2, W // 2, C), np.float64)
+    mask = np.empty((N, D // 2, H // 2, W // 2, C), np.uint8)
+    lib.oracle_avgpool_fwd(N, D, H, W, C, _p(z, _D), _p(b, _D), slope, _p(y, _D), _p(mask, _U8))
+    return y, mask
+
+
+def avgpool_bwd(dy: np.ndarray, mask: np.ndarray, slope: float):
+    """(dz, db) of the average-pool block: dz = dy/8 * LReLU'(z+b) per voxel."""
+    lib = _load()
+    dy = _f64(dy)
+    N, D2, H2, W2, C = dy.shape
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    dz = np.empty((N, 2 * D2, 2 * H2, 2 * W2, C), np.float64)
+    db = np.empty((C,), np.float64)
+    lib.oracle_avgpool_bwd(N, 2 * D2, 2 * H2, 2 * W2, C, _p(dy, _D), _p(mask, _U8), slope, _p(dz, _D), _p(db, _D))
+    return dz, db
+
+
+def act_fwd(z: np.ndarray, bias, slope: float):
+    """y = LReLU(z + b) (an unpooled block)."""
+    lib = _load()
+    z = _f64(z)
+    C = z.shape[-1]
+    b = None if bias is None else _f64(bias)
+    y = np.empty_like(z)
+    lib.oracle_act_fwd(z.size, C, _p(z, _D), _p(b, _D), slope, _p(y, _D))
+    return y
+
+
+def act_bwd(dy: np.ndarray, y: np.ndarray, slope: float):
+    """(dz, db) of an unpooled block: dz = dy * LReLU'(y)."""
+    lib = _load()
+    dy, y = _f64(dy), _f64(y)
+    C = dy.shape[-1]
+    dz = np.empty_like(dy)
+    db = np.empty((C,), np.float64)
+    lib.oracle_act_bwd(dy.size, C, _p(dy, _D), _p(y, _D), slope, _p(dz, _D), _p(db, _D))
+    return dz, db
+
+
+def conv3d_fwd_s2(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """Stride-2 cross-correlation, pad 1: z [N, (D+1)/2, (H+1)/2, (W+1)/2, Co]."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    N, D, H, W, Ci = x.shape
+    Co = w.shape[0]
+    z = np.empty((N, (D + 1) // 2, (H + 1) // 2, (W + 1) // 2, Co), np.float64)
+    lib.oracle_conv3d_fwd_s2(N, D, H, W, Ci, Co, _p(x, _D), _p(w, _D), _p(z, _D))
+    return z
+
+
+def conv3d_dgrad_s2(dz: np.ndarray, w: np.ndarray, in_shape) -> np.ndarray:
+    """dx [N,D,H,W,Ci] of the stride-2 conv (in_shape = (D, H, W) of its input)."""
+    lib = _load()
+    dz, w = _f64(dz), _f64(w)
+    N, Co = dz.shape[0], dz.shape[4]
+    D, H, W = in_shape
+    Ci = w.shape[4]
+    dx = np.empty((N, D, H, W, Ci), np.float64)
+    lib.oracle_conv3d_dgrad_s2(N, D, H, W, Ci, Co, _p(dz, _D), _p(w, _D), _p(dx, _D))
+    return dx
+
+
+def conv3d_wgrad_s2(x: np.ndarray, dz: np.ndarray) -> np.ndarray:
+    """dW of the stride-2 conv from its input x and output gradient dz."""
+    lib = _load()
+    x, dz = _f64(x), _f64(dz)
+    N, D, H, W, Ci = x.shape
+    Co = dz.shape[4]
+    dw = np.empty((Co, 3, 3, 3, Ci), np.float64)
+    lib.oracle_conv3d_wgrad_s2(N, D, H, W, Ci, Co, _p(x, _D), _p(dz, _D), _p(dw, _D))
+    return dw
 
 
 # ----------------------------------------------------------------------------
@@ -319,3 +410,88 @@ def stack_bwd(xs, ys, idxs, ws, dy, slope, mirrored=True):
             dxs[l] = g
             use_y = False
     return dws, dbs, dzs, dxs
+
+
+# ----------------------------------------------------------------------------
+# general chain: per-block stride (1 or 2) and pooling ("max", "avg", "none")
+
+def _upsample2(dz, out_shape):
+    """Zero-insertion of a stride-2 output gradient at the even positions of the
+    input grid (out_shape = (D, H, W))."""
+    N, _, _, _, C = dz.shape
+    D, H, W = out_shape
+    up = np.zeros((N, D, H, W, C))
+    up[:, ::2, ::2, ::2, :] = dz
+    return up
+
+
+def chain_fwd(x, ws, bs, slope, specs, mirrored=True):
+    """Blocks conv (stride s) -> + b -> leaky ReLU -> pooling, one spec
+    (stride, pool) per block, pool in {"max", "avg", "none"}.  Max pooling is
+    taken before the activation (equal by monotonicity), average pooling after
+    it (CosmoFlow page, section III-A/III-C).  Returns (xs, ys, auxs): block
+    inputs, outputs (bf16-rounded in mirrored mode) and the argmax codes (max)
+    or pre-activation sign masks (avg) or None."""
+    xs, ys, auxs = [], [], []
+    cur = _f64(x)
+    for (stride, pool), w, b in zip(specs, ws, bs):
+        xs.append(cur)
+        z = conv3d_fwd(cur, w) if stride == 1 else conv3d_fwd_s2(cur, w)
+        if pool == "max":
+            y, aux = pool_fwd(z, b, slope)
+        elif pool == "avg":
+            y, aux = avgpool_fwd(z, b, slope)
+        else:
+            y, aux = act_fwd(z, b, slope), None
+        if mirrored:
+            y = round_to_bf16(y)
+        ys.append(y)
+        auxs.append(aux)
+        cur = y
+    return xs, ys, auxs
+
+
+def chain_bwd(xs, ys, auxs, ws, dy, slope, specs, mirrored=True):
+    """Backward of chain_fwd from dy at the last output: per block (dW, db) and
+    the dense dZ.  Where the lower block's output derivative is a function of
+    that output (max pooling, no pooling), it is applied to the input gradient
+    right after backward-data, as the GPU stack stores it; an average-pooled
+    block applies the per-voxel derivative itself (from its sign mask)."""
+    L = len(ws)
+    dws, dbs, dzs = [None] * L, [None] * L, [None] * L
+    g = _f64(dy)
+    pre = False  # g already carries the output derivative of block l
+    for l in range(L - 1, -1, -1):
+        stride, pool = specs[l]
+        if pool == "max":
+            dz, _, db = pool_bwd(g, None if pre else ys[l], auxs[l], slope)
+        elif pool == "avg":
+            dz, db = avgpool_bwd(g, auxs[l], slope)
+        elif pre:
+            dz, db = g, g.reshape(-1, g.shape[-1]).sum(0)
+        else:
+            dz, db = act_bwd(g, ys[l], slope)
+        if mirrored:
+            dz = round_to_bf16(dz)
+        dzs[l], dbs[l] = dz, db
+        dws[l] = conv3d_wgrad(xs[l], dz) if stride == 1 else conv3d_wgrad_s2(xs[l], dz)
+        if l > 0:
+            dx = conv3d_dgrad(dz, ws[l]) if stride == 1 else conv3d_dgrad_s2(dz, ws[l], xs[l].shape[1:4])
+            if specs[l - 1][1] != "avg":
+                g, pre = dx * np.where(xs[l] > 0, 1.0, slope), True
+            else:
+                g, pre = dx, False
+            if mirrored:
+                g = round_to_bf16(g)
+    return dws, dbs, dzs
+
+
+# The seven-conv model of the hybrid-parallelism page, Table I, for input width
+# 128: c4 has stride 2, c6 and c7 are not pooled at this width; pooling is max
+# (this build's block), biases present (zero in the synthetic inputs).
+TABLE1_CHANNELS = (4, 16, 32, 64, 128, 256, 256, 256)
+
+
+def table1_specs(wi: int = 128):
+    pooled = {128: 5, 256: 6, 512: 7}[wi]
+    return [(2 if l == 3 else 1, "max" if l < pooled else "none") for l in range(7)]

@@ -438,3 +438,187 @@ void oracle_conv3d_wgrad_routed_pts_bf16(int64_t N, int64_t D, int64_t H, int64_
         if (sabs) sabs[p] = sa;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Page variants ("next" rows).
+ *
+ * Average pooling (CosmoFlow page, section III-C: pooling averages each
+ * channel separately with constant weights 1/KS^3; section III-A: every conv
+ * layer is followed by leaky ReLU): the block is conv -> + bias -> leaky ReLU
+ * -> 2x2x2 average, so
+ *   y[p] = (1/8) * sum_{v in window(p)} LReLU(z[v] + b)
+ * and its backward
+ *   dz[v] = dy[p] / 8 * LReLU'(z[v] + b),   db = sum over v of dz[v].
+ * Unlike the max-pool, pooling does not commute with the activation here, so
+ * the backward needs the sign of every pre-activation of the window; mask[p]
+ * records it (bit dd*4+dh*2+dw set where z + b > 0). */
+void oracle_avgpool_fwd(int64_t N, int64_t D, int64_t H, int64_t W, int32_t C,
+                        const double* z, const double* bias, double slope, double* y, uint8_t* mask)
+{
+    int64_t D2 = D / 2, H2 = H / 2, W2 = W / 2;
+    int64_t planes = N * D2;
+#pragma omp parallel for schedule(static)
+    for (int64_t np = 0; np < planes; ++np) {
+        int64_t n = np / D2, pd = np % D2;
+        for (int64_t ph = 0; ph < H2; ++ph)
+            for (int64_t pw = 0; pw < W2; ++pw)
+                for (int32_t c = 0; c < C; ++c) {
+                    double sum = 0.0;
+                    int m = 0;
+                    for (int dd = 0; dd < 2; ++dd)
+                        for (int dh = 0; dh < 2; ++dh)
+                            for (int dw = 0; dw < 2; ++dw) {
+                                double s = z[I5(n, 2 * pd + dd, 2 * ph + dh, 2 * pw + dw, c, D, H, W, C)] +
+                                           (bias ? bias[c] : 0.0);
+                                if (s > 0) m |= 1 << (dd * 4 + dh * 2 + dw);
+                                sum += s > 0 ? s : slope * s;
+                            }
+                    int64_t o = I5(n, pd, ph, pw, c, D2, H2, W2, C);
+                    y[o] = sum / 8.0;
+                    if (mask) mask[o] = (uint8_t)m;
+                }
+    }
+}
+
+/* dz (full resolution) and db from dy (pooled) and the pre-activation signs. */
+void oracle_avgpool_bwd(int64_t N, int64_t D, int64_t H, int64_t W, int32_t C,
+                        const double* dy, const uint8_t* mask, double slope, double* dz, double* db)
+{
+    int64_t D2 = D / 2, H2 = H / 2, W2 = W / 2;
+    if (db)
+        for (int32_t c = 0; c < C; ++c) db[c] = 0.0;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t pd = 0; pd < D2; ++pd)
+            for (int64_t ph = 0; ph < H2; ++ph)
+                for (int64_t pw = 0; pw < W2; ++pw)
+                    for (int32_t c = 0; c < C; ++c) {
+                        int64_t o = I5(n, pd, ph, pw, c, D2, H2, W2, C);
+                        for (int k = 0; k < 8; ++k) {
+                            int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+                            double g = dy[o] / 8.0 * (((mask[o] >> k) & 1) ? 1.0 : slope);
+                            if (dz) dz[I5(n, 2 * pd + dd, 2 * ph + dh, 2 * pw + dw, c, D, H, W, C)] = g;
+                            if (db) db[c] += g;
+                        }
+                    }
+}
+
+/* Unpooled block (layers of the hybrid-parallelism page's Table I after the
+ * last pooling: convolution followed by leaky ReLU only):
+ *   y = LReLU(z + b);  backward dz = dy * LReLU'(y), db = sum of dz
+ * (y > 0 exactly where z + b > 0). */
+void oracle_act_fwd(int64_t count, int32_t C, const double* z, const double* bias, double slope, double* y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < count; ++i) {
+        double s = z[i] + (bias ? bias[i % C] : 0.0);
+        y[i] = s > 0 ? s : slope * s;
+    }
+}
+
+void oracle_act_bwd(int64_t count, int32_t C, const double* dy, const double* y, double slope, double* dz,
+                    double* db)
+{
+    if (db)
+        for (int32_t c = 0; c < C; ++c) db[c] = 0.0;
+    for (int64_t i = 0; i < count; ++i) {
+        double g = dy[i] * (y[i] > 0 ? 1.0 : slope);
+        if (dz) dz[i] = g;
+        if (db) db[i % C] += g;
+    }
+}
+
+/* Stride-2 convolution (Table I, layer c4: "stride of 2"), padding 1 on
+ * every face ("same" padding), output [N][Do][Ho][Wo] with Do = (D + 1) / 2:
+ *   z[n,o,co] = sum_{t,ci} W[co,t,ci] * x[n, 2*o + t - 1, ci]    (o = (od,oh,ow))
+ * backward data and weight by the same index map:
+ *   dx[n,u,ci] = sum over (t, o) with 2*o + t - 1 = u of W[co,t,ci] * dz[n,o,co]
+ *   dW[co,t,ci] = sum_{n,o} dz[n,o,co] * x[n, 2*o + t - 1, ci]. */
+void oracle_conv3d_fwd_s2(int64_t N, int64_t D, int64_t H, int64_t W, int32_t Ci, int32_t Co,
+                          const double* x, const double* wt, double* z)
+{
+    int64_t Do = (D + 1) / 2, Ho = (H + 1) / 2, Wo = (W + 1) / 2;
+    int64_t planes = N * Do;
+#pragma omp parallel for schedule(static)
+    for (int64_t np = 0; np < planes; ++np) {
+        int64_t n = np / Do, od = np % Do;
+        for (int64_t oh = 0; oh < Ho; ++oh)
+            for (int64_t ow = 0; ow < Wo; ++ow)
+                for (int32_t co = 0; co < Co; ++co) {
+                    double acc = 0.0;
+                    for (int kd = 0; kd < 3; ++kd) {
+                        int64_t id = 2 * od + kd - 1;
+                        if (id < 0 || id >= D) continue;
+                        for (int kh = 0; kh < 3; ++kh) {
+                            int64_t ih = 2 * oh + kh - 1;
+                            if (ih < 0 || ih >= H) continue;
+                            for (int kw = 0; kw < 3; ++kw) {
+                                int64_t iw = 2 * ow + kw - 1;
+                                if (iw < 0 || iw >= W) continue;
+                                for (int32_t ci = 0; ci < Ci; ++ci)
+                                    acc += wt[IW(co, kd, kh, kw, ci, Ci)] * x[I5(n, id, ih, iw, ci, D, H, W, Ci)];
+                            }
+                        }
+                    }
+                    z[I5(n, od, oh, ow, co, Do, Ho, Wo, Co)] = acc;
+                }
+    }
+}
+
+/* dz: [N][Do][Ho][Wo][Co]; dx: [N][D][H][W][Ci].  Scatter form over (o, t). */
+void oracle_conv3d_dgrad_s2(int64_t N, int64_t D, int64_t H, int64_t W, int32_t Ci, int32_t Co,
+                            const double* dz, const double* wt, double* dx)
+{
+    int64_t Do = (D + 1) / 2, Ho = (H + 1) / 2, Wo = (W + 1) / 2;
+    memset(dx, 0, sizeof(double) * (size_t)(N * D * H * W * Ci));
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t od = 0; od < Do; ++od)
+            for (int64_t oh = 0; oh < Ho; ++oh)
+                for (int64_t ow = 0; ow < Wo; ++ow)
+                    for (int kd = 0; kd < 3; ++kd) {
+                        int64_t id = 2 * od + kd - 1;
+                        if (id < 0 || id >= D) continue;
+                        for (int kh = 0; kh < 3; ++kh) {
+                            int64_t ih = 2 * oh + kh - 1;
+                            if (ih < 0 || ih >= H) continue;
+                            for (int kw = 0; kw < 3; ++kw) {
+                                int64_t iw = 2 * ow + kw - 1;
+                                if (iw < 0 || iw >= W) continue;
+                                for (int32_t co = 0; co < Co; ++co) {
+                                    double g = dz[I5(n, od, oh, ow, co, Do, Ho, Wo, Co)];
+                                    for (int32_t ci = 0; ci < Ci; ++ci)
+                                        dx[I5(n, id, ih, iw, ci, D, H, W, Ci)] += wt[IW(co, kd, kh, kw, ci, Ci)] * g;
+                                }
+                            }
+                        }
+                    }
+}
+
+void oracle_conv3d_wgrad_s2(int64_t N, int64_t D, int64_t H, int64_t W, int32_t Ci, int32_t Co,
+                            const double* x, const double* dz, double* dw)
+{
+    int64_t Do = (D + 1) / 2, Ho = (H + 1) / 2, Wo = (W + 1) / 2;
+    int64_t items = (int64_t)Co * 27;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t it = 0; it < items; ++it) {
+        int32_t co = (int32_t)(it / 27);
+        int t = (int)(it % 27), kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
+        for (int32_t ci = 0; ci < Ci; ++ci) {
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                for (int64_t od = 0; od < Do; ++od) {
+                    int64_t id = 2 * od + kd - 1;
+                    if (id < 0 || id >= D) continue;
+                    for (int64_t oh = 0; oh < Ho; ++oh) {
+                        int64_t ih = 2 * oh + kh - 1;
+                        if (ih < 0 || ih >= H) continue;
+                        for (int64_t ow = 0; ow < Wo; ++ow) {
+                            int64_t iw = 2 * ow + kw - 1;
+                            if (iw < 0 || iw >= W) continue;
+                            acc += dz[I5(n, od, oh, ow, co, Do, Ho, Wo, Co)] * x[I5(n, id, ih, iw, ci, D, H, W, Ci)];
+                        }
+                    }
+                }
+            dw[IW(co, kd, kh, kw, ci, Ci)] = acc;
+        }
+    }
+}

@@ -468,3 +468,142 @@ def test_routed_wgrad_points_match_dense(oracle_mod):
     v, s = oracle_mod.conv3d_wgrad_routed_pts(x16, g16, idx, pts)
     np.testing.assert_allclose(v, ref[tuple(pts.T)], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(s, S[tuple(pts.T)], rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- page variants
+
+def test_avgpool_closed_forms(oracle_mod):
+    slope = 0.3
+    # a constant window: the average of eight equal activations
+    y, m = oracle_mod.avgpool_fwd(np.full((1, 2, 2, 2, 1), 2.0), None, slope)
+    assert y.item() == 2.0 and m.item() == 0xFF
+    y, m = oracle_mod.avgpool_fwd(np.full((1, 2, 2, 2, 1), -1.0), None, slope)
+    assert y.item() == pytest.approx(-0.3, abs=1e-15) and m.item() == 0
+    # a window with values -4..3 in (dd,dh,dw) order: activations average to
+    # (0+1+2+3 + 0.3*(-4-3-2-1)) / 8, mask = the four positive positions (0 is not)
+    z = (np.arange(8, dtype=float) - 4).reshape(1, 2, 2, 2, 1)
+    y, m = oracle_mod.avgpool_fwd(z, None, slope)
+    assert y.item() == pytest.approx((0 + 1 + 2 + 3 + slope * (-10)) / 8, abs=1e-15)
+    assert m.item() == 0b11100000
+    # bias shifts before the activation
+    y, m = oracle_mod.avgpool_fwd(z, np.array([4.5]), slope)
+    assert y.item() == pytest.approx(np.mean(np.arange(8) + 0.5), abs=1e-15) and m.item() == 0xFF
+    # the average of a ramp equals numpy's window mean of the activation
+    zz = RNG.normal(size=(2, 4, 6, 4, 3))
+    b = RNG.normal(size=3)
+    y, m = oracle_mod.avgpool_fwd(zz, b, slope)
+    a = np.where(zz + b > 0, zz + b, slope * (zz + b))
+    np.testing.assert_allclose(y, a.reshape(2, 2, 2, 3, 2, 2, 2, 3).mean(axis=(2, 4, 6)), rtol=1e-13, atol=1e-15)
+    bits = (_window_view(zz + b) > 0).astype(np.int64) << np.arange(8)
+    np.testing.assert_array_equal(m, bits.sum(-1))
+
+
+def test_act_closed_forms(oracle_mod):
+    z = np.array([-2.0, -0.0, 0.0, 1.5]).reshape(1, 1, 1, 4, 1)
+    y = oracle_mod.act_fwd(z, np.array([0.5]), 0.3)
+    np.testing.assert_allclose(y.ravel(), [0.3 * -1.5, 0.5, 0.5, 2.0])
+    dz, db = oracle_mod.act_bwd(np.ones_like(z), y, 0.3)
+    np.testing.assert_allclose(dz.ravel(), [0.3, 1, 1, 1])
+    assert db.item() == pytest.approx(3.3)
+
+
+def test_stride2_conv_is_subsampled_stride1(oracle_mod):
+    """Stride 2 with padding 1 evaluates the stride-1 output at even positions;
+    its backward-data and backward-weight are the stride-1 ones applied to the
+    output gradient with zeros inserted at the odd positions; adjoints hold."""
+    rng = np.random.default_rng(41)
+    for shape in ((1, 4, 6, 8, 3), (2, 5, 3, 7, 2)):
+        x = rng.normal(size=shape)
+        w = rng.normal(size=(4, 3, 3, 3, shape[4]))
+        z2 = oracle_mod.conv3d_fwd_s2(x, w)
+        np.testing.assert_allclose(z2, oracle_mod.conv3d_fwd(x, w)[:, ::2, ::2, ::2], rtol=1e-13, atol=1e-13)
+        g = rng.normal(size=z2.shape)
+        up = oracle_mod._upsample2(g, shape[1:4])
+        dx = oracle_mod.conv3d_dgrad_s2(g, w, shape[1:4])
+        np.testing.assert_allclose(dx, oracle_mod.conv3d_dgrad(up, w), rtol=1e-12, atol=1e-12)
+        dw = oracle_mod.conv3d_wgrad_s2(x, g)
+        np.testing.assert_allclose(dw, oracle_mod.conv3d_wgrad(x, up), rtol=1e-12, atol=1e-12)
+        lhs = np.vdot(z2, g)
+        assert abs(lhs - np.vdot(x, dx)) <= 1e-10 * abs(lhs)
+        assert abs(lhs - np.vdot(w, dw)) <= 1e-10 * abs(lhs)
+
+
+def test_chain_with_variants_finite_differences(oracle_mod):
+    """A chain of an average-pooled block, a stride-2 max-pooled block and an
+    unpooled block: every dW and db against central differences of <g, y_top>
+    (exact mode).  Biases put pre-activations on both sides of zero."""
+    slope = 0.3
+    specs = [(1, "avg"), (2, "max"), (1, "none")]
+    ch = (2, 3, 3, 2)
+    rng = np.random.default_rng(42)
+    for _ in range(300):
+        x = rng.normal(size=(1, 8, 8, 8, ch[0]))
+        ws = [rng.normal(size=(ch[l + 1], 3, 3, 3, ch[l])) for l in range(3)]
+        bs = [rng.normal(size=(ch[l + 1],)) * 3 for l in range(3)]
+        xs, ys, auxs = oracle_mod.chain_fwd(x, ws, bs, slope, specs, mirrored=False)
+        # kink-free: every pre-activation away from zero, every max window's gap > 1e-3
+        z0 = oracle_mod.conv3d_fwd(xs[0], ws[0]) + bs[0]
+        z1 = oracle_mod.conv3d_fwd_s2(xs[1], ws[1])
+        z2 = oracle_mod.conv3d_fwd(xs[2], ws[2]) + bs[2]
+        srt = np.sort(_window_view(z1), axis=-1)
+        ok = (np.min(np.abs(z0)) > 1e-3 and np.min(np.abs(z2)) > 1e-3 and np.min(srt[..., -1] - srt[..., -2]) > 1e-3
+              and np.min(np.abs(srt[..., -1] + bs[1])) > 1e-3)
+        ok = ok and np.any(z0 < 0) and np.any(z0 > 0) and np.any(srt[..., -1] + bs[1] < 0)
+        if ok:
+            break
+    else:
+        pytest.fail("could not draw a kink-free case")
+    g = rng.normal(size=ys[-1].shape)
+    dws, dbs, _ = oracle_mod.chain_bwd(xs, ys, auxs, ws, g, slope, specs, mirrored=False)
+
+    def loss(ws_, bs_):
+        return np.vdot(g, oracle_mod.chain_fwd(x, ws_, bs_, slope, specs, mirrored=False)[1][-1])
+
+    h = 1e-6
+    for l in range(3):
+        for _ in range(4):
+            pos = tuple(rng.integers(0, s) for s in ws[l].shape)
+            wp, wm = [w.copy() for w in ws], [w.copy() for w in ws]
+            wp[l][pos] += h
+            wm[l][pos] -= h
+            num = (loss(wp, bs) - loss(wm, bs)) / (2 * h)
+            assert abs(num - dws[l][pos]) <= 1e-5 * max(1.0, abs(num)), (l, pos, num, dws[l][pos])
+        for c in range(ch[l + 1]):
+            bp, bm = [b.copy() for b in bs], [b.copy() for b in bs]
+            bp[l][c] += h
+            bm[l][c] -= h
+            num = (loss(ws, bp) - loss(ws, bm)) / (2 * h)
+            assert abs(num - dbs[l][c]) <= 1e-5 * max(1.0, abs(num)), (l, c, num, dbs[l][c])
+
+
+def test_chain_matches_stack_for_max_blocks(oracle_mod):
+    rng = np.random.default_rng(43)
+    x = oracle_mod.round_to_bf16(rng.normal(size=(1, 8, 8, 8, 4)))
+    ws = [oracle_mod.round_to_bf16(rng.normal(0, 0.2, size=(8, 3, 3, 3, 4))),
+          oracle_mod.round_to_bf16(rng.normal(0, 0.1, size=(16, 3, 3, 3, 8)))]
+    bs = [rng.normal(size=8), rng.normal(size=16)]
+    dy = rng.normal(size=(1, 2, 2, 2, 16))
+    specs = [(1, "max"), (1, "max")]
+    xs, ys, auxs = oracle_mod.chain_fwd(x, ws, bs, 0.3, specs)
+    sx, _, sy, sidx = oracle_mod.stack_fwd(x, ws, bs, 0.3)
+    dws, dbs, dzs = oracle_mod.chain_bwd(xs, ys, auxs, ws, dy, 0.3, specs)
+    sdw, sdb, sdz, _ = oracle_mod.stack_bwd(sx, sy, sidx, ws, dy, 0.3)
+    for a, b in zip(ys + dws + dbs + dzs, sy + sdw + sdb + sdz):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_table1_specs_reproduce_the_flop_rows():
+    """The Table I chain specs (stride-2 c4, pooling while the width allows)
+    give the printed forward FLOPs per sample."""
+    import oracle
+    from cnn_conv3d_gb300 import flops
+    for wi in (128, 256, 512):
+        specs = oracle.table1_specs(wi)
+        s, tot = wi, 0
+        for l, (stride, pool) in enumerate(specs):
+            s //= stride
+            tot += flops.conv_flops(1, oracle.TABLE1_CHANNELS[l], oracle.TABLE1_CHANNELS[l + 1], s ** 3)
+            if pool != "none":
+                s //= 2
+        assert tot == flops.p3_table1_forward_flops(wi)
+        assert s == 2  # 256 x 2^3 = 2048 inputs of fc1
