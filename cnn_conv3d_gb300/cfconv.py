@@ -24,15 +24,17 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 CF_OK, CF_ERR_INVALID_ARG, CF_ERR_UNSUPPORTED, CF_ERR_WORKSPACE, CF_ERR_CUDA, CF_ERR_TIMEOUT = range(6)
 CF_OP_FWD, CF_OP_DGRAD, CF_OP_WGRAD, CF_OP_DGRAD_ROUTED, CF_OP_WGRAD_ROUTED, CF_OP_POOL_BWD = range(6)
+CF_POOL_MAX, CF_POOL_AVG, CF_POOL_NONE = range(3)
 
 
 class cf_conv_desc(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("d", ctypes.c_int64), ("h", ctypes.c_int64), ("w", ctypes.c_int64),
-                ("c_in", ctypes.c_int32), ("c_out", ctypes.c_int32)]
+                ("c_in", ctypes.c_int32), ("c_out", ctypes.c_int32), ("stride", ctypes.c_int32)]
 
 
 class cf_pool_epi(ctypes.Structure):
-    _fields_ = [("bias", ctypes.c_void_p), ("slope", ctypes.c_float), ("argmax", ctypes.c_void_p)]
+    _fields_ = [("bias", ctypes.c_void_p), ("slope", ctypes.c_float), ("argmax", ctypes.c_void_p),
+                ("pool", ctypes.c_int32)]
 
 
 class CfError(RuntimeError):
@@ -54,6 +56,9 @@ _SIGS = {
                                ctypes.c_int),
     "cf_bias_lrelu_pool_bwd_noalloc": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp],
                                        ctypes.c_int),
+    "cf_block_epilogue_fwd": ([_i32, _i64, _i64, _i64, _i64, _i32, _vp, _vp, _f32, _vp, _vp, _vp], ctypes.c_int),
+    "cf_block_epilogue_bwd": ([_i32, _i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _sz,
+                               _vp], ctypes.c_int),
     "cf_workspace_size": ([ctypes.c_int, _DP], _sz),
     "cf_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "cf_last_device_status": ([_vp], ctypes.c_int),
@@ -90,10 +95,11 @@ def _stream(s):
 
 
 def _desc(d):
+    """cf_conv_desc, or a tuple (n, d, h, w, c_in, c_out[, stride])."""
     if isinstance(d, cf_conv_desc):
         return d
-    n, dd, h, w, ci, co = d
-    return cf_conv_desc(n, dd, h, w, ci, co)
+    n, dd, h, w, ci, co = d[:6]
+    return cf_conv_desc(n, dd, h, w, ci, co, d[6] if len(d) > 6 else 1)
 
 
 def _check(st, what):
@@ -111,12 +117,12 @@ def cf_workspace_size(op: int, desc) -> int:
 
 
 def cf_conv3d_fwd(desc, x, w, epi, y, ws=None, ws_bytes=0, stream=None, check=True):
-    """epi: None, or (bias, slope, argmax) / cf_pool_epi."""
+    """epi: None, or (bias, slope, argmax[, pool]) / cf_pool_epi."""
     e = None
     if epi is not None:
         if not isinstance(epi, cf_pool_epi):
-            b, slope, am = epi
-            epi = cf_pool_epi(_ptr(b), float(slope), _ptr(am))
+            b, slope, am = epi[:3]
+            epi = cf_pool_epi(_ptr(b), float(slope), _ptr(am), epi[3] if len(epi) > 3 else CF_POOL_MAX)
         e = ctypes.byref(epi)
     st = _lib.cf_conv3d_fwd(ctypes.byref(_desc(desc)), _ptr(x), _ptr(w), e, _ptr(y), _ptr(ws), ws_bytes,
                             _stream(stream))
@@ -152,6 +158,19 @@ def cf_bias_lrelu_pool_bwd_noalloc(n, d, h, w, c, dy, y, idx, slope, dz, dy_pre,
     st = _lib.cf_bias_lrelu_pool_bwd_noalloc(n, d, h, w, c, _ptr(dy), _ptr(y), _ptr(idx), float(slope), _ptr(dz),
                                              _ptr(dy_pre), _ptr(dbias), _stream(stream))
     return _check(st, "cf_bias_lrelu_pool_bwd_noalloc") if check else st
+
+
+def cf_block_epilogue_fwd(pool, n, d, h, w, c, z, bias, slope, y, aux, stream=None, check=True):
+    st = _lib.cf_block_epilogue_fwd(int(pool), n, d, h, w, c, _ptr(z), _ptr(bias), float(slope), _ptr(y), _ptr(aux),
+                                    _stream(stream))
+    return _check(st, "cf_block_epilogue_fwd") if check else st
+
+
+def cf_block_epilogue_bwd(pool, n, d, h, w, c, dy, y, aux, slope, dz, dy_pre, dbias, ws=None, ws_bytes=0,
+                          stream=None, check=True):
+    st = _lib.cf_block_epilogue_bwd(int(pool), n, d, h, w, c, _ptr(dy), _ptr(y), _ptr(aux), float(slope), _ptr(dz),
+                                    _ptr(dy_pre), _ptr(dbias), _ptr(ws), ws_bytes, _stream(stream))
+    return _check(st, "cf_block_epilogue_bwd") if check else st
 
 
 def cf_last_device_status(stream=None) -> int:

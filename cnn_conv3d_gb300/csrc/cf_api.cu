@@ -59,9 +59,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+int desc_stride(const cf_conv_desc* d) { return d->stride == 2 ? 2 : 1; }
+
 bool desc_ok(const cf_conv_desc* d) {
     if (d == nullptr) return false;
     if (d->n <= 0 || d->d <= 0 || d->h <= 0 || d->w <= 0 || d->c_in <= 0 || d->c_out <= 0) return false;
+    if (d->stride < 0 || d->stride > 2) return false;
     // every index the kernels form stays below 2^31 per dimension and 2^62 in total
     if (d->d > (1 << 20) || d->h > (1 << 20) || d->w > (1 << 20) || d->n > (1 << 24)) return false;
     const double elems = (double)d->n * d->d * d->h * d->w * (double)(d->c_in > d->c_out ? d->c_in : d->c_out);
@@ -70,10 +73,17 @@ bool desc_ok(const cf_conv_desc* d) {
 
 int64_t dense_grad_elems(const cf_conv_desc* d) { return d->n * d->d * d->h * d->w * (int64_t)d->c_out; }
 
+// Workspace bytes of the zero-inserted output gradient of a stride-2 conv
+// (input sizes x c_out bf16), 0 for stride 1.
+size_t upsample_bytes(const cf_conv_desc* d) {
+    return desc_stride(d) == 2 ? round_up((size_t)dense_grad_elems(d) * 2, 256) : 0;
+}
+
 }  // namespace
 
 bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz,
+                 const uint32_t* elem_strides) {
     if (g_encode == nullptr) return false;
     cuuint64_t gd[5];
     cuuint64_t gs[4];
@@ -81,7 +91,7 @@ bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* b
     for (int i = 0; i < rank; ++i) {
         gd[i] = dims[i];
         bx[i] = box[i];
-        es[i] = 1;
+        es[i] = elem_strides ? elem_strides[i] : 1;
         if (i < rank - 1) gs[i] = strides_bytes[i];
     }
     CUresult r = g_encode(m, dt, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -149,11 +159,12 @@ size_t cf_workspace_size(int op, const cf_conv_desc* desc) {
     const size_t dense = round_up((size_t)dense_grad_elems(desc) * 2, 256);
     const size_t part = round_up(
         wgrad_workspace_bytes(ctx.num_sms, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out), 256);
+    const size_t up = upsample_bytes(desc);
     switch (op) {
         case CF_OP_FWD: return 0;
-        case CF_OP_DGRAD: return wt + dgrad_sum_bytes(ctx.num_sms, desc->c_in);
+        case CF_OP_DGRAD: return wt + dgrad_sum_bytes(ctx.num_sms, desc->c_in) + up;
         case CF_OP_DGRAD_ROUTED: return wt + dgrad_sum_bytes(ctx.num_sms, desc->c_in) + dense;
-        case CF_OP_WGRAD: return part;
+        case CF_OP_WGRAD: return part + up;
         case CF_OP_WGRAD_ROUTED: return part + (wgrad_routed_fused(desc->c_in) ? 0 : dense);
         case CF_OP_POOL_BWD: return round_up(pool_bwd_workspace_bytes(ctx.num_sms, desc->c_out), 256);
     }
@@ -166,25 +177,38 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
     (void)ws_bytes;
     if (!desc_ok(desc) || x == nullptr || w == nullptr || y == nullptr) return CF_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return CF_ERR_INVALID_ARG;
+    const int stride = desc_stride(desc);
+    const int pool = epi ? epi->pool : CF_POOL_NONE;
     if (epi != nullptr) {
+        if (pool < CF_POOL_MAX || pool > CF_POOL_NONE) return CF_ERR_INVALID_ARG;
         if ((epi->bias && !aligned16(epi->bias)) || (epi->argmax && !aligned16(epi->argmax)))
             return CF_ERR_INVALID_ARG;
-        if ((desc->d | desc->h | desc->w) & 1) return CF_ERR_UNSUPPORTED;
+        const int64_t od = (desc->d + stride - 1) / stride, oh = (desc->h + stride - 1) / stride,
+                      ow = (desc->w + stride - 1) / stride;
+        if (pool != CF_POOL_NONE && ((od | oh | ow) & 1)) return CF_ERR_UNSUPPORTED;
     }
     const int ci = desc->c_in, co = desc->c_out;
     const bool small = ci == 1 || ci == 4;
     if (!small && ci % 16 != 0) return CF_ERR_UNSUPPORTED;
+    if (small && stride != 1) return CF_ERR_UNSUPPORTED;
     LaunchCtx ctx;
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
-    const int mode = epi ? EPI_POOL : EPI_PLAIN;
+    // epilogue: pooled (max / average), or plain with the optional activation
+    const bool pooled = epi != nullptr && pool != CF_POOL_NONE;
+    const int mode = pooled ? EPI_POOL : EPI_PLAIN;
+    const int pool_kind = pool == CF_POOL_AVG ? 1 : 0;
+    const int act = epi != nullptr && pool == CF_POOL_NONE ? 1 : 0;
     const float* bias = epi ? epi->bias : nullptr;
-    uint8_t* idx = epi ? epi->argmax : nullptr;
+    uint8_t* idx = pooled ? epi->argmax : nullptr;
     const float slope = epi ? epi->slope : 0.f;
-    if (small) return launch_conv_smallc(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, slope);
-    if (halo_path_supported(ci, co))
+    if (small)
+        return launch_conv_smallc(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, slope,
+                                  pool_kind, act);
+    if (stride == 1 && halo_path_supported(ci, co))
         return launch_conv_halo(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, nullptr,
-                                slope);
-    return launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, nullptr, slope);
+                                slope, nullptr, pool_kind, act);
+    return launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, nullptr, slope,
+                             pool_kind, act, stride);
 }
 
 cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx, const uint16_t* w,
@@ -197,17 +221,27 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
     const int ci = desc->c_in, co = desc->c_out;
     if (co % 16 != 0 || ci % 16 != 0) return CF_ERR_UNSUPPORTED;
     if (idx && ((desc->d | desc->h | desc->w) & 1)) return CF_ERR_UNSUPPORTED;
+    const int stride = desc_stride(desc);
+    if (stride == 2 && idx) return CF_ERR_UNSUPPORTED;
     LaunchCtx ctx;
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
     const size_t wt_bytes = round_up((size_t)co * 27 * ci * 2, 256);
     const size_t sum_bytes = dgrad_sum_bytes(ctx.num_sms, ci);
-    const size_t need = wt_bytes + sum_bytes + (idx ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0);
+    const size_t need = wt_bytes + sum_bytes + (idx ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0) +
+                        upsample_bytes(desc);
     if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
     uint16_t* wt = static_cast<uint16_t*>(ws);
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wt_bytes);
     cf_status st = launch_flip_transpose(ctx, co, ci, w, wt);
     if (st != CF_OK) return st;
     const uint16_t* dz_dense = dz;
+    if (stride == 2) {
+        // zeros at the odd positions: the stride-2 backward as a stride-1 one
+        uint16_t* buf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + wt_bytes + sum_bytes);
+        st = launch_upsample2(ctx, desc->n, desc->d, desc->h, desc->w, co, dz, buf);
+        if (st != CF_OK) return st;
+        dz_dense = buf;
+    }
     if (idx) {
         uint16_t* buf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + wt_bytes + sum_bytes);
         st = launch_pool_bwd(ctx, desc->n, desc->d, desc->h, desc->w, co, dz, nullptr, idx, 1.f, buf, nullptr,
@@ -242,13 +276,23 @@ cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uin
     if (!aligned16(x) || !aligned16(dz) || !aligned16(dw) || (idx && !aligned16(idx)) || (ws && !aligned16(ws)))
         return CF_ERR_INVALID_ARG;
     if (idx && ((desc->d | desc->h | desc->w) & 1)) return CF_ERR_UNSUPPORTED;
+    const int stride = desc_stride(desc);
+    if (stride == 2 && (idx || desc->c_in == 1 || desc->c_in == 4)) return CF_ERR_UNSUPPORTED;
     LaunchCtx ctx;
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
     const size_t part = round_up(
         wgrad_workspace_bytes(ctx.num_sms, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out), 256);
     const bool fused = idx && wgrad_routed_fused(desc->c_in);
-    const size_t need = part + (idx && !fused ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0);
+    const size_t need = part + (idx && !fused ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0) +
+                        upsample_bytes(desc);
     if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
+    if (stride == 2) {
+        uint16_t* buf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + part);
+        cf_status st = launch_upsample2(ctx, desc->n, desc->d, desc->h, desc->w, desc->c_out, dz, buf);
+        if (st != CF_OK) return st;
+        return launch_wgrad(ctx, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out, x, buf, nullptr, dw,
+                            accumulate, ws, part);
+    }
     if (fused)
         return launch_wgrad(ctx, desc->n, desc->d, desc->h, desc->w, desc->c_in, desc->c_out, x, dz, idx, dw,
                             accumulate, ws, part);
@@ -287,6 +331,41 @@ cf_status cf_bias_lrelu_pool_bwd(int64_t n, int64_t d, int64_t h, int64_t w, int
     LaunchCtx ctx;
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
     return launch_pool_bwd(ctx, n, d, h, w, c, dy, y, idx, slope, dz, dy_pre, dbias, ws, ws_bytes);
+}
+
+cf_status cf_block_epilogue_fwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                                const uint16_t* z, const float* bias, float slope, uint16_t* y, uint8_t* aux,
+                                void* stream) {
+    if (n <= 0 || d <= 0 || h <= 0 || w <= 0 || c <= 0 || z == nullptr || y == nullptr) return CF_ERR_INVALID_ARG;
+    if (pool < CF_POOL_MAX || pool > CF_POOL_NONE) return CF_ERR_INVALID_ARG;
+    if (!aligned16(z) || !aligned16(y) || (bias && !aligned16(bias)) || (aux && !aligned16(aux)))
+        return CF_ERR_INVALID_ARG;
+    if (c % 8 != 0 || (pool != CF_POOL_NONE && ((d | h | w) & 1))) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    if (pool == CF_POOL_MAX) return launch_pool_fwd(ctx, n, d, h, w, c, z, bias, slope, y, aux);
+    if (pool == CF_POOL_AVG) return launch_avgpool_fwd(ctx, n, d, h, w, c, z, bias, slope, y, aux);
+    return launch_act_fwd(ctx, n * d * h * w * c, c, z, bias, slope, y);
+}
+
+cf_status cf_block_epilogue_bwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                                const uint16_t* dy, const uint16_t* y, const uint8_t* aux, float slope,
+                                uint16_t* dz, uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes,
+                                void* stream) {
+    if (pool == CF_POOL_MAX)
+        return cf_bias_lrelu_pool_bwd(n, d, h, w, c, dy, y, aux, slope, dz, dy_pre, dbias, ws, ws_bytes, stream);
+    if (n <= 0 || d <= 0 || h <= 0 || w <= 0 || c <= 0 || dy == nullptr) return CF_ERR_INVALID_ARG;
+    if (pool != CF_POOL_AVG && pool != CF_POOL_NONE) return CF_ERR_INVALID_ARG;
+    if (dy_pre != nullptr) return CF_ERR_INVALID_ARG;  // max pooling only
+    if (pool == CF_POOL_AVG && aux == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(dy) || (y && !aligned16(y)) || (aux && !aligned16(aux)) || (dz && !aligned16(dz)) ||
+        (dbias && !aligned16(dbias)) || (ws && !aligned16(ws)))
+        return CF_ERR_INVALID_ARG;
+    if (c % 8 != 0 || c > 2048 || (pool == CF_POOL_AVG && ((d | h | w) & 1))) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    if (pool == CF_POOL_AVG) return launch_avgpool_bwd(ctx, n, d, h, w, c, dy, aux, slope, dz, dbias, ws, ws_bytes);
+    return launch_act_bwd(ctx, n * d * h * w * c, c, dy, y, slope, dz, dbias, ws, ws_bytes);
 }
 
 }  // extern "C"

@@ -38,32 +38,40 @@ struct TileGeom {
 };
 TileGeom choose_tile(int64_t d, int64_t h, int64_t w);
 
-// Encodes a tiled TMA descriptor; returns false on failure.
+// Encodes a tiled TMA descriptor; returns false on failure.  elem_strides:
+// traversal stride per dimension (NULL = 1 everywhere); along a dimension with
+// stride s the box loads ceil(box / s) elements, every s-th one.
 bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz,
+                 const uint32_t* elem_strides = nullptr);
 
 // conv_fwd.cu ---------------------------------------------------------------
-// Generic implicit-GEMM conv (c_in a multiple of 32): out = conv(x, wk) where
+// Generic implicit-GEMM conv (c_in a multiple of 16): out = conv(x, wk) where
 // wk is [c_out][27][c_in] (K-major GEMM B operand).  EPI_POOL writes the pooled
-// block output and argmax; EPI_DGRAD multiplies by LReLU'(x_act).
+// block output and argmax codes (pool_kind 0) or the average of the activated
+// window and its sign masks (pool_kind 1); EPI_PLAIN stores z, or LReLU(z + b)
+// with act = 1; EPI_DGRAD multiplies by LReLU'(x_act).  n, d, h, w are the
+// input sizes; stride 2 computes the output at the even input positions,
+// (d + 1) / 2 ... per dimension.
 cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                             int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
-                            uint8_t* idx, const float* bias, const uint16_t* x_act, float slope);
+                            uint8_t* idx, const float* bias, const uint16_t* x_act, float slope,
+                            int pool_kind = 0, int act = 0, int stride = 1);
 
-// conv_halo.cu: same contract as launch_conv_igemm for c_in % 32 == 0 and
-// c_out in {32, 64, 128}, reading A from one halo tile per channel chunk.
+// conv_halo.cu: same contract as launch_conv_igemm (stride 1) for c_in % 16 == 0
+// and c_out in {32, 64, 128}, reading A from one halo tile per channel chunk.
 bool halo_path_supported(int c_in, int c_out);
 // colsum_part (unpooled epilogues, c_out <= 32): [grid][c_out] channel sums of
 // the stored outputs, one row per CTA (grid <= SM count), or NULL.
 cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                            int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
                            uint8_t* idx, const float* bias, const uint16_t* x_act, float slope,
-                           float* colsum_part = nullptr);
+                           float* colsum_part = nullptr, int pool_kind = 0, int act = 0);
 
 // conv_smallc.cu: forward conv for c_in in {1,4} (im2col operand in tensor memory).
 cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                              int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
-                             uint8_t* idx, const float* bias, float slope);
+                             uint8_t* idx, const float* bias, float slope, int pool_kind = 0, int act = 0);
 
 // conv_wgrad_halo.cu: backward weight reading the input once per K block as a
 // halo tile (c_in 32 with c_out 32/64/128, c_in 64 with c_out 64/128); writes
@@ -90,6 +98,23 @@ cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
                           const uint16_t* dy, const uint16_t* y, const uint8_t* idx, float slope, uint16_t* dz,
                           uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes);
 cf_status launch_flip_transpose(const LaunchCtx& ctx, int c_out, int c_in, const uint16_t* w, uint16_t* wt);
+// Page variants of the block epilogue as standalone kernels: average pooling
+// of the activated window (y and sign masks), the unpooled activation, and
+// their backward passes (dz from dy and the masks / the output, bias-gradient
+// partials [blocks][c] in `partial`, reduced by colsum).
+cf_status launch_avgpool_fwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                             const uint16_t* z, const float* bias, float slope, uint16_t* y, uint8_t* mask);
+cf_status launch_avgpool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                             const uint16_t* dy, const uint8_t* mask, float slope, uint16_t* dz, float* dbias,
+                             void* ws, size_t ws_bytes);
+cf_status launch_act_fwd(const LaunchCtx& ctx, int64_t count, int c, const uint16_t* z, const float* bias,
+                         float slope, uint16_t* y);
+cf_status launch_act_bwd(const LaunchCtx& ctx, int64_t count, int c, const uint16_t* dy, const uint16_t* y,
+                         float slope, uint16_t* dz, float* dbias, void* ws, size_t ws_bytes);
+// Zero insertion for the stride-2 backward: out [n][d][h][w][c] holds
+// dz [n][(d+1)/2][(h+1)/2][(w+1)/2][c] at the even positions, zeros elsewhere.
+cf_status launch_upsample2(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                           const uint16_t* dz, uint16_t* out);
 // out[ch] = sum over `rows` of partial[row][ch] (fixed order)
 cf_status launch_colsum(const LaunchCtx& ctx, const float* partial, int rows, int c, float* out);
 // out[ch] = sum over the rows of x [rows][c] bf16 (fixed order); partial holds

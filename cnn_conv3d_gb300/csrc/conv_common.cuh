@@ -68,7 +68,15 @@ struct EpiArgs {
     // backward-data only: per-CTA channel sums of the stored outputs,
     // [gridDim.x][C] fp32 (rows of CTAs without tiles stay as they were), or NULL
     float* colsum_part = nullptr;
+    // EPI_POOL: 0 = max-pool of the pre-activation (idx: first-maximum codes),
+    // 1 = average of the activated window (idx: sign masks, bit dd*4+dh*2+dw
+    // set where z + b > 0)
+    int pool_kind = 0;
+    // EPI_PLAIN: 1 = y = LReLU(z + b) (an unpooled block), 0 = y = z
+    int act = 0;
 };
+
+__device__ __forceinline__ float lrelu(float s, float slope) { return s > 0.f ? s : slope * s; }
 
 // Epilogue of one tile, executed by the 128 epilogue threads (4 warps whose
 // warp index modulo 4 is q; thread row = 32*q + lane is TMEM lane = GEMM row).
@@ -112,6 +120,24 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
                 uint32_t codes = 0;
 #pragma unroll
                 for (int cc = 0; cc < CPT; ++cc) {
+                    const int co = tc.co0 + c + cb + cc;
+                    const float b = (ea.bias != nullptr && co < g.Cout) ? ea.bias[co] : 0.f;
+                    if (ea.pool_kind == 1) {
+                        // average of the activated window; code = the window's sign mask
+                        float sum = 0.f;
+                        int mask = 0;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+                            const int rr = (dd * g.th + 2 * ph_l + dh) * g.tw + 2 * pw_l + dw;
+                            const float s = stg[rr * 33 + cb + cc] + b;
+                            mask |= (s > 0.f ? 1 : 0) << k;
+                            sum += lrelu(s, ea.slope);
+                        }
+                        yv[cc] = sum * 0.125f;
+                        codes |= (uint32_t)mask << (8 * cc);
+                        continue;
+                    }
                     float m = 0.f;
                     int code = 0;
 #pragma unroll
@@ -124,9 +150,7 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
                             code = k;
                         }
                     }
-                    const int co = tc.co0 + c + cb + cc;
-                    const float s = m + ((ea.bias != nullptr && co < g.Cout) ? ea.bias[co] : 0.f);
-                    yv[cc] = s > 0.f ? s : ea.slope * s;
+                    yv[cc] = lrelu(m + b, ea.slope);
                     codes |= (uint32_t)code << (8 * cc);
                 }
                 const int co_first = tc.co0 + c + cb;
@@ -152,6 +176,11 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
                 float v[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(r[q8 * 8 + k]);
+                if (EPI == EPI_PLAIN && ea.act) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        v[k] = lrelu(v[k] + (ea.bias ? ea.bias[tc.co0 + c + q8 * 8 + k] : 0.f), ea.slope);
+                }
                 if (EPI == EPI_DGRAD) {
                     const uint4 xa = *reinterpret_cast<const uint4*>(ea.x_act + o + q8 * 8);
                     const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};

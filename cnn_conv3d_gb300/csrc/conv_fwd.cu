@@ -56,8 +56,9 @@ struct IgemmCfg {
 };
 
 struct IgemmParams {
-    ConvGeom g;
+    ConvGeom g;      // output tiling (output sizes)
     int n_cchunks;
+    int stride;      // 1, or 2: tap (kd,kh,kw) of output voxel o reads input voxel 2*o + k - 1
     EpiArgs ea;
     int* status;
     uint64_t wait_ns;
@@ -140,8 +141,8 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     uint8_t* sa = ring + stage * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    tma_load_5d(sa, &tmA, &full[stage], cc * KC, tc.w0 + kw - 1, tc.h0 + kh - 1, tc.d0 + kd - 1,
-                                tc.n);
+                    tma_load_5d(sa, &tmA, &full[stage], cc * KC, p.stride * tc.w0 + kw - 1,
+                                p.stride * tc.h0 + kh - 1, p.stride * tc.d0 + kd - 1, tc.n);
                     tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], t * g.Cin + cc * KC, tc.co0);
                     issued |= 1u << stage;
                     par = (par & ~(1u << stage)) | (phase << stage);
@@ -244,19 +245,25 @@ TileGeom choose_tile(int64_t d, int64_t h, int64_t w) {
     return t;
 }
 
+// in_d, in_h, in_w: the input sizes (the output's times the stride, rounded
+// up).  With stride 2 the A box spans 2*tw x 2*th x 2*td input voxels and the
+// tensor map's traversal stride 2 loads every second one: the same dense
+// tw x th x td x KC tile as stride 1.
 template <int BN, int KC, int EPI>
 static cf_status run_igemm(const LaunchCtx& ctx, const ConvGeom& g, const uint16_t* x, const uint16_t* wk,
-                           const EpiArgs& ea) {
+                           const EpiArgs& ea, int64_t in_d, int64_t in_h, int64_t in_w, int stride) {
     using C = IgemmCfg<BN, KC, EPI>;
     CUtensorMap ta, tb;
-    const uint64_t da[5] = {(uint64_t)g.Cin, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.D, (uint64_t)g.N};
-    const uint64_t sa[4] = {(uint64_t)g.Cin * 2, (uint64_t)g.W * g.Cin * 2, (uint64_t)g.H * g.W * g.Cin * 2,
-                            (uint64_t)g.D * g.H * g.W * g.Cin * 2};
-    const uint32_t ba[5] = {(uint32_t)KC, (uint32_t)g.tw, (uint32_t)g.th, (uint32_t)g.td, 1u};
+    const uint64_t da[5] = {(uint64_t)g.Cin, (uint64_t)in_w, (uint64_t)in_h, (uint64_t)in_d, (uint64_t)g.N};
+    const uint64_t sa[4] = {(uint64_t)g.Cin * 2, (uint64_t)in_w * g.Cin * 2, (uint64_t)in_h * in_w * g.Cin * 2,
+                            (uint64_t)in_d * in_h * in_w * g.Cin * 2};
+    const uint32_t su = (uint32_t)stride;
+    const uint32_t ba[5] = {(uint32_t)KC, su * g.tw, su * g.th, su * g.td, 1u};
+    const uint32_t es[5] = {1u, su, su, su, 1u};
     const CUtensorMapSwizzle swz = KC == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : KC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
                                               : CU_TENSOR_MAP_SWIZZLE_32B;
-    if (!encode_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, da, sa, ba, swz)) return CF_ERR_CUDA;
+    if (!encode_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, da, sa, ba, swz, es)) return CF_ERR_CUDA;
     const uint64_t db[2] = {(uint64_t)27 * g.Cin, (uint64_t)g.Cout};
     const uint64_t sb[1] = {(uint64_t)27 * g.Cin * 2};
     const uint32_t bb[2] = {(uint32_t)KC, (uint32_t)BN};
@@ -265,6 +272,7 @@ static cf_status run_igemm(const LaunchCtx& ctx, const ConvGeom& g, const uint16
     IgemmParams p;
     p.g = g;
     p.n_cchunks = g.Cin / KC;
+    p.stride = stride;
     p.ea = ea;
     p.status = ctx.status;
     p.wait_ns = ctx.wait_ns;
@@ -278,19 +286,25 @@ static cf_status run_igemm(const LaunchCtx& ctx, const ConvGeom& g, const uint16
 
 template <int BN, int KC>
 static cf_status dispatch_epi(const LaunchCtx& ctx, const ConvGeom& g, const uint16_t* x, const uint16_t* wk,
-                              int epi, const EpiArgs& ea) {
+                              int epi, const EpiArgs& ea, int64_t in_d, int64_t in_h, int64_t in_w, int stride) {
     switch (epi) {
-        case EPI_PLAIN: return run_igemm<BN, KC, EPI_PLAIN>(ctx, g, x, wk, ea);
-        case EPI_POOL: return run_igemm<BN, KC, EPI_POOL>(ctx, g, x, wk, ea);
-        case EPI_DGRAD: return run_igemm<BN, KC, EPI_DGRAD>(ctx, g, x, wk, ea);
+        case EPI_PLAIN: return run_igemm<BN, KC, EPI_PLAIN>(ctx, g, x, wk, ea, in_d, in_h, in_w, stride);
+        case EPI_POOL: return run_igemm<BN, KC, EPI_POOL>(ctx, g, x, wk, ea, in_d, in_h, in_w, stride);
+        case EPI_DGRAD: return run_igemm<BN, KC, EPI_DGRAD>(ctx, g, x, wk, ea, in_d, in_h, in_w, stride);
     }
     return CF_ERR_INVALID_ARG;
 }
 
 cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                             const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
-                            const float* bias, const uint16_t* x_act, float slope) {
+                            const float* bias, const uint16_t* x_act, float slope, int pool_kind, int act,
+                            int stride) {
     if (c_in % 16 != 0 || c_out % 16 != 0) return CF_ERR_UNSUPPORTED;
+    if (stride != 1 && (stride != 2 || epi == EPI_DGRAD)) return CF_ERR_UNSUPPORTED;
+    const int64_t in_d = d, in_h = h, in_w = w;
+    d = (d + stride - 1) / stride;  // from here on: the output sizes
+    h = (h + stride - 1) / stride;
+    w = (w + stride - 1) / stride;
     int bn = c_out <= 256 ? c_out : 256;
     if (c_out > 256 && c_out % 256 != 0) return CF_ERR_UNSUPPORTED;
     // Small grids: narrower N tiles when that clearly shortens the critical
@@ -311,12 +325,14 @@ cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
     }
     const int kc = (c_in % 64 == 0) ? 64 : (c_in % 32 == 0 ? 32 : 16);
     EpiArgs ea{y, idx, bias, x_act, slope};
+    ea.pool_kind = pool_kind;
+    ea.act = act;
     ConvGeom g = make_geom(n, d, h, w, c_in, c_out, bn);
-#define CF_BN_CASE(B)                                                                       \
-    case B:                                                                                 \
-        return kc == 64   ? dispatch_epi<B, 64>(ctx, g, x, wk, epi, ea)                     \
-               : kc == 32 ? dispatch_epi<B, 32>(ctx, g, x, wk, epi, ea)                     \
-                          : dispatch_epi<B, 16>(ctx, g, x, wk, epi, ea);
+#define CF_BN_CASE(B)                                                                              \
+    case B:                                                                                        \
+        return kc == 64   ? dispatch_epi<B, 64>(ctx, g, x, wk, epi, ea, in_d, in_h, in_w, stride)  \
+               : kc == 32 ? dispatch_epi<B, 32>(ctx, g, x, wk, epi, ea, in_d, in_h, in_w, stride)  \
+                          : dispatch_epi<B, 16>(ctx, g, x, wk, epi, ea, in_d, in_h, in_w, stride);
     switch (bn) {
         CF_BN_CASE(16)
         CF_BN_CASE(32)

@@ -341,7 +341,8 @@ bool halo_path_supported(int c_in, int c_out) {
 
 cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                            const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
-                           const float* bias, const uint16_t* x_act, float slope, float* colsum_part) {
+                           const float* bias, const uint16_t* x_act, float slope, float* colsum_part, int pool_kind,
+                           int act) {
     if (!halo_path_supported(c_in, c_out)) return CF_ERR_UNSUPPORTED;
     if (colsum_part && (epi == EPI_POOL || c_out > 32)) return CF_ERR_UNSUPPORTED;
     HaloParams p;
@@ -359,6 +360,8 @@ cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
     set_tile_dividers(p);
     p.n_chunks = 0;
     p.ea = EpiArgs{y, idx, bias, x_act, slope, colsum_part};
+    p.ea.pool_kind = pool_kind;
+    p.ea.act = act;
     p.status = ctx.status;
     p.wait_ns = ctx.wait_ns;
     // The whole filter stays in shared memory when it fits beside two halo

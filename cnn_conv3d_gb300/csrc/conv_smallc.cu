@@ -365,6 +365,33 @@ __global__ void __launch_bounds__(608, 1)
                         if (lane == 0) mbar_arrive(&tempty[acc]);
                         released = true;
                     }
+                    float y[8];
+                    uint32_t codes[2] = {0u, 0u};
+                    if (p.ea.pool_kind == 1) {
+                        // average of the activated window: the lane's four (plane, line)
+                        // values, then the partner lane's (the w neighbour); code = the
+                        // window's sign mask, bit dd*4 + dh*2 + dw
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc) {
+                            const int co = co0 + c + cc;
+                            const float b = (p.ea.bias != nullptr && co < p.Cout) ? __ldg(p.ea.bias + co) : 0.f;
+                            const float s0 = __uint_as_float(r0[cc]) + b, s1 = __uint_as_float(r1[cc]) + b;
+                            const float s2 = __uint_as_float(r2[cc]) + b, s3 = __uint_as_float(r3[cc]) + b;
+                            m[cc] = (lrelu(s0, p.ea.slope) + lrelu(s1, p.ea.slope)) +
+                                    (lrelu(s2, p.ea.slope) + lrelu(s3, p.ea.slope));
+                            k[cc] = ((s0 > 0.f ? 1 : 0) << dw) | ((s1 > 0.f ? 1 : 0) << (2 + dw)) |
+                                    ((s2 > 0.f ? 1 : 0) << (4 + dw)) | ((s3 > 0.f ? 1 : 0) << (6 + dw));
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float kv = dw ? m[8 + i] : m[i];
+                            const int kk = dw ? k[8 + i] : k[i];
+                            const float ov = __shfl_xor_sync(0xffffffffu, dw ? m[i] : m[8 + i], 1);
+                            const int ok2 = __shfl_xor_sync(0xffffffffu, dw ? k[i] : k[8 + i], 1);
+                            y[i] = (kv + ov) * 0.125f;
+                            codes[i >> 2] |= (uint32_t)(kk | ok2) << (8 * (i & 3));
+                        }
+                    } else {
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
                         const float v0 = __uint_as_float(r0[cc]), v1 = __uint_as_float(r1[cc]);
@@ -387,8 +414,6 @@ __global__ void __launch_bounds__(608, 1)
                     // lane pair (dw = 0, 1): each keeps 8 channels and takes the
                     // partner's values for them; larger value wins, ties keep the
                     // smaller code
-                    float y[8];
-                    uint32_t codes[2] = {0u, 0u};
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         float kv = dw ? m[8 + i] : m[i];
@@ -404,6 +429,7 @@ __global__ void __launch_bounds__(608, 1)
                         const float s = kv + bias[ps][i];
                         y[i] = s > 0.f ? s : p.ea.slope * s;
                         codes[i >> 2] |= (uint32_t)kk << (8 * (i & 3));
+                    }
                     }
                     const int D2 = p.D >> 1, H2 = p.H >> 1, W2 = p.W >> 1;
                     const int pd = t.d0 >> 1, ph = (t.h0 >> 1) + lp, pw = (t.w0 + v) >> 1;
@@ -424,6 +450,14 @@ __global__ void __launch_bounds__(608, 1)
                         const int d = t.d0 + (blk >> 1), h = t.h0 + 2 * lp + (blk & 1), w = t.w0 + v;
                         if (d >= p.D || h >= p.H || w >= p.W) continue;
                         const int64_t o = ((((int64_t)t.n * p.D + d) * p.H + h) * p.W + w) * p.Cout + co0 + c;
+                        if (p.ea.act) {  // unpooled block: bias + leaky ReLU
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const int co = co0 + c + q;
+                                const float b = (p.ea.bias != nullptr && co < p.Cout) ? __ldg(p.ea.bias + co) : 0.f;
+                                r[q] = __float_as_uint(lrelu(__uint_as_float(r[q]) + b, p.ea.slope));
+                            }
+                        }
 #pragma unroll
                         for (int q8 = 0; q8 < 2; ++q8) {
                             if (co0 + c + 8 * q8 >= p.Cout) break;
@@ -488,7 +522,7 @@ static cf_status smallc_epi(const LaunchCtx& ctx, const HaloParams& hp, const ui
 
 cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                              const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
-                             const float* bias, float slope) {
+                             const float* bias, float slope, int pool_kind, int act) {
     if (c_out % 8 != 0 || c_out > 256) return CF_ERR_UNSUPPORTED;
     if (c_in != 1 && c_in != 4) return CF_ERR_UNSUPPORTED;
     if ((w * c_in) % 8 != 0) return CF_ERR_UNSUPPORTED;  // halo rows must be 16-byte multiples
@@ -510,6 +544,8 @@ cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t
     set_tile_dividers(hp);
     hp.n_chunks = 1;
     hp.ea = EpiArgs{y, idx, bias, nullptr, slope};
+    hp.ea.pool_kind = pool_kind;
+    hp.ea.act = act;
     hp.status = ctx.status;
     hp.wait_ns = ctx.wait_ns;
 #define CF_SC_CASE(B)                                                        \

@@ -251,6 +251,180 @@ __global__ void pool_bwd_dbias_kernel(const uint16_t* __restrict__ dy, float* __
     }
 }
 
+// Average pooling of the activated window (CosmoFlow page, section III-C:
+// constant weights 1/8 for a 2x2x2 window), one thread per pooled voxel x 8
+// channels: y = (1/8) sum LReLU(z + b), mask bit dd*4+dh*2+dw = (z + b > 0).
+__global__ void avgpool_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ bias, float slope,
+                                   uint16_t* __restrict__ y, uint8_t* __restrict__ mask, int64_t N, int D, int H,
+                                   int W, int C, PoolGrid pg) {
+    const int C8 = C / 8, D2 = D / 2, H2 = H / 2, W2 = W / 2;
+    const int64_t total = N * D2 * H2 * W2 * C8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(i % C8);
+        const int64_t pvox = i / C8;
+        int64_t n;
+        int pd, ph, pw;
+        pool_decode(pg, pvox, n, pd, ph, pw);
+        float b[8], sum[8];
+        uint32_t m[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            b[c] = bias ? bias[8 * c8 + c] : 0.f;
+            sum[c] = 0.f;
+            m[c] = 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+            const int64_t o = ((((n * D + 2 * pd + dd) * H + 2 * ph + dh) * W) + 2 * pw + dw) * C + 8 * c8;
+            float f[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(z + o)), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float v = f[c] + b[c];
+                m[c] |= (v > 0.f ? 1u : 0u) << k;
+                sum[c] += v > 0.f ? v : slope * v;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) sum[c] *= 0.125f;
+        const int64_t po = pvox * C + 8 * c8;
+        *reinterpret_cast<uint4*>(y + po) = pack8(sum);
+        if (mask)
+            *reinterpret_cast<uint2*>(mask + po) =
+                make_uint2(m[0] | (m[1] << 8) | (m[2] << 16) | (m[3] << 24), m[4] | (m[5] << 8) | (m[6] << 16) | (m[7] << 24));
+    }
+}
+
+// Backward of the average pool: dz[v] = dy[p] / 8 * LReLU'(z[v] + b) from the
+// sign mask, all eight voxels of each window written; the bias gradient sums
+// the fp32 dz values per thread (fixed channel group, as pool_bwd_kernel).
+__global__ void avgpool_bwd_kernel(const uint16_t* __restrict__ dy, const uint8_t* __restrict__ mask, float slope,
+                                   uint16_t* __restrict__ dz, float* __restrict__ partial, int64_t N, int D, int H,
+                                   int W, int C, PoolGrid pg) {
+    extern __shared__ float red[];  // [blockDim][8]
+    const int C8 = C / 8, D2 = D / 2, H2 = H / 2, W2 = W / 2;
+    const int64_t total = N * D2 * H2 * W2 * C8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int c8 = (int)(threadIdx.x % C8);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t pstep = stride / C8;
+    int64_t pvox = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / C8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += stride, pvox += pstep) {
+        const int64_t po = pvox * C + 8 * c8;
+        float g[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dy + po)), g);
+        const uint2 mv = __ldg(reinterpret_cast<const uint2*>(mask + po));
+        const uint32_t mw[2] = {mv.x, mv.y};
+        int64_t n;
+        int pd, ph, pw;
+        pool_decode(pg, pvox, n, pd, ph, pw);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+            float o[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const bool pos = (mw[c >> 2] >> (8 * (c & 3) + k)) & 1u;
+                o[c] = g[c] * 0.125f * (pos ? 1.f : slope);
+                acc[c] += o[c];
+            }
+            if (dz) {
+                const int64_t zo = ((((n * D + 2 * pd + dd) * H + 2 * ph + dh) * W) + 2 * pw + dw) * C + 8 * c8;
+                *reinterpret_cast<uint4*>(dz + zo) = pack8(o);
+            }
+        }
+    }
+    if (partial) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) red[threadIdx.x * 8 + c] = acc[c];
+        __syncthreads();
+        for (int ch = threadIdx.x; ch < C; ch += blockDim.x) {
+            const int cg = ch / 8, c = ch % 8;
+            float sum = 0.f;
+            for (int t = cg; t < (int)blockDim.x; t += C8) sum += red[t * 8 + c];
+            partial[(int64_t)blockIdx.x * C + ch] = sum;
+        }
+    }
+}
+
+// Unpooled block: y = LReLU(z + b), 8 channels per thread.
+__global__ void act_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ bias, float slope,
+                               uint16_t* __restrict__ y, int64_t total8, int C) {
+    const int C8 = C / 8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(i % C8);
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(z) + i), f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float v = f[c] + (bias ? bias[8 * c8 + c] : 0.f);
+            f[c] = v > 0.f ? v : slope * v;
+        }
+        reinterpret_cast<uint4*>(y)[i] = pack8(f);
+    }
+}
+
+// Its backward: dz = dy * LReLU'(y) (dy as is when y is NULL), bias-gradient
+// partials of the fp32 dz per thread (fixed channel group).
+__global__ void act_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ y, float slope,
+                               uint16_t* __restrict__ dz, float* __restrict__ partial, int64_t total8, int C) {
+    extern __shared__ float red[];  // [blockDim][8]
+    const int C8 = C / 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float g[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dy) + i), g);
+        if (y) {
+            float yy[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(y) + i), yy);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) g[c] *= (yy[c] > 0.f ? 1.f : slope);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] += g[c];
+        if (dz) reinterpret_cast<uint4*>(dz)[i] = pack8(g);
+    }
+    if (partial) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) red[threadIdx.x * 8 + c] = acc[c];
+        __syncthreads();
+        for (int ch = threadIdx.x; ch < C; ch += blockDim.x) {
+            const int cg = ch / 8, c = ch % 8;
+            float sum = 0.f;
+            for (int t = cg; t < (int)blockDim.x; t += C8) sum += red[t * 8 + c];
+            partial[(int64_t)blockIdx.x * C + ch] = sum;
+        }
+    }
+}
+
+// Zero insertion for the stride-2 backward, 8 channels per thread: out voxel
+// (d, h, w) takes dz (d/2, h/2, w/2) when all three are even, else zero.
+__global__ void upsample2_kernel(const uint16_t* __restrict__ dz, uint16_t* __restrict__ out, int64_t N, int D,
+                                 int H, int W, int C) {
+    const int C8 = C / 8;
+    const int Do = (D + 1) / 2, Ho = (H + 1) / 2, Wo = (W + 1) / 2;
+    const int64_t total = N * D * H * W * C8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(i % C8);
+        int64_t r = i / C8;
+        const int w = (int)(r % W);
+        r /= W;
+        const int h = (int)(r % H);
+        r /= H;
+        const int d = (int)(r % D);
+        const int64_t n = r / D;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (((d | h | w) & 1) == 0)
+            v = __ldg(reinterpret_cast<const uint4*>(dz + ((((n * Do + d / 2) * Ho + h / 2) * Wo + w / 2) * C + 8 * c8)));
+        reinterpret_cast<uint4*>(out)[i] = v;
+    }
+}
+
 __global__ void timeout_probe_kernel(int* status, uint64_t limit_ns) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
@@ -336,6 +510,69 @@ cf_status launch_flip_transpose(const LaunchCtx& ctx, int c_out, int c_in, const
     const int64_t ntiles = 27LL * ((c_out + 31) / 32) * ((c_in + 31) / 32);
     const int blocks = (int)std::min<int64_t>(ntiles, 8LL * ctx.num_sms);
     flip_transpose_kernel<<<blocks, dim3(32, 8), 0, ctx.stream>>>(w, wt, c_out, c_in);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+cf_status launch_avgpool_fwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                             const uint16_t* z, const float* bias, float slope, uint16_t* y, uint8_t* mask) {
+    const int64_t total = n * (d / 2) * (h / 2) * (w / 2) * (c / 8);
+    const int threads = 256;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads, 16LL * ctx.num_sms));
+    avgpool_fwd_kernel<<<blocks, threads, 0, ctx.stream>>>(z, bias, slope, y, mask, n, (int)d, (int)h, (int)w, c,
+                                                           pool_grid(d, h, w));
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+cf_status launch_avgpool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                             const uint16_t* dy, const uint8_t* mask, float slope, uint16_t* dz, float* dbias,
+                             void* ws, size_t ws_bytes) {
+    if (c / 8 > 256) return CF_ERR_UNSUPPORTED;
+    const int threads = pool_bwd_block(c);
+    const int blocks = pool_bwd_grid(ctx.num_sms);
+    float* partial = nullptr;
+    if (dbias) {
+        if (ws == nullptr || ws_bytes < pool_bwd_workspace_bytes(ctx.num_sms, c)) return CF_ERR_WORKSPACE;
+        partial = static_cast<float*>(ws);
+    }
+    avgpool_bwd_kernel<<<blocks, threads, threads * 8 * sizeof(float), ctx.stream>>>(
+        dy, mask, slope, dz, partial, n, (int)d, (int)h, (int)w, c, pool_grid(d, h, w));
+    if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+    return dbias ? launch_colsum(ctx, partial, blocks, c, dbias) : CF_OK;
+}
+
+cf_status launch_act_fwd(const LaunchCtx& ctx, int64_t count, int c, const uint16_t* z, const float* bias,
+                         float slope, uint16_t* y) {
+    const int64_t total8 = count / 8;
+    const int threads = 256;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total8 + threads - 1) / threads, 16LL * ctx.num_sms));
+    act_fwd_kernel<<<blocks, threads, 0, ctx.stream>>>(z, bias, slope, y, total8, c);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+cf_status launch_act_bwd(const LaunchCtx& ctx, int64_t count, int c, const uint16_t* dy, const uint16_t* y,
+                         float slope, uint16_t* dz, float* dbias, void* ws, size_t ws_bytes) {
+    if (c / 8 > 256) return CF_ERR_UNSUPPORTED;
+    // blockDim and the grid stride are multiples of c/8: each thread keeps one
+    // channel group
+    const int threads = pool_bwd_block(c);
+    const int blocks = pool_bwd_grid(ctx.num_sms);
+    float* partial = nullptr;
+    if (dbias) {
+        if (ws == nullptr || ws_bytes < pool_bwd_workspace_bytes(ctx.num_sms, c)) return CF_ERR_WORKSPACE;
+        partial = static_cast<float*>(ws);
+    }
+    act_bwd_kernel<<<blocks, threads, threads * 8 * sizeof(float), ctx.stream>>>(dy, y, slope, dz, partial,
+                                                                                   count / 8, c);
+    if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+    return dbias ? launch_colsum(ctx, partial, blocks, c, dbias) : CF_OK;
+}
+
+cf_status launch_upsample2(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                           const uint16_t* dz, uint16_t* out) {
+    const int64_t total = n * d * h * w * (c / 8);
+    const int threads = 256;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads, 16LL * ctx.num_sms));
+    upsample2_kernel<<<blocks, threads, 0, ctx.stream>>>(dz, out, n, (int)d, (int)h, (int)w, c);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 

@@ -117,15 +117,30 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
             const int kbase = (j & 1) * 2 + (l & 1);
             uint32_t ybits[CH / 2];
             uint32_t codes[CH / 4];
+            const bool avg = p.ea.pool_kind == 1;
 #pragma unroll
             for (int cc = 0; cc < CH; ++cc) {
-                float v = __uint_as_float(a0[cc]);
-                int k = kbase;
-                pool_combine(v, k, __uint_as_float(a1[cc]), kbase + 4);
-                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 1), __shfl_xor_sync(0xffffffffu, k, 1));
-                pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 8), __shfl_xor_sync(0xffffffffu, k, 8));
-                const float s = v + bias[cc];
-                const float y = s > 0.f ? s : p.ea.slope * s;
+                float y;
+                int k;
+                if (avg) {
+                    // average of the activated window: this lane's two voxels (planes 0
+                    // and 1), then the w and h neighbours; code = the window's sign mask
+                    const float s0 = __uint_as_float(a0[cc]) + bias[cc], s1 = __uint_as_float(a1[cc]) + bias[cc];
+                    float sum = lrelu(s0, p.ea.slope) + lrelu(s1, p.ea.slope);
+                    k = ((s0 > 0.f ? 1 : 0) << kbase) | ((s1 > 0.f ? 1 : 0) << (kbase + 4));
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    k |= __shfl_xor_sync(0xffffffffu, k, 1);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+                    k |= __shfl_xor_sync(0xffffffffu, k, 8);
+                    y = sum * 0.125f;
+                } else {
+                    float v = __uint_as_float(a0[cc]);
+                    k = kbase;
+                    pool_combine(v, k, __uint_as_float(a1[cc]), kbase + 4);
+                    pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 1), __shfl_xor_sync(0xffffffffu, k, 1));
+                    pool_combine(v, k, __shfl_xor_sync(0xffffffffu, v, 8), __shfl_xor_sync(0xffffffffu, k, 8));
+                    y = lrelu(v + bias[cc], p.ea.slope);
+                }
                 const uint32_t yb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y));
                 if (cc & 1)
                     ybits[cc >> 1] |= yb << 16;
@@ -158,6 +173,11 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
                     float v[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(a[q8 * 8 + k]);
+                    if (EPI == EPI_PLAIN && p.ea.act) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            v[k] = lrelu(v[k] + (p.ea.bias ? p.ea.bias[t.co0 + c + q8 * 8 + k] : 0.f), p.ea.slope);
+                    }
                     if (EPI == EPI_DGRAD) {
                         const uint4 xa = *reinterpret_cast<const uint4*>(p.ea.x_act + o + q8 * 8);
                         const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};

@@ -40,25 +40,42 @@ def sample_ranges(n: int, chunks: int):
     return [(i * n // k, (i + 1) * n // k) for i in range(k) if (i + 1) * n // k > i * n // k]
 
 
+POOL_CODES = {"max": cf.CF_POOL_MAX, "avg": cf.CF_POOL_AVG, "none": cf.CF_POOL_NONE}
+
+
 class CosmoStack:
+    """specs: optional per-block (stride, pool), stride 1 or 2, pool "max",
+    "avg" or "none" (default: stride 1 and max-pooling everywhere, the
+    CosmoFlow-shaped five-block stack).  The hybrid-parallelism page's Table I
+    model is channels (4, 16, 32, 64, 128, 256, 256, 256) with a stride-2
+    fourth conv and no pooling after the last two at width 128."""
+
     def __init__(self, n: int, spatial: int, channels, slope: float = 0.3, device: str = "cuda",
-                 backward: bool = True, overlap: bool = True):
+                 backward: bool = True, overlap: bool = True, specs=None):
         self.n, self.spatial, self.channels, self.slope = n, spatial, tuple(channels), float(slope)
         self.L = len(channels) - 1
+        self.specs = [tuple(t) for t in specs] if specs is not None else [(1, "max")] * self.L
+        assert len(self.specs) == self.L
         self.device = device
         bf, u8, f32 = torch.bfloat16, torch.uint8, torch.float32
         s = spatial
-        self.dims = []  # (n, d, h, w) of each block's conv input/output
+        self.dims = []   # (n, d, h, w) of each block's conv input
+        self.odims = []  # (n, d, h, w) of each block's conv output
         self.x = torch.empty((n, s, s, s, channels[0]), dtype=bf, device=device)
         self.w, self.b, self.y, self.idx = [], [], [], []
         for l in range(self.L):
             ci, co = channels[l], channels[l + 1]
+            stride, pool = self.specs[l]
+            so = (s + stride - 1) // stride
+            sp = so if pool == "none" else so // 2
             self.dims.append((n, s, s, s))
+            self.odims.append((n, so, so, so))
             self.w.append(torch.empty((co, 3, 3, 3, ci), dtype=bf, device=device))
             self.b.append(torch.zeros((co,), dtype=f32, device=device))
-            self.y.append(torch.empty((n, s // 2, s // 2, s // 2, co), dtype=bf, device=device))
-            self.idx.append(torch.empty((n, s // 2, s // 2, s // 2, co), dtype=u8, device=device))
-            s //= 2
+            self.y.append(torch.empty((n, sp, sp, sp, co), dtype=bf, device=device))
+            # argmax codes (max) or sign masks (avg) of the pooled output
+            self.idx.append(torch.empty((n, sp, sp, sp, co), dtype=u8, device=device) if pool != "none" else None)
+            s = sp
         self.backward_enabled = backward
         # with overlap: the backward-data chain on a high-priority stream (it is the
         # step's critical path), the weight gradients on a normal-priority one
@@ -68,15 +85,21 @@ class CosmoStack:
         if backward:
             self.dz, self.dw, self.db, self.g = [], [], [], []
             for l in range(self.L):
-                n_, d, h, w = self.dims[l]
+                n_, d, h, w = self.odims[l]
                 co = channels[l + 1]
                 self.dz.append(None if self.routed(l) else torch.empty((n_, d, h, w, co), dtype=bf, device=device))
                 self.dw.append(torch.empty((co, 3, 3, 3, channels[l]), dtype=f32, device=device))
                 self.db.append(torch.empty((co,), dtype=f32, device=device))
-                # g[l]: gradient w.r.t. block l's pooled pre-activation (dgrad output of block l+1)
-                # (for a routed top block: its pooled pre-activation gradient)
-                self.g.append(torch.empty((n_, d // 2, h // 2, w // 2, co), dtype=bf, device=device)
-                              if l < self.L - 1 or self.routed(l) else None)
+                # g[l]: the dgrad output of block l+1: the gradient w.r.t. block l's
+                # pooled pre-activation (max), its output (avg); an unpooled block's
+                # dgrad output is its dZ itself (g[l] aliases dz[l])
+                pool = self.specs[l][1]
+                if pool == "none" and l < self.L - 1:
+                    self.g.append(self.dz[l])
+                elif l < self.L - 1 or self.routed(l):
+                    self.g.append(torch.empty(tuple(self.y[l].shape), dtype=bf, device=device))
+                else:
+                    self.g.append(None)
             for l in range(self.L):
                 desc = self.desc(l)
                 ws_w = max(ws_w, cf.cf_workspace_size(
@@ -92,11 +115,15 @@ class CosmoStack:
 
     def routed(self, l) -> bool:
         """Block l's weight gradient takes the pooled gradient + argmax codes."""
-        return l == 0 and self.channels[0] in (1, 4)
+        return l == 0 and self.channels[0] in (1, 4) and self.specs[0] == (1, "max")
 
     def desc(self, l):
         n, d, h, w = self.dims[l]
-        return cf.cf_conv_desc(n, d, h, w, self.channels[l], self.channels[l + 1])
+        return cf.cf_conv_desc(n, d, h, w, self.channels[l], self.channels[l + 1], self.specs[l][0])
+
+    def epi(self, l, idx=None):
+        """Forward epilogue of block l (bias, slope, codes/masks, pooling kind)."""
+        return (self.b[l], self.slope, self.idx[l] if idx is None else idx, POOL_CODES[self.specs[l][1]])
 
     def block_input(self, l):
         return self.x if l == 0 else self.y[l - 1]
@@ -151,13 +178,14 @@ class CosmoStack:
                 main.wait_event(ev)
                 for l in range(first):
                     _, d, h, w = self.dims[l]
-                    cf.cf_conv3d_fwd(cf.cf_conv_desc(n1 - n0, d, h, w, self.channels[l], self.channels[l + 1]),
-                                     self.block_input(l)[n0:n1], self.w[l],
-                                     (self.b[l], self.slope, self.idx[l][n0:n1]), self.y[l][n0:n1], None, 0, main)
+                    idx = self.idx[l][n0:n1] if self.idx[l] is not None else None
+                    cf.cf_conv3d_fwd(cf.cf_conv_desc(n1 - n0, d, h, w, self.channels[l], self.channels[l + 1],
+                                                     self.specs[l][0]),
+                                     self.block_input(l)[n0:n1], self.w[l], self.epi(l, idx), self.y[l][n0:n1],
+                                     None, 0, main)
         for l in range(first, self.L):
             self._run(f"fwd{l + 1}", main, lambda l=l: cf.cf_conv3d_fwd(
-                self.desc(l), self.block_input(l), self.w[l], (self.b[l], self.slope, self.idx[l]), self.y[l],
-                None, 0, main), timer)
+                self.desc(l), self.block_input(l), self.w[l], self.epi(l), self.y[l], None, 0, main), timer)
 
     def backward(self, dy, stream=None, timer=None, serial=False, host_out=None):
         """timer: as in forward (keys "poolbwd<l+1>", "wgrad<l+1>", "dgrad<l+1>").
@@ -186,21 +214,33 @@ class CosmoStack:
                 dst.copy_(src, non_blocking=True)
 
         for l in range(self.L - 1, -1, -1):
-            n, d, h, w = self.dims[l]
+            n, d, h, w = self.odims[l]
             co = self.channels[l + 1]
             routed = self.routed(l)
+            pool = self.specs[l][1]
             if l == self.L - 1:
-                fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope,
-                                                       self.dz[l], self.g[l] if routed else None, self.db[l], ws,
-                                                       wsb, main)
+                if pool == "max":
+                    fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope,
+                                                           self.dz[l], self.g[l] if routed else None, self.db[l],
+                                                           ws, wsb, main)
+                else:
+                    fn = lambda: cf.cf_block_epilogue_bwd(POOL_CODES[pool], n, d, h, w, co, dy,
+                                                          self.y[l] if pool == "none" else None, self.idx[l],
+                                                          self.slope, self.dz[l], None, self.db[l], ws, wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
                 to_host(main, host_out and host_out[1][l], self.db[l])
-            elif not routed:
+            elif pool == "max" and not routed:
                 fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope,
                                                        self.dz[l], None, self.db[l], ws, wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
                 to_host(main, host_out and host_out[1][l], self.db[l])
-            # (a routed block below the top: db[l] came with g[l] from block l+1's dgrad)
+            elif pool == "avg":
+                fn = lambda: cf.cf_block_epilogue_bwd(cf.CF_POOL_AVG, n, d, h, w, co, self.g[l], None, self.idx[l],
+                                                      self.slope, self.dz[l], None, self.db[l], ws, wsb, main)
+                self._run(f"poolbwd{l + 1}", main, fn, timer)
+                to_host(main, host_out and host_out[1][l], self.db[l])
+            # (a routed or unpooled block below the top: db[l] came with g[l] from
+            # block l+1's dgrad, as the channel sums of its output)
             desc = self.desc(l)
             if side is not main:
                 ev = torch.cuda.Event()
@@ -215,9 +255,13 @@ class CosmoStack:
             self._run(f"wgrad{l + 1}", side, fn, timer)
             to_host(side, host_out and host_out[0][l], self.dw[l])
             if l > 0:
-                dsum = self.db[l - 1] if self.routed(l - 1) else None
+                below = self.specs[l - 1][1]
+                dsum = self.db[l - 1] if (self.routed(l - 1) or below == "none") else None
+                # the lower block's output derivative rides on the input gradient
+                # unless it is average-pooled (its derivative is per voxel, from its masks)
+                x_act = self.block_input(l) if below != "avg" else None
                 self._run(f"dgrad{l + 1}", main, lambda: cf.cf_conv3d_dgrad(
-                    desc, self.dz[l], None, self.w[l], self.block_input(l), self.slope, self.g[l - 1], ws, wsb,
+                    desc, self.dz[l], None, self.w[l], x_act, self.slope, self.g[l - 1], ws, wsb,
                     main, dsum=dsum), timer)
                 if dsum is not None:
                     to_host(main, host_out and host_out[1][l - 1], dsum)
@@ -275,9 +319,7 @@ class CosmoStack:
     def _dy_buffer(self, dy_host):
         """Device buffer of the top-output gradient for step_host."""
         if getattr(self, "_dy", None) is None:
-            n, d, h, w = self.dims[self.L - 1]
-            self._dy = torch.empty((n, d // 2, h // 2, w // 2, self.channels[self.L]), dtype=torch.bfloat16,
-                                   device=self.device)
+            self._dy = torch.empty(tuple(self.y[-1].shape), dtype=torch.bfloat16, device=self.device)
         return self._dy
 
     def capture(self, dy, timer=None, keys=None, host=None):
@@ -305,20 +347,24 @@ class CosmoStack:
 
     def launches_per_step(self) -> int:
         """Kernels one step enqueues: fwd 1 per block; pool-bwd 2 (scatter +
-        bias sum) per block except a routed block below the top; wgrad 2
-        (split-K + reduce) per block; dgrad 2 (filter flip + conv) for blocks
-        1..L-1, plus the channel sums for a routed block below: 1 (partials
-        reduction) when fused in the halo-tile epilogue, else 2."""
+        bias sum) per block except a routed or unpooled block below the top;
+        wgrad 2 (split-K + reduce) per block, +1 for a stride-2 block (zero
+        insertion); dgrad 2 (filter flip + conv) for blocks 1..L-1 (+1 for
+        stride 2), plus the channel sums for a routed or unpooled block below:
+        1 (partials reduction) when fused in the halo-tile epilogue, else 2."""
         n = self.L
         if self.backward_enabled:
             ch = self.channels
             for l in range(self.L):
-                n += 2  # wgrad
-                if l == self.L - 1 or not self.routed(l):
+                s2 = self.specs[l][0] == 2
+                n += 2 + s2  # wgrad
+                pool = self.specs[l][1]
+                if l == self.L - 1 or not (self.routed(l) or pool == "none"):
                     n += 2  # pool backward
                 if l > 0:
-                    n += 2  # dgrad
-                    if self.routed(l - 1):
-                        fused = ch[l] <= 32 and ch[l + 1] % 32 == 0 and ch[l] in (32, 64, 128)
+                    n += 2 + s2  # dgrad
+                    if self.routed(l - 1) or self.specs[l - 1][1] == "none":
+                        fused = (not s2 and ch[l] <= 32 and ch[l] % 16 == 0 and ch[l] in (32, 64, 128)
+                                 and ch[l + 1] % 16 == 0)
                         n += 1 if fused else 2
         return n

@@ -49,18 +49,37 @@ typedef enum {
     CF_ERR_TIMEOUT = 5       /* a kernel abandoned a bounded wait (device status word) */
 } cf_status;
 
-/* Geometry of one k=3, stride-1, pad-1 convolution: input and conv output
- * share n,d,h,w. */
+/* Geometry of one k=3, pad-1 convolution.  n, d, h, w are the sizes of its
+ * input.  stride 0 or 1: the conv output has the same sizes; stride 2 (the
+ * hybrid-parallelism page's Table I, layer c4, "stride of 2"): the output is
+ *   Z[n,o,co] = sum_{t,ci} W[co,t,ci] * X[n, 2*o + t - 1, ci]
+ * with (d+1)/2, (h+1)/2, (w+1)/2 voxels (padding 1 on every face).  A
+ * descriptor initialised without the stride member (zero) is stride 1. */
 typedef struct {
     int64_t n, d, h, w;
     int32_t c_in, c_out;
+    int32_t stride;
 } cf_conv_desc;
 
-/* Fused epilogue of the forward conv. */
+/* Pooling of the block epilogue. */
+enum {
+    CF_POOL_MAX = 0,  /* the CosmoFlow block of this library: max over each 2x2x2 window */
+    CF_POOL_AVG = 1,  /* average of the activated window (CosmoFlow page, section III-C:
+                         constant weights 1/KS^3) */
+    CF_POOL_NONE = 2  /* no pooling: y = LReLU(z + b) at the conv output's size
+                         (Table I layers after the last pooling) */
+};
+
+/* Fused epilogue of the forward conv.  A struct initialised without the pool
+ * member (zero) is the max-pool epilogue. */
 typedef struct {
     const float* bias; /* [c_out] fp32 device, or NULL for zero bias */
     float slope;       /* leaky-ReLU negative slope (0.3 in the CosmoFlow block) */
-    uint8_t* argmax;   /* [n][d/2][h/2][w/2][c_out] device, or NULL (inference) */
+    uint8_t* argmax;   /* pooled shape [n][d'/2][h'/2][w'/2][c_out], device, or NULL (inference):
+                          CF_POOL_MAX: first-maximum codes dd*4+dh*2+dw;
+                          CF_POOL_AVG: sign masks, bit dd*4+dh*2+dw set where z + b > 0
+                          (the backward's leaky-ReLU derivatives); CF_POOL_NONE: unused */
+    int32_t pool;      /* CF_POOL_MAX, CF_POOL_AVG or CF_POOL_NONE */
 } cf_pool_epi;
 
 /* Operation ids for cf_workspace_size. */
@@ -72,15 +91,18 @@ enum { CF_OP_FWD = 0, CF_OP_DGRAD = 1, CF_OP_WGRAD = 2, CF_OP_DGRAD_ROUTED = 3,
  * hybrid-parallelism page, Table I: 3^3 filters, "same" padding).
  *   x  : [n][d][h][w][c_in] bf16
  *   w  : [c_out][3][3][3][c_in] bf16
- *   epi: NULL -> y is the plain conv output Z rounded to bf16, [n][d][h][w][c_out];
- *        else y is the pooled block output Y, [n][d/2][h/2][w/2][c_out], and
- *        epi->argmax (if not NULL) receives the window codes.
+ *   epi: NULL -> y is the plain conv output Z rounded to bf16, [n][d'][h'][w'][c_out]
+ *        (d', h', w' the conv output sizes, see cf_conv_desc);
+ *        pool CF_POOL_MAX / CF_POOL_AVG -> y is the pooled block output Y,
+ *        [n][d'/2][h'/2][w'/2][c_out], and epi->argmax (if not NULL) receives the
+ *        window codes / sign masks; CF_POOL_NONE -> y = LReLU(Z + b), [n][d'][h'][w'][c_out].
+ *        Average pooling: Y = (1/8) * sum over the window of LReLU(Z + b).
  *   ws : unused (pass NULL, 0).
  * Supported: c_in in {1, 4} or a multiple of 16 (the CosmoFlow page's rule of
  * channel counts in multiples of 16, section III-A); c_out a multiple of 16 and
  * <= 256 per kernel tile (multiples of 256 above that), or c_out a multiple of 8
  * (<= 256) when c_in is 1 or 4; w * c_in a multiple of 8 when c_in is 1 or 4;
- * d, h, w even when pooling.
+ * d', h', w' even when pooling; stride 2 only for c_in a multiple of 16.
  */
 cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* w,
                         const cf_pool_epi* epi, uint16_t* y, void* ws, size_t ws_bytes,
@@ -102,6 +124,10 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
  *        stored dx (fixed order).  In a block stack dx is the previous block's
  *        pooled pre-activation gradient and dsum its bias gradient (fused into
  *        the epilogue for c_in <= 32, a separate pass over dx otherwise).
+ *   stride 2: dz has the conv output's sizes ((d+1)/2 ...); it is written with
+ *        zeros at the odd positions into the workspace and the stride-1
+ *        backward runs on that (the index map 2*o + t - 1 = u of the forward);
+ *        idx must be NULL.
  * Supported: c_out and c_in multiples of 16.
  */
 cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx,
@@ -119,6 +145,7 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
  *        partials); d, h, w must be even.  Other c_in expand dZ into the
  *        workspace first.  cf_workspace_size(CF_OP_WGRAD_ROUTED) covers both.
  *   dw : [c_out][3][3][3][c_in] fp32; accumulate != 0 adds to it, else overwrites.
+ *   stride 2: as in cf_conv3d_dgrad (dz zero-inserted into the workspace; idx NULL).
  * Supported: c_in in {1, 4} (w * c_in a multiple of 8) or a multiple of 16;
  * c_out a multiple of 16 (at most 256 when c_in is 1 or 4).
  */
@@ -153,6 +180,32 @@ cf_status cf_bias_lrelu_pool_bwd(int64_t n, int64_t d, int64_t h, int64_t w, int
                                  const uint16_t* dy, const uint16_t* y, const uint8_t* idx,
                                  float slope, uint16_t* dz, uint16_t* dy_pre, float* dbias,
                                  void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The block epilogue of any pooling kind (CF_POOL_*) as standalone kernels:
+ * the unfused counterpart of the fused epilogues of cf_conv3d_fwd and the
+ * backward that feeds cf_conv3d_dgrad / cf_conv3d_wgrad with a dense dZ.
+ * Sources: CosmoFlow page, section III-A (every conv layer followed by leaky
+ * ReLU) and III-C (average pooling, constant weights 1/KS^3); hybrid-
+ * parallelism page, Table I (stride-2 pooling; layers without pooling).
+ *   n, d, h, w : sizes of z / dz (full resolution); d, h, w even when pooling.
+ *   forward  : z [n][d][h][w][c] bf16 -> y (pooled shape, or z's for NONE) and
+ *              aux (pooled shape uint8: MAX codes, AVG sign masks, NONE unused).
+ *   backward : g = dy * LReLU'(y) (MAX with y given; NONE: y given, or dy
+ *              itself when y is NULL); MAX routes g to the window's argmax,
+ *              AVG writes dz = dy / 8 * LReLU'(z + b) from the masks, NONE
+ *              writes dz = g.  dy_pre (MAX only, pooled shape): g.  dbias [c]:
+ *              sum of dz over n and voxels (fixed order, workspace of
+ *              cf_workspace_size(CF_OP_POOL_BWD)).  Outputs may be NULL.
+ * Supported: c a multiple of 8 (at most 2048 in the backward).
+ */
+cf_status cf_block_epilogue_fwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                                const uint16_t* z, const float* bias, float slope, uint16_t* y, uint8_t* aux,
+                                void* stream);
+cf_status cf_block_epilogue_bwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                                const uint16_t* dy, const uint16_t* y, const uint8_t* aux, float slope,
+                                uint16_t* dz, uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /*
  * cf_bias_lrelu_pool_bwd without a workspace argument, for callers that

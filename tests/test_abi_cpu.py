@@ -17,7 +17,8 @@ def test_exports_every_header_symbol(cf):
     names = cf.header_symbols()
     expected = {"cf_conv3d_fwd", "cf_conv3d_dgrad", "cf_conv3d_wgrad", "cf_bias_lrelu_pool_fwd",
                 "cf_bias_lrelu_pool_bwd", "cf_workspace_size", "cf_status_string", "cf_last_device_status",
-                "cf_set_wait_limit_ns", "cf_debug_wait_timeout_probe"}
+                "cf_set_wait_limit_ns", "cf_debug_wait_timeout_probe", "cf_block_epilogue_fwd",
+                "cf_block_epilogue_bwd", "cf_bias_lrelu_pool_bwd_noalloc"}
     assert expected <= set(names)
     lib = ctypes.CDLL(cf.LIB_PATH)
     for n in names:
@@ -87,3 +88,17 @@ def test_tile_divider_method():
         for x in xs:
             if 0 <= x < (1 << 32):
                 assert div(x, mss) == x // d, (x, d)
+
+
+def test_variant_argument_errors(cf):
+    # stride 3, an unknown pooling kind, average-pool backward without masks,
+    # dy_pre outside max pooling: all refused before anything is launched
+    d = cf.cf_conv_desc(1, 4, 4, 4, 32, 64, 3)
+    assert cf.cf_conv3d_fwd(d, 16, 16, None, 16, check=False) == cf.CF_ERR_INVALID_ARG
+    d = cf.cf_conv_desc(1, 4, 4, 4, 32, 64, 1)
+    assert cf.cf_conv3d_fwd(d, 16, 16, (None, 0.3, None, 7), 16, check=False) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_block_epilogue_fwd(5, 1, 4, 4, 4, 8, 16, None, 0.3, 16, None, check=False) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_block_epilogue_bwd(cf.CF_POOL_AVG, 1, 4, 4, 4, 8, 16, None, None, 0.3, 32, None, None,
+                                    check=False) == cf.CF_ERR_INVALID_ARG
+    assert cf.cf_block_epilogue_bwd(cf.CF_POOL_NONE, 1, 4, 4, 4, 8, 16, None, None, 0.3, 32, 48, None,
+                                    check=False) == cf.CF_ERR_INVALID_ARG

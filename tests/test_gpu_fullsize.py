@@ -256,3 +256,22 @@ def test_sweep_layer(cf, oracle_mod, shape):
                  f"sweep wgrad {shape} ({len(pts)} tile-covering elements)")
     torch.cuda.synchronize()
     assert cf.cf_last_device_status() == cf.CF_OK
+
+
+def test_table1_model_128_n4(cf, oracle_mod):
+    """The hybrid-parallelism page's Table I model at input width 128 (4 x
+    128^3 per sample, N=4): forward + backward through CosmoStack, every
+    kernel checked on its own GPU inputs (the three large blocks sampled,
+    their weight gradients in full; the rest in full)."""
+    from oracle import TABLE1_CHANNELS, table1_specs
+    from cnn_conv3d_gb300 import flops
+    from tests.test_gpu_chain import check_chain_per_kernel, run_chain
+    st, inp, dy16 = run_chain(cf, 4, 128, TABLE1_CHANNELS, table1_specs(128), seed=20260006)
+    assert tuple(st.y[-1].shape) == (4, 2, 2, 2, 256)
+    check_chain_per_kernel(oracle_mod, st, inp, dy16, big_from=4 * 32 ** 3, rng=np.random.default_rng(6))
+    # the executed forward FLOPs of the chain are Table I's per-sample row x N
+    fwd = 0
+    for l in range(st.L):
+        n, d, h, w = st.odims[l]
+        fwd += flops.conv_flops(n, TABLE1_CHANNELS[l], TABLE1_CHANNELS[l + 1], d * h * w)
+    assert fwd == 4 * flops.p3_table1_forward_flops(128)

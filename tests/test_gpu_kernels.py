@@ -380,3 +380,168 @@ def test_routed_gradients_match_dense(cf, oracle_mod, shape):
         ref = oracle_mod.conv3d_dgrad(rdz, w)
         S = oracle_mod.conv3d_dgrad(np.abs(rdz), np.abs(w))
         assert_close(host_bf16_f64(dx), ref, S, "routed dgrad")
+
+
+# ----------------------------------------------------------------------------- page variants
+
+def _wins(a):
+    N, D, H, W, C = a.shape
+    return a.reshape(N, D // 2, 2, H // 2, 2, W // 2, 2, C).transpose(0, 1, 3, 5, 7, 2, 4, 6).reshape(
+        N, D // 2, H // 2, W // 2, C, 8)
+
+
+def _check_avgpooled(oracle_mod, z, S, b, gy, gmask, what):
+    """Average of the activated window within 1e-2 of the window's mean S (the
+    activation is 1-Lipschitz), and every sign bit whose pre-activation is
+    farther than 1e-2 * S from zero equal to the oracle's."""
+    ry, rmask = oracle_mod.avgpool_fwd(z, b, SLOPE)
+    sw = _wins(S + np.abs(b))
+    assert_close(gy, ry, sw.mean(-1), what)
+    zb = _wins(z + b)
+    sure = np.abs(zb) > 1e-2 * sw
+    gb = (gmask[..., None].astype(np.int64) >> np.arange(8)) & 1
+    rb = (rmask[..., None].astype(np.int64) >> np.arange(8)) & 1
+    np.testing.assert_array_equal(gb[sure], rb[sure], err_msg=what)
+
+
+VARIANT_FWD = [
+    (2, 4, 6, 40, 4, 32),      # first-layer kernel (c_in 4)
+    (1, 4, 6, 16, 32, 64),     # halo tile
+    (1, 2, 4, 8, 64, 256),     # per-tap engine
+    (1, 4, 8, 16, 16, 32),     # halo tile, 16-channel chunks
+]
+
+
+@pytest.mark.parametrize("shape", VARIANT_FWD)
+def test_conv_fwd_avgpool(cf, oracle_mod, shape):
+    import torch
+    N, D, H, W, Ci, Co = shape
+    c = _case(shape, 700 + Ci + Co)
+    y, ycheck = guarded((N, D // 2, H // 2, W // 2, Co), torch.bfloat16, fill=float("nan"))
+    mask, mcheck = guarded(y.shape, torch.uint8, fill=0)
+    cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), (dev(c["b"]), SLOPE, mask, cf.CF_POOL_AVG), y)
+    ycheck("avg y")
+    mcheck("avg mask")
+    x, w = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["w"])
+    z = oracle_mod.conv3d_fwd(x, w)
+    S = oracle_mod.conv3d_fwd(np.abs(x), np.abs(w))
+    _check_avgpooled(oracle_mod, z, S, c["b"].astype(np.float64), host_bf16_f64(y), mask.cpu().numpy(),
+                     f"avg-pooled {shape}")
+
+
+@pytest.mark.parametrize("shape", VARIANT_FWD)
+def test_conv_fwd_unpooled_activation(cf, oracle_mod, shape):
+    import torch
+    N, D, H, W, Ci, Co = shape
+    c = _case(shape, 800 + Ci + Co)
+    y, ycheck = guarded((N, D, H, W, Co), torch.bfloat16, fill=float("nan"))
+    cf.cf_conv3d_fwd(shape, dev_bf16(c["x"]), dev_bf16(c["w"]), (dev(c["b"]), SLOPE, None, cf.CF_POOL_NONE), y)
+    ycheck("act y")
+    x, w = _f64(oracle_mod, c["x"]), _f64(oracle_mod, c["w"])
+    b = c["b"].astype(np.float64)
+    ref = oracle_mod.act_fwd(oracle_mod.conv3d_fwd(x, w), b, SLOPE)
+    S = oracle_mod.conv3d_fwd(np.abs(x), np.abs(w)) + np.abs(b)
+    assert_close(host_bf16_f64(y), ref, S, f"unpooled {shape}")
+
+
+def test_block_epilogue_variants_standalone(cf, oracle_mod):
+    import torch
+    rng = np.random.default_rng(9)
+    N, D, H, W, C = 2, 4, 6, 10, 24
+    z16 = synthdata.to_bf16_bits(rng.normal(size=(N, D, H, W, C)))
+    b = rng.normal(0, 0.3, size=C).astype(np.float32)
+    z = _f64(oracle_mod, z16)
+    bb = b.astype(np.float64)
+    # average pooling: forward
+    y, yc = guarded((N, D // 2, H // 2, W // 2, C), torch.bfloat16, fill=float("nan"))
+    m, mc = guarded(y.shape, torch.uint8)
+    cf.cf_block_epilogue_fwd(cf.CF_POOL_AVG, N, D, H, W, C, dev_bf16(z16), dev(b), SLOPE, y, m)
+    yc("avg y")
+    mc("avg mask")
+    _check_avgpooled(oracle_mod, z, np.abs(z), bb, host_bf16_f64(y), m.cpu().numpy(), "standalone avg")
+    # average pooling: backward from the GPU's own masks
+    dy16 = synthdata.to_bf16_bits(rng.normal(size=y.shape))
+    gmask = m.cpu().numpy()
+    dz, dzc = guarded((N, D, H, W, C), torch.bfloat16, fill=float("nan"))
+    db, dbc = guarded((C,), torch.float32, fill=float("nan"))
+    ws, wsb = _ws(cf, cf.CF_OP_POOL_BWD, cf.cf_conv_desc(N, D, H, W, C, C))
+    cf.cf_block_epilogue_bwd(cf.CF_POOL_AVG, N, D, H, W, C, dev_bf16(dy16), None, m, SLOPE, dz, None, db, ws, wsb)
+    dzc("avg dz")
+    dbc("avg db")
+    rdz, rdb = oracle_mod.avgpool_bwd(_f64(oracle_mod, dy16), gmask, SLOPE)
+    np.testing.assert_allclose(host_bf16_f64(dz), rdz, rtol=2 ** -8, atol=0)
+    assert_close(db.cpu().numpy(), rdb, np.abs(rdz).reshape(-1, C).sum(0), "avg db")
+    # no pooling: forward and backward (with the output, and with y = NULL)
+    ya, yac = guarded((N, D, H, W, C), torch.bfloat16, fill=float("nan"))
+    cf.cf_block_epilogue_fwd(cf.CF_POOL_NONE, N, D, H, W, C, dev_bf16(z16), dev(b), SLOPE, ya, None)
+    yac("act y")
+    ry = oracle_mod.act_fwd(z, bb, SLOPE)
+    np.testing.assert_allclose(host_bf16_f64(ya), ry, rtol=2 ** -8, atol=1e-30)
+    g16 = synthdata.to_bf16_bits(rng.normal(size=(N, D, H, W, C)))
+    dz2, dz2c = guarded((N, D, H, W, C), torch.bfloat16, fill=float("nan"))
+    cf.cf_block_epilogue_bwd(cf.CF_POOL_NONE, N, D, H, W, C, dev_bf16(g16), ya, None, SLOPE, dz2, None, db, ws, wsb)
+    dz2c("act dz")
+    rdz2, rdb2 = oracle_mod.act_bwd(_f64(oracle_mod, g16), host_bf16_f64(ya), SLOPE)
+    np.testing.assert_allclose(host_bf16_f64(dz2), rdz2, rtol=2 ** -8, atol=0)
+    assert_close(db.cpu().numpy(), rdb2, np.abs(rdz2).reshape(-1, C).sum(0), "act db")
+    cf.cf_block_epilogue_bwd(cf.CF_POOL_NONE, N, D, H, W, C, dev_bf16(g16), None, None, SLOPE, dz2, None, None)
+    np.testing.assert_array_equal(host_bf16_f64(dz2), _f64(oracle_mod, g16))
+
+
+STRIDE2_SHAPES = [
+    # N, D, H, W (input), Cin, Cout
+    (1, 8, 8, 16, 32, 64),
+    (2, 6, 10, 8, 16, 48),     # odd output sizes (3, 5, 4)
+    (1, 16, 16, 16, 64, 128),  # the Table I c4 layer at batch 1
+]
+
+
+@pytest.mark.parametrize("shape", STRIDE2_SHAPES)
+def test_stride2_conv(cf, oracle_mod, shape):
+    import torch
+    N, D, H, W, Ci, Co = shape
+    Do, Ho, Wo = (D + 1) // 2, (H + 1) // 2, (W + 1) // 2
+    c = _case(shape, 900 + Ci + Co)
+    desc = cf.cf_conv_desc(N, D, H, W, Ci, Co, 2)
+    x16, w16 = c["x"], c["w"]
+    x, w = _f64(oracle_mod, x16), _f64(oracle_mod, w16)
+    # forward, plain
+    y, yc = guarded((N, Do, Ho, Wo, Co), torch.bfloat16, fill=float("nan"))
+    cf.cf_conv3d_fwd(desc, dev_bf16(x16), dev_bf16(w16), None, y)
+    yc("stride-2 y")
+    ref = oracle_mod.conv3d_fwd_s2(x, w)
+    S = oracle_mod.conv3d_fwd_s2(np.abs(x), np.abs(w))
+    assert_close(host_bf16_f64(y), ref, S, f"stride-2 fwd {shape}")
+    # forward with the pooled epilogue (even output sizes only)
+    if Do % 2 == 0 and Ho % 2 == 0 and Wo % 2 == 0:
+        yp, ypc = guarded((N, Do // 2, Ho // 2, Wo // 2, Co), torch.bfloat16, fill=float("nan"))
+        idx, ic = guarded(yp.shape, torch.uint8, fill=255)
+        cf.cf_conv3d_fwd(desc, dev_bf16(x16), dev_bf16(w16), (dev(c["b"]), SLOPE, idx), yp)
+        ypc("stride-2 pooled y")
+        ic("stride-2 idx")
+        bb = c["b"].astype(np.float64)
+        ry, ridx = oracle_mod.pool_fwd(ref, bb, SLOPE)
+        zw, sw = _wins(ref), _wins(S)
+        srt = np.sort(zw, -1)
+        s_at = np.take_along_axis(sw, ridx[..., None].astype(np.int64), -1)[..., 0] + np.abs(bb)
+        notie = (srt[..., -1] - srt[..., -2]) > 1e-2 * s_at
+        np.testing.assert_array_equal(idx.cpu().numpy()[notie], ridx[notie])
+        assert_close(host_bf16_f64(yp), ry, s_at, f"stride-2 pooled {shape}")
+    # backward data (with the previous block's leaky-ReLU derivative) and weight
+    dz16 = synthdata.to_bf16_bits(np.random.default_rng(Ci).normal(size=(N, Do, Ho, Wo, Co)))
+    dzf = _f64(oracle_mod, dz16)
+    ws, wsb = _ws(cf, cf.CF_OP_DGRAD, desc)
+    dx, dxc = guarded((N, D, H, W, Ci), torch.bfloat16, fill=float("nan"))
+    cf.cf_conv3d_dgrad(desc, dev_bf16(dz16), None, dev_bf16(w16), dev_bf16(x16), SLOPE, dx, ws, wsb)
+    dxc("stride-2 dx")
+    f = np.where(x > 0, 1.0, SLOPE)
+    ref = oracle_mod.conv3d_dgrad_s2(dzf, w, (D, H, W)) * f
+    S = oracle_mod.conv3d_dgrad_s2(np.abs(dzf), np.abs(w), (D, H, W)) * f
+    assert_close(host_bf16_f64(dx), ref, S, f"stride-2 dgrad {shape}")
+    ws, wsb = _ws(cf, cf.CF_OP_WGRAD, desc)
+    dw, dwc = guarded((Co, 3, 3, 3, Ci), torch.float32, fill=float("nan"))
+    cf.cf_conv3d_wgrad(desc, dev_bf16(x16), dev_bf16(dz16), None, dw, 0, ws, wsb)
+    dwc("stride-2 dw")
+    ref = oracle_mod.conv3d_wgrad_s2(x, dzf)
+    S = oracle_mod.conv3d_wgrad_s2(np.abs(x), np.abs(dzf))
+    assert_close(dw.cpu().numpy().astype(np.float64), ref, S, f"stride-2 wgrad {shape}")
