@@ -41,7 +41,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
-                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp])
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -71,6 +71,9 @@ def _load():
         lib.oracle_conv3d_fwd_s2.argtypes = dims + [_D, _D, _D]
         lib.oracle_conv3d_dgrad_s2.argtypes = dims + [_D, _D, _D]
         lib.oracle_conv3d_wgrad_s2.argtypes = dims + [_D, _D, _D]
+        lib.oracle_bn_fwd.argtypes = [_i64, _i32, _D, _D, _D, ctypes.c_double, _D, _D, _D]
+        lib.oracle_bn_bwd.argtypes = [_i64, _i32, _D, _D, _D, ctypes.c_double, _D, _D, _D]
+        lib.oracle_bn_fwd.restype = lib.oracle_bn_bwd.restype = None
         for f in (lib.oracle_avgpool_fwd, lib.oracle_avgpool_bwd, lib.oracle_act_fwd, lib.oracle_act_bwd,
                   lib.oracle_conv3d_fwd_s2, lib.oracle_conv3d_dgrad_s2, lib.oracle_conv3d_wgrad_s2):
             f.restype = None
@@ -221,6 +224,31 @@ def act_bwd(dy: np.ndarray, y: np.ndarray, slope: float):
     db = np.empty((C,), np.float64)
     lib.oracle_act_bwd(dy.size, C, _p(dy, _D), _p(y, _D), slope, _p(dz, _D), _p(db, _D))
     return dz, db
+
+
+def bn_fwd(z: np.ndarray, gamma, beta, eps: float = 1e-5):
+    """(u, mean, var): batch normalisation of z [..., C] with the batch's
+    per-channel statistics (biased variance)."""
+    lib = _load()
+    z = _f64(z)
+    C = z.shape[-1]
+    u = np.empty_like(z)
+    mean, var = np.empty(C), np.empty(C)
+    lib.oracle_bn_fwd(z.size // C, C, _p(z, _D), _p(_f64(gamma), _D), _p(_f64(beta), _D), eps, _p(u, _D),
+                      _p(mean, _D), _p(var, _D))
+    return u, mean, var
+
+
+def bn_bwd(z: np.ndarray, du: np.ndarray, gamma, eps: float = 1e-5):
+    """(dz, dgamma, dbeta) of bn_fwd (training mode)."""
+    lib = _load()
+    z, du = _f64(z), _f64(du)
+    C = z.shape[-1]
+    dz = np.empty_like(z)
+    dg, db = np.empty(C), np.empty(C)
+    lib.oracle_bn_bwd(z.size // C, C, _p(z, _D), _p(du, _D), _p(_f64(gamma), _D), eps, _p(dz, _D), _p(dg, _D),
+                      _p(db, _D))
+    return dz, dg, db
 
 
 def conv3d_fwd_s2(x: np.ndarray, w: np.ndarray) -> np.ndarray:
@@ -425,18 +453,34 @@ def _upsample2(dz, out_shape):
     return up
 
 
-def chain_fwd(x, ws, bs, slope, specs, mirrored=True):
+def chain_fwd(x, ws, bs, slope, specs, mirrored=True, gammas=None, bn_state=None):
     """Blocks conv (stride s) -> + b -> leaky ReLU -> pooling, one spec
     (stride, pool) per block, pool in {"max", "avg", "none"}.  Max pooling is
     taken before the activation (equal by monotonicity), average pooling after
-    it (CosmoFlow page, section III-A/III-C).  Returns (xs, ys, auxs): block
-    inputs, outputs (bf16-rounded in mirrored mode) and the argmax codes (max)
-    or pre-activation sign masks (avg) or None."""
+    it (CosmoFlow page, section III-A/III-C).  A spec (stride, pool, "bn")
+    puts batch normalisation between the conv and the activation
+    (hybrid-parallelism page, section IV): z = conv(x) (stored bf16 in
+    mirrored mode), u = gammas[l] * zh + bs[l] (bs[l] is the BN shift beta),
+    then the activation and pooling of u; bn_state (a list) receives (z, mean,
+    var) per BN block.  Returns (xs, ys, auxs): block inputs, outputs
+    (bf16-rounded in mirrored mode) and the argmax codes (max) or
+    pre-activation sign masks (avg) or None."""
     xs, ys, auxs = [], [], []
     cur = _f64(x)
-    for (stride, pool), w, b in zip(specs, ws, bs):
+    for l, (spec, w, b) in enumerate(zip(specs, ws, bs)):
+        stride, pool = spec[0], spec[1]
         xs.append(cur)
         z = conv3d_fwd(cur, w) if stride == 1 else conv3d_fwd_s2(cur, w)
+        if len(spec) > 2 and spec[2] == "bn":
+            if mirrored:
+                z = round_to_bf16(z)
+            zb = z
+            z, mean, var = bn_fwd(zb, gammas[l], b)
+            if bn_state is not None:
+                bn_state.append((zb, mean, var))
+            b = None
+        elif bn_state is not None:
+            bn_state.append(None)
         if pool == "max":
             y, aux = pool_fwd(z, b, slope)
         elif pool == "avg":
@@ -451,18 +495,21 @@ def chain_fwd(x, ws, bs, slope, specs, mirrored=True):
     return xs, ys, auxs
 
 
-def chain_bwd(xs, ys, auxs, ws, dy, slope, specs, mirrored=True):
+def chain_bwd(xs, ys, auxs, ws, dy, slope, specs, mirrored=True, gammas=None, bn_state=None, dgammas=None):
     """Backward of chain_fwd from dy at the last output: per block (dW, db) and
     the dense dZ.  Where the lower block's output derivative is a function of
     that output (max pooling, no pooling), it is applied to the input gradient
     right after backward-data, as the GPU stack stores it; an average-pooled
-    block applies the per-voxel derivative itself (from its sign mask)."""
+    block applies the per-voxel derivative itself (from its sign mask).  For a
+    BN block, db is dbeta and dgammas[l] receives dgamma; dZ is the batch-norm
+    backward of the activation/pooling backward."""
     L = len(ws)
     dws, dbs, dzs = [None] * L, [None] * L, [None] * L
     g = _f64(dy)
     pre = False  # g already carries the output derivative of block l
     for l in range(L - 1, -1, -1):
-        stride, pool = specs[l]
+        stride, pool = specs[l][0], specs[l][1]
+        bn = len(specs[l]) > 2 and specs[l][2] == "bn"
         if pool == "max":
             dz, _, db = pool_bwd(g, None if pre else ys[l], auxs[l], slope)
         elif pool == "avg":
@@ -471,6 +518,11 @@ def chain_bwd(xs, ys, auxs, ws, dy, slope, specs, mirrored=True):
             dz, db = g, g.reshape(-1, g.shape[-1]).sum(0)
         else:
             dz, db = act_bwd(g, ys[l], slope)
+        if bn:
+            zb = bn_state[l][0]
+            dz, dgamma, db = bn_bwd(zb, dz, gammas[l])
+            if dgammas is not None:
+                dgammas[l] = dgamma
         if mirrored:
             dz = round_to_bf16(dz)
         dzs[l], dbs[l] = dz, db

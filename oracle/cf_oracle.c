@@ -42,6 +42,7 @@
 #include <stdint.h>
 #include <stddef.h>
 #include <string.h>
+#include <math.h>
 
 #define I5(n, d, h, w, c, D, H, W, C) \
     (((((int64_t)(n) * (D) + (d)) * (H) + (h)) * (W) + (w)) * (int64_t)(C) + (c))
@@ -620,5 +621,64 @@ void oracle_conv3d_wgrad_s2(int64_t N, int64_t D, int64_t H, int64_t W, int32_t 
                 }
             dw[IW(co, kd, kh, kw, ci, Ci)] = acc;
         }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Batch normalisation after the convolution (the hybrid-parallelism page,
+ * section IV: "a batch normalization layer after every convolutional layer"),
+ * in training mode with the statistics of the batch, per channel c over all
+ * n and voxels (count = N*D*H*W):
+ *   mu = mean(z),  var = mean((z - mu)^2)  (biased),  zh = (z - mu) / sqrt(var + eps)
+ *   u = gamma * zh + beta
+ * followed by the block's leaky ReLU and pooling.  Backward, from du:
+ *   dgamma = sum(du * zh),  dbeta = sum(du)
+ *   dz = gamma / sqrt(var + eps) * (du - dbeta / count - zh * dgamma / count).
+ * z, u, du, dz: [count][C]; mean, var, dgamma, dbeta: [C]. */
+void oracle_bn_fwd(int64_t count, int32_t C, const double* z, const double* gamma, const double* beta, double eps,
+                   double* u, double* mean, double* var)
+{
+    for (int32_t c = 0; c < C; ++c) {
+        double s = 0.0;
+        for (int64_t i = 0; i < count; ++i) s += z[i * C + c];
+        double mu = s / (double)count;
+        double q = 0.0;
+        for (int64_t i = 0; i < count; ++i) {
+            double t = z[i * C + c] - mu;
+            q += t * t;
+        }
+        double v = q / (double)count;
+        double inv = 1.0 / sqrt(v + eps);
+        for (int64_t i = 0; i < count; ++i) u[i * C + c] = gamma[c] * (z[i * C + c] - mu) * inv + beta[c];
+        if (mean) mean[c] = mu;
+        if (var) var[c] = v;
+    }
+}
+
+void oracle_bn_bwd(int64_t count, int32_t C, const double* z, const double* du, const double* gamma, double eps,
+                   double* dz, double* dgamma, double* dbeta)
+{
+    for (int32_t c = 0; c < C; ++c) {
+        double s = 0.0;
+        for (int64_t i = 0; i < count; ++i) s += z[i * C + c];
+        double mu = s / (double)count;
+        double q = 0.0;
+        for (int64_t i = 0; i < count; ++i) {
+            double t = z[i * C + c] - mu;
+            q += t * t;
+        }
+        double inv = 1.0 / sqrt(q / (double)count + eps);
+        double sg = 0.0, sb = 0.0;
+        for (int64_t i = 0; i < count; ++i) {
+            double zh = (z[i * C + c] - mu) * inv;
+            sg += du[i * C + c] * zh;
+            sb += du[i * C + c];
+        }
+        for (int64_t i = 0; i < count; ++i) {
+            double zh = (z[i * C + c] - mu) * inv;
+            dz[i * C + c] = gamma[c] * inv * (du[i * C + c] - sb / (double)count - zh * sg / (double)count);
+        }
+        if (dgamma) dgamma[c] = sg;
+        if (dbeta) dbeta[c] = sb;
     }
 }

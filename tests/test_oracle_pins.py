@@ -607,3 +607,83 @@ def test_table1_specs_reproduce_the_flop_rows():
                 s //= 2
         assert tot == flops.p3_table1_forward_flops(wi)
         assert s == 2  # 256 x 2^3 = 2048 inputs of fc1
+
+
+# ----------------------------------------------------------------------------- batch normalisation
+
+def test_bn_closed_forms(oracle_mod):
+    """Normalised output: per-channel mean beta and variance gamma^2 *
+    var/(var + eps); the backward's dz sums to zero per channel (shift
+    invariance) and its projection on the normalised input is the closed form
+    of scale invariance with eps."""
+    rng = np.random.default_rng(51)
+    z = rng.normal(3.0, 2.0, size=(2, 4, 3, 5, 6))
+    g, b, eps = rng.normal(size=6), rng.normal(size=6), 1e-5
+    u, mean, var = oracle_mod.bn_fwd(z, g, b, eps)
+    zz = z.reshape(-1, 6)
+    np.testing.assert_allclose(mean, zz.mean(0), rtol=1e-13)
+    np.testing.assert_allclose(var, zz.var(0), rtol=1e-12)
+    uu = u.reshape(-1, 6)
+    np.testing.assert_allclose(uu.mean(0), b, atol=1e-12)
+    np.testing.assert_allclose(uu.var(0), g ** 2 * var / (var + eps), rtol=1e-10)
+    du = rng.normal(size=z.shape)
+    dz, dg, db = oracle_mod.bn_bwd(z, du, g, eps)
+    dzz = dz.reshape(-1, 6)
+    np.testing.assert_allclose(dzz.sum(0), 0, atol=1e-10)
+    zh = (zz - zz.mean(0)) / np.sqrt(zz.var(0) + eps)
+    # scale invariance up to eps: sum(dz * zh) = g * dgamma * eps / ((var + eps) * sqrt(var + eps))
+    np.testing.assert_allclose((dzz * zh).sum(0), g * dg * eps / ((var + eps) * np.sqrt(var + eps)),
+                               rtol=1e-6, atol=1e-12)
+    np.testing.assert_allclose(db, du.reshape(-1, 6).sum(0), rtol=1e-12)
+
+
+def test_bn_chain_finite_differences(oracle_mod):
+    """conv -> BN -> leaky ReLU -> max-pool, then conv -> BN -> leaky ReLU
+    (unpooled): dW, dgamma, dbeta of both blocks against central differences
+    of <g, y_top> (exact mode)."""
+    slope = 0.3
+    specs = [(1, "max", "bn"), (1, "none", "bn")]
+    ch = (2, 3, 2)
+    rng = np.random.default_rng(52)
+    for _ in range(300):
+        x = rng.normal(size=(2, 4, 4, 4, ch[0]))
+        ws = [rng.normal(size=(ch[l + 1], 3, 3, 3, ch[l])) for l in range(2)]
+        gs = [rng.normal(size=ch[l + 1]) for l in range(2)]
+        bs = [rng.normal(size=ch[l + 1]) * 0.5 for l in range(2)]
+        state = []
+        xs, ys, auxs = oracle_mod.chain_fwd(x, ws, bs, slope, specs, mirrored=False, gammas=gs, bn_state=state)
+        u0 = oracle_mod.bn_fwd(state[0][0], gs[0], bs[0])[0]
+        u1 = oracle_mod.bn_fwd(state[1][0], gs[1], bs[1])[0]
+        srt = np.sort(_window_view(u0), -1)
+        if (np.min(srt[..., -1] - srt[..., -2]) > 1e-3 and np.min(np.abs(srt[..., -1])) > 1e-3
+                and np.min(np.abs(u1)) > 1e-3 and np.any(u1 < 0) and np.any(srt[..., -1] < 0)):
+            break
+    else:
+        pytest.fail("could not draw a kink-free case")
+    g = rng.normal(size=ys[-1].shape)
+    dgs = [None, None]
+    dws, dbs, _ = oracle_mod.chain_bwd(xs, ys, auxs, ws, g, slope, specs, mirrored=False, gammas=gs,
+                                       bn_state=state, dgammas=dgs)
+
+    def loss(ws_, gs_, bs_):
+        return np.vdot(g, oracle_mod.chain_fwd(x, ws_, bs_, slope, specs, mirrored=False, gammas=gs_)[1][-1])
+
+    h = 1e-6
+    for l in range(2):
+        for _ in range(4):
+            pos = tuple(rng.integers(0, s) for s in ws[l].shape)
+            wp, wm = [w.copy() for w in ws], [w.copy() for w in ws]
+            wp[l][pos] += h
+            wm[l][pos] -= h
+            num = (loss(wp, gs, bs) - loss(wm, gs, bs)) / (2 * h)
+            assert abs(num - dws[l][pos]) <= 1e-5 * max(1.0, abs(num)), (l, pos, num, dws[l][pos])
+        for c in range(ch[l + 1]):
+            for arr, grad in ((gs, dgs[l]), (bs, dbs[l])):
+                ap, am = [a.copy() for a in arr], [a.copy() for a in arr]
+                ap[l][c] += h
+                am[l][c] -= h
+                if arr is gs:
+                    num = (loss(ws, ap, bs) - loss(ws, am, bs)) / (2 * h)
+                else:
+                    num = (loss(ws, gs, ap) - loss(ws, gs, am)) / (2 * h)
+                assert abs(num - grad[c]) <= 1e-5 * max(1.0, abs(num)), (l, c, num, grad[c])
