@@ -23,7 +23,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 CF_OK, CF_ERR_INVALID_ARG, CF_ERR_UNSUPPORTED, CF_ERR_WORKSPACE, CF_ERR_CUDA, CF_ERR_TIMEOUT = range(6)
-CF_OP_FWD, CF_OP_DGRAD, CF_OP_WGRAD, CF_OP_DGRAD_ROUTED, CF_OP_WGRAD_ROUTED, CF_OP_POOL_BWD = range(6)
+CF_OP_FWD, CF_OP_DGRAD, CF_OP_WGRAD, CF_OP_DGRAD_ROUTED, CF_OP_WGRAD_ROUTED, CF_OP_POOL_BWD, CF_OP_BN = range(7)
 CF_POOL_MAX, CF_POOL_AVG, CF_POOL_NONE = range(3)
 
 
@@ -51,6 +51,7 @@ _SIGS = {
     "cf_conv3d_fwd": ([_DP, _vp, _vp, _EP, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_conv3d_dgrad": ([_DP, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_conv3d_wgrad": ([_DP, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _sz, _vp], ctypes.c_int),
+    "cf_conv3d_dgrad_pool_bwd": ([_DP, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_bias_lrelu_pool_fwd": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _f32, _vp, _vp, _vp], ctypes.c_int),
     "cf_bias_lrelu_pool_bwd": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _sz, _vp],
                                ctypes.c_int),
@@ -59,6 +60,11 @@ _SIGS = {
     "cf_block_epilogue_fwd": ([_i32, _i64, _i64, _i64, _i64, _i32, _vp, _vp, _f32, _vp, _vp, _vp], ctypes.c_int),
     "cf_block_epilogue_bwd": ([_i32, _i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _sz,
                                _vp], ctypes.c_int),
+    "cf_bn_stats": ([_i64, _i32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "cf_bn_act_pool_fwd": ([_i32, _i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _vp, _vp],
+                           ctypes.c_int),
+    "cf_bn_act_pool_bwd": ([_i32, _i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _vp,
+                            _vp, _sz, _vp], ctypes.c_int),
     "cf_workspace_size": ([ctypes.c_int, _DP], _sz),
     "cf_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "cf_last_device_status": ([_vp], ctypes.c_int),
@@ -135,6 +141,14 @@ def cf_conv3d_dgrad(desc, dz, idx, w, x_act, slope, dx, ws=None, ws_bytes=0, str
     return _check(st, "cf_conv3d_dgrad") if check else st
 
 
+def cf_conv3d_dgrad_pool_bwd(desc, dz, w, x_act, slope, dx, prev_idx, prev_dz, ws=None, ws_bytes=0, stream=None,
+                             check=True, dsum=None):
+    st = _lib.cf_conv3d_dgrad_pool_bwd(ctypes.byref(_desc(desc)), _ptr(dz), _ptr(w), _ptr(x_act), float(slope),
+                                       _ptr(dx), _ptr(dsum), _ptr(prev_idx), _ptr(prev_dz), _ptr(ws), ws_bytes,
+                                       _stream(stream))
+    return _check(st, "cf_conv3d_dgrad_pool_bwd") if check else st
+
+
 def cf_conv3d_wgrad(desc, x, dz, idx, dw, accumulate=0, ws=None, ws_bytes=0, stream=None, check=True):
     st = _lib.cf_conv3d_wgrad(ctypes.byref(_desc(desc)), _ptr(x), _ptr(dz), _ptr(idx), _ptr(dw), int(accumulate),
                               _ptr(ws), ws_bytes, _stream(stream))
@@ -171,6 +185,25 @@ def cf_block_epilogue_bwd(pool, n, d, h, w, c, dy, y, aux, slope, dz, dy_pre, db
     st = _lib.cf_block_epilogue_bwd(int(pool), n, d, h, w, c, _ptr(dy), _ptr(y), _ptr(aux), float(slope), _ptr(dz),
                                     _ptr(dy_pre), _ptr(dbias), _ptr(ws), ws_bytes, _stream(stream))
     return _check(st, "cf_block_epilogue_bwd") if check else st
+
+
+def cf_bn_stats(rows, c, z, sums, ws=None, ws_bytes=0, stream=None, check=True):
+    st = _lib.cf_bn_stats(rows, c, _ptr(z), _ptr(sums), _ptr(ws), ws_bytes, _stream(stream))
+    return _check(st, "cf_bn_stats") if check else st
+
+
+def cf_bn_act_pool_fwd(pool, n, d, h, w, c, z, sums, gamma, beta, eps, slope, y, aux, stream=None, check=True):
+    st = _lib.cf_bn_act_pool_fwd(int(pool), n, d, h, w, c, _ptr(z), _ptr(sums), _ptr(gamma), _ptr(beta), float(eps),
+                                 float(slope), _ptr(y), _ptr(aux), _stream(stream))
+    return _check(st, "cf_bn_act_pool_fwd") if check else st
+
+
+def cf_bn_act_pool_bwd(pool, n, d, h, w, c, dy, y, aux, z, sums, gamma, eps, slope, dz, dsums, ws=None, ws_bytes=0,
+                       stream=None, check=True):
+    st = _lib.cf_bn_act_pool_bwd(int(pool), n, d, h, w, c, _ptr(dy), _ptr(y), _ptr(aux), _ptr(z), _ptr(sums),
+                                 _ptr(gamma), float(eps), float(slope), _ptr(dz), _ptr(dsums), _ptr(ws), ws_bytes,
+                                 _stream(stream))
+    return _check(st, "cf_bn_act_pool_bwd") if check else st
 
 
 def cf_last_device_status(stream=None) -> int:

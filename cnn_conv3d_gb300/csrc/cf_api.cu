@@ -167,6 +167,7 @@ size_t cf_workspace_size(int op, const cf_conv_desc* desc) {
         case CF_OP_WGRAD: return part + up;
         case CF_OP_WGRAD_ROUTED: return part + (wgrad_routed_fused(desc->c_in) ? 0 : dense);
         case CF_OP_POOL_BWD: return round_up(pool_bwd_workspace_bytes(ctx.num_sms, desc->c_out), 256);
+        case CF_OP_BN: return round_up(bn_workspace_bytes(ctx.num_sms, desc->c_out), 256);
     }
     return 0;
 }
@@ -211,10 +212,14 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
                              pool_kind, act, stride);
 }
 
-cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx, const uint16_t* w,
-                          const uint16_t* x_act, float slope, uint16_t* dx, float* dsum, void* ws,
-                          size_t ws_bytes, void* stream) {
+// Backward data; prev_idx / prev_dz (both or neither): the previous block's
+// max-pool backward fused into the epilogue (see cf_conv3d_dgrad_pool_bwd).
+static cf_status dgrad_impl(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx, const uint16_t* w,
+                            const uint16_t* x_act, float slope, uint16_t* dx, float* dsum, const uint8_t* prev_idx,
+                            uint16_t* prev_dz, void* ws, size_t ws_bytes, void* stream) {
     if (!desc_ok(desc) || dz == nullptr || w == nullptr || dx == nullptr) return CF_ERR_INVALID_ARG;
+    if ((prev_idx == nullptr) != (prev_dz == nullptr)) return CF_ERR_INVALID_ARG;
+    if ((prev_idx && !aligned16(prev_idx)) || (prev_dz && !aligned16(prev_dz))) return CF_ERR_INVALID_ARG;
     if (!aligned16(dz) || !aligned16(w) || !aligned16(dx) || (x_act && !aligned16(x_act)) ||
         (idx && !aligned16(idx)) || (ws && !aligned16(ws)) || (dsum && !aligned16(dsum)))
         return CF_ERR_INVALID_ARG;
@@ -259,15 +264,30 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
         if (fused && cudaMemsetAsync(part, 0, (size_t)ctx.num_sms * ci * sizeof(float), ctx.stream) != cudaSuccess)
             return CF_ERR_CUDA;
         st = launch_conv_halo(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt, epi, dx, nullptr,
-                              nullptr, x_act, slope, fused ? part : nullptr);
+                              nullptr, x_act, slope, fused ? part : nullptr, 0, 0, prev_dz, prev_idx);
         if (st != CF_OK || dsum == nullptr) return st;
         if (fused) return launch_colsum(ctx, part, ctx.num_sms, ci, dsum);
     } else {
         st = launch_conv_igemm(ctx, desc->n, desc->d, desc->h, desc->w, co, ci, dz_dense, wt, epi, dx, nullptr,
-                               nullptr, x_act, slope);
+                               nullptr, x_act, slope, 0, 0, 1, prev_dz, prev_idx);
         if (st != CF_OK || dsum == nullptr) return st;
     }
     return launch_channel_sums(ctx, dx, desc->n * desc->d * desc->h * desc->w, ci, part, dsum);
+}
+
+cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx, const uint16_t* w,
+                          const uint16_t* x_act, float slope, uint16_t* dx, float* dsum, void* ws,
+                          size_t ws_bytes, void* stream) {
+    return dgrad_impl(desc, dz, idx, w, x_act, slope, dx, dsum, nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+cf_status cf_conv3d_dgrad_pool_bwd(const cf_conv_desc* desc, const uint16_t* dz, const uint16_t* w,
+                                   const uint16_t* x_act, float slope, uint16_t* dx, float* dsum,
+                                   const uint8_t* prev_idx, uint16_t* prev_dz, void* ws, size_t ws_bytes,
+                                   void* stream) {
+    if (prev_idx == nullptr || prev_dz == nullptr) return CF_ERR_INVALID_ARG;
+    if (desc_stride(desc) != 1 || !desc_ok(desc)) return desc_ok(desc) ? CF_ERR_UNSUPPORTED : CF_ERR_INVALID_ARG;
+    return dgrad_impl(desc, dz, nullptr, w, x_act, slope, dx, dsum, prev_idx, prev_dz, ws, ws_bytes, stream);
 }
 
 cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* dz, const uint8_t* idx,
@@ -277,6 +297,7 @@ cf_status cf_conv3d_wgrad(const cf_conv_desc* desc, const uint16_t* x, const uin
         return CF_ERR_INVALID_ARG;
     if (idx && ((desc->d | desc->h | desc->w) & 1)) return CF_ERR_UNSUPPORTED;
     const int stride = desc_stride(desc);
+    if (!wgrad_shape_supported(desc->c_in, desc->c_out)) return CF_ERR_UNSUPPORTED;
     if (stride == 2 && (idx || desc->c_in == 1 || desc->c_in == 4)) return CF_ERR_UNSUPPORTED;
     LaunchCtx ctx;
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
@@ -366,6 +387,47 @@ cf_status cf_block_epilogue_bwd(int32_t pool, int64_t n, int64_t d, int64_t h, i
     if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
     if (pool == CF_POOL_AVG) return launch_avgpool_bwd(ctx, n, d, h, w, c, dy, aux, slope, dz, dbias, ws, ws_bytes);
     return launch_act_bwd(ctx, n * d * h * w * c, c, dy, y, slope, dz, dbias, ws, ws_bytes);
+}
+
+cf_status cf_bn_stats(int64_t rows, int32_t c, const uint16_t* z, float* sums, void* ws, size_t ws_bytes,
+                      void* stream) {
+    if (rows <= 0 || c <= 0 || z == nullptr || sums == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(z) || !aligned16(sums) || (ws && !aligned16(ws))) return CF_ERR_INVALID_ARG;
+    if (c % 8 != 0 || c > 2048) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_channel_stats(ctx, rows, c, z, sums, ws, ws_bytes);
+}
+
+cf_status cf_bn_act_pool_fwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c, const uint16_t* z,
+                             const float* sums, const float* gamma, const float* beta, float eps, float slope,
+                             uint16_t* y, uint8_t* aux, void* stream) {
+    if (n <= 0 || d <= 0 || h <= 0 || w <= 0 || c <= 0 || !z || !sums || !gamma || !beta || !y)
+        return CF_ERR_INVALID_ARG;
+    if (pool < CF_POOL_MAX || pool > CF_POOL_NONE || !(eps >= 0.f)) return CF_ERR_INVALID_ARG;
+    if (!aligned16(z) || !aligned16(y) || !aligned16(sums) || (aux && !aligned16(aux))) return CF_ERR_INVALID_ARG;
+    if (c % 8 != 0 || (pool != CF_POOL_NONE && ((d | h | w) & 1))) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_bn_act_pool_fwd(ctx, pool, n, d, h, w, c, z, sums, gamma, beta, eps, slope, y, aux);
+}
+
+cf_status cf_bn_act_pool_bwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                             const uint16_t* dy, const uint16_t* y, const uint8_t* aux, const uint16_t* z,
+                             const float* sums, const float* gamma, float eps, float slope, uint16_t* dz,
+                             float* dsums, void* ws, size_t ws_bytes, void* stream) {
+    if (n <= 0 || d <= 0 || h <= 0 || w <= 0 || c <= 0 || !dy || !z || !sums || !gamma || !dz || !dsums)
+        return CF_ERR_INVALID_ARG;
+    if (pool < CF_POOL_MAX || pool > CF_POOL_NONE || !(eps >= 0.f)) return CF_ERR_INVALID_ARG;
+    if (pool != CF_POOL_NONE && aux == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(dy) || (y && !aligned16(y)) || (aux && !aligned16(aux)) || !aligned16(z) || !aligned16(dz) ||
+        !aligned16(dsums) || (ws && !aligned16(ws)))
+        return CF_ERR_INVALID_ARG;
+    if (c % 8 != 0 || c > 2048 || (pool != CF_POOL_NONE && ((d | h | w) & 1))) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_bn_act_pool_bwd(ctx, pool, n, d, h, w, c, dy, y, aux, z, sums, gamma, eps, slope, dz, dsums, ws,
+                                  ws_bytes);
 }
 
 }  // extern "C"

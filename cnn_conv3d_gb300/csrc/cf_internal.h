@@ -22,7 +22,11 @@ enum : int {
     WAIT_PROBE = 0x1FF,
 };
 
-enum EpiMode : int { EPI_PLAIN = 0, EPI_POOL = 1, EPI_DGRAD = 2 };
+// Epilogue of a conv kernel (a compile-time mode): plain bf16 store, max-pool
+// (+ bias, leaky ReLU, argmax codes), backward-data leaky-ReLU derivative,
+// average pool of the activated window (+ sign masks), bias + leaky ReLU
+// without pooling.
+enum EpiMode : int { EPI_PLAIN = 0, EPI_POOL = 1, EPI_DGRAD = 2, EPI_AVG = 3, EPI_ACT = 4 };
 
 struct LaunchCtx {
     cudaStream_t stream;
@@ -56,7 +60,8 @@ bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* b
 cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                             int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
                             uint8_t* idx, const float* bias, const uint16_t* x_act, float slope,
-                            int pool_kind = 0, int act = 0, int stride = 1);
+                            int pool_kind = 0, int act = 0, int stride = 1, uint16_t* route_dz = nullptr,
+                            const uint8_t* route_idx = nullptr);
 
 // conv_halo.cu: same contract as launch_conv_igemm (stride 1) for c_in % 16 == 0
 // and c_out in {32, 64, 128}, reading A from one halo tile per channel chunk.
@@ -66,7 +71,8 @@ bool halo_path_supported(int c_in, int c_out);
 cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                            int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,
                            uint8_t* idx, const float* bias, const uint16_t* x_act, float slope,
-                           float* colsum_part = nullptr, int pool_kind = 0, int act = 0);
+                           float* colsum_part = nullptr, int pool_kind = 0, int act = 0,
+                           uint16_t* route_dz = nullptr, const uint8_t* route_idx = nullptr);
 
 // conv_smallc.cu: forward conv for c_in in {1,4} (im2col operand in tensor memory).
 cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
@@ -83,6 +89,8 @@ cf_status launch_wgrad_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
 
 // conv_wgrad.cu -------------------------------------------------------------
 size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out);
+// the (c_in, c_out) pairs launch_wgrad implements
+bool wgrad_shape_supported(int c_in, int c_out);
 // true when launch_wgrad takes the routed form (idx != NULL: dz pooled, the
 // dense dZ expanded on chip) for this c_in
 bool wgrad_routed_fused(int c_in);
@@ -122,6 +130,21 @@ cf_status launch_colsum(const LaunchCtx& ctx, const float* partial, int rows, in
 size_t channel_sums_workspace_bytes(int num_sms, int c);
 cf_status launch_channel_sums(const LaunchCtx& ctx, const uint16_t* x, int64_t rows, int c, float* partial,
                               float* out);
+// Batch normalisation (training mode): the per-channel sums of z and z^2
+// ([2c] fp32, fixed order) of rows x c bf16; the normalisation + leaky ReLU +
+// pooling (pool 0 max, 1 average, 2 none) from those sums; and the backward,
+// du implicit from the pooling backward, dsums = [dbeta, dgamma] ([2c]), dz
+// written dense.  Workspace: bn_workspace_bytes.
+size_t bn_workspace_bytes(int num_sms, int c);
+cf_status launch_channel_stats(const LaunchCtx& ctx, int64_t rows, int c, const uint16_t* z, float* sums, void* ws,
+                               size_t ws_bytes);
+cf_status launch_bn_act_pool_fwd(const LaunchCtx& ctx, int pool, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                                 const uint16_t* z, const float* sums, const float* gamma, const float* beta,
+                                 float eps, float slope, uint16_t* y, uint8_t* aux);
+cf_status launch_bn_act_pool_bwd(const LaunchCtx& ctx, int pool, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                                 const uint16_t* dy, const uint16_t* y, const uint8_t* aux, const uint16_t* z,
+                                 const float* sums, const float* gamma, float eps, float slope, uint16_t* dz,
+                                 float* dsums, void* ws, size_t ws_bytes);
 cf_status launch_timeout_probe(const LaunchCtx& ctx);
 
 }  // namespace cf

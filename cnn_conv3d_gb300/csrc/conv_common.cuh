@@ -68,15 +68,45 @@ struct EpiArgs {
     // backward-data only: per-CTA channel sums of the stored outputs,
     // [gridDim.x][C] fp32 (rows of CTAs without tiles stay as they were), or NULL
     float* colsum_part = nullptr;
-    // EPI_POOL: 0 = max-pool of the pre-activation (idx: first-maximum codes),
-    // 1 = average of the activated window (idx: sign masks, bit dd*4+dh*2+dw
-    // set where z + b > 0)
-    int pool_kind = 0;
-    // EPI_PLAIN: 1 = y = LReLU(z + b) (an unpooled block), 0 = y = z
-    int act = 0;
+    // EPI_DGRAD, optional: the previous block's max-pool backward fused in.  The
+    // stored output (the previous block's pooled pre-activation gradient g, same
+    // NDHWC grid as y) is also routed to its window's argmax voxel in route_dz
+    // ([n][2d][2h][2w][C] bf16, zero at the other seven voxels), by the codes
+    // route_idx (same grid as y).
+    uint16_t* route_dz = nullptr;
+    const uint8_t* route_idx = nullptr;
 };
 
 __device__ __forceinline__ float lrelu(float s, float slope) { return s > 0.f ? s : slope * s; }
+
+// 32-bit masks, all ones where the code byte of a channel differs from `code`
+// (channels 2h, 2h+1 of the word: half h).  Bit 7 of each byte of
+// ((b ^ code) & 0x7f) + 0x7f, or of b ^ code, is set iff the byte differs; the
+// permute replicates that bit over two bytes.
+__device__ __forceinline__ void code_mismatch(uint32_t codes4, uint32_t code4, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = codes4 ^ code4;
+    const uint32_t nz = ((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x;
+    asm("prmt.b32 %0, %1, 0, 0x9988;" : "=r"(lo) : "r"(nz));
+    asm("prmt.b32 %0, %1, 0, 0xBBAA;" : "=r"(hi) : "r"(nz));
+}
+
+// Max-pool backward of one pooled voxel x 8 channels: the bf16 values `pk`
+// (channels 2i, 2i+1 in word i) written to the window voxel whose code
+// dd*4+dh*2+dw the channel's code byte (cv) names, zero to the other seven.
+// dz0 points at channel c0 of window voxel (0,0,0); the window's other voxels
+// are dw*ws + dh*hs + dd*ds elements away.
+__device__ __forceinline__ void route_window(uint16_t* dz0, uint4 pk, uint2 cv, int64_t ws, int64_t hs,
+                                             int64_t ds) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t code4 = (uint32_t)k * 0x01010101u;
+        uint32_t m0, m1, m2, m3;
+        code_mismatch(cv.x, code4, m0, m1);
+        code_mismatch(cv.y, code4, m2, m3);
+        *reinterpret_cast<uint4*>(dz0 + (k >> 2) * ds + ((k >> 1) & 1) * hs + (k & 1) * ws) =
+            make_uint4(pk.x & ~m0, pk.y & ~m1, pk.z & ~m2, pk.w & ~m3);
+    }
+}
 
 // Epilogue of one tile, executed by the 128 epilogue threads (4 warps whose
 // warp index modulo 4 is q; thread row = 32*q + lane is TMEM lane = GEMM row).
@@ -103,7 +133,7 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
         else
             tmem_ld16(lane_addr + c, r);
         tmem_ld_wait();
-        if (EPI == EPI_POOL) {
+        if (EPI == EPI_POOL || EPI == EPI_AVG) {
 #pragma unroll
             for (int k = 0; k < CH; ++k) stg[row * 33 + k] = __uint_as_float(r[k]);
             named_bar_sync(1, 128);
@@ -122,7 +152,7 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
                 for (int cc = 0; cc < CPT; ++cc) {
                     const int co = tc.co0 + c + cb + cc;
                     const float b = (ea.bias != nullptr && co < g.Cout) ? ea.bias[co] : 0.f;
-                    if (ea.pool_kind == 1) {
+                    if (EPI == EPI_AVG) {
                         // average of the activated window; code = the window's sign mask
                         float sum = 0.f;
                         int mask = 0;
@@ -176,7 +206,7 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
                 float v[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(r[q8 * 8 + k]);
-                if (EPI == EPI_PLAIN && ea.act) {
+                if (EPI == EPI_ACT) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         v[k] = lrelu(v[k] + (ea.bias ? ea.bias[tc.co0 + c + q8 * 8 + k] : 0.f), ea.slope);
@@ -198,6 +228,14 @@ __device__ __forceinline__ void conv_epilogue(const ConvGeom& g, const TileCoord
                 pk.z = pack_bf16x2(v[4], v[5]);
                 pk.w = pack_bf16x2(v[6], v[7]);
                 *reinterpret_cast<uint4*>(ea.y + o + q8 * 8) = pk;
+                if (EPI == EPI_DGRAD && ea.route_dz != nullptr) {
+                    const uint2 cv = *reinterpret_cast<const uint2*>(ea.route_idx + o + q8 * 8);
+                    const int64_t ws = g.Cout, hs = 2 * (int64_t)g.W * g.Cout, ds = 4 * (int64_t)g.H * g.W * g.Cout;
+                    uint16_t* dz0 = ea.route_dz +
+                                    ((((int64_t)tc.n * 2 * g.D + 2 * d) * 2 * g.H + 2 * h) * 2 * g.W + 2 * w) * g.Cout +
+                                    tc.co0 + c + q8 * 8;
+                    route_window(dz0, pk, cv, ws, hs, ds);
+                }
             }
         }
     }

@@ -39,7 +39,7 @@ struct IgemmCfg {
     static constexpr uint32_t A_BYTES = BM * KC * 2;
     static constexpr uint32_t B_BYTES = BN * KC * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t STG_BYTES = EPI == EPI_POOL ? 128 * 33 * 4 : 0;
+    static constexpr uint32_t STG_BYTES = (EPI == EPI_POOL || EPI == EPI_AVG) ? 128 * 33 * 4 : 0;
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr uint32_t BUDGET = 227 * 1024 - 1024 - STG_BYTES - BAR_BYTES;
     static constexpr int STAGES_RAW = (int)(BUDGET / STAGE_BYTES);
@@ -290,6 +290,8 @@ static cf_status dispatch_epi(const LaunchCtx& ctx, const ConvGeom& g, const uin
     switch (epi) {
         case EPI_PLAIN: return run_igemm<BN, KC, EPI_PLAIN>(ctx, g, x, wk, ea, in_d, in_h, in_w, stride);
         case EPI_POOL: return run_igemm<BN, KC, EPI_POOL>(ctx, g, x, wk, ea, in_d, in_h, in_w, stride);
+        case EPI_AVG: return run_igemm<BN, KC, EPI_AVG>(ctx, g, x, wk, ea, in_d, in_h, in_w, stride);
+        case EPI_ACT: return run_igemm<BN, KC, EPI_ACT>(ctx, g, x, wk, ea, in_d, in_h, in_w, stride);
         case EPI_DGRAD: return run_igemm<BN, KC, EPI_DGRAD>(ctx, g, x, wk, ea, in_d, in_h, in_w, stride);
     }
     return CF_ERR_INVALID_ARG;
@@ -298,15 +300,22 @@ static cf_status dispatch_epi(const LaunchCtx& ctx, const ConvGeom& g, const uin
 cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                             const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
                             const float* bias, const uint16_t* x_act, float slope, int pool_kind, int act,
-                            int stride) {
+                            int stride, uint16_t* route_dz, const uint8_t* route_idx) {
     if (c_in % 16 != 0 || c_out % 16 != 0) return CF_ERR_UNSUPPORTED;
     if (stride != 1 && (stride != 2 || epi == EPI_DGRAD)) return CF_ERR_UNSUPPORTED;
     const int64_t in_d = d, in_h = h, in_w = w;
     d = (d + stride - 1) / stride;  // from here on: the output sizes
     h = (h + stride - 1) / stride;
     w = (w + stride - 1) / stride;
-    int bn = c_out <= 256 ? c_out : 256;
-    if (c_out > 256 && c_out % 256 != 0) return CF_ERR_UNSUPPORTED;
+    // N tile: the narrowest compiled width that holds c_out (at most 256; the
+    // filter rows past c_out read as zero, out-of-bounds fill, and the
+    // epilogues skip those channels)
+    int bn = 256;
+    for (int b : {16, 32, 64, 96, 128, 192, 256})
+        if (c_out <= b) {
+            bn = b;
+            break;
+        }
     // Small grids: narrower N tiles when that clearly shortens the critical
     // path (by 20%: narrower tiles re-fetch A once more per N tile).  Cost of a
     // CTA's share = waves x cycles per K step of one MMA 128 x bn x 16,
@@ -325,8 +334,10 @@ cf_status launch_conv_igemm(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
     }
     const int kc = (c_in % 64 == 0) ? 64 : (c_in % 32 == 0 ? 32 : 16);
     EpiArgs ea{y, idx, bias, x_act, slope};
-    ea.pool_kind = pool_kind;
-    ea.act = act;
+    if (epi == EPI_POOL && pool_kind == 1) epi = EPI_AVG;
+    if (epi == EPI_PLAIN && act) epi = EPI_ACT;
+    ea.route_dz = route_dz;
+    ea.route_idx = route_idx;
     ConvGeom g = make_geom(n, d, h, w, c_in, c_out, bn);
 #define CF_BN_CASE(B)                                                                              \
     case B:                                                                                        \

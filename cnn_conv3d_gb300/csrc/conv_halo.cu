@@ -17,6 +17,17 @@
 // the L2->SM traffic of A by ~10x against per-tap loads; the filter slab of
 // each tap streams through a separate ring.
 //
+// Plane pairs (GEMM N <= 64): halo plane p feeds output plane 0 through tap
+// row kd = p and output plane 1 through kd = p - 1 with the SAME A operand, so
+// for p = 1, 2 one MMA of width 2*N takes B = the two filter slabs stacked
+// (kd = p above kd = p - 1: the resident filter keeps, per (kh, kw), the slabs
+// in the order kd = 2, 1, 0) and writes both planes' accumulators, which lie
+// N columns apart.  Per (kh, kw) and k step that is 4 MMAs (two of width 2N,
+// two of width N for p = 0, 3) instead of 6, and A is read from shared memory
+// 4 times instead of 6.  Issuer warp 1 takes halo planes 0, 1 and warp 6
+// planes 2, 3, each into its own pair of plane accumulators; the epilogue
+// adds the two.
+//
 // Epilogues: plain bf16 store, backward-data leaky-ReLU derivative, or the
 // CosmoFlow bias + leaky ReLU + 2x2x2 max-pool: the two planes of a window
 // are in the same TMEM lane (two accumulators), the w and h neighbours are
@@ -28,6 +39,7 @@ namespace cf {
 
 template <int BN, int KC, int EPI, bool RES>
 struct HaloCfg {
+    static constexpr bool STK = BN <= 64;  // plane pairs stacked into one MMA (see above)
     static constexpr uint32_t ROW = KC * 2;
     static constexpr uint32_t HALO_BYTES = H_ROWS * ROW;  // 23040, 46080 or 92160
     static constexpr uint32_t HALO_STRIDE = (HALO_BYTES + 1023) / 1024 * 1024;
@@ -41,10 +53,13 @@ struct HaloCfg {
     static constexpr uint32_t SWZ = KC == 64 ? SWZ_128B : (KC == 32 ? SWZ_64B : SWZ_32B);
     static constexpr uint32_t SBO_A = HH_W * ROW;  // one halo line
     static constexpr uint32_t SBO_B = 8 * ROW;
-    static constexpr uint32_t TMEM_COLS = 4 * BN <= 128 ? 128 : (4 * BN <= 256 ? 256 : 512);
+    // per tile buffer: plane 0 | plane 1 (BN columns each), one pair per issuer when stacked
+    static constexpr uint32_t ACC_STRIDE = STK ? 4 * BN : 2 * BN;
+    static constexpr uint32_t TMEM_COLS = 2 * ACC_STRIDE <= 128 ? 128 : (2 * ACC_STRIDE <= 256 ? 256 : 512);
     static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
+    static constexpr uint32_t IDESC2 = idesc_bf16(128, STK ? 2 * BN : BN, 0, 0);
     static_assert(RES || WS >= 3, "shared memory");
-    static_assert(4 * BN <= 512, "tensor memory");
+    static_assert(2 * ACC_STRIDE <= 512, "tensor memory");
     // shared memory: halo ring, then either the resident filter (n_chunks * 27
     // slabs, sized at launch) or the streamed filter ring
     static uint32_t smem_bytes(int n_chunks) {
@@ -118,8 +133,12 @@ __global__ void __launch_bounds__(224, 1)
             if (RES && blockIdx.x < p.num_tiles) {
                 mbar_arrive_expect_tx(wres, (uint32_t)p.n_chunks * 27 * C::W_BYTES);
                 for (int ch = 0; ch < p.n_chunks; ++ch)
-                    for (int tap = 0; tap < 27; ++tap)
-                        tma_load_2d(wsm + (ch * 27 + tap) * C::W_BYTES, &tmW, wres, tap * p.Cin + ch * KC, 0);
+                    for (int tap = 0; tap < 27; ++tap) {
+                        // stacked: slot (kh, kw, 2 - kd); else slot = tap
+                        const int kd = tap / 9, r = tap - 9 * kd;
+                        const int slot = C::STK ? r * 3 + (2 - kd) : tap;
+                        tma_load_2d(wsm + (ch * 27 + slot) * C::W_BYTES, &tmW, wres, tap * p.Cin + ch * KC, 0);
+                    }
                 res_issued = true;
             }
             for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
@@ -145,9 +164,11 @@ __global__ void __launch_bounds__(224, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&wfull[ws], C::TPS * C::W_BYTES);
+                        // a stage: stacked, the kd = 2, 1, 0 slabs of (kh, kw) = g; else the
+                        // kw = 0, 1, 2 slabs of (kd, kh) = g
                         for (int u = 0; u < C::TPS; ++u)
                             tma_load_2d(wsm + (ws * C::TPS + u) * C::W_BYTES, &tmW, &wfull[ws],
-                                        (g * C::TPS + u) * p.Cin + ch * KC, t.co0);
+                                        (C::STK ? (2 - u) * 9 + g : g * C::TPS + u) * p.Cin + ch * KC, t.co0);
                         wiss |= 1u << ws;
                         wpar = (wpar & ~(1u << ws)) | (wph << ws);
                         if (++ws == C::WS) {
@@ -186,7 +207,7 @@ __global__ void __launch_bounds__(224, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + acc * 2 * BN;
+                const uint32_t d0 = tmem_base + acc * C::ACC_STRIDE;
                 for (int ch = 0; ch < p.n_chunks && ok; ++ch) {
                     if (!mbar_wait(&hfull[hs], hph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
                         ok = false;
@@ -208,18 +229,37 @@ __global__ void __launch_bounds__(224, 1)
                             bg = bdesc0 + ((ws * C::TPS * C::W_BYTES) >> 4);
                         }
                         tc_fence_after();
+                        constexpr uint32_t plane_rows = HH_H * HH_W;
+                        const uint32_t first = (ch | g) != 0;
+                        if (C::STK) {
+                            // (kh, kw) = g; slabs kd = 2, 1, 0 at bg, +1, +2 slab.  Issuer i
+                            // owns halo planes 2i, 2i+1 and accumulator pair i; the wide MMA
+                            // goes first (it starts both planes' sums on the first group)
+                            const int kh = g / 3, kw = g % 3;
+                            const int pw = 1 + i, pn = 3 * i;  // wide / narrow halo plane
+                            const uint32_t dp = d0 + i * 2 * BN;
+                            const uint64_t aw = ah + (((uint32_t)((pw * HH_H + kh) * HH_W + kw) * C::ROW) >> 4);
+                            const uint64_t an = ah + (((uint32_t)((pn * HH_H + kh) * HH_W + kw) * C::ROW) >> 4);
+                            const uint64_t bw = bg + (((uint32_t)(1 - i) * C::W_BYTES) >> 4);  // kd = 1 / 2, then kd - 1
+                            const uint64_t bn = bg + (((uint32_t)(i == 0 ? 2 : 0) * C::W_BYTES) >> 4);  // kd = 0 / 2
+#pragma unroll
+                            for (int k = 0; k < KC / 16; ++k)
+                                umma_bf16(dp, aw + ((k * 32) >> 4), bw + ((k * 32) >> 4), C::IDESC2, (first | k) != 0);
+#pragma unroll
+                            for (int k = 0; k < KC / 16; ++k)
+                                umma_bf16(dp + i * BN, an + ((k * 32) >> 4), bn + ((k * 32) >> 4), C::IDESC, 1u);
+                        } else {
                         const int kd = g / 3, kh = g % 3;
                         const uint64_t ag = ah + (((uint32_t)((kd * HH_H + kh) * HH_W) * C::ROW) >> 4);
-                        const uint32_t first = (ch | g) != 0;
 #pragma unroll
                         for (int kw = 0; kw < 3; ++kw) {
                             const uint64_t bw = bg + ((kw * C::W_BYTES) >> 4);
 #pragma unroll
                             for (int k = 0; k < KC / 16; ++k) {
-                                constexpr uint32_t plane_rows = HH_H * HH_W;
                                 const uint64_t ad = ag + (((i * plane_rows + kw) * C::ROW + k * 32) >> 4);
                                 umma_bf16(d0 + i * BN, ad, bw + ((k * 32) >> 4), C::IDESC, (first | kw | k) != 0);
                             }
+                        }
                         }
                         if (!RES) {
                             umma_commit(&wempty[ws]);
@@ -251,7 +291,7 @@ __global__ void __launch_bounds__(224, 1)
         // unpooled outputs with BN <= 32, on request: channel sums of the stored
         // outputs (in backward data, the bias gradient of the previous block), per
         // thread over its tiles, then over the CTA
-        constexpr bool DSUM = EPI != EPI_POOL && BN <= 32;
+        constexpr bool DSUM = (EPI == EPI_PLAIN || EPI == EPI_DGRAD) && BN <= 32;
         const bool dsum_on = DSUM && p.ea.colsum_part != nullptr;
         float dsum[DSUM ? BN : 1];
 #pragma unroll
@@ -262,7 +302,8 @@ __global__ void __launch_bounds__(224, 1)
             if (!epi_wait(&tfull[acc], use & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
             tc_fence_after();
             const HTile t = halo_decode(p, tile, BN);
-            halo_epilogue<BN, EPI>(p, t, tmem_base, acc * 2 * BN, q, lane, 0, 0, dsum_on ? dsum : nullptr);
+            halo_epilogue<BN, EPI>(p, t, tmem_base, acc * C::ACC_STRIDE, q, lane, 0, 0, dsum_on ? dsum : nullptr,
+                                   C::STK ? acc * C::ACC_STRIDE + 2 * BN : 0xFFFFFFFFu);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
@@ -325,6 +366,8 @@ static cf_status halo_epi(const LaunchCtx& ctx, const HaloParams& p, const uint1
     switch (epi) {
         case EPI_PLAIN: return run_halo<BN, KC, EPI_PLAIN, RES>(ctx, p, x, wk);
         case EPI_POOL: return run_halo<BN, KC, EPI_POOL, RES>(ctx, p, x, wk);
+        case EPI_AVG: return run_halo<BN, KC, EPI_AVG, RES>(ctx, p, x, wk);
+        case EPI_ACT: return run_halo<BN, KC, EPI_ACT, RES>(ctx, p, x, wk);
         case EPI_DGRAD: return run_halo<BN, KC, EPI_DGRAD, RES>(ctx, p, x, wk);
     }
     return CF_ERR_INVALID_ARG;
@@ -342,9 +385,11 @@ bool halo_path_supported(int c_in, int c_out) {
 cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                            const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y, uint8_t* idx,
                            const float* bias, const uint16_t* x_act, float slope, float* colsum_part, int pool_kind,
-                           int act) {
+                           int act, uint16_t* route_dz, const uint8_t* route_idx) {
     if (!halo_path_supported(c_in, c_out)) return CF_ERR_UNSUPPORTED;
-    if (colsum_part && (epi == EPI_POOL || c_out > 32)) return CF_ERR_UNSUPPORTED;
+    if (epi == EPI_POOL && pool_kind == 1) epi = EPI_AVG;
+    if (epi == EPI_PLAIN && act) epi = EPI_ACT;
+    if (colsum_part && (!(epi == EPI_PLAIN || epi == EPI_DGRAD) || c_out > 32)) return CF_ERR_UNSUPPORTED;
     HaloParams p;
     p.N = (int)n;
     p.D = (int)d;
@@ -360,8 +405,8 @@ cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
     set_tile_dividers(p);
     p.n_chunks = 0;
     p.ea = EpiArgs{y, idx, bias, x_act, slope, colsum_part};
-    p.ea.pool_kind = pool_kind;
-    p.ea.act = act;
+    p.ea.route_dz = route_dz;
+    p.ea.route_idx = route_idx;
     p.status = ctx.status;
     p.wait_ns = ctx.wait_ns;
     // The whole filter stays in shared memory when it fits beside two halo

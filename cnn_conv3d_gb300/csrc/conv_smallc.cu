@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(608, 1)
             for (int ps = 0; ps < NPASS; ++ps) {
                 const int c = 32 * ps + 16 * half;  // first of the warp's 16 accumulator columns
                 if (c >= BN) break;
-                if (EPI == EPI_POOL) {
+                if (EPI == EPI_POOL || EPI == EPI_AVG) {
                     // per channel: first maximum over the lane's four (plane, line) values,
                     // in the window's scan order (code dd*4 + dh*2 + dw)
                     uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(608, 1)
                     }
                     float y[8];
                     uint32_t codes[2] = {0u, 0u};
-                    if (p.ea.pool_kind == 1) {
+                    if (EPI == EPI_AVG) {
                         // average of the activated window: the lane's four (plane, line)
                         // values, then the partner lane's (the w neighbour); code = the
                         // window's sign mask, bit dd*4 + dh*2 + dw
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(608, 1)
                         const int d = t.d0 + (blk >> 1), h = t.h0 + 2 * lp + (blk & 1), w = t.w0 + v;
                         if (d >= p.D || h >= p.H || w >= p.W) continue;
                         const int64_t o = ((((int64_t)t.n * p.D + d) * p.H + h) * p.W + w) * p.Cout + co0 + c;
-                        if (p.ea.act) {  // unpooled block: bias + leaky ReLU
+                        if (EPI == EPI_ACT) {  // unpooled block: bias + leaky ReLU
 #pragma unroll
                             for (int q = 0; q < 16; ++q) {
                                 const int co = co0 + c + q;
@@ -516,6 +516,8 @@ template <int CIN, int BN>
 static cf_status smallc_epi(const LaunchCtx& ctx, const HaloParams& hp, const uint16_t* x, const uint16_t* wk,
                             int epi) {
     if (epi == EPI_POOL) return run_smallc<CIN, BN, EPI_POOL>(ctx, hp, x, wk);
+    if (epi == EPI_AVG) return run_smallc<CIN, BN, EPI_AVG>(ctx, hp, x, wk);
+    if (epi == EPI_ACT) return run_smallc<CIN, BN, EPI_ACT>(ctx, hp, x, wk);
     if (epi == EPI_PLAIN) return run_smallc<CIN, BN, EPI_PLAIN>(ctx, hp, x, wk);
     return CF_ERR_UNSUPPORTED;
 }
@@ -544,8 +546,8 @@ cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t
     set_tile_dividers(hp);
     hp.n_chunks = 1;
     hp.ea = EpiArgs{y, idx, bias, nullptr, slope};
-    hp.ea.pool_kind = pool_kind;
-    hp.ea.act = act;
+    if (epi == EPI_POOL && pool_kind == 1) epi = EPI_AVG;
+    if (epi == EPI_PLAIN && act) epi = EPI_ACT;
     hp.status = ctx.status;
     hp.wait_ns = ctx.wait_ns;
 #define CF_SC_CASE(B)                                                        \

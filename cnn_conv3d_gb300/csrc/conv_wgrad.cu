@@ -319,6 +319,12 @@ static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_
 
 bool wgrad_routed_fused(int c_in) { return c_in == 1 || c_in == 4; }
 
+bool wgrad_shape_supported(int c_in, int c_out) {
+    const bool small = c_in == 1 || c_in == 4;
+    if (!small && c_in % 16 != 0) return false;
+    return c_out % 16 == 0 && (!small || c_out <= 256);
+}
+
 size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out) {
     if (wgrad_halo_supported(c_in, c_out))
         return wgrad_halo_workspace_bytes(num_sms, n, d, h, w, c_in, c_out);
@@ -389,10 +395,8 @@ static cf_status launch_splitk_reduce(const LaunchCtx& ctx, const float* part, f
 cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                        const uint16_t* x, const uint16_t* dz, const uint8_t* idx, float* dw, int accumulate, void* ws,
                        size_t ws_bytes) {
-    if (!(c_in == 1 || c_in == 4 || c_in % 16 == 0)) return CF_ERR_UNSUPPORTED;
+    if (!wgrad_shape_supported(c_in, c_out)) return CF_ERR_UNSUPPORTED;
     if (idx && !wgrad_routed_fused(c_in)) return CF_ERR_UNSUPPORTED;
-    if (c_out % 16 != 0) return CF_ERR_UNSUPPORTED;
-    if ((c_in == 1 || c_in == 4) && c_out > 256) return CF_ERR_UNSUPPORTED;
     if ((c_in == 1 || c_in == 4) && (w * c_in) % 8 != 0) return CF_ERR_UNSUPPORTED;
     const size_t need = wgrad_workspace_bytes(ctx.num_sms, n, d, h, w, c_in, c_out);
     if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;

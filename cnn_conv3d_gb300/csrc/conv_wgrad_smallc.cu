@@ -95,17 +95,6 @@ __device__ __forceinline__ int dz_chunk_xor(int r) {
     return SUBB == 64 ? (r & 7) : (SUBB == 32 ? ((r >> 1) & 3) : ((r >> 2) & 1));
 }
 
-// 16-bit masks, all ones where the code byte of a channel differs from `code`
-// (channels 2h, 2h+1 of the word: half h).  Bit 7 of each byte of
-// ((b ^ code) & 0x7f) + 0x7f, or of b ^ code, is set iff the byte differs; the
-// permute replicates that bit over two bytes.
-__device__ __forceinline__ void code_mismatch(uint32_t codes4, uint32_t code4, uint32_t& lo, uint32_t& hi) {
-    const uint32_t x = codes4 ^ code4;
-    const uint32_t nz = ((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x;
-    asm("prmt.b32 %0, %1, 0, 0x9988;" : "=r"(lo) : "r"(nz));
-    asm("prmt.b32 %0, %1, 0, 0xBBAA;" : "=r"(hi) : "r"(nz));
-}
-
 // Box bookkeeping shared by the roles: each walks its CTA's units in order
 // and the boxes of each unit in order; lb counts the CTA's boxes.
 template <int CIN, int BN, int SUBB, bool ROUTED>

@@ -425,6 +425,241 @@ __global__ void upsample2_kernel(const uint16_t* __restrict__ dz, uint16_t* __re
     }
 }
 
+// ---------------------------------------------------------------------------
+// Batch normalisation after the conv (hybrid-parallelism page, section IV),
+// training mode: per-channel statistics of the stored conv output z over all
+// n and voxels.
+
+// Per-thread sums of one 8-channel group of z and of its squares over the rows
+// i, i + stride, ... (fixed order); partial[block][2C]: sums, then squares.
+__global__ void channel_stats_kernel(const uint16_t* __restrict__ z, float* __restrict__ partial, int64_t total8,
+                                     int C) {
+    extern __shared__ float red[];  // [blockDim][16]
+    const int C8 = C / 8;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total8; i += stride) {
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(z) + i), f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            s[c] += f[c];
+            q[c] = fmaf(f[c], f[c], q[c]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        red[threadIdx.x * 16 + c] = s[c];
+        red[threadIdx.x * 16 + 8 + c] = q[c];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < 2 * C; e += blockDim.x) {
+        const int which = e / C, ch = e % C, cg = ch / 8, c = ch % 8;
+        float acc = 0.f;
+        for (int t = cg; t < (int)blockDim.x; t += C8) acc += red[t * 16 + 8 * which + c];
+        partial[(int64_t)blockIdx.x * 2 * C + e] = acc;
+    }
+}
+
+// Batch statistics of channel ch from the sums: mean and 1 / sqrt(var + eps),
+// var = E[z^2] - mean^2 (in fp64 from the fp32 channel sums).
+__device__ __forceinline__ void bn_stats(const float* __restrict__ sums, int C, int ch, double count, float eps,
+                                         double& mean, double& inv) {
+    mean = (double)sums[ch] / count;
+    const double var = fmax((double)sums[C + ch] / count - mean * mean, 0.0);
+    inv = 1.0 / sqrt(var + (double)eps);
+}
+
+// Normalisation coefficients: u = a * z + b, a = gamma * inv, b = beta - mean * a.
+__device__ __forceinline__ void bn_coef(const float* __restrict__ sums, int C, int ch, double count,
+                                        const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
+                                        float& a, float& b) {
+    double m, iv;
+    bn_stats(sums, C, ch, count, eps, m, iv);
+    a = (float)((double)gamma[ch] * iv);
+    b = (float)((double)beta[ch] - m * (double)gamma[ch] * iv);
+}
+
+// u = a*z + b, then the block's activation and pooling (POOL: 0 max with
+// codes, 1 average with sign masks, 2 none), one thread per output voxel x 8
+// channels.  sums: [2C] (channel sums, sums of squares).
+template <int POOL>
+__global__ void bn_act_pool_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ sums,
+                                       const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
+                                       float slope, uint16_t* __restrict__ y, uint8_t* __restrict__ aux, int64_t N,
+                                       int D, int H, int W, int C, PoolGrid pg) {
+    const int C8 = C / 8;
+    const double count = (double)N * D * H * W;
+    const int64_t total = POOL == 2 ? N * D * H * W * C8 : N * (D / 2) * (H / 2) * (W / 2) * C8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(i % C8);
+        const int64_t vox = i / C8;
+        float a[8], b[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) bn_coef(sums, C, 8 * c8 + c, count, gamma, beta, eps, a[c], b[c]);
+        if (POOL == 2) {
+            float f[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(z) + i), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float u = fmaf(a[c], f[c], b[c]);
+                f[c] = u > 0.f ? u : slope * u;
+            }
+            reinterpret_cast<uint4*>(y)[i] = pack8(f);
+            continue;
+        }
+        int64_t n;
+        int pd, ph, pw;
+        pool_decode(pg, vox, n, pd, ph, pw);
+        float m[8];
+        uint32_t code[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            m[c] = 0.f;
+            code[c] = 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+            const int64_t o = ((((n * D + 2 * pd + dd) * H + 2 * ph + dh) * W) + 2 * pw + dw) * C + 8 * c8;
+            float f[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(z + o)), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float u = fmaf(a[c], f[c], b[c]);
+                if (POOL == 0) {
+                    if (k == 0 || u > m[c]) {
+                        m[c] = u;
+                        code[c] = k;
+                    }
+                } else {
+                    code[c] |= (u > 0.f ? 1u : 0u) << k;
+                    m[c] += u > 0.f ? u : slope * u;
+                }
+            }
+        }
+        float out[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) out[c] = POOL == 0 ? (m[c] > 0.f ? m[c] : slope * m[c]) : m[c] * 0.125f;
+        const int64_t po = vox * C + 8 * c8;
+        *reinterpret_cast<uint4*>(y + po) = pack8(out);
+        if (aux)
+            *reinterpret_cast<uint2*>(aux + po) =
+                make_uint2(code[0] | (code[1] << 8) | (code[2] << 16) | (code[3] << 24),
+                           code[4] | (code[5] << 8) | (code[6] << 16) | (code[7] << 24));
+    }
+}
+
+// The activation/pooling backward folded into the batch-norm backward: du at
+// full resolution is implicit (POOL 0: g = dy * LReLU'(y) at the argmax voxel,
+// else 0; 1: dy / 8 * LReLU'(u) from the mask; 2: dy * LReLU'(y)), with y
+// NULL meaning dy already carries LReLU'.  PASS 0: per-thread sums of du and
+// du * zh over its 8-channel group (partial[block][2C]: dbeta, then dgamma);
+// PASS 1: dz = a * (du - dbeta/count - zh * dgamma/count) for every voxel of
+// the thread's window(s), written dense.  red: [2C] reduced dbeta, dgamma.
+template <int POOL, int PASS>
+__global__ void bn_act_pool_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ y,
+                                       const uint8_t* __restrict__ aux, const uint16_t* __restrict__ z,
+                                       const float* __restrict__ sums, const float* __restrict__ gamma, float eps,
+                                       float slope, const float* __restrict__ dsums, uint16_t* __restrict__ dz,
+                                       float* __restrict__ partial, int64_t N, int D, int H, int W, int C,
+                                       PoolGrid pg) {
+    extern __shared__ float red[];  // [blockDim][16]
+    const int C8 = C / 8;
+    const double count = (double)N * D * H * W;
+    const int64_t total = POOL == 2 ? N * D * H * W * C8 : N * (D / 2) * (H / 2) * (W / 2) * C8;
+    const int c8 = (int)(threadIdx.x % C8);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    float a[8], mean[8], inv[8], m1[8], m2[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        double m, iv;
+        bn_stats(sums, C, 8 * c8 + c, count, eps, m, iv);
+        mean[c] = (float)m;
+        inv[c] = (float)iv;
+        a[c] = (float)((double)gamma[8 * c8 + c] * iv);
+        if (PASS == 1) {
+            m1[c] = (float)((double)dsums[8 * c8 + c] / count);
+            m2[c] = (float)((double)dsums[C + 8 * c8 + c] / count);
+        }
+    }
+    float sb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, sg[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t vox = i / C8;
+        float g[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dy) + i), g);
+        if (y && POOL != 1) {
+            float yy[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(y) + i), yy);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) g[c] *= (yy[c] > 0.f ? 1.f : slope);
+        }
+        if (POOL == 2) {
+            float f[8], o[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(z) + i), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float zh = (f[c] - mean[c]) * inv[c];
+                if (PASS == 0) {
+                    sb[c] += g[c];
+                    sg[c] = fmaf(g[c], zh, sg[c]);
+                } else {
+                    o[c] = a[c] * (g[c] - m1[c] - zh * m2[c]);
+                }
+            }
+            if (PASS == 1) reinterpret_cast<uint4*>(dz)[i] = pack8(o);
+            continue;
+        }
+        uint32_t cw[2] = {0u, 0u};
+        const uint2 cv = __ldg(reinterpret_cast<const uint2*>(aux) + i);
+        cw[0] = cv.x;
+        cw[1] = cv.y;
+        int64_t n;
+        int pd, ph, pw;
+        pool_decode(pg, vox, n, pd, ph, pw);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int dd = k >> 2, dh = (k >> 1) & 1, dw = k & 1;
+            const int64_t o = ((((n * D + 2 * pd + dd) * H + 2 * ph + dh) * W) + 2 * pw + dw) * C + 8 * c8;
+            float f[8], out[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(z + o)), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t byte = (cw[c >> 2] >> (8 * (c & 3))) & 0xFFu;
+                float du;
+                if (POOL == 0) {
+                    du = byte == (uint32_t)k ? g[c] : 0.f;
+                } else {
+                    du = g[c] * 0.125f * (((byte >> k) & 1u) ? 1.f : slope);
+                }
+                const float zh = (f[c] - mean[c]) * inv[c];
+                if (PASS == 0) {
+                    sb[c] += du;
+                    sg[c] = fmaf(du, zh, sg[c]);
+                } else {
+                    out[c] = a[c] * (du - m1[c] - zh * m2[c]);
+                }
+            }
+            if (PASS == 1) *reinterpret_cast<uint4*>(dz + o) = pack8(out);
+        }
+    }
+    if (PASS == 0) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            red[threadIdx.x * 16 + c] = sb[c];
+            red[threadIdx.x * 16 + 8 + c] = sg[c];
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < 2 * C; e += blockDim.x) {
+            const int which = e / C, ch = e % C, cg = ch / 8, c = ch % 8;
+            float acc = 0.f;
+            for (int t = cg; t < (int)blockDim.x; t += C8) acc += red[t * 16 + 8 * which + c];
+            partial[(int64_t)blockIdx.x * 2 * C + e] = acc;
+        }
+    }
+}
+
 __global__ void timeout_probe_kernel(int* status, uint64_t limit_ns) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
@@ -573,6 +808,72 @@ cf_status launch_upsample2(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
     const int threads = 256;
     const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads, 16LL * ctx.num_sms));
     upsample2_kernel<<<blocks, threads, 0, ctx.stream>>>(dz, out, n, (int)d, (int)h, (int)w, c);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+size_t bn_workspace_bytes(int num_sms, int c) { return (size_t)pool_bwd_grid(num_sms) * 2 * c * sizeof(float); }
+
+cf_status launch_channel_stats(const LaunchCtx& ctx, int64_t rows, int c, const uint16_t* z, float* sums, void* ws,
+                               size_t ws_bytes) {
+    if (c % 8 != 0 || c / 8 > 256) return CF_ERR_UNSUPPORTED;
+    if (ws == nullptr || ws_bytes < bn_workspace_bytes(ctx.num_sms, c)) return CF_ERR_WORKSPACE;
+    const int threads = pool_bwd_block(c);
+    const int blocks = pool_bwd_grid(ctx.num_sms);
+    float* partial = static_cast<float*>(ws);
+    channel_stats_kernel<<<blocks, threads, threads * 16 * sizeof(float), ctx.stream>>>(z, partial, rows * (c / 8), c);
+    if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+    return launch_colsum(ctx, partial, blocks, 2 * c, sums);
+}
+
+cf_status launch_bn_act_pool_fwd(const LaunchCtx& ctx, int pool, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                                 const uint16_t* z, const float* sums, const float* gamma, const float* beta,
+                                 float eps, float slope, uint16_t* y, uint8_t* aux) {
+    const int64_t total = (pool == 2 ? n * d * h * w : n * (d / 2) * (h / 2) * (w / 2)) * (c / 8);
+    const int threads = 256;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads, 16LL * ctx.num_sms));
+    const PoolGrid pg = pool_grid(std::max<int64_t>(d, 2), std::max<int64_t>(h, 2), std::max<int64_t>(w, 2));
+    if (pool == 0)
+        bn_act_pool_fwd_kernel<0><<<blocks, threads, 0, ctx.stream>>>(z, sums, gamma, beta, eps, slope, y, aux, n,
+                                                                      (int)d, (int)h, (int)w, c, pg);
+    else if (pool == 1)
+        bn_act_pool_fwd_kernel<1><<<blocks, threads, 0, ctx.stream>>>(z, sums, gamma, beta, eps, slope, y, aux, n,
+                                                                      (int)d, (int)h, (int)w, c, pg);
+    else
+        bn_act_pool_fwd_kernel<2><<<blocks, threads, 0, ctx.stream>>>(z, sums, gamma, beta, eps, slope, y, aux, n,
+                                                                      (int)d, (int)h, (int)w, c, pg);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+cf_status launch_bn_act_pool_bwd(const LaunchCtx& ctx, int pool, int64_t n, int64_t d, int64_t h, int64_t w, int c,
+                                 const uint16_t* dy, const uint16_t* y, const uint8_t* aux, const uint16_t* z,
+                                 const float* sums, const float* gamma, float eps, float slope, uint16_t* dz,
+                                 float* dsums, void* ws, size_t ws_bytes) {
+    if (c % 8 != 0 || c / 8 > 256) return CF_ERR_UNSUPPORTED;
+    if (ws == nullptr || ws_bytes < bn_workspace_bytes(ctx.num_sms, c)) return CF_ERR_WORKSPACE;
+    const int threads = pool_bwd_block(c);
+    const int blocks = pool_bwd_grid(ctx.num_sms);
+    float* partial = static_cast<float*>(ws);
+    const PoolGrid pg = pool_grid(std::max<int64_t>(d, 2), std::max<int64_t>(h, 2), std::max<int64_t>(w, 2));
+    const size_t sh = threads * 16 * sizeof(float);
+#define CF_BN_BWD(P, S)                                                                                          \
+    bn_act_pool_bwd_kernel<P, S><<<blocks, threads, sh, ctx.stream>>>(dy, y, aux, z, sums, gamma, eps, slope, dsums, \
+                                                                     dz, partial, n, (int)d, (int)h, (int)w, c, pg)
+    if (pool == 0)
+        CF_BN_BWD(0, 0);
+    else if (pool == 1)
+        CF_BN_BWD(1, 0);
+    else
+        CF_BN_BWD(2, 0);
+    if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+    cf_status st = launch_colsum(ctx, partial, blocks, 2 * c, dsums);
+    if (st != CF_OK) return st;
+    if (pool == 0)
+        CF_BN_BWD(0, 1);
+    else if (pool == 1)
+        CF_BN_BWD(1, 1);
+    else
+        CF_BN_BWD(2, 1);
+#undef CF_BN_BWD
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 

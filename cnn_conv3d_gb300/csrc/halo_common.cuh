@@ -81,14 +81,18 @@ __device__ __forceinline__ void pool_combine(float& v, int& k, float v2, int k2)
 // warps per TMEM lane quarter can thus split the channels of a tile.
 // dsum (backward-data, BN <= 32): per-channel running sums of the stored
 // bf16 outputs of this thread's voxels, or NULL.
+// acc_col2: a second accumulator pair (plane 0 | plane 1) added to the first,
+// or 0xFFFFFFFF for none.
 template <int BN, int EPI, int CH_ = 0>
 __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& t, uint32_t tmem_base,
                                               uint32_t acc_col, int q, int lane, int c_begin = 0,
-                                              int c_step = 0, float* dsum = nullptr) {
+                                              int c_step = 0, float* dsum = nullptr,
+                                              uint32_t acc_col2 = 0xFFFFFFFFu) {
     constexpr int CH = CH_ != 0 ? CH_ : (BN >= 32 ? 32 : 16);  // accumulator columns per pass
     const int r = q * 32 + lane;
     const int j = r >> 3, l = r & 7;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
+    const uint32_t lane_addr2 = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col2;
     const int h = t.h0 + j, w = t.w0 + l;
     const int step = c_step != 0 ? c_step : CH;
 #pragma unroll 1
@@ -101,10 +105,26 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
             tmem_ld16(lane_addr + c, a0);
             tmem_ld16(lane_addr + BN + c, a1);
         }
+        if (acc_col2 != 0xFFFFFFFFu) {
+            uint32_t b0[32], b1[32];
+            if (CH == 32) {
+                tmem_ld32(lane_addr2 + c, b0);
+                tmem_ld32(lane_addr2 + BN + c, b1);
+            } else {
+                tmem_ld16(lane_addr2 + c, b0);
+                tmem_ld16(lane_addr2 + BN + c, b1);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                a0[k] = __float_as_uint(__uint_as_float(a0[k]) + __uint_as_float(b0[k]));
+                a1[k] = __float_as_uint(__uint_as_float(a1[k]) + __uint_as_float(b1[k]));
+            }
+        }
         tmem_ld_wait();
         // channels of this pass that exist (c_out is a multiple of 8)
         const int nvalid = min(CH, p.Cout - (t.co0 + c));
-        if (EPI == EPI_POOL) {
+        if (EPI == EPI_POOL || EPI == EPI_AVG) {
             float bias[CH];  // the pass's bias values, loaded before the reduction chain
 #pragma unroll
             for (int cc = 0; cc < CH; ++cc) {
@@ -117,7 +137,7 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
             const int kbase = (j & 1) * 2 + (l & 1);
             uint32_t ybits[CH / 2];
             uint32_t codes[CH / 4];
-            const bool avg = p.ea.pool_kind == 1;
+            constexpr bool avg = EPI == EPI_AVG;
 #pragma unroll
             for (int cc = 0; cc < CH; ++cc) {
                 float y;
@@ -173,7 +193,7 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
                     float v[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(a[q8 * 8 + k]);
-                    if (EPI == EPI_PLAIN && p.ea.act) {
+                    if (EPI == EPI_ACT) {
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             v[k] = lrelu(v[k] + (p.ea.bias ? p.ea.bias[t.co0 + c + q8 * 8 + k] : 0.f), p.ea.slope);
@@ -195,6 +215,14 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
                     pk.z = pack_bf16x2(v[4], v[5]);
                     pk.w = pack_bf16x2(v[6], v[7]);
                     *reinterpret_cast<uint4*>(p.ea.y + o + q8 * 8) = pk;
+                    if (EPI == EPI_DGRAD && p.ea.route_dz != nullptr) {
+                        const uint2 cv = *reinterpret_cast<const uint2*>(p.ea.route_idx + o + q8 * 8);
+                        const int64_t ws = p.Cout, hs = 2 * (int64_t)p.W * p.Cout, ds = 4 * (int64_t)p.H * p.W * p.Cout;
+                        uint16_t* dz0 = p.ea.route_dz +
+                                        ((((int64_t)t.n * 2 * p.D + 2 * d) * 2 * p.H + 2 * h) * 2 * p.W + 2 * w) * p.Cout +
+                                        t.co0 + c + q8 * 8;
+                        route_window(dz0, pk, cv, ws, hs, ds);
+                    }
                     if (BN <= 32 && dsum != nullptr) {
                         const uint32_t pw[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll

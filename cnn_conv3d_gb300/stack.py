@@ -14,6 +14,10 @@ One training step of the stack (forward + backward):
             l > 0: cf_conv3d_dgrad(dZ_l, W_l, x_act = x_l) -> g_{l-1}
             (g_{l-1} already carries the leaky-ReLU derivative of block l-1;
             the first block's input gradient has no consumer and is skipped)
+  With fuse_pool_bwd set, a max-pooled block below the top gets its dense dZ
+  (and its bias gradient, the channel sums of g) from the backward-data launch
+  of the block above (cf_conv3d_dgrad_pool_bwd routes g to the argmax in its
+  epilogue) instead of a pool-backward launch.
   The first block, when its input has 1 or 4 channels, needs dZ only for its
   weight gradient: cf_conv3d_wgrad takes the pooled gradient with the argmax
   codes (routed form), expanding dZ on chip, so its dense dZ is never
@@ -113,9 +117,22 @@ class CosmoStack:
         # the weight gradients' workspace (the main one when they share the stream)
         self.ws_w = torch.empty((max(ws_w, 256),), dtype=torch.uint8, device=device) if self.side else self.ws
 
+    # lower max-pooled blocks take their dZ (and bias gradient) from the
+    # backward-data launch of the block above (cf_conv3d_dgrad_pool_bwd) when
+    # set.  Off by default: that epilogue's lanes own voxels, so its routed
+    # stores scatter over 32 rows per instruction, and measured slower than
+    # the separate pool backward whose lanes own channel groups (dgrad3 +
+    # routing 0.248 ms against 0.101 + 0.060 ms for N = 8 x 4 x 128^3)
+    fuse_pool_bwd = False
+
     def routed(self, l) -> bool:
         """Block l's weight gradient takes the pooled gradient + argmax codes."""
         return l == 0 and self.channels[0] in (1, 4) and self.specs[0] == (1, "max")
+
+    def pool_bwd_fused(self, l) -> bool:
+        """Block l's max-pool backward runs in block l+1's backward-data epilogue."""
+        return (self.fuse_pool_bwd and l < self.L - 1 and self.specs[l][1] == "max" and not self.routed(l)
+                and self.specs[l + 1][0] == 1)
 
     def desc(self, l):
         n, d, h, w = self.dims[l]
@@ -229,7 +246,7 @@ class CosmoStack:
                                                           self.slope, self.dz[l], None, self.db[l], ws, wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
                 to_host(main, host_out and host_out[1][l], self.db[l])
-            elif pool == "max" and not routed:
+            elif pool == "max" and not routed and not self.pool_bwd_fused(l):
                 fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope,
                                                        self.dz[l], None, self.db[l], ws, wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
@@ -239,8 +256,9 @@ class CosmoStack:
                                                       self.slope, self.dz[l], None, self.db[l], ws, wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
                 to_host(main, host_out and host_out[1][l], self.db[l])
-            # (a routed or unpooled block below the top: db[l] came with g[l] from
-            # block l+1's dgrad, as the channel sums of its output)
+            # (a routed, unpooled or fused block below the top: db[l] came with g[l]
+            # from block l+1's dgrad, as the channel sums of its output; a fused
+            # one's dZ too)
             desc = self.desc(l)
             if side is not main:
                 ev = torch.cuda.Event()
@@ -256,13 +274,19 @@ class CosmoStack:
             to_host(side, host_out and host_out[0][l], self.dw[l])
             if l > 0:
                 below = self.specs[l - 1][1]
-                dsum = self.db[l - 1] if (self.routed(l - 1) or below == "none") else None
+                fused = self.pool_bwd_fused(l - 1)
+                dsum = self.db[l - 1] if (self.routed(l - 1) or below == "none" or fused) else None
                 # the lower block's output derivative rides on the input gradient
                 # unless it is average-pooled (its derivative is per voxel, from its masks)
                 x_act = self.block_input(l) if below != "avg" else None
-                self._run(f"dgrad{l + 1}", main, lambda: cf.cf_conv3d_dgrad(
-                    desc, self.dz[l], None, self.w[l], x_act, self.slope, self.g[l - 1], ws, wsb,
-                    main, dsum=dsum), timer)
+                if fused:
+                    fn = lambda: cf.cf_conv3d_dgrad_pool_bwd(desc, self.dz[l], self.w[l], x_act, self.slope,
+                                                             self.g[l - 1], self.idx[l - 1], self.dz[l - 1], ws, wsb,
+                                                             main, dsum=dsum)
+                else:
+                    fn = lambda: cf.cf_conv3d_dgrad(desc, self.dz[l], None, self.w[l], x_act, self.slope,
+                                                    self.g[l - 1], ws, wsb, main, dsum=dsum)
+                self._run(f"dgrad{l + 1}", main, fn, timer)
                 if dsum is not None:
                     to_host(main, host_out and host_out[1][l - 1], dsum)
         for s in (main, side) + ((host_out[2],) if host_out is not None else ()):
@@ -359,11 +383,11 @@ class CosmoStack:
                 s2 = self.specs[l][0] == 2
                 n += 2 + s2  # wgrad
                 pool = self.specs[l][1]
-                if l == self.L - 1 or not (self.routed(l) or pool == "none"):
+                if l == self.L - 1 or not (self.routed(l) or pool == "none" or self.pool_bwd_fused(l)):
                     n += 2  # pool backward
                 if l > 0:
                     n += 2 + s2  # dgrad
-                    if self.routed(l - 1) or self.specs[l - 1][1] == "none":
+                    if self.routed(l - 1) or self.specs[l - 1][1] == "none" or self.pool_bwd_fused(l - 1):
                         fused = (not s2 and ch[l] <= 32 and ch[l] % 16 == 0 and ch[l] in (32, 64, 128)
                                  and ch[l + 1] % 16 == 0)
                         n += 1 if fused else 2

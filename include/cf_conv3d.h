@@ -84,7 +84,7 @@ typedef struct {
 
 /* Operation ids for cf_workspace_size. */
 enum { CF_OP_FWD = 0, CF_OP_DGRAD = 1, CF_OP_WGRAD = 2, CF_OP_DGRAD_ROUTED = 3,
-       CF_OP_WGRAD_ROUTED = 4, CF_OP_POOL_BWD = 5 };
+       CF_OP_WGRAD_ROUTED = 4, CF_OP_POOL_BWD = 5, CF_OP_BN = 6 };
 
 /*
  * Forward convolution (CosmoFlow page, section III-A/III-C "forward data";
@@ -99,9 +99,8 @@ enum { CF_OP_FWD = 0, CF_OP_DGRAD = 1, CF_OP_WGRAD = 2, CF_OP_DGRAD_ROUTED = 3,
  *        Average pooling: Y = (1/8) * sum over the window of LReLU(Z + b).
  *   ws : unused (pass NULL, 0).
  * Supported: c_in in {1, 4} or a multiple of 16 (the CosmoFlow page's rule of
- * channel counts in multiples of 16, section III-A); c_out a multiple of 16 and
- * <= 256 per kernel tile (multiples of 256 above that), or c_out a multiple of 8
- * (<= 256) when c_in is 1 or 4; w * c_in a multiple of 8 when c_in is 1 or 4;
+ * channel counts in multiples of 16, section III-A); c_out a multiple of 16, or
+ * a multiple of 8 (<= 256) when c_in is 1 or 4; w * c_in a multiple of 8 when c_in is 1 or 4;
  * d', h', w' even when pooling; stride 2 only for c_in a multiple of 16.
  */
 cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint16_t* w,
@@ -133,6 +132,26 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
 cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx,
                           const uint16_t* w, const uint16_t* x_act, float slope, uint16_t* dx,
                           float* dsum, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward data fused with the previous block's max-pool backward (CosmoFlow
+ * page, section III-C "backward data"; the block's pool backward as in
+ * cf_bias_lrelu_pool_bwd): everything cf_conv3d_dgrad computes for a dense dz
+ * (idx NULL, stride 1) -- dx = the previous block's pooled pre-activation
+ * gradient g (x_act given) and optionally its channel sums dsum = that
+ * block's bias gradient -- and in the same epilogue
+ *   prev_dz [n][2d][2h][2w][c_in] bf16: g routed to the voxel of each 2x2x2
+ *           window that prev_idx ([n][d][h][w][c_in], the previous block's
+ *           argmax codes) names, zero at the other seven
+ * (the previous block's dense dZ, which its weight gradient and backward data
+ * read), so that no separate pool-backward pass re-reads g.  Same values, bit
+ * for bit, as cf_conv3d_dgrad followed by cf_bias_lrelu_pool_bwd(g, NULL, prev_idx).
+ * Supported: as cf_conv3d_dgrad; prev_idx and prev_dz required.
+ */
+cf_status cf_conv3d_dgrad_pool_bwd(const cf_conv_desc* desc, const uint16_t* dz, const uint16_t* w,
+                                   const uint16_t* x_act, float slope, uint16_t* dx, float* dsum,
+                                   const uint8_t* prev_idx, uint16_t* prev_dz, void* ws, size_t ws_bytes,
+                                   void* stream);
 
 /*
  * Backward weight (CosmoFlow page, section III-C "backward weights", work
@@ -206,6 +225,40 @@ cf_status cf_block_epilogue_bwd(int32_t pool, int64_t n, int64_t d, int64_t h, i
                                 const uint16_t* dy, const uint16_t* y, const uint8_t* aux, float slope,
                                 uint16_t* dz, uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes,
                                 void* stream);
+
+/*
+ * Batch normalisation between the conv and the activation (the
+ * hybrid-parallelism page, section IV: a batch normalization layer after
+ * every convolutional layer), training mode with the batch's statistics, per
+ * channel over all n and voxels (count = n*d*h*w; biased variance):
+ *   u = gamma * (z - mean) / sqrt(var + eps) + beta,  then LReLU and pooling
+ * The conv output z is stored (cf_conv3d_fwd with epi NULL), because the
+ * statistics need all of it before any voxel can be normalised.
+ *   cf_bn_stats        : sums [2c] fp32 = (sum of z, sum of z^2) per channel over
+ *                        `rows` voxels of z [rows][c] bf16 (fixed order).
+ *   cf_bn_act_pool_fwd : y, aux from z and the sums, as cf_block_epilogue_fwd
+ *                        with u in place of z + b (max-pool codes are taken on u).
+ *   cf_bn_act_pool_bwd : from dy (pooled shape, or z's for CF_POOL_NONE; with y
+ *                        given, dy is the gradient at the block output and the
+ *                        leaky-ReLU derivative is applied; with y NULL, dy already
+ *                        carries it), du is the pooling backward (max: routed to
+ *                        the argmax; avg: dy/8 * LReLU'(u) from the masks; none:
+ *                        dy), and
+ *                          dgamma = sum du * zh,  dbeta = sum du,
+ *                          dz = gamma / sqrt(var + eps) * (du - dbeta/count - zh * dgamma/count)
+ *                        written dense to dz [n][d][h][w][c]; dsums [2c] = (dbeta, dgamma).
+ * Workspace: cf_workspace_size(CF_OP_BN, desc with c_out = c).  Supported: c a
+ * multiple of 8 (<= 2048); d, h, w even when pooling.
+ */
+cf_status cf_bn_stats(int64_t rows, int32_t c, const uint16_t* z, float* sums, void* ws, size_t ws_bytes,
+                      void* stream);
+cf_status cf_bn_act_pool_fwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c, const uint16_t* z,
+                             const float* sums, const float* gamma, const float* beta, float eps, float slope,
+                             uint16_t* y, uint8_t* aux, void* stream);
+cf_status cf_bn_act_pool_bwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                             const uint16_t* dy, const uint16_t* y, const uint8_t* aux, const uint16_t* z,
+                             const float* sums, const float* gamma, float eps, float slope, uint16_t* dz,
+                             float* dsums, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * cf_bias_lrelu_pool_bwd without a workspace argument, for callers that

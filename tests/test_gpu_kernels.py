@@ -283,6 +283,19 @@ def test_conv_dgrad(cf, oracle_mod, shape, with_act):
         f = np.where(_f64(oracle_mod, c["x"]) > 0, 1.0, SLOPE)
         ref, S = ref * f, S * f
     assert_close(host_bf16_f64(dx), ref, S, f"dgrad {shape} act={with_act}")
+    if with_act:
+        # the previous block's max-pool backward fused into the epilogue: the same
+        # dx, and its routing by the codes equals the standalone pool backward's
+        pidx = torch.from_numpy(np.random.default_rng(Ci).integers(0, 8, size=(N, D, H, W, Ci)).astype(np.uint8)).cuda()
+        dx2, dx2c = guarded((N, D, H, W, Ci), torch.bfloat16, fill=float("nan"))
+        pdz, pdzc = guarded((N, 2 * D, 2 * H, 2 * W, Ci), torch.bfloat16, fill=float("nan"))
+        cf.cf_conv3d_dgrad_pool_bwd(desc, dev_bf16(c["dz"]), dev_bf16(c["w"]), x_act, SLOPE, dx2, pidx, pdz, ws, wsb)
+        dx2c("fused dx")
+        pdzc("fused routed dz")
+        assert torch.equal(dx2, dx)
+        rdz = empty_bf16((N, 2 * D, 2 * H, 2 * W, Ci))
+        cf.cf_bias_lrelu_pool_bwd(N, 2 * D, 2 * H, 2 * W, Ci, dx, None, pidx, SLOPE, rdz, None, None)
+        assert torch.equal(pdz, rdz)
     # dsum against the oracle: channel sums of the exact dx (each stored element
     # is within 1e-2*S of it, so the sums are within 1e-2 * sum(S))
     assert_close(dsum.cpu().numpy().astype(np.float64), ref.reshape(-1, Ci).sum(0), S.reshape(-1, Ci).sum(0),

@@ -93,3 +93,26 @@ def test_host_step_matches(torch_cuda, shape):
     assert cf.cf_last_device_status() == cf.CF_OK
     for a, b in zip(ref, got):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("shape", [(2, 32, (4, 32, 64, 128)), (1, 32, (32, 64, 128, 64))])
+def test_fused_pool_backward_matches_separate(torch_cuda, shape):
+    """Lower blocks' pool backward inside the backward-data epilogue of the
+    block above gives the bits of the separate pool-backward launches."""
+    torch = torch_cuda
+    from cnn_conv3d_gb300 import cfconv as cf
+    from cnn_conv3d_gb300.stack import CosmoStack
+    n, s, ch = shape
+    inp = synthdata.stack_inputs(n, s, ch, seed=4545, with_dy=True)
+    dy = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).cuda()
+    out = []
+    for fuse in (False, True):  # the stack's default, then the fused path
+        st = CosmoStack(n, s, ch, 0.3, backward=True)
+        st.fuse_pool_bwd = fuse
+        st.load(inp["x"], inp["w"], inp["b"])
+        st.step(dy)
+        torch.cuda.synchronize()
+        out.append([t.clone() for t in st.y + st.dw + st.db] + [t.clone() for t in st.dz if t is not None])
+    assert cf.cf_last_device_status() == cf.CF_OK
+    for a, b in zip(*out):
+        assert torch.equal(a, b)
