@@ -547,3 +547,77 @@ TABLE1_CHANNELS = (4, 16, 32, 64, 128, 256, 256, 256)
 def table1_specs(wi: int = 128):
     pooled = {128: 5, 256: 6, 512: 7}[wi]
     return [(2 if l == 3 else 1, "max" if l < pooled else "none") for l in range(7)]
+
+
+# ----------------------------------------------------------------------------
+# the rest of the network (hybrid-parallelism page, section IV and Table I:
+# fc1 2048 -> fc2 256 -> fc3 4 outputs; leaky ReLU after every layer but the
+# last; dropout with keep probability 0.8 after the fully connected layers;
+# mean squared error; Adam with beta1 0.9, beta2 0.999, eps 1e-8 and a linear
+# learning-rate decay to 0.01x).  Readings: dropout after the two hidden fc
+# layers (not on the regression outputs); the dropout draws are inputs (keep
+# masks), scaled by 1/keep where kept.
+
+def fc_fwd(x, w, b):
+    """y [M,N] = x [M,K] @ w[N,K]^T + b (fp64)."""
+    return _f64(x) @ _f64(w).T + _f64(b)
+
+
+def fc_bwd(x, w, dy):
+    """(dx, dw, db) of fc_fwd."""
+    x, w, dy = _f64(x), _f64(w), _f64(dy)
+    return dy @ w, dy.T @ x, dy.sum(0)
+
+
+def head_fwd(feat, fcs, masks, keep, slope):
+    """feat [M, F] -> predictions [M, 4] through the fc layers fcs = [(w, b)]:
+    hidden layers leaky ReLU then dropout (masks[i] of 0/1, scale 1/keep), the
+    last layer linear.  Returns (hs, pred): hs[i] = input of layer i."""
+    hs = [_f64(feat)]
+    cur = hs[0]
+    for i, (w, b) in enumerate(fcs):
+        z = fc_fwd(cur, w, b)
+        if i < len(fcs) - 1:
+            z = np.where(z > 0, z, slope * z) * _f64(masks[i]) / keep
+            hs.append(z)
+        cur = z
+    return hs, cur
+
+
+def head_bwd(hs, fcs, masks, keep, slope, dpred):
+    """Backward of head_fwd from dpred: ([(dw, db)], dfeat).  The leaky-ReLU
+    derivative of a hidden layer is read from its stored output (its sign is
+    the pre-activation's wherever the mask kept it; elsewhere the gradient is
+    zero)."""
+    grads = [None] * len(fcs)
+    g = _f64(dpred)
+    for i in range(len(fcs) - 1, -1, -1):
+        dx, dw, db = fc_bwd(hs[i], fcs[i][0], g)
+        grads[i] = (dw, db)
+        if i > 0:
+            h = hs[i]
+            g = dx * _f64(masks[i - 1]) / keep * np.where(h > 0, 1.0, slope)
+        else:
+            g = dx
+    return grads, g
+
+
+def mse(pred, target):
+    """(loss, dpred): mean over every element of (pred - target)^2 and its gradient."""
+    d = _f64(pred) - _f64(target)
+    return float(np.mean(d * d)), 2.0 * d / d.size
+
+
+def adam_step(w, g, m, v, lr, t, beta1=0.9, beta2=0.999, eps=1e-8):
+    """One Adam step (bias-corrected moments, step t >= 1); returns (w, m, v)."""
+    w, g, m, v = _f64(w), _f64(g), _f64(m), _f64(v)
+    m = beta1 * m + (1 - beta1) * g
+    v = beta2 * v + (1 - beta2) * g * g
+    mh = m / (1 - beta1 ** t)
+    vh = v / (1 - beta2 ** t)
+    return w - lr * mh / (np.sqrt(vh) + eps), m, v
+
+
+def linear_decay_lr(lr0, step, total_steps, final_frac=0.01):
+    """Linear decay from lr0 to final_frac * lr0 over total_steps, then constant."""
+    return lr0 * (1.0 - (1.0 - final_frac) * min(step / total_steps, 1.0))

@@ -687,3 +687,70 @@ def test_bn_chain_finite_differences(oracle_mod):
                 else:
                     num = (loss(ws, gs, ap) - loss(ws, gs, am)) / (2 * h)
                 assert abs(num - grad[c]) <= 1e-5 * max(1.0, abs(num)), (l, c, num, grad[c])
+
+
+# ----------------------------------------------------------------------------- rest of the network
+
+def test_head_finite_differences(oracle_mod):
+    """fc -> LReLU -> dropout -> fc -> LReLU -> dropout -> fc -> MSE: every
+    weight, bias and input gradient against central differences."""
+    rng = np.random.default_rng(61)
+    M, F, H1, H2, O = 3, 10, 8, 6, 4
+    fcs = [(rng.normal(size=(H1, F)), rng.normal(size=H1)), (rng.normal(size=(H2, H1)), rng.normal(size=H2)),
+           (rng.normal(size=(O, H2)), rng.normal(size=O))]
+    masks = [(rng.random((M, H1)) < 0.8).astype(np.uint8), (rng.random((M, H2)) < 0.8).astype(np.uint8)]
+    feat, target = rng.normal(size=(M, F)), rng.normal(size=(M, O))
+    keep, slope = 0.8, 0.3
+
+    def loss(fcs_, feat_):
+        return oracle_mod.mse(oracle_mod.head_fwd(feat_, fcs_, masks, keep, slope)[1], target)[0]
+
+    hs, pred = oracle_mod.head_fwd(feat, fcs, masks, keep, slope)
+    l0, dpred = oracle_mod.mse(pred, target)
+    grads, dfeat = oracle_mod.head_bwd(hs, fcs, masks, keep, slope, dpred)
+    h = 1e-6
+    for i in range(3):
+        for j in (0, 1):
+            arr = fcs[i][j]
+            for _ in range(4):
+                pos = tuple(rng.integers(0, s) for s in arr.shape)
+                fp = [[a.copy() for a in p] for p in fcs]
+                fm = [[a.copy() for a in p] for p in fcs]
+                fp[i][j][pos] += h
+                fm[i][j][pos] -= h
+                num = (loss(fp, feat) - loss(fm, feat)) / (2 * h)
+                assert abs(num - grads[i][j][pos]) <= 1e-6 * max(1.0, abs(num)), (i, j, pos)
+    for _ in range(5):
+        pos = tuple(rng.integers(0, s) for s in feat.shape)
+        fp, fm = feat.copy(), feat.copy()
+        fp[pos] += h
+        fm[pos] -= h
+        num = (loss(fcs, fp) - loss(fcs, fm)) / (2 * h)
+        assert abs(num - dfeat[pos]) <= 1e-6 * max(1.0, abs(num))
+
+
+def test_adam_and_decay_closed_forms(oracle_mod):
+    """Adam's first step from zero moments moves each weight by lr * g / (|g| +
+    eps) (the bias corrections make m_hat = g, v_hat = g^2); with a constant
+    gradient every later step moves by the same amount; the linear decay runs
+    from lr0 to 0.01 lr0."""
+    g = np.array([0.5, -2.0, 1e-3, 0.0])
+    w = np.zeros(4)
+    w1, m, v = oracle_mod.adam_step(w, g, np.zeros(4), np.zeros(4), lr=0.1, t=1)
+    np.testing.assert_allclose(w1, -0.1 * g / (np.abs(g) + 1e-8), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(m, 0.1 * g)
+    np.testing.assert_allclose(v, 0.001 * g * g)
+    w2, _, _ = oracle_mod.adam_step(w1, g, m, v, lr=0.1, t=2)
+    np.testing.assert_allclose(w2 - w1, -0.1 * g / (np.abs(g) + 1e-8), rtol=1e-9, atol=1e-15)
+    assert oracle_mod.linear_decay_lr(2.0, 0, 100) == 2.0
+    assert oracle_mod.linear_decay_lr(2.0, 100, 100) == pytest.approx(0.02)
+    assert oracle_mod.linear_decay_lr(2.0, 50, 100) == pytest.approx(1.01)
+    assert oracle_mod.linear_decay_lr(2.0, 500, 100) == pytest.approx(0.02)
+
+
+def test_mse_closed_form(oracle_mod):
+    pred = np.array([[1.0, 2.0], [3.0, 4.0]])
+    tgt = np.array([[1.0, 0.0], [0.0, 0.0]])
+    loss, d = oracle_mod.mse(pred, tgt)
+    assert loss == pytest.approx((0 + 4 + 9 + 16) / 4)
+    np.testing.assert_allclose(d, 2 * (pred - tgt) / 4)
