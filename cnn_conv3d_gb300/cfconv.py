@@ -65,6 +65,11 @@ _SIGS = {
                            ctypes.c_int),
     "cf_bn_act_pool_bwd": ([_i32, _i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _vp,
                             _vp, _sz, _vp], ctypes.c_int),
+    "cf_fc_fwd": ([_i64, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _f32, _vp, _f32, _vp, _vp], ctypes.c_int),
+    "cf_fc_bwd": ([_i64, _i32, _i32, _vp, _i32, _vp, _vp, _f32, _vp, _f32, _vp, _vp, _i32, _vp, _vp, _vp],
+                  ctypes.c_int),
+    "cf_mse": ([_i64, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
+    "cf_adam_step": ([_i64, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32, _i64, _vp], ctypes.c_int),
     "cf_workspace_size": ([ctypes.c_int, _DP], _sz),
     "cf_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "cf_last_device_status": ([_vp], ctypes.c_int),
@@ -204,6 +209,30 @@ def cf_bn_act_pool_bwd(pool, n, d, h, w, c, dy, y, aux, z, sums, gamma, eps, slo
                                  _ptr(gamma), float(eps), float(slope), _ptr(dz), _ptr(dsums), _ptr(ws), ws_bytes,
                                  _stream(stream))
     return _check(st, "cf_bn_act_pool_bwd") if check else st
+
+
+def cf_fc_fwd(m, k, n, x, x_is_bf16, w, b, act, slope, keep_mask, keep, y, stream=None, check=True):
+    st = _lib.cf_fc_fwd(m, k, n, _ptr(x), int(x_is_bf16), _ptr(w), _ptr(b), int(act), float(slope), _ptr(keep_mask),
+                        float(keep), _ptr(y), _stream(stream))
+    return _check(st, "cf_fc_fwd") if check else st
+
+
+def cf_fc_bwd(m, k, n, x, x_is_bf16, w, h, slope, keep_mask, keep, dy, dx, dx_is_bf16, dw, db, stream=None,
+              check=True):
+    st = _lib.cf_fc_bwd(m, k, n, _ptr(x), int(x_is_bf16), _ptr(w), _ptr(h), float(slope), _ptr(keep_mask),
+                        float(keep), _ptr(dy), _ptr(dx), int(dx_is_bf16), _ptr(dw), _ptr(db), _stream(stream))
+    return _check(st, "cf_fc_bwd") if check else st
+
+
+def cf_mse(count, pred, target, loss, dpred, stream=None, check=True):
+    st = _lib.cf_mse(count, _ptr(pred), _ptr(target), _ptr(loss), _ptr(dpred), _stream(stream))
+    return _check(st, "cf_mse") if check else st
+
+
+def cf_adam_step(count, w, w_bf16, g, m, v, lr, beta1, beta2, eps, t, stream=None, check=True):
+    st = _lib.cf_adam_step(count, _ptr(w), _ptr(w_bf16), _ptr(g), _ptr(m), _ptr(v), float(lr), float(beta1),
+                           float(beta2), float(eps), int(t), _stream(stream))
+    return _check(st, "cf_adam_step") if check else st
 
 
 def cf_last_device_status(stream=None) -> int:

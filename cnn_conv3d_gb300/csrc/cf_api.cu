@@ -55,6 +55,13 @@ bool device_ctx(LaunchCtx* ctx, void* stream) {
     return true;
 }
 
+}  // namespace
+
+// The per-device launch context for the other translation units' entry points.
+bool cf_device_ctx(LaunchCtx* ctx, void* stream) { return device_ctx(ctx, stream); }
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

@@ -35,6 +35,9 @@ struct LaunchCtx {
     uint64_t wait_ns;  // bounded-wait limit
 };
 
+// Fills ctx for the current device and `stream` (cf_api.cu); false on a CUDA error.
+bool cf_device_ctx(LaunchCtx* ctx, void* stream);
+
 // Geometry of the 128-voxel output tile of the implicit GEMM: a box of
 // td x th x tw voxels (td = 2 so that pooled tiles hold whole windows).
 struct TileGeom {

@@ -48,11 +48,16 @@ POOL_CODES = {"max": cf.CF_POOL_MAX, "avg": cf.CF_POOL_AVG, "none": cf.CF_POOL_N
 
 
 class CosmoStack:
-    """specs: optional per-block (stride, pool), stride 1 or 2, pool "max",
-    "avg" or "none" (default: stride 1 and max-pooling everywhere, the
-    CosmoFlow-shaped five-block stack).  The hybrid-parallelism page's Table I
+    """specs: optional per-block (stride, pool) or (stride, pool, "bn"), stride
+    1 or 2, pool "max", "avg" or "none" (default: stride 1 and max-pooling
+    everywhere, the CosmoFlow-shaped five-block stack); "bn" puts batch
+    normalisation (batch statistics, gamma / beta = self.gamma[l] / self.b[l])
+    between the conv and the activation.  The hybrid-parallelism page's Table I
     model is channels (4, 16, 32, 64, 128, 256, 256, 256) with a stride-2
     fourth conv and no pooling after the last two at width 128."""
+
+    # batch-norm epsilon of blocks with spec (stride, pool, "bn")
+    bn_eps = 1e-5
 
     def __init__(self, n: int, spatial: int, channels, slope: float = 0.3, device: str = "cuda",
                  backward: bool = True, overlap: bool = True, specs=None):
@@ -69,7 +74,7 @@ class CosmoStack:
         self.w, self.b, self.y, self.idx = [], [], [], []
         for l in range(self.L):
             ci, co = channels[l], channels[l + 1]
-            stride, pool = self.specs[l]
+            stride, pool = self.specs[l][0], self.specs[l][1]
             so = (s + stride - 1) // stride
             sp = so if pool == "none" else so // 2
             self.dims.append((n, s, s, s))
@@ -80,25 +85,47 @@ class CosmoStack:
             # argmax codes (max) or sign masks (avg) of the pooled output
             self.idx.append(torch.empty((n, sp, sp, sp, co), dtype=u8, device=device) if pool != "none" else None)
             s = sp
+        # batch-norm blocks: the stored conv output, the channel sums (sum z,
+        # sum z^2), gamma
+        self.zc, self.stats, self.gamma = [None] * self.L, [None] * self.L, [None] * self.L
+        for l in range(self.L):
+            if self.bn(l):
+                n_, d, h, w = self.odims[l]
+                co = channels[l + 1]
+                self.zc[l] = torch.empty((n_, d, h, w, co), dtype=bf, device=device)
+                self.stats[l] = torch.empty((2 * co,), dtype=f32, device=device)
+                self.gamma[l] = torch.ones((co,), dtype=f32, device=device)
         self.backward_enabled = backward
         # with overlap: the backward-data chain on a high-priority stream (it is the
         # step's critical path), the weight gradients on a normal-priority one
         self.side = torch.cuda.Stream(device=device) if (backward and overlap) else None
         self.crit = torch.cuda.Stream(device=device, priority=-1) if (backward and overlap) else None
         ws = ws_w = 0
+        for l in range(self.L):
+            if self.bn(l):
+                ws = max(ws, cf.cf_workspace_size(cf.CF_OP_BN, cf.cf_conv_desc(1, 1, 1, 1, 1, channels[l + 1])))
         if backward:
             self.dz, self.dw, self.db, self.g = [], [], [], []
+            self.dgamma = [None] * self.L
+            self.dsums = [None] * self.L
             for l in range(self.L):
                 n_, d, h, w = self.odims[l]
                 co = channels[l + 1]
                 self.dz.append(None if self.routed(l) else torch.empty((n_, d, h, w, co), dtype=bf, device=device))
                 self.dw.append(torch.empty((co, 3, 3, 3, channels[l]), dtype=f32, device=device))
-                self.db.append(torch.empty((co,), dtype=f32, device=device))
+                if self.bn(l):
+                    # (dbeta, dgamma) side by side, as the batch-norm backward writes them
+                    self.dsums[l] = torch.empty((2 * co,), dtype=f32, device=device)
+                    self.db.append(self.dsums[l][:co])
+                    self.dgamma[l] = self.dsums[l][co:]
+                else:
+                    self.db.append(torch.empty((co,), dtype=f32, device=device))
                 # g[l]: the dgrad output of block l+1: the gradient w.r.t. block l's
                 # pooled pre-activation (max), its output (avg); an unpooled block's
-                # dgrad output is its dZ itself (g[l] aliases dz[l])
+                # dgrad output is its dZ itself (g[l] aliases dz[l]) unless it is
+                # batch-normalised
                 pool = self.specs[l][1]
-                if pool == "none" and l < self.L - 1:
+                if pool == "none" and l < self.L - 1 and not self.bn(l):
                     self.g.append(self.dz[l])
                 elif l < self.L - 1 or self.routed(l):
                     self.g.append(torch.empty(tuple(self.y[l].shape), dtype=bf, device=device))
@@ -129,18 +156,39 @@ class CosmoStack:
         """Block l's weight gradient takes the pooled gradient + argmax codes."""
         return l == 0 and self.channels[0] in (1, 4) and self.specs[0] == (1, "max")
 
+    def bn(self, l) -> bool:
+        """Block l has batch normalisation between its conv and its activation."""
+        return len(self.specs[l]) > 2 and self.specs[l][2] == "bn"
+
     def pool_bwd_fused(self, l) -> bool:
         """Block l's max-pool backward runs in block l+1's backward-data epilogue."""
         return (self.fuse_pool_bwd and l < self.L - 1 and self.specs[l][1] == "max" and not self.routed(l)
-                and self.specs[l + 1][0] == 1)
+                and not self.bn(l) and self.specs[l + 1][0] == 1)
 
     def desc(self, l):
         n, d, h, w = self.dims[l]
         return cf.cf_conv_desc(n, d, h, w, self.channels[l], self.channels[l + 1], self.specs[l][0])
 
     def epi(self, l, idx=None):
-        """Forward epilogue of block l (bias, slope, codes/masks, pooling kind)."""
+        """Forward epilogue of block l (bias, slope, codes/masks, pooling kind);
+        None for a batch-normalised block (its conv output is stored plain)."""
+        if self.bn(l):
+            return None
         return (self.b[l], self.slope, self.idx[l] if idx is None else idx, POOL_CODES[self.specs[l][1]])
+
+    def _fwd_block(self, l, stream):
+        """Block l's forward launches: the conv with its fused epilogue, or, with
+        batch normalisation, the plain conv, the channel sums and the
+        normalisation + activation + pooling."""
+        if not self.bn(l):
+            cf.cf_conv3d_fwd(self.desc(l), self.block_input(l), self.w[l], self.epi(l), self.y[l], None, 0, stream)
+            return
+        n, d, h, w = self.odims[l]
+        co = self.channels[l + 1]
+        cf.cf_conv3d_fwd(self.desc(l), self.block_input(l), self.w[l], None, self.zc[l], None, 0, stream)
+        cf.cf_bn_stats(n * d * h * w, co, self.zc[l], self.stats[l], self.ws, self.ws.numel(), stream)
+        cf.cf_bn_act_pool_fwd(POOL_CODES[self.specs[l][1]], n, d, h, w, co, self.zc[l], self.stats[l], self.gamma[l],
+                              self.b[l], self.bn_eps, self.slope, self.y[l], self.idx[l], stream)
 
     def block_input(self, l):
         return self.x if l == 0 else self.y[l - 1]
@@ -191,6 +239,8 @@ class CosmoStack:
         first = 0
         if x_chunks is not None:
             first = max(1, self._chunked_blocks())
+            if any(self.bn(l) for l in range(first)):
+                first = 0  # batch statistics need the whole batch: no per-sample blocks
             for n0, n1, ev in x_chunks:
                 main.wait_event(ev)
                 for l in range(first):
@@ -200,9 +250,11 @@ class CosmoStack:
                                                      self.specs[l][0]),
                                      self.block_input(l)[n0:n1], self.w[l], self.epi(l, idx), self.y[l][n0:n1],
                                      None, 0, main)
+        if x_chunks is not None and first == 0:
+            for _, _, ev in x_chunks:
+                main.wait_event(ev)
         for l in range(first, self.L):
-            self._run(f"fwd{l + 1}", main, lambda l=l: cf.cf_conv3d_fwd(
-                self.desc(l), self.block_input(l), self.w[l], self.epi(l), self.y[l], None, 0, main), timer)
+            self._run(f"fwd{l + 1}", main, lambda l=l: self._fwd_block(l, main), timer)
 
     def backward(self, dy, stream=None, timer=None, serial=False, host_out=None):
         """timer: as in forward (keys "poolbwd<l+1>", "wgrad<l+1>", "dgrad<l+1>").
@@ -235,7 +287,18 @@ class CosmoStack:
             co = self.channels[l + 1]
             routed = self.routed(l)
             pool = self.specs[l][1]
-            if l == self.L - 1:
+            if self.bn(l):
+                # batch norm (with the activation / pooling backward folded in):
+                # dZ, dbeta (db[l]) and dgamma from dy or g
+                top = l == self.L - 1
+                src = dy if top else self.g[l]
+                fn = lambda: cf.cf_bn_act_pool_bwd(POOL_CODES[pool], n, d, h, w, co, src,
+                                                   self.y[l] if top else None, self.idx[l], self.zc[l],
+                                                   self.stats[l], self.gamma[l], self.bn_eps, self.slope,
+                                                   self.dz[l], self.dsums[l], ws, wsb, main)
+                self._run(f"poolbwd{l + 1}", main, fn, timer)
+                to_host(main, host_out and host_out[1][l], self.db[l])
+            elif l == self.L - 1:
                 if pool == "max":
                     fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope,
                                                            self.dz[l], self.g[l] if routed else None, self.db[l],
@@ -275,7 +338,8 @@ class CosmoStack:
             if l > 0:
                 below = self.specs[l - 1][1]
                 fused = self.pool_bwd_fused(l - 1)
-                dsum = self.db[l - 1] if (self.routed(l - 1) or below == "none" or fused) else None
+                dsum = self.db[l - 1] if (not self.bn(l - 1) and (self.routed(l - 1) or below == "none" or fused)) \
+                    else None
                 # the lower block's output derivative rides on the input gradient
                 # unless it is average-pooled (its derivative is per voxel, from its masks)
                 x_act = self.block_input(l) if below != "avg" else None
@@ -376,18 +440,22 @@ class CosmoStack:
         insertion); dgrad 2 (filter flip + conv) for blocks 1..L-1 (+1 for
         stride 2), plus the channel sums for a routed or unpooled block below:
         1 (partials reduction) when fused in the halo-tile epilogue, else 2."""
-        n = self.L
+        n = self.L + 3 * sum(1 for l in range(self.L) if self.bn(l))  # BN: sums, reduction, normalisation
         if self.backward_enabled:
             ch = self.channels
             for l in range(self.L):
                 s2 = self.specs[l][0] == 2
                 n += 2 + s2  # wgrad
                 pool = self.specs[l][1]
-                if l == self.L - 1 or not (self.routed(l) or pool == "none" or self.pool_bwd_fused(l)):
+                if self.bn(l):
+                    n += 3  # batch-norm backward: sums, their reduction, dZ
+                elif l == self.L - 1 or not (self.routed(l) or pool == "none" or self.pool_bwd_fused(l)):
                     n += 2  # pool backward
                 if l > 0:
                     n += 2 + s2  # dgrad
-                    if self.routed(l - 1) or self.specs[l - 1][1] == "none" or self.pool_bwd_fused(l - 1):
+                    if self.bn(l - 1):
+                        pass
+                    elif self.routed(l - 1) or self.specs[l - 1][1] == "none" or self.pool_bwd_fused(l - 1):
                         fused = (not s2 and ch[l] <= 32 and ch[l] % 16 == 0 and ch[l] in (32, 64, 128)
                                  and ch[l + 1] % 16 == 0)
                         n += 1 if fused else 2

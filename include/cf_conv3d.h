@@ -261,6 +261,39 @@ cf_status cf_bn_act_pool_bwd(int32_t pool, int64_t n, int64_t d, int64_t h, int6
                              float* dsums, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The rest of the network around the conv stack (the hybrid-parallelism
+ * page, section IV and Table I: fc1 2048 -> fc2 256 -> fc3 4 outputs, leaky
+ * ReLU after every layer but the last, dropout with keep probability 0.8
+ * after the hidden fully connected layers, mean squared error; Adam with
+ * beta1 0.9, beta2 0.999, eps 1e-8).  Activations and weights fp32, row-major;
+ * m rows (samples).  Dropout draws are inputs: keep_mask [m][n] uint8 (1 =
+ * kept), kept values scaled by 1/keep.
+ *   cf_fc_fwd : y [m][n] = act(x [m][k] . w[j] (w [n][k]) + b[j]) masked; act 0 =
+ *               linear, 1 = leaky ReLU(slope); x bf16 when x_is_bf16 (e.g. the
+ *               flattened NDHWC stack output), else fp32.
+ *   cf_fc_bwd : from dy [m][n] (gradient at y), with h = this layer's stored y
+ *               (NULL for a linear layer: no leaky-ReLU derivative) and the same
+ *               keep_mask / keep: dw [n][k] = sum_i g[i][j] x[i][k], db [n] = sum_i
+ *               g[i][j], dx [m][k] = sum_j g[i][j] w[j][k] (bf16 when dx_is_bf16),
+ *               g = dy * mask/keep * LReLU'(h); dx, dw, db may be NULL.
+ *   cf_mse    : loss [1] = mean of (pred - target)^2 over count values,
+ *               dpred = 2 (pred - target) / count (either may be NULL).
+ *   cf_adam_step : m = b1 m + (1-b1) g, v = b2 v + (1-b2) g^2,
+ *               w -= lr * (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps), step t >= 1;
+ *               w_bf16 (may be NULL) receives w rounded to bf16.
+ * Reductions have a fixed order.  Pointers 16-byte aligned.
+ */
+cf_status cf_fc_fwd(int64_t m, int32_t k, int32_t n, const void* x, int32_t x_is_bf16, const float* w,
+                    const float* b, int32_t act, float slope, const uint8_t* keep_mask, float keep, float* y,
+                    void* stream);
+cf_status cf_fc_bwd(int64_t m, int32_t k, int32_t n, const void* x, int32_t x_is_bf16, const float* w, const float* h,
+                    float slope, const uint8_t* keep_mask, float keep, const float* dy, void* dx, int32_t dx_is_bf16,
+                    float* dw, float* db, void* stream);
+cf_status cf_mse(int64_t count, const float* pred, const float* target, float* loss, float* dpred, void* stream);
+cf_status cf_adam_step(int64_t count, float* w, uint16_t* w_bf16, const float* g, float* m, float* v, float lr,
+                       float beta1, float beta2, float eps, int64_t t, void* stream);
+
+/*
  * cf_bias_lrelu_pool_bwd without a workspace argument, for callers that
  * cannot allocate device memory (for example an operator plugged into a host
  * framework that owns all device allocations and hands its plug-ins neither

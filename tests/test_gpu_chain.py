@@ -49,6 +49,10 @@ def run_chain(cf, n, spatial, channels, specs, seed):
     inp["b"] = [rng.normal(0, 0.5, size=c).astype(np.float32) for c in channels[1:]]
     st = CosmoStack(n, spatial, channels, SLOPE, backward=True, specs=specs)
     st.load(inp["x"], inp["w"], inp["b"])
+    inp["gamma"] = [rng.normal(1.0, 0.5, size=c).astype(np.float32) for c in channels[1:]]
+    for l in range(st.L):
+        if st.bn(l):
+            st.gamma[l].copy_(torch.from_numpy(inp["gamma"][l]))
     dy16 = synthdata.to_bf16_bits(rng.normal(size=tuple(st.y[-1].shape)))
     dy = torch.from_numpy(dy16.view(np.int16)).view(torch.bfloat16).cuda()
     st.step(dy)
@@ -115,14 +119,28 @@ def check_chain_per_kernel(oracle, st, inp, dy16, big_from=None, rng=None):
         if _big(st, l, big_from):
             check_big_block(oracle, st, inp, dy16, l, rng)
             continue
-        stride, pool = st.specs[l]
+        stride, pool = st.specs[l][0], st.specs[l][1]
         x = f(u16(st.block_input(l)))
         w = f(inp["w"][l])
         b = inp["b"][l].astype(np.float64)
         conv = oracle.conv3d_fwd if stride == 1 else oracle.conv3d_fwd_s2
         z, S = conv(x, w), conv(np.abs(x), np.abs(w))
         gy = f(u16(st.y[l]))
-        what = f"block {l + 1} forward ({stride}, {pool})"
+        what = f"block {l + 1} forward {st.specs[l]}"
+        if st.bn(l):
+            # the stored conv output, then the normalisation + activation + pooling
+            # on that stored bf16 z: u = a*z + c with the batch statistics of z
+            zg = f(u16(st.zc[l]))
+            assert_close(zg, z, S, f"{what}: conv output")
+            gam = inp["gamma"][l].astype(np.float64)
+            mean, var = zg.reshape(-1, zg.shape[-1]).mean(0), zg.reshape(-1, zg.shape[-1]).var(0)
+            np.testing.assert_allclose(st.stats[l].cpu().numpy()[:zg.shape[-1]] / zg[..., 0].size, mean,
+                                       rtol=1e-4, atol=1e-5 * np.abs(zg).max())
+            u, _, _ = oracle.bn_fwd(zg, gam, b, st.bn_eps)
+            # scale of u's rounding: |a| |z| + |c| (fp32 coefficients, bf16 output)
+            a = gam / np.sqrt(var + st.bn_eps)
+            Su = np.abs(a) * np.abs(zg) + np.abs(b - a * mean)
+            z, S, b = u, Su, np.zeros_like(b)
         if pool == "max":
             ry, ridx = oracle.pool_fwd(z, b, SLOPE)
             zw, sw = _wins(z), _wins(S)
@@ -145,7 +163,7 @@ def check_chain_per_kernel(oracle, st, inp, dy16, big_from=None, rng=None):
     for l in range(L - 1, -1, -1):
         if _big(st, l, big_from):
             continue  # done in check_big_block
-        stride, pool = st.specs[l]
+        stride, pool = st.specs[l][0], st.specs[l][1]
         x = f(u16(st.block_input(l)))
         w = f(inp["w"][l])
         what = f"block {l + 1} ({stride}, {pool})"
@@ -160,9 +178,29 @@ def check_chain_per_kernel(oracle, st, inp, dy16, big_from=None, rng=None):
             rdz, rdb = oracle.act_bwd(g, f(u16(st.y[l])), SLOPE)
         else:
             rdz, rdb = g, g.reshape(-1, g.shape[-1]).sum(0)  # the dgrad output is dZ itself
-        assert_close(st.db[l].cpu().numpy().astype(np.float64), rdb,
-                     np.abs(rdz).reshape(-1, rdz.shape[-1]).sum(0), f"db {what}")
-        if st.routed(l):
+        if st.bn(l):
+            # the batch-norm backward of du = the pooling backward above, on the
+            # stored z: dz, dgamma, dbeta (db)
+            zg = f(u16(st.zc[l]))
+            gam = inp["gamma"][l].astype(np.float64)
+            du = rdz
+            rdz, rdg, rdb = oracle.bn_bwd(zg, du, gam, st.bn_eps)
+            C = zg.shape[-1]
+            zz = zg.reshape(-1, C)
+            inv = 1 / np.sqrt(zz.var(0) + st.bn_eps)
+            zh = (zz - zz.mean(0)) * inv
+            dd = du.reshape(-1, C)
+            assert_close(st.dgamma[l].cpu().numpy().astype(np.float64), rdg, np.abs(dd * zh).sum(0), f"dgamma {what}")
+            assert_close(st.db[l].cpu().numpy().astype(np.float64), rdb, np.abs(dd).sum(0), f"dbeta {what}")
+            Sdz = np.abs(gam * inv) * (np.abs(dd) + np.abs(dd).mean(0) + np.abs(zh) * np.abs(dd * zh).mean(0))
+            dz = f(u16(st.dz[l]))
+            assert_close(dz, rdz, Sdz.reshape(dz.shape), f"dZ {what}")
+        else:
+            assert_close(st.db[l].cpu().numpy().astype(np.float64), rdb,
+                         np.abs(rdz).reshape(-1, rdz.shape[-1]).sum(0), f"db {what}")
+        if st.bn(l):
+            pass
+        elif st.routed(l):
             dz = oracle.round_to_bf16(rdz)  # routed on chip from the same bf16 values
         else:
             dz = f(u16(st.dz[l]))
@@ -216,3 +254,14 @@ def test_variant_chain_schedules_agree(cf):
     torch.cuda.synchronize()
     for a, b in zip(ref, st.y + st.dw + st.db):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("specs,channels", [
+    ([(1, "max", "bn"), (1, "max", "bn"), (1, "none", "bn")], (4, 16, 32, 32)),
+    ([(1, "avg", "bn"), (2, "max", "bn"), (1, "none")], (16, 32, 64, 32)),
+])
+def test_batchnorm_chain_32(cf, oracle_mod, specs, channels):
+    """Batch normalisation after every conv (hybrid-parallelism page, section
+    IV), chained with max / average / no pooling and a stride-2 block."""
+    st, inp, dy16 = run_chain(cf, 2, 32, channels, specs, seed=5353)
+    check_chain_per_kernel(oracle_mod, st, inp, dy16)
