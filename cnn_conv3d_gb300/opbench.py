@@ -102,6 +102,19 @@ def main(argv=None):
                 else:
                     fn = lambda: cf.cf_conv3d_wgrad(desc, x, dz, None, dw, 0, ws, ws_n, stream)
                     nbytes = x.numel() * 2 + dz.numel() * 2 + dw.numel() * 4
+            elif op == "poolbwd":
+                # the block's pool / leaky-ReLU backward (routed dZ and bias gradient)
+                dy = torch.randn((n, sp // 2, sp // 2, sp // 2, co), device=dev).to(torch.bfloat16)
+                yp = torch.randn_like(dy)
+                ip = torch.randint(0, 8, dy.shape, dtype=torch.uint8, device=dev)
+                dzz = torch.empty((n, sp, sp, sp, co), dtype=torch.bfloat16, device=dev)
+                dbb = torch.empty((co,), dtype=torch.float32, device=dev)
+                pws = max(cf.cf_workspace_size(cf.CF_OP_POOL_BWD, desc), 256)
+                pw = torch.empty((pws,), dtype=torch.uint8, device=dev)
+                fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, sp, sp, sp, co, dy, yp, ip, 0.3, dzz, None, dbb, pw, pws,
+                                                       stream)
+                nbytes = dy.numel() * 5 + dzz.numel() * 2
+                flops = 0.0
             else:
                 raise SystemExit(f"unknown op {op}")
             for _ in range(a.warmup):
@@ -120,6 +133,7 @@ def main(argv=None):
                 raise SystemExit("device status word set")
             ms = float(np.median(ts))
             tf = flops / (ms * 1e-3) / 1e12
+            flops = 2.0 * co * ci * 27 * n * sp ** 3
             tag = "+pool" if (op == "fwd" and a.pool) else ("+routed" if (op == "wgrad" and a.routed) else "")
             rec = {"shape": label, "op": op + tag, "n": n, "c_in": ci,
                    "c_out": co, "spatial": sp, "ms": round(ms, 4), "tflops": round(tf, 1),

@@ -72,15 +72,22 @@ def test_training_step_stages(torch_cuda, oracle_mod):
     m.backward()
     torch.cuda.synchronize()
     assert cf.cf_last_device_status() == cf.CF_OK
+    # each layer's backward on its own GPU inputs: stored activations and the
+    # gradient the layer above produced; S = sums of |products|
     hs = [feat] + [t.cpu().numpy().astype(np.float64) for t in m.h]
-    grads, dfeat = oracle_mod.head_bwd(hs, fcs, masks, KEEP, SLOPE, m.dpred.cpu().numpy())
-    for i, (dw, db) in enumerate(grads):
-        gw = m.dfw[i].cpu().numpy().astype(np.float64)
-        assert_close(gw, dw, np.abs(dw) + 1e-6 * np.abs(dw).max(), f"fc{i + 1} dW", rel_l2=1e-4, elem=1e-3)
-        assert_close(m.dfb[i].cpu().numpy(), db, np.abs(db) + 1e-6 * np.abs(db).max(), f"fc{i + 1} db",
-                     rel_l2=1e-4, elem=1e-3)
-    gdf = f(m.dfeat.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)).reshape(n, -1)
-    assert_close(gdf, dfeat, np.abs(dfeat) + 1e-3 * np.abs(dfeat).max(), "dfeat (bf16)", rel_l2=5e-3, elem=1e-2)
+    L = len(fcs)
+    for i in range(L - 1, -1, -1):
+        dy = (m.dpred if i == L - 1 else m.dh[i]).cpu().numpy().astype(np.float64)
+        g = dy if i == L - 1 else dy * masks[i] / KEEP * np.where(hs[i + 1] > 0, 1.0, SLOPE)
+        dx, dw, db = oracle_mod.fc_bwd(hs[i], fcs[i][0], g)
+        assert_close(m.dfw[i].cpu().numpy(), dw, np.abs(g).T @ np.abs(hs[i]), f"fc{i + 1} dW")
+        assert_close(m.dfb[i].cpu().numpy(), db, np.abs(g).sum(0), f"fc{i + 1} db")
+        Sx = np.abs(g) @ np.abs(fcs[i][0].astype(np.float64))
+        if i > 0:
+            assert_close(m.dh[i - 1].cpu().numpy(), dx, Sx, f"fc{i + 1} dx")
+        else:
+            gdf = f(m.dfeat.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)).reshape(n, -1)
+            assert_close(gdf, dx, Sx, "dfeat (bf16)")
     # Adam on every parameter, from the gradients just computed
     before = [(p.cpu().numpy().astype(np.float64), g.cpu().numpy().astype(np.float64)) for p, _, g in m.params()]
     m.update(1e-3)
