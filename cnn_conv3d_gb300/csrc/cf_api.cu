@@ -209,6 +209,8 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
     const float* bias = epi ? epi->bias : nullptr;
     uint8_t* idx = pooled ? epi->argmax : nullptr;
     const float slope = epi ? epi->slope : 0.f;
+    if (small && mode == EPI_POOL && pool_kind == 0 && quad_path_supported(desc->d, desc->h, desc->w, ci, co))
+        return launch_conv_quad(ctx, desc->n, desc->d, desc->h, desc->w, co, x, w, y, idx, bias, slope);
     if (small)
         return launch_conv_smallc(ctx, desc->n, desc->d, desc->h, desc->w, ci, co, x, w, mode, y, idx, bias, slope,
                                   pool_kind, act);

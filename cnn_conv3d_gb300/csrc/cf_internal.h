@@ -77,6 +77,14 @@ cf_status launch_conv_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h
                            float* colsum_part = nullptr, int pool_kind = 0, int act = 0,
                            uint16_t* route_dz = nullptr, const uint8_t* route_idx = nullptr);
 
+// conv_quad.cu -------------------------------------------------------------
+// First-layer forward (c_in 4, c_out 16 or 32) with the max-pool epilogue,
+// A read straight from the input tile: d even, h a multiple of 16, w of 32.
+bool quad_path_supported(int64_t d, int64_t h, int64_t w, int c_in, int c_out);
+cf_status launch_conv_quad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_out,
+                           const uint16_t* x, const uint16_t* wk, uint16_t* y, uint8_t* idx, const float* bias,
+                           float slope);
+
 // conv_smallc.cu: forward conv for c_in in {1,4} (im2col operand in tensor memory).
 cf_status launch_conv_smallc(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                              int c_out, const uint16_t* x, const uint16_t* wk, int epi, uint16_t* y,

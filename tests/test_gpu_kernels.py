@@ -207,6 +207,10 @@ SMALLC_SHAPES = [
     (1, 16, 16, 16, 1, 8),  # the single-block CosmoFlow case: 1 -> 8 channels at 16^3
     (1, 4, 6, 24, 1, 16),
     (2, 2, 4, 10, 4, 32),   # ragged tile in w (10 = 8 + 2)
+    # pooled: the first-layer quad-row forward (d even, h % 16 == 0, w % 32 == 0)
+    (2, 4, 32, 64, 4, 32),  # several tiles in every dimension
+    (1, 2, 16, 32, 4, 16),  # c_out 16: MMA width 64
+    (1, 6, 16, 96, 4, 32),  # three tiles along w, three plane pairs
 ]
 
 
