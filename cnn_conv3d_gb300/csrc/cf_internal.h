@@ -101,6 +101,13 @@ cf_status launch_wgrad_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
 // conv_wgrad.cu -------------------------------------------------------------
 size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out);
 // the (c_in, c_out) pairs launch_wgrad implements
+// conv_wgrad_quad.cu: first-layer weight gradient (c_in 4, c_out 32) with the
+// max-pool backward fused, d even, h a multiple of 16, w of 32; writes
+// *n_splits phase-major split-K partials of 32 x 108 floats.
+bool wgrad_quad_supported(int64_t d, int64_t h, int64_t w, int c_in, int c_out);
+size_t wgrad_quad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w);
+cf_status launch_wgrad_quad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, const uint16_t* x,
+                            const uint16_t* g, const uint8_t* idx, float* part, int* n_splits);
 bool wgrad_shape_supported(int c_in, int c_out);
 // true when launch_wgrad takes the routed form (idx != NULL: dz pooled, the
 // dense dZ expanded on chip) for this c_in

@@ -329,7 +329,10 @@ size_t wgrad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64
     if (wgrad_halo_supported(c_in, c_out))
         return wgrad_halo_workspace_bytes(num_sms, n, d, h, w, c_in, c_out);
     WgradGeom g = wgrad_geom(num_sms, n, d, h, w, c_in, c_out);
-    return (size_t)g.n_splits * c_out * 27 * c_in * sizeof(float);
+    const size_t generic = (size_t)g.n_splits * c_out * 27 * c_in * sizeof(float);
+    if (wgrad_quad_supported(d, h, w, c_in, c_out))
+        return std::max(generic, wgrad_quad_workspace_bytes(num_sms, n, d, h, w));
+    return generic;
 }
 
 template <typename K>
@@ -405,6 +408,11 @@ cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, in
     cf_status st;
     if (wgrad_halo_supported(c_in, c_out)) {
         st = launch_wgrad_halo(ctx, n, d, h, w, c_in, c_out, x, dz, part, &n_splits);
+        if (st != CF_OK) return st;
+        return launch_splitk_reduce(ctx, part, dw, (int64_t)c_out * 27 * c_in, n_splits, accumulate);
+    }
+    if (idx && wgrad_quad_supported(d, h, w, c_in, c_out)) {
+        st = launch_wgrad_quad(ctx, n, d, h, w, x, dz, idx, part, &n_splits);
         if (st != CF_OK) return st;
         return launch_splitk_reduce(ctx, part, dw, (int64_t)c_out * 27 * c_in, n_splits, accumulate);
     }

@@ -1,0 +1,363 @@
+// conv_wgrad_quad.cu -- backward-weight conv of the CosmoFlow first layer
+// (c_in = 4, c_out = 32) with the max-pool backward fused in, as the weight
+// gradient of the quad-row forward (conv_quad.cu).
+//
+// (CosmoFlow page, section III-C "backward weights".)
+//   dW[co, t, ci] = sum_{n,v} dZ[n,v,co] * X[n, v + t - 1, ci]
+//
+// The quad-row forward computes, per tap pair (kd, kh) and half hf,
+//   Z[r, (f, co)] += sum_k A_{kd,kh,hf}[r, k] * B_{kd,kh,hf}[(f, co), k]
+// with row r a quad of voxels 4r .. 4r+3, phase f the voxel 4r + f, and K slot
+// k = (voxel slot s, ci) of the input rows E / O (even / odd voxel pairs).
+// Its weight gradient is the transposed product
+//   G_{kd,hf}[(f, co), (kh, k)] = sum_r dZ[4r + f, co] * A_{kd,kh,hf}[r, k]
+// and dW[co, kd, kh, kw, ci] = sum_f G[(f, co), (kh, (s, ci))] with
+// s = f + kw - 1 (one K slot per phase and tap).  Here:
+//   A operand (tensor memory): dZ arranged as M = (phase f, co) = 128 lanes by
+//     K = rows of the tile; built per tile by four builder warps (warp f, lane
+//     co) from the pooled gradient and the argmax codes: dZ at voxel v is the
+//     gradient of v's window where the window's code is v's position, else 0.
+//   B operand (shared memory, MN-major, no swizzle): the E / O input rows,
+//     N = 4 line offsets kh x 8 (two voxels x 4 channels), K = 16 rows (2 lines
+//     x 8 quads) per MMA; both the N groups (next kh) and the K groups (next
+//     line) are one line pitch apart.  The fourth line offset (kh = 3) is not
+//     a tap and is dropped.
+// Per K step 12 MMAs of 128 x 32 x 16: 3 kd x 4 row parts (E[r], O[r+1],
+// E[r+1], O[r], i.e. voxel slots 0-1, 2-3, 4-5, -2..-1), one accumulator of 32
+// columns each (384 of the 512 tensor-memory columns; the rest hold two dZ
+// tiles).  Four issuer threads take one row part each.
+//
+// Tile: 1 plane x 16 lines x 32 voxels (128 rows).  Each CTA sums a
+// contiguous range of tiles and writes, per phase, its 32 x 108 partial dW
+// (phase-major split-K partials, summed afterwards in a fixed order).
+//
+// Roles (288 threads): warp 0 TMA producer; warps 1, 2, 3, 8 MMA issuers
+// (row parts 0..3); warps 4..7 builders of the dZ tiles (warp 4 + f: phase f)
+// and, after the last tile, the epilogue.
+#include <algorithm>
+
+#include "conv_common.cuh"
+
+namespace cf {
+
+constexpr int WQ_W = 32, WQ_H = 16;                 // tile (one plane)
+constexpr int WQ_QUADS = WQ_W / 4 + 1;              // E / O entries per line (9)
+constexpr int WQ_LINES = WQ_H + 2, WQ_PLANES = 3;
+constexpr uint32_t WQ_LP = WQ_QUADS * 16;           // 144: line pitch of a box
+constexpr uint32_t WQ_BOX = WQ_PLANES * WQ_LINES * WQ_LP;  // 7776
+constexpr uint32_t WQ_O = 7808;                     // O box (128-byte aligned)
+constexpr uint32_t WQ_G = 16384;                    // pooled gradient [8][16][32] bf16
+constexpr uint32_t WQ_I = 24576;                    // codes [8][16][32]
+constexpr uint32_t WQ_STAGE = 28672;
+constexpr uint32_t WQ_TX = 2 * WQ_BOX + 8192 + 4096;
+constexpr uint32_t WQ_BAR = 256;
+constexpr int WQ_STAGES = (int)((227 * 1024 - 1024 - WQ_BAR) / WQ_STAGE);
+constexpr uint32_t WQ_SMEM = 1024 + WQ_STAGES * WQ_STAGE + WQ_BAR;
+constexpr uint32_t WQ_ACOL = 384;                   // first column of the dZ tiles
+constexpr uint32_t WQ_IDESC = idesc_bf16(128, 32, 0, 1);
+static_assert(WQ_O >= WQ_BOX && WQ_O % 128 == 0, "O box");
+static_assert(WQ_G >= WQ_O + WQ_BOX + 3 * WQ_LP, "the dropped kh = 3 rows stay inside the stage");
+static_assert(WQ_STAGES >= 2, "shared memory");
+static_assert(8 * (2 * WQ_STAGES + 2 + 2 + 1 + 4) + 8 <= (int)WQ_BAR, "barrier area");
+
+struct WqParams {
+    int N, D, H, W;
+    int tiles_w, tiles_h, num_tiles;
+    FastDiv fd_w, fd_h, fd_d;
+    float* part;  // [units][4 phases][32][108]
+    int* status;
+    uint64_t wait_ns;
+};
+
+struct WqTile {
+    int n, d0, h0, w0;
+};
+
+// Tiles are numbered w fastest, then h, d (one plane each), n.
+__device__ __forceinline__ WqTile wq_decode(const WqParams& p, int tile) {
+    WqTile t;
+    uint32_t m = (uint32_t)tile, q = p.fd_w.div(m);
+    t.w0 = (int)(m - q * p.fd_w.d) * WQ_W;
+    m = q;
+    q = p.fd_h.div(m);
+    t.h0 = (int)(m - q * p.fd_h.d) * WQ_H;
+    m = q;
+    q = p.fd_d.div(m);
+    t.d0 = (int)(m - q * p.fd_d.d);
+    t.n = (int)q;
+    return t;
+}
+
+// The CTA's tile range: num_tiles split into gridDim.x near-equal contiguous parts.
+__device__ __forceinline__ void wq_range(const WqParams& p, int& t0, int& t1) {
+    const int G = (int)gridDim.x, u = (int)blockIdx.x;
+    const int base = p.num_tiles / G, rem = p.num_tiles - base * G;
+    t0 = u * base + min(u, rem);
+    t1 = t0 + base + (u < rem ? 1 : 0);
+}
+
+__global__ void __launch_bounds__(288, 1)
+    wgrad_quad_kernel(const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmO,
+                      const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmI,
+                      const WqParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* ring = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WQ_STAGES * WQ_STAGE);
+    uint64_t* full = bars;
+    uint64_t* empty = full + WQ_STAGES;
+    uint64_t* afull = empty + WQ_STAGES;
+    uint64_t* aempty = afull + 2;
+    uint64_t* tfull = aempty + 2;
+    uint64_t* drain = tfull + 1;  // [4]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int t0, t1;
+    wq_range(p, t0, t1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < WQ_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 8);  // four issuers' MMAs + four builder warps
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&afull[b], 4);   // four builder warps
+            mbar_init(&aempty[b], 4);  // four issuers' MMAs
+        }
+        mbar_init(tfull, 4);
+        for (int k = 0; k < 4; ++k) mbar_init(&drain[k], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmE);
+        tma_prefetch_desc(&tmO);
+        tma_prefetch_desc(&tmG);
+        tma_prefetch_desc(&tmI);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer: E / O input rows, pooled gradient, codes
+            int s = 0;
+            uint32_t ph = 0, issued = 0, par = 0;
+            bool ok = true;
+            for (int tile = t0; tile < t1; ++tile) {
+                const WqTile t = wq_decode(p, tile);
+                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = ring + s * WQ_STAGE;
+                mbar_arrive_expect_tx(&full[s], WQ_TX);
+                const int q0 = t.w0 >> 2;
+                tma_load_5d(st, &tmE, &full[s], 0, q0, t.h0 - 1, t.d0 - 1, t.n);
+                tma_load_5d(st + WQ_O, &tmO, &full[s], 0, q0 - 1, t.h0 - 1, t.d0 - 1, t.n);
+                tma_load_5d(st + WQ_G, &tmG, &full[s], 0, t.w0 >> 1, t.h0 >> 1, t.d0 >> 1, t.n);
+                tma_load_5d(st + WQ_I, &tmI, &full[s], 0, t.w0 >> 1, t.h0 >> 1, t.d0 >> 1, t.n);
+                issued |= 1u << s;
+                par = (par & ~(1u << s)) | (ph << s);
+                if (++s == WQ_STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            if (!ok) {
+                for (int k = 0; k < WQ_STAGES; ++k)
+                    if (issued & (1u << k)) mbar_wait_timed(&full[k], (par >> k) & 1, p.wait_ns);
+            }
+        }
+    } else if (warp <= 3 || warp == 8) {
+        if (lane == 0) {
+            // ---------------- MMA issuer of row part pt (voxel slots 0-1, 2-3, 4-5, -2..-1)
+            const int pt = warp == 8 ? 3 : warp - 1;
+            const uint32_t part_off = pt == 0 ? 0u : pt == 1 ? WQ_O + 16 : pt == 2 ? 16u : WQ_O;
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int tile = t0, lt = 0; tile < t1; ++tile, ++lt) {
+                const uint32_t b = lt & 1;
+                if (!mbar_wait(&full[s], ph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL) ||
+                    !mbar_wait(&afull[b], (lt >> 1) & 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t rows = smem_u32(ring + s * WQ_STAGE) + part_off;
+                const uint32_t a_tmem = tmem_base + WQ_ACOL + b * 64;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int kd = 0; kd < 3; ++kd)
+                        umma_bf16_tmem_a(tmem_base + (pt * 3 + kd) * 32, a_tmem + 8 * j,
+                                         sdesc(rows + (kd * WQ_LINES + 2 * j) * WQ_LP, WQ_LP, WQ_LP, SWZ_NONE),
+                                         WQ_IDESC, (lt | j) ? 1u : 0u);
+                umma_commit(&empty[s]);
+                umma_commit(&aempty[b]);
+                if (++s == WQ_STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            if (ok) {
+                umma_commit(tfull);
+            } else {
+                umma_commit(&drain[pt]);
+                mbar_wait_timed(&drain[pt], 0, p.wait_ns);
+            }
+        }
+    } else {
+        // ---------------- builders (phase f = warp - 4, channel co = lane), then the epilogue
+        const int f = warp & 3, co = lane;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(f * 32) << 16);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = t0, lt = 0; tile < t1; ++tile, ++lt) {
+            const uint32_t b = lt & 1;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&full[s], ph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL) &&
+                                mbar_wait(&aempty[b], ((lt >> 1) & 1) ^ 1, abort_flag, p.wait_ns, p.status,
+                                          WAIT_PRODUCER_EMPTY))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int dd = wq_decode(p, tile).d0 & 1;
+            const uint8_t* st = ring + s * WQ_STAGE;
+            const uint16_t* gp = reinterpret_cast<const uint16_t*>(st + WQ_G) + co;
+            const uint8_t* ip = st + WQ_I + co;
+            // column c holds rows 2c, 2c+1 = quads i, i+1 of line c/4 (i = 2 (c % 4)):
+            // voxels w = 4i + f and 4i + 4 + f, pooled w 2i + f/2 and 2i + 2 + f/2
+            uint32_t col[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const int gl = c >> 2, i = 2 * (c & 3);
+                const int pw = 2 * i + (f >> 1), pr = (gl >> 1) * 16;
+                const uint32_t code = (uint32_t)(dd * 4 + (gl & 1) * 2 + (f & 1));
+                const uint32_t v0 = ip[(pr + pw) * 32] == code ? gp[(pr + pw) * 32] : 0u;
+                const uint32_t v1 = ip[(pr + pw + 2) * 32] == code ? gp[(pr + pw + 2) * 32] : 0u;
+                col[c] = v0 | (v1 << 16);
+            }
+            tmem_st32(lane_addr + WQ_ACOL + b * 64, col);
+            tmem_st32(lane_addr + WQ_ACOL + b * 64 + 32, col + 32);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&afull[b]);
+                mbar_arrive(&empty[s]);
+            }
+            if (++s == WQ_STAGES) {
+                s = 0;
+                ph ^= 1;
+            }
+        }
+        // ---------------- epilogue: this lane's (f, co) partial of every dW entry
+        if (ok && __all_sync(0xffffffffu, mbar_wait(tfull, 0, abort_flag, p.wait_ns, p.status, WAIT_EPI_TMEM_FULL))) {
+            tc_fence_after();
+            float* out = p.part + (((int64_t)blockIdx.x * 4 + f) * 32 + co) * 108;
+#pragma unroll 1
+            for (int pt = 0; pt < 4; ++pt) {
+                const int s0 = pt == 0 ? 0 : pt == 1 ? 2 : pt == 2 ? 4 : -2;  // voxel slot of the part's first pair
+#pragma unroll 1
+                for (int kd = 0; kd < 3; ++kd) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + (pt * 3 + kd) * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int kw = s0 + (e >> 2) - f + 1;
+                            if (kw >= 0 && kw <= 2)
+                                out[(kd * 9 + kh * 3 + kw) * 4 + (e & 3)] = __uint_as_float(r[kh * 8 + e]);
+                        }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+bool wgrad_quad_supported(int64_t d, int64_t h, int64_t w, int c_in, int c_out) {
+    return c_in == 4 && c_out == 32 && d % 2 == 0 && h % WQ_H == 0 && w % WQ_W == 0;
+}
+
+static int64_t wq_tiles(int64_t n, int64_t d, int64_t h, int64_t w) { return n * d * (h / WQ_H) * (w / WQ_W); }
+
+static int wq_units(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, wq_tiles(n, d, h, w)));
+}
+
+size_t wgrad_quad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w) {
+    return (size_t)wq_units(num_sms, n, d, h, w) * 4 * 32 * 108 * sizeof(float);
+}
+
+static bool wq_rows_map(CUtensorMap* m, const void* base, int64_t n, int64_t d, int64_t h, int64_t w) {
+    const uint64_t dims[5] = {8u, (uint64_t)(w / 4), (uint64_t)h, (uint64_t)d, (uint64_t)n};
+    const uint64_t str[4] = {32u, (uint64_t)w * 8, (uint64_t)(h * w * 8), (uint64_t)(d * h * w * 8)};
+    const uint32_t box[5] = {8u, (uint32_t)WQ_QUADS, (uint32_t)WQ_LINES, (uint32_t)WQ_PLANES, 1u};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+static bool wq_pooled_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz, int64_t n, int64_t d,
+                          int64_t h, int64_t w) {
+    const uint64_t d2 = d / 2, h2 = h / 2, w2 = w / 2;
+    const uint64_t dims[5] = {32u, w2, h2, d2, (uint64_t)n};
+    const uint64_t str[4] = {(uint64_t)32 * esz, w2 * 32 * esz, h2 * w2 * 32 * esz, d2 * h2 * w2 * 32 * esz};
+    const uint32_t box[5] = {32u, (uint32_t)(WQ_W / 2), (uint32_t)(WQ_H / 2), 1u, 1u};
+    return encode_tmap(m, dt, 5, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+cf_status launch_wgrad_quad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, const uint16_t* x,
+                            const uint16_t* g, const uint8_t* idx, float* part, int* n_splits) {
+    if (!wgrad_quad_supported(d, h, w, 4, 32)) return CF_ERR_UNSUPPORTED;
+    const int64_t tiles = wq_tiles(n, d, h, w);
+    if (tiles > INT32_MAX) return CF_ERR_UNSUPPORTED;
+    CUtensorMap te, to, tg, ti;
+    if (!wq_rows_map(&te, x, n, d, h, w) || !wq_rows_map(&to, reinterpret_cast<const uint8_t*>(x) + 16, n, d, h, w) ||
+        !wq_pooled_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, d, h, w) ||
+        !wq_pooled_map(&ti, idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, n, d, h, w))
+        return CF_ERR_CUDA;
+    WqParams p;
+    p.N = (int)n;
+    p.D = (int)d;
+    p.H = (int)h;
+    p.W = (int)w;
+    p.tiles_w = (int)(w / WQ_W);
+    p.tiles_h = (int)(h / WQ_H);
+    p.num_tiles = (int)tiles;
+    p.fd_w = FastDiv::make((uint32_t)p.tiles_w);
+    p.fd_h = FastDiv::make((uint32_t)p.tiles_h);
+    p.fd_d = FastDiv::make((uint32_t)d);
+    p.part = part;
+    p.status = ctx.status;
+    p.wait_ns = ctx.wait_ns;
+    if (cudaFuncSetAttribute(wgrad_quad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WQ_SMEM) != cudaSuccess)
+        return CF_ERR_CUDA;
+    const int grid = wq_units(ctx.num_sms, n, d, h, w);
+    wgrad_quad_kernel<<<grid, 288, WQ_SMEM, ctx.stream>>>(te, to, tg, ti, p);
+    if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+    *n_splits = grid * 4;
+    return CF_OK;
+}
+
+}  // namespace cf

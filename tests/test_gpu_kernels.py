@@ -363,6 +363,10 @@ ROUTED_SHAPES = [
     (1, 2, 4, 16, 4, 256),
     (1, 2, 4, 16, 4, 48),      # routed small c_in with a padded N tile
     (1, 2, 4, 16, 16, 32),     # 16-channel input, dZ expanded in the workspace
+    # the first-layer quad-row weight gradient (c_in 4, c_out 32; h % 16 == 0, w % 32 == 0)
+    (2, 4, 32, 64, 4, 32),
+    (1, 6, 16, 96, 4, 32),
+    (1, 2, 48, 32, 4, 32),
 ]
 
 
