@@ -18,22 +18,27 @@
 //     co) from the pooled gradient and the argmax codes: dZ at voxel v is the
 //     gradient of v's window where the window's code is v's position, else 0.
 //   B operand (shared memory, MN-major, no swizzle): the E / O input rows,
-//     N = 4 line offsets kh x 8 (two voxels x 4 channels), K = 16 rows (2 lines
-//     x 8 quads) per MMA; both the N groups (next kh) and the K groups (next
-//     line) are one line pitch apart.  The fourth line offset (kh = 3) is not
-//     a tap and is dropped.
-// Per K step 12 MMAs of 128 x 32 x 16: 3 kd x 4 row parts (E[r], O[r+1],
-// E[r+1], O[r], i.e. voxel slots 0-1, 2-3, 4-5, -2..-1), one accumulator of 32
-// columns each (384 of the 512 tensor-memory columns; the rest hold two dZ
-// tiles).  Four issuer threads take one row part each.
+//     N = (kh, E/O, two voxels x 4 channels), K = 16 rows (2 lines x 8 quads)
+//     per MMA.  The input lines arrive as one TMA box of plain lines (288-byte
+//     rows: a box of 16-byte E / O rows measured TMA-bound) and the builder
+//     warps copy their pairs into the E and O rows.
+// The builders store each input line as [E row | O row], so that one MMA
+// takes the pairs E[r] and O[r] (voxel slots 0-1 and -2..-1, the low half) or
+// E[r+1] and O[r+1] (slots 4-5 and 2-3, the high half) of the three lines kh:
+// N = 3 kh x 2 x 8 = 48, the N groups one row (144 bytes) apart.  Per K step 6
+// MMAs of 128 x 48 x 16 (3 kd x 2 halves), one accumulator of 48 columns
+// each (288 of the 512 tensor-memory columns; columns 384.. hold two dZ
+// tiles).  Three issuer threads take one kd each (measured: N = 32 MMAs with
+// A in tensor memory run at ~27 cycles, so fewer wider MMAs pay).
 //
 // Tile: 1 plane x 16 lines x 32 voxels (128 rows).  Each CTA sums a
 // contiguous range of tiles and writes, per phase, its 32 x 108 partial dW
 // (phase-major split-K partials, summed afterwards in a fixed order).
 //
-// Roles (288 threads): warp 0 TMA producer; warps 1, 2, 3, 8 MMA issuers
-// (row parts 0..3); warps 4..7 builders of the dZ tiles (warp 4 + f: phase f)
-// and, after the last tile, the epilogue.
+// Roles (384 threads): warp 0 TMA producer; warps 1, 2, 3 MMA issuers
+// (kd = 0, 1, 2); warps 4..11 builders of the dZ tiles (warps 4 + f and
+// 8 + f: phase f, pooled lines 0-3 / 4-7) and, after the last tile, warps 4..7
+// the epilogue.
 #include <algorithm>
 
 #include "conv_common.cuh"
@@ -43,20 +48,26 @@ namespace cf {
 constexpr int WQ_W = 32, WQ_H = 16;                 // tile (one plane)
 constexpr int WQ_QUADS = WQ_W / 4 + 1;              // E / O entries per line (9)
 constexpr int WQ_LINES = WQ_H + 2, WQ_PLANES = 3;
-constexpr uint32_t WQ_LP = WQ_QUADS * 16;           // 144: line pitch of a box
-constexpr uint32_t WQ_BOX = WQ_PLANES * WQ_LINES * WQ_LP;  // 7776
-constexpr uint32_t WQ_O = 7808;                     // O box (128-byte aligned)
-constexpr uint32_t WQ_G = 16384;                    // pooled gradient [8][16][32] bf16
-constexpr uint32_t WQ_I = 24576;                    // codes [8][16][32]
-constexpr uint32_t WQ_STAGE = 28672;
-constexpr uint32_t WQ_TX = 2 * WQ_BOX + 8192 + 4096;
+constexpr uint32_t WQ_RP = WQ_QUADS * 16;           // 144: one E or O row
+constexpr uint32_t WQ_LP = 2 * WQ_RP;               // 288: line pitch of the rows ([E | O] per line)
+constexpr int WQ_PAIRS = 2 * WQ_QUADS;              // 18 voxel pairs per input line (w0-2 .. w0+33)
+constexpr uint32_t WQ_PBOX = WQ_PLANES * WQ_LINES * WQ_PAIRS * 16;  // 15552: the TMA box (plain lines)
+constexpr uint32_t WQ_EO = 15616;                   // the E / O rows
+constexpr uint32_t WQ_G = 31744;                    // pooled gradient [8][16][32] bf16
+constexpr uint32_t WQ_I = WQ_G + 8192;              // codes [8][16][32]
+constexpr uint32_t WQ_STAGE = WQ_I + 4096;
+constexpr uint32_t WQ_TX = WQ_PBOX + 8192 + 4096;
 constexpr uint32_t WQ_BAR = 256;
 constexpr int WQ_STAGES = (int)((227 * 1024 - 1024 - WQ_BAR) / WQ_STAGE);
 constexpr uint32_t WQ_SMEM = 1024 + WQ_STAGES * WQ_STAGE + WQ_BAR;
 constexpr uint32_t WQ_ACOL = 384;                   // first column of the dZ tiles
-constexpr uint32_t WQ_IDESC = idesc_bf16(128, 32, 0, 1);
-static_assert(WQ_O >= WQ_BOX && WQ_O % 128 == 0, "O box");
-static_assert(WQ_G >= WQ_O + WQ_BOX + 3 * WQ_LP, "the dropped kh = 3 rows stay inside the stage");
+constexpr int WQ_N = 48;                            // 3 kh x (E, O) x 8
+constexpr uint32_t WQ_IDESC = idesc_bf16(128, WQ_N, 0, 1);
+static_assert(WQ_EO >= WQ_PBOX, "stage layout");
+// the last B operand (kd = 2, K step 7, high half) ends inside the stage under
+// either order of the two descriptor strides (one of them is 144, the other 288)
+static_assert(WQ_G >= WQ_EO + (2 * WQ_LINES + 14) * WQ_LP + 16 + 5 * WQ_LP + WQ_RP + 128, "B operand bounds");
+static_assert(6 * WQ_N <= (int)WQ_ACOL, "tensor memory");
 static_assert(WQ_STAGES >= 2, "shared memory");
 static_assert(8 * (2 * WQ_STAGES + 2 + 2 + 1 + 4) + 8 <= (int)WQ_BAR, "barrier area");
 
@@ -73,17 +84,19 @@ struct WqTile {
     int n, d0, h0, w0;
 };
 
-// Tiles are numbered w fastest, then h, d (one plane each), n.
+// Tiles are numbered d fastest (one plane each), then w, h, n: the next tile of
+// a CTA reads two of the same three input planes and, every other plane, the
+// same pooled tile, which are still in L2.
 __device__ __forceinline__ WqTile wq_decode(const WqParams& p, int tile) {
     WqTile t;
-    uint32_t m = (uint32_t)tile, q = p.fd_w.div(m);
+    uint32_t m = (uint32_t)tile, q = p.fd_d.div(m);
+    t.d0 = (int)(m - q * p.fd_d.d);
+    m = q;
+    q = p.fd_w.div(m);
     t.w0 = (int)(m - q * p.fd_w.d) * WQ_W;
     m = q;
     q = p.fd_h.div(m);
     t.h0 = (int)(m - q * p.fd_h.d) * WQ_H;
-    m = q;
-    q = p.fd_d.div(m);
-    t.d0 = (int)(m - q * p.fd_d.d);
     t.n = (int)q;
     return t;
 }
@@ -96,9 +109,9 @@ __device__ __forceinline__ void wq_range(const WqParams& p, int& t0, int& t1) {
     t1 = t0 + base + (u < rem ? 1 : 0);
 }
 
-__global__ void __launch_bounds__(288, 1)
-    wgrad_quad_kernel(const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmO,
-                      const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmI,
+__global__ void __launch_bounds__(384, 1)
+    wgrad_quad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
+                      const __grid_constant__ CUtensorMap tmI,
                       const WqParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -120,18 +133,17 @@ __global__ void __launch_bounds__(288, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < WQ_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 8);  // four issuers' MMAs + four builder warps
+            mbar_init(&empty[s], 11);  // three issuers' MMAs + eight builder warps
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&afull[b], 4);   // four builder warps
-            mbar_init(&aempty[b], 4);  // four issuers' MMAs
+            mbar_init(&afull[b], 8);   // eight builder warps
+            mbar_init(&aempty[b], 3);  // three issuers' MMAs
         }
-        mbar_init(tfull, 4);
-        for (int k = 0; k < 4; ++k) mbar_init(&drain[k], 1);
+        mbar_init(tfull, 3);
+        for (int k = 0; k < 3; ++k) mbar_init(&drain[k], 1);
         *abort_flag = 0;
         fence_barrier_init();
-        tma_prefetch_desc(&tmE);
-        tma_prefetch_desc(&tmO);
+        tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmG);
         tma_prefetch_desc(&tmI);
     }
@@ -158,9 +170,7 @@ __global__ void __launch_bounds__(288, 1)
                 }
                 uint8_t* st = ring + s * WQ_STAGE;
                 mbar_arrive_expect_tx(&full[s], WQ_TX);
-                const int q0 = t.w0 >> 2;
-                tma_load_5d(st, &tmE, &full[s], 0, q0, t.h0 - 1, t.d0 - 1, t.n);
-                tma_load_5d(st + WQ_O, &tmO, &full[s], 0, q0 - 1, t.h0 - 1, t.d0 - 1, t.n);
+                tma_load_5d(st, &tmX, &full[s], 4 * t.w0 - 8, t.h0 - 1, t.d0 - 1, t.n, 0);
                 tma_load_5d(st + WQ_G, &tmG, &full[s], 0, t.w0 >> 1, t.h0 >> 1, t.d0 >> 1, t.n);
                 tma_load_5d(st + WQ_I, &tmI, &full[s], 0, t.w0 >> 1, t.h0 >> 1, t.d0 >> 1, t.n);
                 issued |= 1u << s;
@@ -175,11 +185,12 @@ __global__ void __launch_bounds__(288, 1)
                     if (issued & (1u << k)) mbar_wait_timed(&full[k], (par >> k) & 1, p.wait_ns);
             }
         }
-    } else if (warp <= 3 || warp == 8) {
+    } else if (warp <= 3) {
         if (lane == 0) {
-            // ---------------- MMA issuer of row part pt (voxel slots 0-1, 2-3, 4-5, -2..-1)
-            const int pt = warp == 8 ? 3 : warp - 1;
-            const uint32_t part_off = pt == 0 ? 0u : pt == 1 ? WQ_O + 16 : pt == 2 ? 16u : WQ_O;
+            // ---------------- MMA issuer of input plane kd: per K step the low half
+            // (E[r] | O[r]: voxel slots 0-1 | -2..-1) and the high half (E[r+1] | O[r+1]:
+            // slots 4-5 | 2-3), N = (kh, E/O, 8)
+            const int kd = warp - 1;
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -191,15 +202,17 @@ __global__ void __launch_bounds__(288, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t rows = smem_u32(ring + s * WQ_STAGE) + part_off;
+                const uint32_t rows = smem_u32(ring + s * WQ_STAGE) + WQ_EO + kd * WQ_LINES * WQ_LP;
                 const uint32_t a_tmem = tmem_base + WQ_ACOL + b * 64;
+                // MN-major without swizzle: K groups (the next output line) WQ_LP apart
+                // (leading byte offset), N groups (kh, E/O) WQ_RP apart (stride byte offset)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
 #pragma unroll
-                    for (int kd = 0; kd < 3; ++kd)
-                        umma_bf16_tmem_a(tmem_base + (pt * 3 + kd) * 32, a_tmem + 8 * j,
-                                         sdesc(rows + (kd * WQ_LINES + 2 * j) * WQ_LP, WQ_LP, WQ_LP, SWZ_NONE),
-                                         WQ_IDESC, (lt | j) ? 1u : 0u);
+                    for (int hl = 0; hl < 2; ++hl)
+                        umma_bf16_tmem_a(tmem_base + (kd * 2 + hl) * WQ_N, a_tmem + 8 * j,
+                                         sdesc(rows + 2 * j * WQ_LP + 16 * hl, WQ_LP, WQ_RP, SWZ_NONE), WQ_IDESC,
+                                         (lt | j) ? 1u : 0u);
                 umma_commit(&empty[s]);
                 umma_commit(&aempty[b]);
                 if (++s == WQ_STAGES) {
@@ -210,13 +223,14 @@ __global__ void __launch_bounds__(288, 1)
             if (ok) {
                 umma_commit(tfull);
             } else {
-                umma_commit(&drain[pt]);
-                mbar_wait_timed(&drain[pt], 0, p.wait_ns);
+                umma_commit(&drain[kd]);
+                mbar_wait_timed(&drain[kd], 0, p.wait_ns);
             }
         }
     } else {
-        // ---------------- builders (phase f = warp - 4, channel co = lane), then the epilogue
-        const int f = warp & 3, co = lane;
+        // ---------------- builders (phase f, pooled lines 4*hb .. 4*hb + 3, channel co =
+        // lane), then the epilogue
+        const int f = warp & 3, hb = (warp - 4) >> 2, co = lane;
         const uint32_t lane_addr = tmem_base + ((uint32_t)(f * 32) << 16);
         int s = 0;
         uint32_t ph = 0;
@@ -232,23 +246,33 @@ __global__ void __launch_bounds__(288, 1)
             }
             tc_fence_after();
             const int dd = wq_decode(p, tile).d0 & 1;
-            const uint8_t* st = ring + s * WQ_STAGE;
+            uint8_t* st = ring + s * WQ_STAGE;
+            // the input lines' voxel pairs (w0-2 .. w0+33: O[0], E[0], O[1], ...) into
+            // the E and O rows of the MMA's B operand
+            for (int k = threadIdx.x - 128; k < WQ_PLANES * WQ_LINES * WQ_PAIRS; k += 256) {
+                const int line = k / WQ_PAIRS, pr = k - line * WQ_PAIRS;
+                const uint4 v = *reinterpret_cast<const uint4*>(st + k * 16);
+                *reinterpret_cast<uint4*>(st + WQ_EO + line * WQ_LP + ((pr & 1) ? 0u : WQ_RP) + (pr >> 1) * 16) = v;
+            }
+            fence_proxy_async_smem();
             const uint16_t* gp = reinterpret_cast<const uint16_t*>(st + WQ_G) + co;
             const uint8_t* ip = st + WQ_I + co;
             // column c holds rows 2c, 2c+1 = quads i, i+1 of line c/4 (i = 2 (c % 4)):
-            // voxels w = 4i + f and 4i + 4 + f, pooled w 2i + f/2 and 2i + 2 + f/2
-            uint32_t col[64];
+            // voxels w = 4i + f and 4i + 4 + f, pooled w 2i + f/2 and 2i + 2 + f/2.
+            // Lines 2l and 2l + 1 (columns c and c + 4) share their pooled values.
+            uint32_t col[32];
+            const uint32_t code0 = (uint32_t)(dd * 4 + (f & 1)), code1 = code0 + 2;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const int gl = c >> 2, i = 2 * (c & 3);
-                const int pw = 2 * i + (f >> 1), pr = (gl >> 1) * 16;
-                const uint32_t code = (uint32_t)(dd * 4 + (gl & 1) * 2 + (f & 1));
-                const uint32_t v0 = ip[(pr + pw) * 32] == code ? gp[(pr + pw) * 32] : 0u;
-                const uint32_t v1 = ip[(pr + pw + 2) * 32] == code ? gp[(pr + pw + 2) * 32] : 0u;
-                col[c] = v0 | (v1 << 16);
-            }
-            tmem_st32(lane_addr + WQ_ACOL + b * 64, col);
-            tmem_st32(lane_addr + WQ_ACOL + b * 64 + 32, col + 32);
+            for (int l = 0; l < 4; ++l)
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int o = (4 * hb + l) * 16 + 4 * q4 + (f >> 1);
+                    const uint32_t k0 = ip[o * 32], k1 = ip[(o + 2) * 32];
+                    const uint32_t g0 = gp[o * 32], g1 = gp[(o + 2) * 32];
+                    col[8 * l + q4] = (k0 == code0 ? g0 : 0u) | ((k1 == code0 ? g1 : 0u) << 16);
+                    col[8 * l + 4 + q4] = (k0 == code1 ? g0 : 0u) | ((k1 == code1 ? g1 : 0u) << 16);
+                }
+            tmem_st32(lane_addr + WQ_ACOL + b * 64 + 32 * hb, col);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -262,27 +286,35 @@ __global__ void __launch_bounds__(288, 1)
             }
         }
         // ---------------- epilogue: this lane's (f, co) partial of every dW entry
-        if (ok && __all_sync(0xffffffffu, mbar_wait(tfull, 0, abort_flag, p.wait_ns, p.status, WAIT_EPI_TMEM_FULL))) {
+        if (ok && hb == 0 &&
+            __all_sync(0xffffffffu, mbar_wait(tfull, 0, abort_flag, p.wait_ns, p.status, WAIT_EPI_TMEM_FULL))) {
             tc_fence_after();
             float* out = p.part + (((int64_t)blockIdx.x * 4 + f) * 32 + co) * 108;
 #pragma unroll 1
-            for (int pt = 0; pt < 4; ++pt) {
-                const int s0 = pt == 0 ? 0 : pt == 1 ? 2 : pt == 2 ? 4 : -2;  // voxel slot of the part's first pair
+            for (int kd = 0; kd < 3; ++kd)
 #pragma unroll 1
-                for (int kd = 0; kd < 3; ++kd) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + (pt * 3 + kd) * 32, r);
+                for (int hl = 0; hl < 2; ++hl) {
+                    uint32_t ra[32], rb[32];  // columns 0-31, 32-47
+                    tmem_ld32(lane_addr + (kd * 2 + hl) * WQ_N, ra);
+                    tmem_ld16(lane_addr + (kd * 2 + hl) * WQ_N + 32, rb);
                     tmem_ld_wait();
 #pragma unroll
                     for (int kh = 0; kh < 3; ++kh)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int kw = s0 + (e >> 2) - f + 1;
-                            if (kw >= 0 && kw <= 2)
-                                out[(kd * 9 + kh * 3 + kw) * 4 + (e & 3)] = __uint_as_float(r[kh * 8 + e]);
-                        }
+                        for (int eo = 0; eo < 2; ++eo)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                // voxel slot of the E / O pair: low half 0-1 / -2..-1, high half 4-5 / 2-3
+                                const int s0 = hl == 0 ? (eo == 0 ? 0 : -2) : (eo == 0 ? 4 : 2);
+                                const int kw = s0 + (e >> 2) - f + 1;
+                                if (kw >= 0 && kw <= 2)
+                                {
+                                    const int n = kh * 16 + eo * 8 + e;
+                                    out[(kd * 9 + kh * 3 + kw) * 4 + (e & 3)] =
+                                        __uint_as_float(n < 32 ? ra[n] : rb[n - 32]);
+                                }
+                            }
                 }
-            }
         }
     }
 
@@ -311,11 +343,13 @@ size_t wgrad_quad_workspace_bytes(int num_sms, int64_t n, int64_t d, int64_t h, 
     return (size_t)wq_units(num_sms, n, d, h, w) * 4 * 32 * 108 * sizeof(float);
 }
 
-static bool wq_rows_map(CUtensorMap* m, const void* base, int64_t n, int64_t d, int64_t h, int64_t w) {
-    const uint64_t dims[5] = {8u, (uint64_t)(w / 4), (uint64_t)h, (uint64_t)d, (uint64_t)n};
-    const uint64_t str[4] = {32u, (uint64_t)w * 8, (uint64_t)(h * w * 8), (uint64_t)(d * h * w * 8)};
-    const uint32_t box[5] = {8u, (uint32_t)WQ_QUADS, (uint32_t)WQ_LINES, (uint32_t)WQ_PLANES, 1u};
-    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+// The input as (4*W elements per line, H, D, N, 1); box: 36 voxels x 18 lines x 3 planes.
+static bool wq_lines_map(CUtensorMap* m, const void* x, int64_t n, int64_t d, int64_t h, int64_t w) {
+    const uint64_t dims[5] = {(uint64_t)w * 4, (uint64_t)h, (uint64_t)d, (uint64_t)n, 1u};
+    const uint64_t str[4] = {(uint64_t)w * 8, (uint64_t)(h * w * 8), (uint64_t)(d * h * w * 8),
+                             (uint64_t)(n * d * h * w * 8)};
+    const uint32_t box[5] = {(uint32_t)(WQ_PAIRS * 8), (uint32_t)WQ_LINES, (uint32_t)WQ_PLANES, 1u, 1u};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 static bool wq_pooled_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz, int64_t n, int64_t d,
@@ -332,8 +366,8 @@ cf_status launch_wgrad_quad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
     if (!wgrad_quad_supported(d, h, w, 4, 32)) return CF_ERR_UNSUPPORTED;
     const int64_t tiles = wq_tiles(n, d, h, w);
     if (tiles > INT32_MAX) return CF_ERR_UNSUPPORTED;
-    CUtensorMap te, to, tg, ti;
-    if (!wq_rows_map(&te, x, n, d, h, w) || !wq_rows_map(&to, reinterpret_cast<const uint8_t*>(x) + 16, n, d, h, w) ||
+    CUtensorMap tx, tg, ti;
+    if (!wq_lines_map(&tx, x, n, d, h, w) ||
         !wq_pooled_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, d, h, w) ||
         !wq_pooled_map(&ti, idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, n, d, h, w))
         return CF_ERR_CUDA;
@@ -354,7 +388,7 @@ cf_status launch_wgrad_quad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
     if (cudaFuncSetAttribute(wgrad_quad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WQ_SMEM) != cudaSuccess)
         return CF_ERR_CUDA;
     const int grid = wq_units(ctx.num_sms, n, d, h, w);
-    wgrad_quad_kernel<<<grid, 288, WQ_SMEM, ctx.stream>>>(te, to, tg, ti, p);
+    wgrad_quad_kernel<<<grid, 384, WQ_SMEM, ctx.stream>>>(tx, tg, ti, p);
     if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
     *n_splits = grid * 4;
     return CF_OK;
