@@ -427,6 +427,7 @@ def _check_avgpooled(oracle_mod, z, S, b, gy, gmask, what):
 
 VARIANT_FWD = [
     (2, 4, 6, 40, 4, 32),      # first-layer kernel (c_in 4)
+    (1, 2, 16, 64, 4, 32),     # first-layer quad-row kernel (unpooled: bias + leaky ReLU; average: im2col kernel)
     (1, 4, 6, 16, 32, 64),     # halo tile
     (1, 2, 4, 8, 64, 256),     # per-tap engine
     (1, 4, 8, 16, 16, 32),     # halo tile, 16-channel chunks
