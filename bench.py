@@ -377,7 +377,7 @@ def run_ours(args, rank, world, local_rank):
     def step_with_events(evs, serial=False):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        st.forward(stream, evs)
+        st.forward(stream, evs, serial=serial)
         st.backward(dy, stream, evs, serial)
         e1.record(stream)
         return e0, e1

@@ -50,6 +50,8 @@ _EP = ctypes.POINTER(cf_pool_epi)
 _SIGS = {
     "cf_conv3d_fwd": ([_DP, _vp, _vp, _EP, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_conv3d_dgrad": ([_DP, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "cf_conv3d_dgrad_flipped": ([_DP, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "cf_filter_flip": ([_i32, _i32, _vp, _vp, _vp], ctypes.c_int),
     "cf_conv3d_wgrad": ([_DP, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _sz, _vp], ctypes.c_int),
     "cf_conv3d_dgrad_pool_bwd": ([_DP, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_bias_lrelu_pool_fwd": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _f32, _vp, _vp, _vp], ctypes.c_int),
@@ -144,6 +146,18 @@ def cf_conv3d_dgrad(desc, dz, idx, w, x_act, slope, dx, ws=None, ws_bytes=0, str
     st = _lib.cf_conv3d_dgrad(ctypes.byref(_desc(desc)), _ptr(dz), _ptr(idx), _ptr(w), _ptr(x_act), float(slope),
                               _ptr(dx), _ptr(dsum), _ptr(ws), ws_bytes, _stream(stream))
     return _check(st, "cf_conv3d_dgrad") if check else st
+
+
+def cf_conv3d_dgrad_flipped(desc, dz, idx, wt, x_act, slope, dx, ws=None, ws_bytes=0, stream=None, check=True,
+                            dsum=None):
+    st = _lib.cf_conv3d_dgrad_flipped(ctypes.byref(_desc(desc)), _ptr(dz), _ptr(idx), _ptr(wt), _ptr(x_act),
+                                      float(slope), _ptr(dx), _ptr(dsum), _ptr(ws), ws_bytes, _stream(stream))
+    return _check(st, "cf_conv3d_dgrad_flipped") if check else st
+
+
+def cf_filter_flip(c_out, c_in, w, wt, stream=None, check=True):
+    st = _lib.cf_filter_flip(int(c_out), int(c_in), _ptr(w), _ptr(wt), _stream(stream))
+    return _check(st, "cf_filter_flip") if check else st
 
 
 def cf_conv3d_dgrad_pool_bwd(desc, dz, w, x_act, slope, dx, prev_idx, prev_dz, ws=None, ws_bytes=0, stream=None,

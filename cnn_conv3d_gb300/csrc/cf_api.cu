@@ -223,9 +223,10 @@ cf_status cf_conv3d_fwd(const cf_conv_desc* desc, const uint16_t* x, const uint1
 
 // Backward data; prev_idx / prev_dz (both or neither): the previous block's
 // max-pool backward fused into the epilogue (see cf_conv3d_dgrad_pool_bwd).
+// w is the forward filter, or (flipped) already the backward-data filter.
 static cf_status dgrad_impl(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx, const uint16_t* w,
                             const uint16_t* x_act, float slope, uint16_t* dx, float* dsum, const uint8_t* prev_idx,
-                            uint16_t* prev_dz, void* ws, size_t ws_bytes, void* stream) {
+                            uint16_t* prev_dz, void* ws, size_t ws_bytes, void* stream, bool flipped = false) {
     if (!desc_ok(desc) || dz == nullptr || w == nullptr || dx == nullptr) return CF_ERR_INVALID_ARG;
     if ((prev_idx == nullptr) != (prev_dz == nullptr)) return CF_ERR_INVALID_ARG;
     if ((prev_idx && !aligned16(prev_idx)) || (prev_dz && !aligned16(prev_dz))) return CF_ERR_INVALID_ARG;
@@ -244,10 +245,15 @@ static cf_status dgrad_impl(const cf_conv_desc* desc, const uint16_t* dz, const 
     const size_t need = wt_bytes + sum_bytes + (idx ? round_up((size_t)dense_grad_elems(desc) * 2, 256) : 0) +
                         upsample_bytes(desc);
     if (ws == nullptr || ws_bytes < need) return CF_ERR_WORKSPACE;
-    uint16_t* wt = static_cast<uint16_t*>(ws);
+    const uint16_t* wt = w;
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wt_bytes);
-    cf_status st = launch_flip_transpose(ctx, co, ci, w, wt);
-    if (st != CF_OK) return st;
+    cf_status st = CF_OK;
+    if (!flipped) {
+        uint16_t* buf = static_cast<uint16_t*>(ws);
+        st = launch_flip_transpose(ctx, co, ci, w, buf);
+        if (st != CF_OK) return st;
+        wt = buf;
+    }
     const uint16_t* dz_dense = dz;
     if (stride == 2) {
         // zeros at the odd positions: the stride-2 backward as a stride-1 one
@@ -288,6 +294,21 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
                           const uint16_t* x_act, float slope, uint16_t* dx, float* dsum, void* ws,
                           size_t ws_bytes, void* stream) {
     return dgrad_impl(desc, dz, idx, w, x_act, slope, dx, dsum, nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+cf_status cf_conv3d_dgrad_flipped(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx,
+                                  const uint16_t* wt, const uint16_t* x_act, float slope, uint16_t* dx, float* dsum,
+                                  void* ws, size_t ws_bytes, void* stream) {
+    return dgrad_impl(desc, dz, idx, wt, x_act, slope, dx, dsum, nullptr, nullptr, ws, ws_bytes, stream, true);
+}
+
+cf_status cf_filter_flip(int32_t c_out, int32_t c_in, const uint16_t* w, uint16_t* wt, void* stream) {
+    if (w == nullptr || wt == nullptr || c_out <= 0 || c_in <= 0 || !aligned16(w) || !aligned16(wt))
+        return CF_ERR_INVALID_ARG;
+    if (c_out % 16 != 0 || c_in % 16 != 0) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_flip_transpose(ctx, c_out, c_in, w, wt);
 }
 
 cf_status cf_conv3d_dgrad_pool_bwd(const cf_conv_desc* desc, const uint16_t* dz, const uint16_t* w,

@@ -106,6 +106,9 @@ class CosmoStack:
                 ws = max(ws, cf.cf_workspace_size(cf.CF_OP_BN, cf.cf_conv_desc(1, 1, 1, 1, 1, channels[l + 1])))
         if backward:
             self.dz, self.dw, self.db, self.g = [], [], [], []
+            # backward-data filters of blocks 2..L (cf_filter_flip), see backward
+            self.wt = [None] + [torch.empty((channels[l], 3, 3, 3, channels[l + 1]), dtype=bf, device=device)
+                                for l in range(1, self.L)]
             self.dgamma = [None] * self.L
             self.dsums = [None] * self.L
             for l in range(self.L):
@@ -151,6 +154,11 @@ class CosmoStack:
     # the separate pool backward whose lanes own channel groups (dgrad3 +
     # routing 0.248 ms against 0.101 + 0.060 ms for N = 8 x 4 x 128^3)
     fuse_pool_bwd = False
+
+    # the backward-data filters are flipped once per step on the side stream,
+    # during the forward (cf_filter_flip), instead of inside each backward-data
+    # call on the critical stream
+    preflip = True
 
     def routed(self, l) -> bool:
         """Block l's weight gradient takes the pooled gradient + argmax codes."""
@@ -229,13 +237,39 @@ class CosmoStack:
     def _chunked_blocks(self) -> int:
         return sum(1 for l in range(self.L) if self.dims[l][1] >= 32)
 
-    def forward(self, stream=None, timer=None, x_chunks=None):
+    def _issue_flips(self, caller, side, timer):
+        """The backward-data filters of blocks 2..L (cf_filter_flip) on `side`,
+        after the work enqueued on `caller` so far.  Returns the event the
+        critical stream waits on before its first backward-data launch (None
+        when `side` is `caller`)."""
+        if side is not caller:
+            ev = torch.cuda.Event()
+            ev.record(caller)
+            side.wait_event(ev)
+
+        def flips():
+            for l in range(1, self.L):
+                cf.cf_filter_flip(self.channels[l + 1], self.channels[l], self.w[l], self.wt[l], side)
+
+        self._run("flip", side, flips, timer)
+        if side is caller:
+            return None
+        ev = torch.cuda.Event()
+        ev.record(side)
+        return ev
+
+    def forward(self, stream=None, timer=None, x_chunks=None, serial=False):
         """timer: optional list receiving (key, start event, end event) per launch.
         x_chunks: optional [(n0, n1, event)]: the leading blocks (those of
         _chunked_blocks) run per sample range [n0, n1), each range after its
         event (its input has landed); a sample's outputs do not depend on the
-        others, so the results are the same bits as launches over the batch."""
+        others, so the results are the same bits as launches over the batch.
+        With the backward enabled, the backward-data filters are flipped on the
+        side stream while the forward runs (serial: on the caller's stream)."""
         main = self._main(stream)
+        if self.backward_enabled and self.preflip and self.L > 1:
+            side = self.side if (self.side is not None and not serial) else main
+            self._flips = (self._issue_flips(main, side, timer),)
         first = 0
         if x_chunks is not None:
             first = max(1, self._chunked_blocks())
@@ -271,6 +305,12 @@ class CosmoStack:
             main.wait_event(ev)
         ws, wsb = self.ws, self.ws.numel()
         wsw, wswb = self.ws_w, self.ws_w.numel()
+        # the backward-data filters (flipped, transposed) of blocks 2..L: issued by
+        # the forward of this step, else here on the side stream
+        flip_ev = None
+        flips = self.__dict__.pop("_flips", None)
+        if self.preflip and self.L > 1:
+            flip_ev = flips[0] if flips is not None else self._issue_flips(caller, side, timer)
 
         def to_host(src_stream, dst, src):
             if host_out is None:
@@ -347,6 +387,12 @@ class CosmoStack:
                     fn = lambda: cf.cf_conv3d_dgrad_pool_bwd(desc, self.dz[l], self.w[l], x_act, self.slope,
                                                              self.g[l - 1], self.idx[l - 1], self.dz[l - 1], ws, wsb,
                                                              main, dsum=dsum)
+                elif self.preflip:
+                    if flip_ev is not None:
+                        main.wait_event(flip_ev)
+                        flip_ev = None
+                    fn = lambda: cf.cf_conv3d_dgrad_flipped(desc, self.dz[l], None, self.wt[l], x_act, self.slope,
+                                                            self.g[l - 1], ws, wsb, main, dsum=dsum)
                 else:
                     fn = lambda: cf.cf_conv3d_dgrad(desc, self.dz[l], None, self.w[l], x_act, self.slope,
                                                     self.g[l - 1], ws, wsb, main, dsum=dsum)
@@ -360,7 +406,7 @@ class CosmoStack:
                 caller.wait_event(ev)
 
     def step(self, dy, stream=None, timer=None, serial=False):
-        self.forward(stream, timer)
+        self.forward(stream, timer, serial=serial)
         if self.backward_enabled:
             self.backward(dy, stream, timer, serial)
 

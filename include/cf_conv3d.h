@@ -134,6 +134,29 @@ cf_status cf_conv3d_dgrad(const cf_conv_desc* desc, const uint16_t* dz, const ui
                           float* dsum, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The filter of the backward-data convolution written as a forward filter
+ * (CosmoFlow page, section III-C "backward data": dX is the convolution of dZ
+ * with the flipped, transposed filter):
+ *   wt[ci][t][co] = w[co][26 - t][ci],  t = 9*kd + 3*kh + kw
+ * w: [c_out][27][c_in] bf16; wt: [c_in][27][c_out] bf16; both device,
+ * caller-owned, 16-byte aligned.  cf_conv3d_dgrad computes this into its
+ * workspace on every call; a caller that reuses one filter, or wants the flip
+ * off its critical path (on another stream, before the backward), computes
+ * it once here and calls cf_conv3d_dgrad_flipped.
+ * Supported: c_out and c_in multiples of 16.
+ */
+cf_status cf_filter_flip(int32_t c_out, int32_t c_in, const uint16_t* w, uint16_t* wt, void* stream);
+
+/*
+ * cf_conv3d_dgrad with the filter given already flipped (wt from
+ * cf_filter_flip for this desc's c_out, c_in).  Same arguments, results and
+ * workspace size otherwise; bit-identical to cf_conv3d_dgrad.
+ */
+cf_status cf_conv3d_dgrad_flipped(const cf_conv_desc* desc, const uint16_t* dz, const uint8_t* idx,
+                                  const uint16_t* wt, const uint16_t* x_act, float slope, uint16_t* dx,
+                                  float* dsum, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Backward data fused with the previous block's max-pool backward (CosmoFlow
  * page, section III-C "backward data"; the block's pool backward as in
  * cf_bias_lrelu_pool_bwd): everything cf_conv3d_dgrad computes for a dense dz

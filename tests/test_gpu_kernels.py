@@ -287,6 +287,20 @@ def test_conv_dgrad(cf, oracle_mod, shape, with_act):
         f = np.where(_f64(oracle_mod, c["x"]) > 0, 1.0, SLOPE)
         ref, S = ref * f, S * f
     assert_close(host_bf16_f64(dx), ref, S, f"dgrad {shape} act={with_act}")
+    # the filter flipped once (cf_filter_flip) and passed to the pre-flipped entry:
+    # the flipped filter is the reversed-tap transpose, and dx and dsum are the same bits
+    wt, wtc = guarded((Ci, 3, 3, 3, Co), torch.bfloat16, fill=float("nan"))
+    cf.cf_filter_flip(Co, Ci, dev_bf16(c["w"]), wt)
+    wtc("flipped filter")
+    w16 = c["w"].reshape(Co, 27, Ci)
+    want = w16[:, ::-1, :].transpose(2, 1, 0)
+    assert np.array_equal(wt.contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(Ci, 27, Co), want)
+    dxf, dxfc = guarded((N, D, H, W, Ci), torch.bfloat16, fill=float("nan"))
+    dsf, dsfc = guarded((Ci,), torch.float32, fill=float("nan"))
+    cf.cf_conv3d_dgrad_flipped(desc, dev_bf16(c["dz"]), None, wt, x_act, SLOPE, dxf, ws, wsb, dsum=dsf)
+    dxfc("flipped dgrad dx")
+    dsfc("flipped dgrad dsum")
+    assert torch.equal(dxf, dx) and torch.equal(dsf, dsum)
     if with_act:
         # the previous block's max-pool backward fused into the epilogue: the same
         # dx, and its routing by the codes equals the standalone pool backward's
