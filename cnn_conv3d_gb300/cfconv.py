@@ -52,6 +52,10 @@ _SIGS = {
     "cf_conv3d_dgrad": ([_DP, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_conv3d_dgrad_flipped": ([_DP, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_filter_flip": ([_i32, _i32, _vp, _vp, _vp], ctypes.c_int),
+    "cf_bias_lrelu_pool_bwd_partials": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _sz,
+                                         _vp], ctypes.c_int),
+    "cf_pool_bwd_partial_rows": ([], ctypes.c_int64),
+    "cf_column_sums": ([_i64, _i32, _vp, _vp, _vp], ctypes.c_int),
     "cf_conv3d_wgrad": ([_DP, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _sz, _vp], ctypes.c_int),
     "cf_conv3d_dgrad_pool_bwd": ([_DP, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "cf_bias_lrelu_pool_fwd": ([_i64, _i64, _i64, _i64, _i32, _vp, _vp, _f32, _vp, _vp, _vp], ctypes.c_int),
@@ -158,6 +162,22 @@ def cf_conv3d_dgrad_flipped(desc, dz, idx, wt, x_act, slope, dx, ws=None, ws_byt
 def cf_filter_flip(c_out, c_in, w, wt, stream=None, check=True):
     st = _lib.cf_filter_flip(int(c_out), int(c_in), _ptr(w), _ptr(wt), _stream(stream))
     return _check(st, "cf_filter_flip") if check else st
+
+
+def cf_bias_lrelu_pool_bwd_partials(n, d, h, w, c, dy, y, idx, slope, dz, dy_pre, partial, stream=None, check=True):
+    st = _lib.cf_bias_lrelu_pool_bwd_partials(n, d, h, w, c, _ptr(dy), _ptr(y), _ptr(idx), float(slope), _ptr(dz),
+                                              _ptr(dy_pre), _ptr(partial), partial.numel() * partial.element_size(),
+                                              _stream(stream))
+    return _check(st, "cf_bias_lrelu_pool_bwd_partials") if check else st
+
+
+def cf_pool_bwd_partial_rows():
+    return int(_lib.cf_pool_bwd_partial_rows())
+
+
+def cf_column_sums(rows, c, partial, out, stream=None, check=True):
+    st = _lib.cf_column_sums(int(rows), int(c), _ptr(partial), _ptr(out), _stream(stream))
+    return _check(st, "cf_column_sums") if check else st
 
 
 def cf_conv3d_dgrad_pool_bwd(desc, dz, w, x_act, slope, dx, prev_idx, prev_dz, ws=None, ws_bytes=0, stream=None,

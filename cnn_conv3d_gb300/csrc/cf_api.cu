@@ -384,6 +384,34 @@ cf_status cf_bias_lrelu_pool_bwd(int64_t n, int64_t d, int64_t h, int64_t w, int
     return launch_pool_bwd(ctx, n, d, h, w, c, dy, y, idx, slope, dz, dy_pre, dbias, ws, ws_bytes);
 }
 
+cf_status cf_bias_lrelu_pool_bwd_partials(int64_t n, int64_t d, int64_t h, int64_t w, int32_t c, const uint16_t* dy,
+                                          const uint16_t* y, const uint8_t* idx, float slope, uint16_t* dz,
+                                          uint16_t* dy_pre, float* partial, size_t partial_bytes, void* stream) {
+    if (n <= 0 || d <= 0 || h <= 0 || w <= 0 || c <= 0 || dy == nullptr || partial == nullptr)
+        return CF_ERR_INVALID_ARG;
+    if (dz != nullptr && idx == nullptr) return CF_ERR_INVALID_ARG;
+    if (!aligned16(dy) || (y && !aligned16(y)) || (idx && !aligned16(idx)) || (dz && !aligned16(dz)) ||
+        (dy_pre && !aligned16(dy_pre)) || !aligned16(partial))
+        return CF_ERR_INVALID_ARG;
+    if (c % 8 != 0 || c > 2048 || ((d | h | w) & 1)) return CF_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_pool_bwd(ctx, n, d, h, w, c, dy, y, idx, slope, dz, dy_pre, partial, partial, partial_bytes, false);
+}
+
+int64_t cf_pool_bwd_partial_rows(void) {
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, nullptr)) return 0;
+    return (int64_t)(pool_bwd_workspace_bytes(ctx.num_sms, 1) / sizeof(float));
+}
+
+cf_status cf_column_sums(int64_t rows, int32_t c, const float* partial, float* out, void* stream) {
+    if (rows <= 0 || rows > INT32_MAX || c <= 0 || partial == nullptr || out == nullptr) return CF_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    if (!device_ctx(&ctx, stream)) return CF_ERR_CUDA;
+    return launch_colsum(ctx, partial, (int)rows, c, out);
+}
+
 cf_status cf_block_epilogue_fwd(int32_t pool, int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
                                 const uint16_t* z, const float* bias, float slope, uint16_t* y, uint8_t* aux,
                                 void* stream) {

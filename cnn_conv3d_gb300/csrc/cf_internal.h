@@ -120,9 +120,12 @@ cf_status launch_wgrad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, in
 cf_status launch_pool_fwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
                           const uint16_t* z, const float* bias, float slope, uint16_t* y, uint8_t* idx);
 size_t pool_bwd_workspace_bytes(int num_sms, int c);
+// reduce = false: the bias gradient is left as the per-block partial sums in ws
+// ([pool_bwd_workspace_bytes / (4 c)][c]); dbias must then be non-NULL (it only
+// requests the partials).
 cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
                           const uint16_t* dy, const uint16_t* y, const uint8_t* idx, float slope, uint16_t* dz,
-                          uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes);
+                          uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes, bool reduce = true);
 cf_status launch_flip_transpose(const LaunchCtx& ctx, int c_out, int c_in, const uint16_t* w, uint16_t* wt);
 // Page variants of the block epilogue as standalone kernels: average pooling
 // of the activated window (y and sign masks), the unpooled activation, and

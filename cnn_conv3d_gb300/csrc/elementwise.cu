@@ -696,7 +696,7 @@ cf_status launch_pool_fwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
 
 cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c,
                           const uint16_t* dy, const uint16_t* y, const uint8_t* idx, float slope, uint16_t* dz,
-                          uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes) {
+                          uint16_t* dy_pre, float* dbias, void* ws, size_t ws_bytes, bool reduce) {
     if (c / 8 > 256) return CF_ERR_UNSUPPORTED;
     const int threads = pool_bwd_block(c);
     const int blocks = pool_bwd_grid(ctx.num_sms);
@@ -714,7 +714,7 @@ cf_status launch_pool_bwd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h,
             dy, y, idx, slope, dz, dy_pre, partial, n, (int)d, (int)h, (int)w, c, pool_grid(d, h, w));
     }
     if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
-    if (dbias) {
+    if (dbias && reduce) {
         colsum_kernel<<<c, 256, 0, ctx.stream>>>(partial, blocks, c, dbias);
         if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
     }

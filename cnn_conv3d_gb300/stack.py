@@ -106,6 +106,11 @@ class CosmoStack:
                 ws = max(ws, cf.cf_workspace_size(cf.CF_OP_BN, cf.cf_conv_desc(1, 1, 1, 1, 1, channels[l + 1])))
         if backward:
             self.dz, self.dw, self.db, self.g = [], [], [], []
+            # per-block partial bias sums of each max-pooled block's pool backward,
+            # reduced on the side stream (see backward)
+            self.bpart_rows = cf.cf_pool_bwd_partial_rows()
+            self.bpart = [torch.empty((self.bpart_rows, channels[l + 1]), dtype=f32, device=device)
+                          for l in range(self.L)]
             # backward-data filters of blocks 2..L (cf_filter_flip), see backward
             self.wt = [None] + [torch.empty((channels[l], 3, 3, 3, channels[l + 1]), dtype=bf, device=device)
                                 for l in range(1, self.L)]
@@ -154,6 +159,11 @@ class CosmoStack:
     # the separate pool backward whose lanes own channel groups (dgrad3 +
     # routing 0.248 ms against 0.101 + 0.060 ms for N = 8 x 4 x 128^3)
     fuse_pool_bwd = False
+
+    # the max-pool backward leaves its bias gradient as partial sums that the
+    # side stream reduces (cf_bias_lrelu_pool_bwd_partials, cf_column_sums):
+    # nothing on the critical stream reads it
+    defer_bias_sums = True
 
     # the backward-data filters are flipped once per step on the side stream,
     # during the forward (cf_filter_flip), instead of inside each backward-data
@@ -327,6 +337,7 @@ class CosmoStack:
             co = self.channels[l + 1]
             routed = self.routed(l)
             pool = self.specs[l][1]
+            deferred = False  # the bias gradient left as partial sums for the side stream
             if self.bn(l):
                 # batch norm (with the activation / pooling backward folded in):
                 # dZ, dbeta (db[l]) and dgamma from dy or g
@@ -339,7 +350,13 @@ class CosmoStack:
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
                 to_host(main, host_out and host_out[1][l], self.db[l])
             elif l == self.L - 1:
-                if pool == "max":
+                if pool == "max" and self.defer_bias_sums:
+                    fn = lambda: cf.cf_bias_lrelu_pool_bwd_partials(n, d, h, w, co, dy, self.y[l], self.idx[l],
+                                                                    self.slope, self.dz[l],
+                                                                    self.g[l] if routed else None, self.bpart[l],
+                                                                    main)
+                    deferred = True
+                elif pool == "max":
                     fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, dy, self.y[l], self.idx[l], self.slope,
                                                            self.dz[l], self.g[l] if routed else None, self.db[l],
                                                            ws, wsb, main)
@@ -348,12 +365,19 @@ class CosmoStack:
                                                           self.y[l] if pool == "none" else None, self.idx[l],
                                                           self.slope, self.dz[l], None, self.db[l], ws, wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
-                to_host(main, host_out and host_out[1][l], self.db[l])
+                if not deferred:
+                    to_host(main, host_out and host_out[1][l], self.db[l])
             elif pool == "max" and not routed and not self.pool_bwd_fused(l):
-                fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope,
-                                                       self.dz[l], None, self.db[l], ws, wsb, main)
+                if self.defer_bias_sums:
+                    fn = lambda: cf.cf_bias_lrelu_pool_bwd_partials(n, d, h, w, co, self.g[l], None, self.idx[l],
+                                                                    self.slope, self.dz[l], None, self.bpart[l], main)
+                    deferred = True
+                else:
+                    fn = lambda: cf.cf_bias_lrelu_pool_bwd(n, d, h, w, co, self.g[l], None, self.idx[l], self.slope,
+                                                           self.dz[l], None, self.db[l], ws, wsb, main)
                 self._run(f"poolbwd{l + 1}", main, fn, timer)
-                to_host(main, host_out and host_out[1][l], self.db[l])
+                if not deferred:
+                    to_host(main, host_out and host_out[1][l], self.db[l])
             elif pool == "avg":
                 fn = lambda: cf.cf_block_epilogue_bwd(cf.CF_POOL_AVG, n, d, h, w, co, self.g[l], None, self.idx[l],
                                                       self.slope, self.dz[l], None, self.db[l], ws, wsb, main)
@@ -367,6 +391,12 @@ class CosmoStack:
                 ev = torch.cuda.Event()
                 ev.record(main)
                 side.wait_event(ev)
+            if deferred:
+                # the bias gradient from the pool backward's partial sums, off the
+                # critical stream
+                self._run(f"poolbwd{l + 1}_sum", side,
+                          lambda: cf.cf_column_sums(self.bpart_rows, co, self.bpart[l], self.db[l], side), timer)
+                to_host(side, host_out and host_out[1][l], self.db[l])
             if routed:
                 fn = lambda: cf.cf_conv3d_wgrad(desc, self.block_input(l), self.g[l], self.idx[l], self.dw[l], 0,
                                                 wsw, wswb, side)

@@ -224,6 +224,31 @@ cf_status cf_bias_lrelu_pool_bwd(int64_t n, int64_t d, int64_t h, int64_t w, int
                                  void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * cf_bias_lrelu_pool_bwd with its bias-gradient reduction left to the caller,
+ * so that it can run on another stream (nothing downstream of the pool
+ * backward reads the bias gradient): dz and dy_pre as there; the bias gradient
+ * is left as per-block partial sums
+ *   partial : [R][c] fp32, R = cf_pool_bwd_partial_rows(), partial_bytes >= 4*R*c
+ * and cf_column_sums(R, c, partial, dbias) turns them into the same dbias, bit
+ * for bit, as cf_bias_lrelu_pool_bwd.  Supported: as cf_bias_lrelu_pool_bwd.
+ */
+cf_status cf_bias_lrelu_pool_bwd_partials(int64_t n, int64_t d, int64_t h, int64_t w, int32_t c,
+                                          const uint16_t* dy, const uint16_t* y, const uint8_t* idx,
+                                          float slope, uint16_t* dz, uint16_t* dy_pre, float* partial,
+                                          size_t partial_bytes, void* stream);
+
+/* Rows R of the partial sums of cf_bias_lrelu_pool_bwd_partials on the current
+ * device (0 on a CUDA error). */
+int64_t cf_pool_bwd_partial_rows(void);
+
+/*
+ * out[j] = sum over r = 0 .. rows-1, in that order, of partial[r][j]; partial
+ * [rows][c] fp32 and out [c] fp32 device pointers.  The fixed-order column
+ * reduction of the library's bias gradients.
+ */
+cf_status cf_column_sums(int64_t rows, int32_t c, const float* partial, float* out, void* stream);
+
+/*
  * The block epilogue of any pooling kind (CF_POOL_*) as standalone kernels:
  * the unfused counterpart of the fused epilogues of cf_conv3d_fwd and the
  * backward that feeds cf_conv3d_dgrad / cf_conv3d_wgrad with a dense dZ.

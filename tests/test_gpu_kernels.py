@@ -121,6 +121,18 @@ def test_pool_bwd_standalone(cf, oracle_mod):
     np.testing.assert_allclose(gdz, rdz, rtol=2 ** -8, atol=0)
     np.testing.assert_allclose(host_bf16_f64(dyp), rdyp, rtol=2 ** -8, atol=0)
     assert_close(db.cpu().numpy(), rdb, np.abs(rdyp).sum(axis=(0, 1, 2, 3)), "db")
+    # the bias gradient left as per-block partial sums and reduced separately:
+    # the same dz, dy_pre and db bits
+    rows = cf.cf_pool_bwd_partial_rows()
+    assert rows > 0
+    part, pcheck = guarded((rows, C), torch.float32, fill=float("nan"))
+    dz3, dy3 = empty_bf16((N, D, H, W, C)), empty_bf16(ry.shape)
+    cf.cf_bias_lrelu_pool_bwd_partials(N, D, H, W, C, dev_bf16(dy16), dev_bf16(y16), dev(ridx), SLOPE, dz3, dy3, part)
+    pcheck("partials")
+    db3, db3check = guarded((C,), torch.float32, fill=float("nan"))
+    cf.cf_column_sums(rows, C, part, db3)
+    db3check("column sums")
+    assert torch.equal(dz3, dz) and torch.equal(dy3, dyp) and torch.equal(db3, db)
     # y=None: dy is already the pre-activation gradient; no dbias
     dz2 = empty_bf16((N, D, H, W, C))
     cf.cf_bias_lrelu_pool_bwd(N, D, H, W, C, dyp, None, dev(ridx), SLOPE, dz2, None, None)
