@@ -480,13 +480,78 @@ class CosmoStack:
             ev.record(cp)
             main.wait_event(ev)
 
+    def _input_buffers(self):
+        """The two input buffer pairs (x, dY at the top) of step_host_pipelined."""
+        if getattr(self, "_xbuf", None) is None:
+            dy_shape = tuple(self.y[-1].shape)
+            self._xbuf = [self.x, torch.empty_like(self.x)]
+            self._dybuf = [torch.empty(dy_shape, dtype=torch.bfloat16, device=self.device) for _ in range(2)]
+            self._pf = torch.cuda.Stream(device=self.device)
+            self._parity = 0
+        return self._xbuf, self._dybuf
+
+    def prefetch_host(self, x_host, dy_host, stream=None):
+        """Copies the first batch of a step_host_pipelined loop (pinned host x and
+        dY) into the input buffers its next call computes on."""
+        main = self._main(stream)
+        xs, dys = self._input_buffers()
+        p = self._parity
+        with torch.cuda.stream(main):
+            xs[p].copy_(x_host.view(xs[p].shape), non_blocking=True)
+            dys[p].copy_(dy_host.view(dys[p].shape), non_blocking=True)
+
+    def step_host_pipelined(self, x_next, dy_next, dw_host, db_host, stream=None):
+        """One step of a host-fed training loop with double-buffered input: the
+        step computes on the batch the previous call (or prefetch_host) copied
+        in, while the next batch (x_next, dy_next: pinned host) goes over on the
+        copy stream into the other buffer pair; every dW[l] and db[l] is copied
+        out to dw_host[l] / db_host[l] as soon as it is final.  Per call: one
+        batch in, one set of gradients out, like step_host; the results are the
+        same bits as load + step + copy-back of the batch computed on.  The host
+        tensors must stay untouched until the caller's stream has passed the call."""
+        main = self._main(stream)
+        cp = self._copy_stream()
+        xs, dys = self._input_buffers()
+        pf = self._pf  # host-to-device, beside the device-to-host gradient copies on cp
+        p = self._parity
+        ev = torch.cuda.Event()
+        ev.record(main)
+        cp.wait_event(ev)
+        pf.wait_event(ev)  # the other buffer pair was last read by the previous call
+        with torch.cuda.stream(pf):
+            xs[1 - p].copy_(x_next.view(xs[1 - p].shape), non_blocking=True)
+            dys[1 - p].copy_(dy_next.view(dys[1 - p].shape), non_blocking=True)
+        self.x = xs[p]
+        try:
+            self.forward(main)
+            if self.backward_enabled:
+                self.backward(dys[p], main, host_out=(dw_host, db_host, cp))
+        finally:
+            self.x = xs[0]
+        for s in (cp, pf):
+            ev = torch.cuda.Event()
+            ev.record(s)
+            main.wait_event(ev)
+        self._parity = 1 - p
+
     def _dy_buffer(self, dy_host):
         """Device buffer of the top-output gradient for step_host."""
         if getattr(self, "_dy", None) is None:
             self._dy = torch.empty(tuple(self.y[-1].shape), dtype=torch.bfloat16, device=self.device)
         return self._dy
 
-    def capture(self, dy, timer=None, keys=None, host=None):
+    def capture_pipelined(self, x_host, dy_host, dw_host, db_host):
+        """The two CUDA graphs of step_host_pipelined (one per input buffer
+        pair), to be replayed alternately starting with the first after
+        prefetch_host; the parity is back at its value on entry."""
+        self._input_buffers()
+        self._copy_stream()
+        p0 = self._parity
+        graphs = [self.capture(None, host=(x_host, dy_host, dw_host, db_host), pipelined=True) for _ in range(2)]
+        assert self._parity == p0
+        return graphs
+
+    def capture(self, dy, timer=None, keys=None, host=None, pipelined=False):
         """Records one step into a CUDA graph (replay() then re-runs it with no
         per-launch host work).  The buffers, dy included, are bound at capture.
         With a timer list, the events of the ops in `keys` (all if None) become
@@ -500,7 +565,9 @@ class CosmoStack:
         try:
             with torch.cuda.stream(s):
                 with torch.cuda.graph(g, stream=s):
-                    if host is not None:
+                    if host is not None and pipelined:
+                        self.step_host_pipelined(*host, stream=s)
+                    elif host is not None:
                         self.step_host(*host, stream=s)
                     else:
                         self.step(dy, s, timer)

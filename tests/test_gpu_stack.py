@@ -95,6 +95,56 @@ def test_host_step_matches(torch_cuda, shape):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("shape", [(2, 64, (4, 32, 64, 128))])
+def test_pipelined_host_steps_match(torch_cuda, shape):
+    """step_host_pipelined (the next batch copied in while this one computes,
+    two input buffers), eager and as its pair of CUDA graphs, gives each batch
+    the gradient bits of load + step."""
+    torch = torch_cuda
+    from cnn_conv3d_gb300 import cfconv as cf
+    from cnn_conv3d_gb300.stack import CosmoStack
+    n, s, ch = shape
+    st = CosmoStack(n, s, ch, 0.3, backward=True)
+    batches, refs = [], []
+    for seed in (5151, 5252):
+        inp = synthdata.stack_inputs(n, s, ch, seed=seed, with_dy=True)
+        if not batches:
+            w, b = inp["w"], inp["b"]  # one set of weights for both batches
+        st.load(inp["x"], w, b)
+        dy = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).cuda()
+        st.step(dy)
+        torch.cuda.synchronize()
+        refs.append([t.cpu() for t in st.dw + st.db])
+        batches.append((torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+                        dy.cpu().pin_memory()))
+    dw_host = [torch.full(t.shape, float("nan"), dtype=t.dtype).pin_memory() for t in st.dw]
+    db_host = [torch.full(t.shape, float("nan"), dtype=t.dtype).pin_memory() for t in st.db]
+
+    def check(k):
+        torch.cuda.synchronize()
+        assert cf.cf_last_device_status() == cf.CF_OK
+        for a, b in zip(refs[k], dw_host + db_host):
+            assert torch.equal(a, b)
+        for t in dw_host + db_host:
+            t.fill_(float("nan"))
+
+    st.prefetch_host(*batches[0])
+    st.step_host_pipelined(*batches[1], dw_host, db_host)
+    check(0)
+    st.step_host_pipelined(*batches[0], dw_host, db_host)
+    check(1)
+    # the graphs bind one pinned pair for the next batch; the loop refills it
+    xh, dyh = torch.empty_like(batches[0][0]).pin_memory(), torch.empty_like(batches[0][1]).pin_memory()
+    graphs = st.capture_pipelined(xh, dyh, dw_host, db_host)
+    st.prefetch_host(*batches[1])
+    for k, g in enumerate(graphs * 2):
+        nxt = batches[k % 2]
+        xh.copy_(nxt[0])
+        dyh.copy_(nxt[1])
+        g.replay()
+        check((k + 1) % 2)
+
+
 @pytest.mark.parametrize("shape", [(2, 32, (4, 32, 64, 128)), (1, 32, (32, 64, 128, 64))])
 def test_fused_pool_backward_matches_separate(torch_cuda, shape):
     """Lower blocks' pool backward inside the backward-data epilogue of the
