@@ -155,8 +155,10 @@ FWD_SHAPES = [
     (1, 2, 4, 24, 16, 48),     # 16-channel chunks, per-tap engine, N tile 48
     (1, 2, 6, 8, 48, 64),      # three 16-channel chunks, halo tile
     (2, 2, 4, 8, 32, 80),      # N tile 80
-    (1, 6, 4, 16, 32, 64),     # 4-plane halo tile: a full and a half tile in depth
-    (1, 2, 4, 16, 64, 32),     # 4-plane halo tile deeper than the volume, two chunks
+    (1, 6, 4, 16, 32, 64),     # halo tile: a full and a half tile in depth
+    (1, 2, 4, 16, 64, 32),     # halo tile deeper than the volume, two chunks
+    (1, 2, 16, 16, 128, 256),  # per-tap engine, N tile 256, several tiles per sample
+    (1, 4, 16, 8, 32, 384),    # per-tap engine, two N tiles (256 + 128)
 ]
 
 
@@ -272,8 +274,9 @@ DGRAD_SHAPES = [
     (1, 4, 6, 16, 16, 32),     # the Table I c2 layer: dX has 16 channels
     (1, 2, 4, 8, 48, 16),      # dZ has 16 channels: 16-channel K chunks
     (1, 2, 4, 16, 32, 80),     # dZ has 80 channels: five 16-channel chunks, halo tile
-    (1, 6, 4, 16, 32, 64),     # 4-plane halo tile (N 32, two chunks): a full and a half tile in depth
-    (1, 6, 4, 8, 64, 128),     # 4-plane halo tile (N 64, four chunks), ragged in depth
+    (1, 6, 4, 16, 32, 64),     # halo tile (N 32, two chunks): a full and a half tile in depth
+    (1, 6, 4, 8, 64, 128),     # halo tile (N 64, four chunks), ragged in depth
+    (1, 2, 16, 8, 256, 64),    # dX has 256 channels: per-tap engine
 ]
 
 
@@ -360,6 +363,7 @@ WGRAD_SHAPES = [
     (1, 2, 4, 16, 4, 80),      # small c_in, c_out 80 in a 128-wide tile
     (1, 3, 6, 16, 32, 64),     # depth-stacked halo wgrad (c_in 32): odd depth, the last K block half empty
     (1, 5, 20, 24, 32, 32),    # depth-stacked, one output-channel set, ragged in d, h and w
+    (1, 3, 20, 16, 64, 128),   # halo wgrad, 64-channel chunks, ragged in d, h and w
 ]
 
 
