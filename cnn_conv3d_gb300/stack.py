@@ -28,7 +28,10 @@ One training step of the stack (forward + backward):
   step reads dW), so by default they run on a second stream, each after its
   block's pool backward (event), with their own workspace; the step ends by
   joining that stream.  Kernels of the two chains overlap where one leaves
-  SMs idle (the small deep layers, grid tails).
+  SMs idle (the small deep layers, grid tails).  The first block's weight
+  gradient is the exception: it goes on the critical stream right after
+  block 2's backward data, so that it does not queue behind block 2's weight
+  gradient (measured: 1.426 -> 1.409 ms per step).
 """
 from __future__ import annotations
 
@@ -148,6 +151,9 @@ class CosmoStack:
                     ws = max(ws, cf.cf_workspace_size(cf.CF_OP_DGRAD, desc))
         if self.side is None:
             ws = max(ws, ws_w)
+        elif backward and self.first_wgrad_on_main:
+            ws = max(ws, cf.cf_workspace_size(cf.CF_OP_WGRAD_ROUTED if self.routed(0) else cf.CF_OP_WGRAD,
+                                              self.desc(0)))
         self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=device)
         # the weight gradients' workspace (the main one when they share the stream)
         self.ws_w = torch.empty((max(ws_w, 256),), dtype=torch.uint8, device=device) if self.side else self.ws
@@ -169,6 +175,9 @@ class CosmoStack:
     # during the forward (cf_filter_flip), instead of inside each backward-data
     # call on the critical stream
     preflip = True
+    # the first block's weight gradient on the critical stream, right after the
+    # backward data of block 2 (its input), with the critical stream's workspace
+    first_wgrad_on_main = True
 
     def routed(self, l) -> bool:
         """Block l's weight gradient takes the pooled gradient + argmax codes."""
@@ -397,14 +406,19 @@ class CosmoStack:
                 self._run(f"poolbwd{l + 1}_sum", side,
                           lambda: cf.cf_column_sums(self.bpart_rows, co, self.bpart[l], self.db[l], side), timer)
                 to_host(side, host_out and host_out[1][l], self.db[l])
+            # (the first block's weight gradient: after block 2's backward data, below)
+            if l == 0 and self.first_wgrad_on_main and side is not main:
+                wst, wws, wwsb = main, ws, wsb
+            else:
+                wst, wws, wwsb = side, wsw, wswb
             if routed:
                 fn = lambda: cf.cf_conv3d_wgrad(desc, self.block_input(l), self.g[l], self.idx[l], self.dw[l], 0,
-                                                wsw, wswb, side)
+                                                wws, wwsb, wst)
             else:
-                fn = lambda: cf.cf_conv3d_wgrad(desc, self.block_input(l), self.dz[l], None, self.dw[l], 0, wsw,
-                                                wswb, side)
-            self._run(f"wgrad{l + 1}", side, fn, timer)
-            to_host(side, host_out and host_out[0][l], self.dw[l])
+                fn = lambda: cf.cf_conv3d_wgrad(desc, self.block_input(l), self.dz[l], None, self.dw[l], 0, wws,
+                                                wwsb, wst)
+            self._run(f"wgrad{l + 1}", wst, fn, timer)
+            to_host(wst, host_out and host_out[0][l], self.dw[l])
             if l > 0:
                 below = self.specs[l - 1][1]
                 fused = self.pool_bwd_fused(l - 1)
