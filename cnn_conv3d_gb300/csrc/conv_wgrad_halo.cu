@@ -400,13 +400,15 @@ __global__ void __launch_bounds__(224, 1)
                 wh_unit(g, u, (int)gridDim.x, set, split);
                 const int64_t k0 = (int64_t)split * g.kb_per_split;
                 const int64_t k1 = k0 + g.kb_per_split < g.total_kb ? k0 + g.kb_per_split : g.total_kb;
+                // K blocks depth fastest: consecutive blocks share two of their
+                // four dZ planes, which the next load then finds in L2
                 int64_t b = k0;
+                int bd = (int)(b % g.nb_d);
+                b /= g.nb_d;
                 int bw = (int)(b % g.nb_w);
                 b /= g.nb_w;
                 int bh = (int)(b % g.nb_h);
-                b /= g.nb_h;
-                int bd = (int)(b % g.nb_d);
-                int n = (int)(b / g.nb_d);
+                int n = (int)(b / g.nb_h);
                 for (int64_t kb = k0; kb < k1; ++kb) {
                     const int w0 = bw * 8, h0 = bh * 16, d0 = bd * WK_PLANES;
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns, p.status, WAIT_PRODUCER_EMPTY)) {
@@ -423,12 +425,12 @@ __global__ void __launch_bounds__(224, 1)
                         stage = 0;
                         phase ^= 1;
                     }
-                    if (++bw == g.nb_w) {
-                        bw = 0;
-                        if (++bh == g.nb_h) {
-                            bh = 0;
-                            if (++bd == g.nb_d) {
-                                bd = 0;
+                    if (++bd == g.nb_d) {
+                        bd = 0;
+                        if (++bw == g.nb_w) {
+                            bw = 0;
+                            if (++bh == g.nb_h) {
+                                bh = 0;
                                 ++n;
                             }
                         }
