@@ -27,8 +27,8 @@
 // E[r+1] and O[r+1] (slots 4-5 and 2-3, the high half) of the three lines kh:
 // N = 3 kh x 2 x 8 = 48, the N groups one row (144 bytes) apart.  Per K step 6
 // MMAs of 128 x 48 x 16 (3 kd x 2 halves), one accumulator of 48 columns
-// each (288 of the 512 tensor-memory columns; columns 384.. hold two dZ
-// tiles).  Three issuer threads take one kd each (measured: N = 32 MMAs with
+// each (288 of the 512 tensor-memory columns; columns 288.. hold three dZ
+// tiles, so the builders can run two tiles ahead of the MMAs).  Three issuer threads take one kd each (measured: N = 32 MMAs with
 // A in tensor memory run at ~27 cycles, so fewer wider MMAs pay).
 //
 // Tile: 1 plane x 16 lines x 32 voxels (128 rows).  Each CTA sums a
@@ -60,16 +60,17 @@ constexpr uint32_t WQ_TX = WQ_PBOX + 8192 + 4096;
 constexpr uint32_t WQ_BAR = 256;
 constexpr int WQ_STAGES = (int)((227 * 1024 - 1024 - WQ_BAR) / WQ_STAGE);
 constexpr uint32_t WQ_SMEM = 1024 + WQ_STAGES * WQ_STAGE + WQ_BAR;
-constexpr uint32_t WQ_ACOL = 384;                   // first column of the dZ tiles
+constexpr int WQ_NSLOT = 3;                         // dZ tiles in tensor memory (builders run two tiles ahead)
+constexpr uint32_t WQ_ACOL = 288;                   // first column of the dZ tiles (after 6 x 48 accumulator columns)
 constexpr int WQ_N = 48;                            // 3 kh x (E, O) x 8
 constexpr uint32_t WQ_IDESC = idesc_bf16(128, WQ_N, 0, 1);
 static_assert(WQ_EO >= WQ_PBOX, "stage layout");
 // the last B operand (kd = 2, K step 7, high half) ends inside the stage under
 // either order of the two descriptor strides (one of them is 144, the other 288)
 static_assert(WQ_G >= WQ_EO + (2 * WQ_LINES + 14) * WQ_LP + 16 + 5 * WQ_LP + WQ_RP + 128, "B operand bounds");
-static_assert(6 * WQ_N <= (int)WQ_ACOL, "tensor memory");
+static_assert(6 * WQ_N <= (int)WQ_ACOL && WQ_ACOL + WQ_NSLOT * 64 <= 512, "tensor memory");
 static_assert(WQ_STAGES >= 2, "shared memory");
-static_assert(8 * (2 * WQ_STAGES + 2 + 2 + 1 + 4) + 8 <= (int)WQ_BAR, "barrier area");
+static_assert(8 * (2 * WQ_STAGES + 2 * WQ_NSLOT + 1 + 4) + 8 <= (int)WQ_BAR, "barrier area");
 
 struct WqParams {
     int N, D, H, W;
@@ -120,8 +121,8 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t* full = bars;
     uint64_t* empty = full + WQ_STAGES;
     uint64_t* afull = empty + WQ_STAGES;
-    uint64_t* aempty = afull + 2;
-    uint64_t* tfull = aempty + 2;
+    uint64_t* aempty = afull + WQ_NSLOT;
+    uint64_t* tfull = aempty + WQ_NSLOT;
     uint64_t* drain = tfull + 1;  // [4]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 11);  // three issuers' MMAs + eight builder warps
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < WQ_NSLOT; ++b) {
             mbar_init(&afull[b], 8);   // eight builder warps
             mbar_init(&aempty[b], 3);  // three issuers' MMAs
         }
@@ -194,10 +195,10 @@ __global__ void __launch_bounds__(384, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
+            uint32_t b = 0, bph = 0;  // dZ slot and its phase
             for (int tile = t0, lt = 0; tile < t1; ++tile, ++lt) {
-                const uint32_t b = lt & 1;
                 if (!mbar_wait(&full[s], ph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL) ||
-                    !mbar_wait(&afull[b], (lt >> 1) & 1, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                    !mbar_wait(&afull[b], bph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
                     ok = false;
                     break;
                 }
@@ -219,6 +220,10 @@ __global__ void __launch_bounds__(384, 1)
                     s = 0;
                     ph ^= 1;
                 }
+                if (++b == WQ_NSLOT) {
+                    b = 0;
+                    bph ^= 1;
+                }
             }
             if (ok) {
                 umma_commit(tfull);
@@ -235,11 +240,11 @@ __global__ void __launch_bounds__(384, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
+        uint32_t b = 0, bph = 0;  // dZ slot and its phase
         for (int tile = t0, lt = 0; tile < t1; ++tile, ++lt) {
-            const uint32_t b = lt & 1;
             if (!__all_sync(0xffffffffu,
                             mbar_wait(&full[s], ph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL) &&
-                                mbar_wait(&aempty[b], ((lt >> 1) & 1) ^ 1, abort_flag, p.wait_ns, p.status,
+                                mbar_wait(&aempty[b], bph ^ 1, abort_flag, p.wait_ns, p.status,
                                           WAIT_PRODUCER_EMPTY))) {
                 ok = false;
                 break;
@@ -283,6 +288,10 @@ __global__ void __launch_bounds__(384, 1)
             if (++s == WQ_STAGES) {
                 s = 0;
                 ph ^= 1;
+            }
+            if (++b == WQ_NSLOT) {
+                b = 0;
+                bph ^= 1;
             }
         }
         // ---------------- epilogue: this lane's (f, co) partial of every dW entry
