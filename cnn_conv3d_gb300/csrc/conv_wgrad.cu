@@ -307,11 +307,13 @@ static WgradGeom wgrad_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_
     g.nb_h = (int)((h + g.vh - 1) / g.vh);
     g.nb_d = (int)((d + g.vd - 1) / g.vd);
     g.total_boxes = n * g.nb_d * g.nb_h * g.nb_w;
-    // about one unit per SM, each unit at least 8 boxes long (measured in the
-    // five-block step: two units per SM, i.e. twice the partial sums to write
-    // and reduce, made the step 0.035 ms slower)
+    // at most one unit per SM (one round of CTAs: rounding the split count up
+    // would leave a second round of a few units that doubles the kernel's
+    // time), each unit at least 8 boxes long (measured in the five-block step:
+    // two units per SM, i.e. twice the partial sums to write and reduce, made
+    // the step 0.035 ms slower)
     const int tiles = g.n_mblocks * g.n_ntiles;
-    int64_t target = std::max<int64_t>(1, ((int64_t)num_sms + tiles - 1) / tiles);
+    int64_t target = std::max<int64_t>(1, (int64_t)num_sms / tiles);
     target = std::min<int64_t>(target, std::max<int64_t>(1, g.total_boxes / 8));
     g.boxes_per_split = (g.total_boxes + target - 1) / target;
     g.n_splits = (int)((g.total_boxes + g.boxes_per_split - 1) / g.boxes_per_split);

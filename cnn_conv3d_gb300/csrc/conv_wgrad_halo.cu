@@ -558,9 +558,10 @@ static WhGeom wh_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, i
     g.sets_per_chunk = (g.blocks_per_chunk + C::GMAX - 1) / C::GMAX;
     g.g_per_set = (g.blocks_per_chunk + g.sets_per_chunk - 1) / g.sets_per_chunk;
     g.n_sets = g.sets_per_chunk * g.n_chunks;
-    // one unit per SM: half the partial sums of two units per SM (measured in the
-    // five-block step: 1.470 -> 1.416 ms together with the per-tap kernel's)
-    int64_t target = std::max<int64_t>(1, ((int64_t)num_sms + g.n_sets - 1) / g.n_sets);
+    // at most one unit per SM (one round of CTAs): half the partial sums of two
+    // units per SM (measured in the five-block step: 1.470 -> 1.416 ms together
+    // with the per-tap kernel's)
+    int64_t target = std::max<int64_t>(1, (int64_t)num_sms / g.n_sets);
     target = std::min<int64_t>(target, std::max<int64_t>(1, g.total_kb / 4));
     g.kb_per_split = (g.total_kb + target - 1) / target;
     g.n_splits = (int)((g.total_kb + g.kb_per_split - 1) / g.kb_per_split);
@@ -587,9 +588,10 @@ static WhGeom wk_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, i
     g.sets_per_chunk = c_out / 32;
     g.g_per_set = 3;
     g.n_sets = g.sets_per_chunk;
-    // one unit per SM: half the partial sums of two units per SM (measured in the
-    // five-block step: 1.470 -> 1.416 ms together with the per-tap kernel's)
-    int64_t target = std::max<int64_t>(1, ((int64_t)num_sms + g.n_sets - 1) / g.n_sets);
+    // at most one unit per SM (one round of CTAs): half the partial sums of two
+    // units per SM (measured in the five-block step: 1.470 -> 1.416 ms together
+    // with the per-tap kernel's)
+    int64_t target = std::max<int64_t>(1, (int64_t)num_sms / g.n_sets);
     target = std::min<int64_t>(target, std::max<int64_t>(1, g.total_kb / 4));
     g.kb_per_split = (g.total_kb + target - 1) / target;
     g.n_splits = (int)((g.total_kb + g.kb_per_split - 1) / g.kb_per_split);
