@@ -580,7 +580,14 @@ def run_ours(args, rank, world, local_rank):
                 "flops_per_launch": dom_flops, "algorithmic_bytes": dom_bytes,
                 "hbm": {"achieved_gbs": round(gbs, 1), "peak_gbs": pk["hbm_gbs"],
                         "frac": round(gbs / pk["hbm_gbs"], 4),
-                        "traffic_gbs": round(tr / (op_ms[dom] * 1e-3) / 1e9, 1) if tr else None}}
+                        "traffic_gbs": round(tr / (op_ms[dom] * 1e-3) / 1e9, 1) if tr else None},
+                # the launch duration above is the one inside the timed steps, where
+                # other kernels of the step may share the GPU with it; the same
+                # kernel alone (the instrumented serial steps) for comparison
+                "alone": {"ms": round(float(np.mean(inst[dom])), 4),
+                          "achieved": round(dom_flops / (float(np.mean(inst[dom])) * 1e-3) / 1e12, 2),
+                          "frac": round(dom_flops / (float(np.mean(inst[dom])) * 1e-3) / 1e12 / pk["bf16_tflops"], 4)},
+                "timed_ms": round(op_ms[dom], 4)}
 
     value = whole_job_rate(total_flops, world, ms) / 1e12
     res = {

@@ -81,18 +81,18 @@ __device__ __forceinline__ void pool_combine(float& v, int& k, float v2, int k2)
 // warps per TMEM lane quarter can thus split the channels of a tile.
 // dsum (backward-data, BN <= 32): per-channel running sums of the stored
 // bf16 outputs of this thread's voxels, or NULL.
-// acc_col2: a second accumulator pair (plane 0 | plane 1) added to the first,
-// or 0xFFFFFFFF for none.
+// add0 / add1: accumulator columns added to plane 0 / plane 1 (partial sums of
+// a second issuer), or 0xFFFFFFFF for none.
 template <int BN, int EPI, int CH_ = 0>
 __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& t, uint32_t tmem_base,
                                               uint32_t acc_col, int q, int lane, int c_begin = 0,
                                               int c_step = 0, float* dsum = nullptr,
-                                              uint32_t acc_col2 = 0xFFFFFFFFu) {
+                                              uint32_t add0 = 0xFFFFFFFFu, uint32_t add1 = 0xFFFFFFFFu) {
     constexpr int CH = CH_ != 0 ? CH_ : (BN >= 32 ? 32 : 16);  // accumulator columns per pass
     const int r = q * 32 + lane;
     const int j = r >> 3, l = r & 7;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
-    const uint32_t lane_addr2 = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col2;
+    const uint32_t lane_q = tmem_base + ((uint32_t)(q * 32) << 16);
     const int h = t.h0 + j, w = t.w0 + l;
     const int step = c_step != 0 ? c_step : CH;
 #pragma unroll 1
@@ -105,20 +105,28 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
             tmem_ld16(lane_addr + c, a0);
             tmem_ld16(lane_addr + BN + c, a1);
         }
-        if (acc_col2 != 0xFFFFFFFFu) {
+        if (add0 != 0xFFFFFFFFu || add1 != 0xFFFFFFFFu) {  // warp-uniform
             uint32_t b0[32], b1[32];
-            if (CH == 32) {
-                tmem_ld32(lane_addr2 + c, b0);
-                tmem_ld32(lane_addr2 + BN + c, b1);
-            } else {
-                tmem_ld16(lane_addr2 + c, b0);
-                tmem_ld16(lane_addr2 + BN + c, b1);
+            if (add0 != 0xFFFFFFFFu) {
+                if (CH == 32)
+                    tmem_ld32(lane_q + add0 + c, b0);
+                else
+                    tmem_ld16(lane_q + add0 + c, b0);
+            }
+            if (add1 != 0xFFFFFFFFu) {
+                if (CH == 32)
+                    tmem_ld32(lane_q + add1 + c, b1);
+                else
+                    tmem_ld16(lane_q + add1 + c, b1);
             }
             tmem_ld_wait();
+            if (add0 != 0xFFFFFFFFu) {
 #pragma unroll
-            for (int k = 0; k < CH; ++k) {
-                a0[k] = __float_as_uint(__uint_as_float(a0[k]) + __uint_as_float(b0[k]));
-                a1[k] = __float_as_uint(__uint_as_float(a1[k]) + __uint_as_float(b1[k]));
+                for (int k = 0; k < CH; ++k) a0[k] = __float_as_uint(__uint_as_float(a0[k]) + __uint_as_float(b0[k]));
+            }
+            if (add1 != 0xFFFFFFFFu) {
+#pragma unroll
+                for (int k = 0; k < CH; ++k) a1[k] = __float_as_uint(__uint_as_float(a1[k]) + __uint_as_float(b1[k]));
             }
         }
         tmem_ld_wait();
@@ -181,6 +189,24 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
                 }
             }
         } else {
+            // backward data: the stored activations of this pass's voxels and
+            // channels, all loaded before the first store (the stores may alias
+            // nothing the compiler can see, so loads inside the store loop would
+            // each wait out their latency)
+            uint4 xa_all[EPI == EPI_DGRAD ? 2 * (CH / 8) : 1];
+            if (EPI == EPI_DGRAD) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int d = t.d0 + i;
+                    const bool in = d < p.D && h < p.H && w < p.W;
+                    const int64_t o = ((((int64_t)t.n * p.D + d) * p.H + h) * p.W + w) * p.Cout + t.co0 + c;
+#pragma unroll
+                    for (int q8 = 0; q8 < CH / 8; ++q8)
+                        xa_all[i * (CH / 8) + q8] = (in && q8 * 8 < nvalid)
+                                                        ? *reinterpret_cast<const uint4*>(p.ea.x_act + o + q8 * 8)
+                                                        : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int d = t.d0 + i;
@@ -199,7 +225,7 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
                             v[k] = lrelu(v[k] + (p.ea.bias ? p.ea.bias[t.co0 + c + q8 * 8 + k] : 0.f), p.ea.slope);
                     }
                     if (EPI == EPI_DGRAD) {
-                        const uint4 xa = *reinterpret_cast<const uint4*>(p.ea.x_act + o + q8 * 8);
+                        const uint4 xa = xa_all[EPI == EPI_DGRAD ? i * (CH / 8) + q8 : 0];
                         const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -236,5 +262,11 @@ __device__ __forceinline__ void halo_epilogue(const HaloParams& p, const HTile& 
         }
     }
 }
+
+// The 4-plane tile for c_out 32 (conv_halo4.cu); p carries the problem (sizes,
+// epilogue arguments), the tile counts are its own.
+bool halo4_path_supported(int c_in, int c_out);
+cf_status launch_conv_halo4(const LaunchCtx& ctx, const HaloParams& p, const uint16_t* x, const uint16_t* wk,
+                            int epi);
 
 }  // namespace cf
