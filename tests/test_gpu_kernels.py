@@ -277,6 +277,7 @@ DGRAD_SHAPES = [
     (1, 6, 4, 16, 32, 64),     # halo tile (N 32, two chunks): a full and a half tile in depth
     (1, 6, 4, 8, 64, 128),     # halo tile (N 64, four chunks), ragged in depth
     (1, 2, 16, 8, 256, 64),    # dX has 256 channels: per-tap engine
+    (1, 6, 6, 16, 64, 32),     # halo tile with N 64 (dX 64 channels from 32), ragged in depth
 ]
 
 
