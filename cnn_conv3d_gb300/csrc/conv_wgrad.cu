@@ -393,7 +393,8 @@ static cf_status launch_splitk_reduce(const LaunchCtx& ctx, const float* part, f
         const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((count + cols - 1) / cols, 8LL * ctx.num_sms));
         kern<<<blocks, 256, 0, ctx.stream>>>(part, dw, count, splits, accumulate);
     };
-    if (splits >= 64) launch(splitk_reduce_kernel<8>, 32);
+    if (splits >= 256) launch(splitk_reduce_kernel<32>, 8);  // the first layer's per-CTA, per-phase partials
+    else if (splits >= 64) launch(splitk_reduce_kernel<8>, 32);
     else if (splits >= 16) launch(splitk_reduce_kernel<4>, 64);
     else launch(splitk_reduce_kernel<1>, 256);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
