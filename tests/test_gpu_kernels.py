@@ -158,6 +158,7 @@ FWD_SHAPES = [
     (1, 6, 4, 16, 32, 64),     # halo tile: a full and a half tile in depth
     (1, 2, 4, 16, 64, 32),     # halo tile deeper than the volume, two chunks
     (1, 2, 16, 16, 128, 256),  # per-tap engine, N tile 256, several tiles per sample
+    (1, 6, 18, 10, 32, 32),    # 4-plane halo tile ragged in d, h and w (pooled: all even)
     (1, 4, 16, 8, 32, 384),    # per-tap engine, two N tiles (256 + 128)
 ]
 
@@ -278,6 +279,7 @@ DGRAD_SHAPES = [
     (1, 6, 4, 8, 64, 128),     # halo tile (N 64, four chunks), ragged in depth
     (1, 2, 16, 8, 256, 64),    # dX has 256 channels: per-tap engine
     (1, 6, 6, 16, 64, 32),     # halo tile with N 64 (dX 64 channels from 32), ragged in depth
+    (1, 5, 20, 12, 32, 48),    # 4-plane halo tile (N 32, three 16-channel chunks), ragged in d, h and w
 ]
 
 
