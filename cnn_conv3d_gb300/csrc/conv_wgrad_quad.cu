@@ -21,24 +21,29 @@
 //     N = (kh, E/O, two voxels x 4 channels), K = 16 rows (2 lines x 8 quads)
 //     per MMA.  The input lines arrive as one TMA box of plain lines (288-byte
 //     rows: a box of 16-byte E / O rows measured TMA-bound) and the builder
-//     warps copy their pairs into the E and O rows.
+//     warps copy their pairs into the E and O rows, in an order that hits
+//     every shared-memory bank once per eight pairs.
 // The builders store each input line as [E row | O row], so that one MMA
 // takes the pairs E[r] and O[r] (voxel slots 0-1 and -2..-1, the low half) or
 // E[r+1] and O[r+1] (slots 4-5 and 2-3, the high half) of the three lines kh:
 // N = 3 kh x 2 x 8 = 48, the N groups one row (144 bytes) apart.  Per K step 6
 // MMAs of 128 x 48 x 16 (3 kd x 2 halves), one accumulator of 48 columns
-// each (288 of the 512 tensor-memory columns; columns 288.. hold three dZ
-// tiles, so the builders can run two tiles ahead of the MMAs).  Three issuer threads take one kd each (measured: N = 32 MMAs with
-// A in tensor memory run at ~27 cycles, so fewer wider MMAs pay).
+// each (288 of the 512 tensor-memory columns; columns 288.. hold one dZ tile
+// per builder group).  Three issuer threads take one kd each (measured: N = 32
+// MMAs with A in tensor memory run at ~27 cycles, so fewer wider MMAs pay).
 //
 // Tile: 1 plane x 16 lines x 32 voxels (128 rows).  Each CTA sums a
 // contiguous range of tiles and writes, per phase, its 32 x 108 partial dW
 // (phase-major split-K partials, summed afterwards in a fixed order).
 //
-// Roles (384 threads): warp 0 TMA producer; warps 1, 2, 3 MMA issuers
-// (kd = 0, 1, 2); warps 4..11 builders of the dZ tiles (warps 4 + f and
-// 8 + f: phase f, pooled lines 0-3 / 4-7) and, after the last tile, warps 4..7
-// the epilogue.
+// Roles (512 threads): warp 0 TMA producer; warps 1, 2, 3 MMA issuers
+// (kd = 0, 1, 2); warps 4..15 three builder groups of four warps.  Group g
+// takes every third tile (g, g + 3, ...), with its own dZ slot and E / O
+// buffer, so three tiles are built at once: one group building a tile (a
+// chain of waits, shared-memory loads and tensor-memory stores) was the
+// bound with all eight builder warps on the same tile.  Warp f of a group
+// builds phase f (lane = channel co) over all 16 lines; after the last tile
+// group 0 runs the epilogue.
 #include <algorithm>
 
 #include "conv_common.cuh"
@@ -52,24 +57,28 @@ constexpr uint32_t WQ_RP = WQ_QUADS * 16;           // 144: one E or O row
 constexpr uint32_t WQ_LP = 2 * WQ_RP;               // 288: line pitch of the rows ([E | O] per line)
 constexpr int WQ_PAIRS = 2 * WQ_QUADS;              // 18 voxel pairs per input line (w0-2 .. w0+33)
 constexpr uint32_t WQ_PBOX = WQ_PLANES * WQ_LINES * WQ_PAIRS * 16;  // 15552: the TMA box (plain lines)
-constexpr uint32_t WQ_EO = 15616;                   // the E / O rows
-constexpr uint32_t WQ_G = 31744;                    // pooled gradient [8][16][32] bf16
+constexpr uint32_t WQ_G = 15616;                    // pooled gradient [8][16][32] bf16
 constexpr uint32_t WQ_I = WQ_G + 8192;              // codes [8][16][32]
-constexpr uint32_t WQ_STAGE = WQ_I + 4096;
+constexpr uint32_t WQ_STAGE = WQ_I + 4096;          // one TMA stage: box, pooled gradient, codes
 constexpr uint32_t WQ_TX = WQ_PBOX + 8192 + 4096;
+constexpr int WQ_GROUPS = 3;                        // builder groups, taking every third tile
+constexpr int WQ_STAGES = 2 * WQ_GROUPS;            // stage s is only ever read by group s % 3
+// E / O rows of one tile (the B operand), one buffer per builder group,
+// including the last MMA's descriptor extent past the rows
+constexpr uint32_t WQ_EOB = (2 * WQ_LINES + 14) * WQ_LP + 16 + 5 * WQ_LP + WQ_RP + 128;
+constexpr uint32_t WQ_EO0 = WQ_STAGES * WQ_STAGE;   // first E / O buffer
 constexpr uint32_t WQ_BAR = 256;
-constexpr int WQ_STAGES = (int)((227 * 1024 - 1024 - WQ_BAR) / WQ_STAGE);
-constexpr uint32_t WQ_SMEM = 1024 + WQ_STAGES * WQ_STAGE + WQ_BAR;
-constexpr int WQ_NSLOT = 3;                         // dZ tiles in tensor memory (builders run two tiles ahead)
+constexpr uint32_t WQ_SMEM = 1024 + WQ_EO0 + WQ_GROUPS * WQ_EOB + WQ_BAR;
+constexpr int WQ_NSLOT = WQ_GROUPS;                 // dZ tiles in tensor memory, one per builder group
+constexpr int WQ_THREADS = 128 + 128 * WQ_GROUPS;
 constexpr uint32_t WQ_ACOL = 288;                   // first column of the dZ tiles (after 6 x 48 accumulator columns)
 constexpr int WQ_N = 48;                            // 3 kh x (E, O) x 8
 constexpr uint32_t WQ_IDESC = idesc_bf16(128, WQ_N, 0, 1);
-static_assert(WQ_EO >= WQ_PBOX, "stage layout");
-// the last B operand (kd = 2, K step 7, high half) ends inside the stage under
-// either order of the two descriptor strides (one of them is 144, the other 288)
-static_assert(WQ_G >= WQ_EO + (2 * WQ_LINES + 14) * WQ_LP + 16 + 5 * WQ_LP + WQ_RP + 128, "B operand bounds");
+static_assert(WQ_G >= WQ_PBOX && WQ_STAGE % 128 == 0 && WQ_EOB % 128 == 0, "stage layout");
+static_assert(WQ_EOB >= WQ_PLANES * WQ_LINES * WQ_LP, "E / O rows");
+static_assert(WQ_SMEM <= 227 * 1024, "shared memory");
 static_assert(6 * WQ_N <= (int)WQ_ACOL && WQ_ACOL + WQ_NSLOT * 64 <= 512, "tensor memory");
-static_assert(WQ_STAGES >= 2, "shared memory");
+static_assert(WQ_STAGES % WQ_GROUPS == 0, "stage ownership");
 static_assert(8 * (2 * WQ_STAGES + 2 * WQ_NSLOT + 1 + 4) + 8 <= (int)WQ_BAR, "barrier area");
 
 struct WqParams {
@@ -110,14 +119,48 @@ __device__ __forceinline__ void wq_range(const WqParams& p, int& t0, int& t1) {
     t1 = t0 + base + (u < rem ? 1 : 0);
 }
 
-__global__ void __launch_bounds__(384, 1)
+// De-interleave of one stage: item k < 972 copies one 16-byte voxel pair of the
+// TMA box (54 lines x 18 pairs; pair 2q + 1 is E[q], pair 2q is O[q]) to its E
+// or O row.  Items run in groups of eight that each hit all 32 banks once, on
+// both the load and the store side (a line starts 288 = 32 mod 128 bytes after
+// the previous one, in the box and in the rows; the O row 144 = 16 mod 128
+// bytes after the E row): per line E[0..3] with O[3..6], then E[4..7] with
+// O[7], O[0..2] (864 items), then E[8] and O[8] of four consecutive lines per
+// group.  Returns source | destination << 16 (stage offsets), or all ones past
+// the last item.
+constexpr int WQ_DEINT = WQ_PLANES * WQ_LINES * WQ_PAIRS;  // 972
+constexpr int WQ_DEINT_PER = (WQ_DEINT + 127) / 128;       // items per builder thread
+__host__ __device__ constexpr uint32_t wq_deint_offsets(int k) {
+    if (k >= WQ_DEINT) return 0xffffffffu;
+    int line = 0, q = 0;
+    bool odd = false;  // E (odd pair) or O
+    if (k < 16 * WQ_PLANES * WQ_LINES) {
+        const int e = k & 7, half = (k >> 3) & 1;
+        line = k >> 4;
+        odd = e < 4;
+        q = half == 0 ? (odd ? e : e - 1) : (odd ? 4 + e : (e + 3) & 7);
+    } else {
+        const int j = k - 16 * WQ_PLANES * WQ_LINES;
+        line = j >> 1;
+        odd = (j & 1) == 0;
+        q = 8;
+    }
+    const uint32_t src = (uint32_t)(line * WQ_PAIRS + 2 * q + (odd ? 1 : 0)) * 16u;
+    const uint32_t dst = (uint32_t)line * WQ_LP + (odd ? 0u : WQ_RP) + (uint32_t)q * 16u;
+    return src | (dst << 16);
+}
+static_assert((WQ_PLANES * WQ_LINES - 1) * WQ_LP + WQ_RP + 8 * 16 + 16 <= 65535, "packed offsets");
+// only the last item of a thread can lie past the end (the guard in the builders)
+static_assert(127 + 128 * (WQ_DEINT_PER - 2) < WQ_DEINT, "de-interleave items");
+
+__global__ void __launch_bounds__(WQ_THREADS, 1)
     wgrad_quad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                       const __grid_constant__ CUtensorMap tmI,
                       const WqParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* ring = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WQ_STAGES * WQ_STAGE);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WQ_EO0 + WQ_GROUPS * WQ_EOB);
     uint64_t* full = bars;
     uint64_t* empty = full + WQ_STAGES;
     uint64_t* afull = empty + WQ_STAGES;
@@ -134,11 +177,11 @@ __global__ void __launch_bounds__(384, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < WQ_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 11);  // three issuers' MMAs + eight builder warps
+            mbar_init(&empty[s], 4);  // the four warps of one builder group
         }
         for (int b = 0; b < WQ_NSLOT; ++b) {
-            mbar_init(&afull[b], 8);   // eight builder warps
-            mbar_init(&aempty[b], 3);  // three issuers' MMAs
+            mbar_init(&afull[b], 4);   // the four warps of builder group b
+            mbar_init(&aempty[b], 3);  // three issuers' MMAs (dZ slot and E / O rows b)
         }
         mbar_init(tfull, 3);
         for (int k = 0; k < 3; ++k) mbar_init(&drain[k], 1);
@@ -192,18 +235,15 @@ __global__ void __launch_bounds__(384, 1)
             // (E[r] | O[r]: voxel slots 0-1 | -2..-1) and the high half (E[r+1] | O[r+1]:
             // slots 4-5 | 2-3), N = (kh, E/O, 8)
             const int kd = warp - 1;
-            int s = 0;
-            uint32_t ph = 0;
             bool ok = true;
-            uint32_t b = 0, bph = 0;  // dZ slot and its phase
+            uint32_t b = 0, bph = 0;  // dZ slot / E-O buffer and its phase
             for (int tile = t0, lt = 0; tile < t1; ++tile, ++lt) {
-                if (!mbar_wait(&full[s], ph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL) ||
-                    !mbar_wait(&afull[b], bph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
+                if (!mbar_wait(&afull[b], bph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t rows = smem_u32(ring + s * WQ_STAGE) + WQ_EO + kd * WQ_LINES * WQ_LP;
+                const uint32_t rows = smem_u32(ring + WQ_EO0 + b * WQ_EOB) + kd * WQ_LINES * WQ_LP;
                 const uint32_t a_tmem = tmem_base + WQ_ACOL + b * 64;
                 // MN-major without swizzle: K groups (the next output line) WQ_LP apart
                 // (leading byte offset), N groups (kh, E/O) WQ_RP apart (stride byte offset)
@@ -214,12 +254,7 @@ __global__ void __launch_bounds__(384, 1)
                         umma_bf16_tmem_a(tmem_base + (kd * 2 + hl) * WQ_N, a_tmem + 8 * j,
                                          sdesc(rows + 2 * j * WQ_LP + 16 * hl, WQ_LP, WQ_RP, SWZ_NONE), WQ_IDESC,
                                          (lt | j) ? 1u : 0u);
-                umma_commit(&empty[s]);
                 umma_commit(&aempty[b]);
-                if (++s == WQ_STAGES) {
-                    s = 0;
-                    ph ^= 1;
-                }
                 if (++b == WQ_NSLOT) {
                     b = 0;
                     bph ^= 1;
@@ -233,31 +268,46 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
     } else {
-        // ---------------- builders (phase f, pooled lines 4*hb .. 4*hb + 3, channel co =
-        // lane), then the epilogue
-        const int f = warp & 3, hb = (warp - 4) >> 2, co = lane;
+        // ---------------- builders: group g = warps 4 + 4g .. 7 + 4g takes the CTA's
+        // tiles g, g + 3, ... (three tiles in flight) into dZ slot g and E / O buffer g;
+        // warp f of a group builds phase f (lane = channel co) over all 16 lines,
+        // then group 0 runs the epilogue
+        const int f = warp & 3, grp = (warp - 4) >> 2, co = lane, gt = threadIdx.x - 128 - 128 * grp;
         const uint32_t lane_addr = tmem_base + ((uint32_t)(f * 32) << 16);
-        int s = 0;
-        uint32_t ph = 0;
+        const uint32_t a_col = WQ_ACOL + (uint32_t)grp * 64;
+        uint8_t* eo = ring + WQ_EO0 + grp * WQ_EOB;
+        uint32_t doff[WQ_DEINT_PER];  // (source | destination << 16) of this thread's voxel pairs
+#pragma unroll
+        for (int i = 0; i < WQ_DEINT_PER; ++i) doff[i] = wq_deint_offsets(gt + 128 * i);
+        int s = grp;
+        uint32_t ph = 0, bph = 0;  // stage phase, slot phase
         bool ok = true;
-        uint32_t b = 0, bph = 0;  // dZ slot and its phase
-        for (int tile = t0, lt = 0; tile < t1; ++tile, ++lt) {
+        for (int tile = t0 + grp; tile < t1; tile += WQ_GROUPS) {
+            // the stage's data, and the slot (dZ tile and E / O rows) free of the
+            // MMAs of this group's previous tile
             if (!__all_sync(0xffffffffu,
                             mbar_wait(&full[s], ph, abort_flag, p.wait_ns, p.status, WAIT_MMA_FULL) &&
-                                mbar_wait(&aempty[b], bph ^ 1, abort_flag, p.wait_ns, p.status,
+                                mbar_wait(&aempty[grp], bph ^ 1, abort_flag, p.wait_ns, p.status,
                                           WAIT_PRODUCER_EMPTY))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int dd = wq_decode(p, tile).d0 & 1;
-            uint8_t* st = ring + s * WQ_STAGE;
+            const uint8_t* st = ring + s * WQ_STAGE;
             // the input lines' voxel pairs (w0-2 .. w0+33: O[0], E[0], O[1], ...) into
-            // the E and O rows of the MMA's B operand
-            for (int k = threadIdx.x - 128; k < WQ_PLANES * WQ_LINES * WQ_PAIRS; k += 256) {
-                const int line = k / WQ_PAIRS, pr = k - line * WQ_PAIRS;
-                const uint4 v = *reinterpret_cast<const uint4*>(st + k * 16);
-                *reinterpret_cast<uint4*>(st + WQ_EO + line * WQ_LP + ((pr & 1) ? 0u : WQ_RP) + (pr >> 1) * 16) = v;
+            // the E and O rows of the MMA's B operand: all loads of a thread, then its
+            // stores, in the bank-conflict-free order of wq_deint_offsets
+            {
+                uint4 dv[WQ_DEINT_PER];
+#pragma unroll
+                for (int i = 0; i < WQ_DEINT_PER; ++i)
+                    if (i < WQ_DEINT_PER - 1 || doff[i] != 0xffffffffu)
+                        dv[i] = *reinterpret_cast<const uint4*>(st + (doff[i] & 0xffffu));
+#pragma unroll
+                for (int i = 0; i < WQ_DEINT_PER; ++i)
+                    if (i < WQ_DEINT_PER - 1 || doff[i] != 0xffffffffu)
+                        *reinterpret_cast<uint4*>(eo + (doff[i] >> 16)) = dv[i];
             }
             fence_proxy_async_smem();
             const uint16_t* gp = reinterpret_cast<const uint16_t*>(st + WQ_G) + co;
@@ -265,37 +315,39 @@ __global__ void __launch_bounds__(384, 1)
             // column c holds rows 2c, 2c+1 = quads i, i+1 of line c/4 (i = 2 (c % 4)):
             // voxels w = 4i + f and 4i + 4 + f, pooled w 2i + f/2 and 2i + 2 + f/2.
             // Lines 2l and 2l + 1 (columns c and c + 4) share their pooled values.
-            uint32_t col[32];
+            // Two halves of 32 columns (pooled lines 0-3, 4-7).
             const uint32_t code0 = (uint32_t)(dd * 4 + (f & 1)), code1 = code0 + 2;
 #pragma unroll
-            for (int l = 0; l < 4; ++l)
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t col[32];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int o = (4 * hb + l) * 16 + 4 * q4 + (f >> 1);
-                    const uint32_t k0 = ip[o * 32], k1 = ip[(o + 2) * 32];
-                    const uint32_t g0 = gp[o * 32], g1 = gp[(o + 2) * 32];
-                    col[8 * l + q4] = (k0 == code0 ? g0 : 0u) | ((k1 == code0 ? g1 : 0u) << 16);
-                    col[8 * l + 4 + q4] = (k0 == code1 ? g0 : 0u) | ((k1 == code1 ? g1 : 0u) << 16);
-                }
-            tmem_st32(lane_addr + WQ_ACOL + b * 64 + 32 * hb, col);
+                for (int l = 0; l < 4; ++l)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int o = (4 * hf + l) * 16 + 4 * q4 + (f >> 1);
+                        const uint32_t k0 = ip[o * 32], k1 = ip[(o + 2) * 32];
+                        const uint32_t g0 = gp[o * 32], g1 = gp[(o + 2) * 32];
+                        col[8 * l + q4] = (k0 == code0 ? g0 : 0u) | ((k1 == code0 ? g1 : 0u) << 16);
+                        col[8 * l + 4 + q4] = (k0 == code1 ? g0 : 0u) | ((k1 == code1 ? g1 : 0u) << 16);
+                    }
+                tmem_st32(lane_addr + a_col + 32 * hf, col);
+            }
+            // the stage is no longer read by this warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&afull[b]);
-                mbar_arrive(&empty[s]);
-            }
-            if (++s == WQ_STAGES) {
-                s = 0;
+            if (lane == 0) mbar_arrive(&afull[grp]);
+            s += WQ_GROUPS;
+            if (s >= WQ_STAGES) {
+                s -= WQ_STAGES;
                 ph ^= 1;
             }
-            if (++b == WQ_NSLOT) {
-                b = 0;
-                bph ^= 1;
-            }
+            bph ^= 1;
         }
         // ---------------- epilogue: this lane's (f, co) partial of every dW entry
-        if (ok && hb == 0 &&
+        if (ok && grp == 0 &&
             __all_sync(0xffffffffu, mbar_wait(tfull, 0, abort_flag, p.wait_ns, p.status, WAIT_EPI_TMEM_FULL))) {
             tc_fence_after();
             float* out = p.part + (((int64_t)blockIdx.x * 4 + f) * 32 + co) * 108;
@@ -397,7 +449,7 @@ cf_status launch_wgrad_quad(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t 
     if (cudaFuncSetAttribute(wgrad_quad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WQ_SMEM) != cudaSuccess)
         return CF_ERR_CUDA;
     const int grid = wq_units(ctx.num_sms, n, d, h, w);
-    wgrad_quad_kernel<<<grid, 384, WQ_SMEM, ctx.stream>>>(tx, tg, ti, p);
+    wgrad_quad_kernel<<<grid, WQ_THREADS, WQ_SMEM, ctx.stream>>>(tx, tg, ti, p);
     if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
     *n_splits = grid * 4;
     return CF_OK;
