@@ -406,6 +406,7 @@ ROUTED_SHAPES = [
     (2, 4, 32, 64, 4, 32),
     (1, 6, 16, 96, 4, 32),
     (1, 2, 48, 32, 4, 32),
+    (3, 16, 64, 96, 4, 32),    # 576 tiles: 3-4 per CTA, all three builder groups, stage and slot reuse
 ]
 
 
