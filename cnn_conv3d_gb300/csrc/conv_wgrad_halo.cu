@@ -24,9 +24,10 @@
 // afterwards in a fixed order.  The halo makes each input row feed every tap
 // group of the CTA instead of being re-fetched per tap.
 //
-// c_in 32 with c_out 32 or 64 runs the depth-stacked variant further down
-// (the depth tap moved onto the B operand: 3 MMAs of N = 96 per K step
-// instead of 9 of N = 64).
+// c_in 32 with c_out 32 or 64 and c_in 64 with c_out 64 or 128 run the
+// depth-stacked variant further down (the depth tap moved onto the B operand:
+// per K step 3 MMAs of N = 96 instead of 9 of N = 64 for c_in 32, 5 instead of
+// 14 of N = 128 for c_in 64).
 #include "conv_common.cuh"
 
 namespace cf {
@@ -317,46 +318,74 @@ __global__ void __launch_bounds__(224, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Depth-stacked variant for c_in = 32 (the layer-2 shape 32 -> 64):
+// Depth-stacked variant for c_in = 32 or 64 (the layer-2 and layer-3 shapes):
 //
 //   dW[co, (kd,kh,kw), ci] = sum_u dZ[u - (kd-1) e_d, co] * X[u + (0, kh-1, kw-1), ci]
 //
 // (the sum over v with u = v + (kd-1) e_d).  The depth tap moves from the A
 // operand to the B operand: A = the input halo of the K block without a depth
-// halo (PLANES x 18 x 10 rows), M atoms kw = 0, 1, 2 one row apart (+ one
-// unused atom), one M block per kh; B = dZ of the block's planes and one
-// plane on either side, for one set of 32 output channels, and its N atoms
-// are the kd = 2, 1, 0 shifts of it, one plane (8 KB) apart, so one MMA of
-// width 96 covers all three depth taps.  Per K step that is 3 MMAs of N = 96
-// (A 4 KB + B 3 KB of shared-memory reads each) instead of 9 of N = 64
-// (A 4 KB + B 2 KB), for the same useful work.  Accumulator of kh block m:
-// TMEM columns m*96 + a*32 + co (a = 2 - kd), lanes kw*32 + ci.  A CTA unit is
-// one 32-channel output set and a contiguous K range.
+// halo (PLANES x 18 x 10 rows); B = dZ of the block's planes and one plane on
+// either side, for one set of 32 output channels, and its N atoms are the
+// kd = 2, 1, 0 shifts of it, one plane (8 KB) apart, so one MMA of width 96
+// covers all three depth taps.  M blocks cover the nine (kh, kw) taps:
+//   c_in 32 (64-byte rows): one block per kh, atoms kw = 0, 1, 2 one row
+//     apart plus an unused fourth atom;
+//   c_in 64 (128-byte rows): blocks of two taps in (kh, kw) order, the second
+//     atom at its own row distance (LBO), the fifth block one tap.
+// Per K step that is 3 (or 5) MMAs of N = 96 instead of 9 (or 14) MMAs of
+// N = 64 (or 128) over a depth halo, and each K block is loaded once per
+// 32-channel output set with a third of the input planes.  Accumulator of
+// block m: TMEM columns m*96 + a*32 + co (a = 2 - kd), lanes atom*KC + ci.
+// A CTA unit is one output set and a contiguous K range.
 namespace {
 constexpr int WK_PLANES = 2;
 constexpr int WK_KV = 128 * WK_PLANES;  // voxels per K block
-constexpr uint32_t WK_X_BYTES = 10 * 18 * WK_PLANES * 64;
-constexpr uint32_t WK_X_STRIDE = (WK_X_BYTES + 1024 + 1023) / 1024 * 1024;  // + slack read by the unused atom
-constexpr uint32_t WK_G_PLANE = 128 * 64;                                    // one dZ plane of the set
+constexpr uint32_t WK_G_PLANE = 128 * 64;  // one dZ plane of the set
 constexpr uint32_t WK_G_BYTES = (WK_PLANES + 2) * WK_G_PLANE;
-constexpr uint32_t WK_STAGE = WK_X_STRIDE + WK_G_BYTES;
-constexpr int WK_STAGES_RAW = (int)((227 * 1024 - 1024 - 256) / WK_STAGE);
-constexpr int WK_STAGES = WK_STAGES_RAW > 4 ? 4 : WK_STAGES_RAW;
-constexpr uint32_t WK_SMEM = 1024 + WK_STAGES * WK_STAGE + 256;
 constexpr uint32_t WK_IDESC = idesc_bf16(128, 96, 1, 1);
-static_assert(WK_STAGES >= 2, "shared memory");
+
+template <int KC>
+struct WkCfg {
+    static constexpr uint32_t ROW = KC * 2;
+    static constexpr uint32_t X_BYTES = 10 * 18 * WK_PLANES * ROW;
+    static constexpr uint32_t X_STRIDE = (X_BYTES + 1024 + 1023) / 1024 * 1024;  // + slack read by a spare atom
+    static constexpr uint32_t STAGE = X_STRIDE + WK_G_BYTES;
+    static constexpr int STAGES_RAW = (int)((227 * 1024 - 1024 - 256) / STAGE);
+    static constexpr int STAGES = STAGES_RAW > 4 ? 4 : STAGES_RAW;
+    static constexpr uint32_t SMEM = 1024 + STAGES * STAGE + 256;
+    static constexpr int NBLK = KC == 32 ? 3 : 5;
+    static constexpr uint32_t SWZ = KC == 32 ? SWZ_64B : SWZ_128B;
+    static_assert(STAGES >= 2, "shared memory");
+    static_assert(NBLK * 96 <= 512, "tensor memory");
+};
+
+// Row offset of (kh, kw) tap p in the halo, its block's first row and the row
+// distance of the block's second atom.
+__host__ __device__ constexpr int wk_tap_rows(int p) { return (p / 3) * 10 + p % 3; }
+template <int KC>
+__device__ __forceinline__ void wk_block(int m, int& first_rows, int& lbo_rows) {
+    if (KC == 32) {
+        first_rows = m * 10;
+        lbo_rows = 1;
+    } else {
+        first_rows = wk_tap_rows(2 * m);
+        lbo_rows = 2 * m + 1 < 9 ? wk_tap_rows(2 * m + 1) - first_rows : 1;
+    }
+}
 }  // namespace
 
+template <int KC>
 __global__ void __launch_bounds__(224, 1)
     wgrad_halo_kd_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                          const WhParams p) {
+    using C = WkCfg<KC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* ring = smem;  // stage: [input halo][dZ planes d0-1 .. d0+PLANES]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WK_STAGES * WK_STAGE);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
     uint64_t* full = bars;
-    uint64_t* empty = bars + WK_STAGES;
-    uint64_t* tfull = bars + 2 * WK_STAGES;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* tfull = bars + 2 * C::STAGES;
     uint64_t* tempty = tfull + 1;
     uint64_t* drain = tempty + 1;  // [2]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
@@ -367,7 +396,7 @@ __global__ void __launch_bounds__(224, 1)
     const WhGeom& g = p.g;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < WK_STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 2);
         }
@@ -415,13 +444,13 @@ __global__ void __launch_bounds__(224, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* st = ring + stage * WK_STAGE;
-                    mbar_arrive_expect_tx(&full[stage], WK_X_BYTES + WK_G_BYTES);
+                    uint8_t* st = ring + stage * C::STAGE;
+                    mbar_arrive_expect_tx(&full[stage], C::X_BYTES + WK_G_BYTES);
                     tma_load_5d(st, &tmX, &full[stage], 0, w0 - 1, h0 - 1, d0, n);
-                    tma_load_5d(st + WK_X_STRIDE, &tmG, &full[stage], set * 32, w0, h0, d0 - 1, n);
+                    tma_load_5d(st + C::X_STRIDE, &tmG, &full[stage], set * 32, w0, h0, d0 - 1, n);
                     issued |= 1u << stage;
                     par = (par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == WK_STAGES) {
+                    if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -438,19 +467,19 @@ __global__ void __launch_bounds__(224, 1)
                 }
             }
             if (!ok) {
-                for (int s = 0; s < WK_STAGES; ++s)
+                for (int s = 0; s < C::STAGES; ++s)
                     if (issued & (1u << s)) mbar_wait_timed(&full[s], (par >> s) & 1, p.wait_ns);
             }
         }
     } else if (warp == 1 || warp == 6) {
         if (lane == 0) {
-            // ---------------- MMA issuers: warp 1 takes kh blocks 0 and 2, warp 6 block 1
+            // ---------------- MMA issuers: warp 1 takes the even M blocks, warp 6 the odd ones
             const int mi = warp == 1 ? 0 : 1;
             int stage = 0;
             uint32_t phase = 0, local = 0;
             bool ok = true;
-            const uint64_t adesc_base = sdesc(smem_u32(ring), 64, 10 * 64, SWZ_64B);
-            const uint64_t bdesc_base = sdesc(smem_u32(ring) + WK_X_STRIDE, WK_G_PLANE, 8 * 64, SWZ_64B);
+            const uint64_t adesc_base = sdesc(smem_u32(ring), 0, 10 * C::ROW, C::SWZ);
+            const uint64_t bdesc_base = sdesc(smem_u32(ring) + C::X_STRIDE, WK_G_PLANE, 8 * 64, SWZ_64B);
             for (int u = blockIdx.x; u < g.num_units && ok; u += gridDim.x, ++local) {
                 int set, split;
                 wh_unit(g, u, (int)gridDim.x, set, split);
@@ -467,21 +496,25 @@ __global__ void __launch_bounds__(224, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a_st = adesc_base + ((stage * WK_STAGE) >> 4);
-                    const uint64_t b_st = bdesc_base + ((stage * WK_STAGE) >> 4);
-                    for (int m = mi; m < 3; m += 2) {
+                    const uint64_t a_st = adesc_base + ((stage * C::STAGE) >> 4);
+                    const uint64_t b_st = bdesc_base + ((stage * C::STAGE) >> 4);
+                    for (int m = mi; m < C::NBLK; m += 2) {
+                        int first_rows, lbo_rows;
+                        wk_block<KC>(m, first_rows, lbo_rows);
+                        const uint64_t a_m = (a_st + ((uint32_t)(first_rows * C::ROW) >> 4)) |
+                                             ((uint64_t)(((uint32_t)(lbo_rows * C::ROW) >> 4) & 0x3FFFu) << 16);
                         const uint32_t d_tmem = tmem_base + m * 96;
 #pragma unroll
                         for (int s = 0; s < WK_KV / 16; ++s) {
                             // K step s: voxels 16s..16s+15 = plane s/8, lines 2(s%8), 2(s%8)+1
                             const int i = s >> 3, j = 2 * (s & 7);
-                            const uint64_t ad = a_st + ((uint32_t)((i * 18 + j + m) * 10 * 64) >> 4);
+                            const uint64_t ad = a_m + ((uint32_t)((i * 18 + j) * 10 * C::ROW) >> 4);
                             const uint64_t bd = b_st + ((uint32_t)((i * 128 + j * 8) * 64) >> 4);
                             umma_bf16(d_tmem, ad, bd, WK_IDESC, (kb != k0 || s != 0) ? 1u : 0u);
                         }
                     }
                     umma_commit(&empty[stage]);
-                    if (++stage == WK_STAGES) {
+                    if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -495,8 +528,8 @@ __global__ void __launch_bounds__(224, 1)
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..5): lane quarter q = kw (quarter 3 is the
-        // unused atom), lane = ci; column a*32 + c of block kh -> co = set*32 + c, kd = 2 - a
+        // ---------------- epilogue (warps 2..5): lane r = atom*KC + ci; column a*32 + c
+        // of block m -> co = set*32 + c, kd = 2 - a, (kh, kw) tap p of the atom
         const int q = warp & 3;
         const int et = threadIdx.x - 64;
         const int KK = 27 * g.Cin;
@@ -506,8 +539,11 @@ __global__ void __launch_bounds__(224, 1)
             wh_unit(g, u, (int)gridDim.x, set, split);
             if (!epi_wait(tfull, local & 1, et, epi_flag, abort_flag, p.wait_ns, p.status)) break;
             tc_fence_after();
-            if (q < 3) {
-                for (int m = 0; m < 3; ++m) {
+            const int r = q * 32 + lane, atom = r / KC, ci = r % KC;
+            for (int m = 0; m < C::NBLK; ++m) {
+                const int p9 = KC == 32 ? m * 3 + atom : 2 * m + atom;  // (kh, kw) tap
+                if ((KC == 32 && atom == 3) || p9 >= 9) continue;        // spare atom: whole warp skips
+                {
                     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + m * 96;
 #pragma unroll 1
                     for (int c = 0; c < 96; c += 16) {
@@ -515,9 +551,9 @@ __global__ void __launch_bounds__(224, 1)
                         tmem_ld16(lane_addr + c, v);
                         tmem_ld_wait();
                         const int a = c >> 5, kd = 2 - a;
-                        const int t = kd * 9 + m * 3 + q;
+                        const int t = kd * 9 + p9;
                         float* dst = p.part + (int64_t)split * g.Cout * KK + (int64_t)(set * 32 + (c & 31)) * KK +
-                                     t * g.Cin + lane;
+                                     t * g.Cin + ci;
 #pragma unroll
                         for (int k = 0; k < 16; ++k) dst[(int64_t)k * KK] = __uint_as_float(v[k]);
                     }
@@ -583,10 +619,10 @@ static WhGeom wk_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, i
     g.nb_h = (int)((h + 15) / 16);
     g.nb_d = (int)((d + WK_PLANES - 1) / WK_PLANES);
     g.total_kb = n * g.nb_d * g.nb_h * g.nb_w;
-    g.blocks_per_chunk = 3;
+    g.blocks_per_chunk = c_in == 32 ? WkCfg<32>::NBLK : WkCfg<64>::NBLK;
     g.n_chunks = 1;
     g.sets_per_chunk = c_out / 32;
-    g.g_per_set = 3;
+    g.g_per_set = g.blocks_per_chunk;
     g.n_sets = g.sets_per_chunk;
     // at most one unit per SM (one round of CTAs): half the partial sums of two
     // units per SM (measured in the five-block step: 1.470 -> 1.416 ms together
@@ -599,9 +635,13 @@ static WhGeom wk_geom(int num_sms, int64_t n, int64_t d, int64_t h, int64_t w, i
     return g;
 }
 
-// c_in 32 with one or two output-channel sets takes the depth-stacked variant
-// (measured on the layer-2 shape, 8 x 64^3, 32 -> 64: 0.246 -> 0.184 ms).
-static bool wk_path(int c_in, int c_out) { return c_in == 32 && (c_out == 32 || c_out == 64); }
+// c_in 32 with one or two output-channel sets and c_in 64 with two or four
+// take the depth-stacked variant (measured on the layer-2 shape, 8 x 64^3,
+// 32 -> 64: 0.246 -> 0.184 ms; on the layer-3 shape, 8 x 32^3, 64 -> 128:
+// 0.097 -> 0.088 ms alone, and the five-block step 1.338 -> 1.315 ms).
+static bool wk_path(int c_in, int c_out) {
+    return (c_in == 32 && (c_out == 32 || c_out == 64)) || (c_in == 64 && (c_out == 64 || c_out == 128));
+}
 
 bool wgrad_halo_supported(int c_in, int c_out) {
     return (c_in == 32 && (c_out == 32 || c_out == 64 || c_out == 128)) ||
@@ -655,6 +695,7 @@ static cf_status run_wgrad_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int6
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
+template <int KC>
 static cf_status run_wgrad_halo_kd(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in,
                                    int c_out, const uint16_t* x, const uint16_t* dz, float* part, int* n_splits) {
     WhGeom g = wk_geom(ctx.num_sms, n, d, h, w, c_in, c_out);
@@ -663,8 +704,9 @@ static cf_status run_wgrad_halo_kd(const LaunchCtx& ctx, int64_t n, int64_t d, i
     const uint64_t dx[5] = {(uint64_t)c_in, (uint64_t)w, (uint64_t)h, (uint64_t)d, (uint64_t)n};
     const uint64_t sx[4] = {(uint64_t)c_in * 2, (uint64_t)w * c_in * 2, (uint64_t)h * w * c_in * 2,
                             (uint64_t)d * h * w * c_in * 2};
-    const uint32_t bx[5] = {32u, 10u, 18u, (uint32_t)WK_PLANES, 1u};
-    if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, dx, sx, bx, CU_TENSOR_MAP_SWIZZLE_64B))
+    const uint32_t bx[5] = {(uint32_t)KC, 10u, 18u, (uint32_t)WK_PLANES, 1u};
+    if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, dx, sx, bx,
+                     KC == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
         return CF_ERR_CUDA;
     const uint64_t dg[5] = {(uint64_t)c_out, (uint64_t)w, (uint64_t)h, (uint64_t)d, (uint64_t)n};
     const uint64_t sg[4] = {(uint64_t)c_out * 2, (uint64_t)w * c_out * 2, (uint64_t)h * w * c_out * 2,
@@ -673,17 +715,19 @@ static cf_status run_wgrad_halo_kd(const LaunchCtx& ctx, int64_t n, int64_t d, i
     if (!encode_tmap(&tg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, dz, dg, sg, bg, CU_TENSOR_MAP_SWIZZLE_64B))
         return CF_ERR_CUDA;
     WhParams p{g, part, ctx.status, ctx.wait_ns};
-    if (cudaFuncSetAttribute(wgrad_halo_kd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WK_SMEM) !=
-        cudaSuccess)
+    auto kern = wgrad_halo_kd_kernel<KC>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WkCfg<KC>::SMEM) != cudaSuccess)
         return CF_ERR_CUDA;
     const int grid = std::max(1, std::min(g.num_units, ctx.num_sms));
-    wgrad_halo_kd_kernel<<<grid, 224, WK_SMEM, ctx.stream>>>(tx, tg, p);
+    kern<<<grid, 224, WkCfg<KC>::SMEM, ctx.stream>>>(tx, tg, p);
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
 cf_status launch_wgrad_halo(const LaunchCtx& ctx, int64_t n, int64_t d, int64_t h, int64_t w, int c_in, int c_out,
                             const uint16_t* x, const uint16_t* dz, float* part, int* n_splits) {
-    if (wk_path(c_in, c_out)) return run_wgrad_halo_kd(ctx, n, d, h, w, c_in, c_out, x, dz, part, n_splits);
+    if (wk_path(c_in, c_out))
+        return c_in == 32 ? run_wgrad_halo_kd<32>(ctx, n, d, h, w, c_in, c_out, x, dz, part, n_splits)
+                          : run_wgrad_halo_kd<64>(ctx, n, d, h, w, c_in, c_out, x, dz, part, n_splits);
     if (c_in == 32) {
         if (c_out == 128) return run_wgrad_halo<32, 128, 1>(ctx, n, d, h, w, c_in, c_out, x, dz, part, n_splits);
     } else if (c_in == 64) {
